@@ -1,0 +1,414 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Each test checks the oracle against something other than itself: a value the
+pages print, a hand-derived worked example (tests/golden/), a library routine
+(numpy's binary16 conversion, torch's float64 attention), a closed form, an
+invariant, or the pages' error bound.
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _f16(x):
+    return np.asarray(x, np.float16)
+
+
+def _bits(x):
+    return _f16(x).view(np.uint16)
+
+
+# ----------------------------------------------------------------------------- binary16 conversions
+def test_f16_widening_matches_numpy_for_every_pattern():
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = pats.view(np.float16).astype(np.float32)
+    got = np.array([oracle.f32_from_f16(int(p)) for p in pats], np.float32)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+
+
+def _conversion_probe_values():
+    rng = np.random.default_rng(1)
+    vals = [rng.standard_normal(4000).astype(np.float32) * s for s in (1e-6, 1e-3, 1.0, 100.0, 3e4)]
+    # exact midpoints between neighbouring binary16 values (ties), and points just beside them
+    h = rng.integers(0, 0x7BFF, 4000).astype(np.uint16)
+    lo = h.view(np.float16).astype(np.float64)
+    hi = (h + 1).view(np.float16).astype(np.float64)
+    mid = ((lo + hi) / 2).astype(np.float32)  # exact in binary32
+    vals += [mid, np.nextafter(mid, np.float32(np.inf)), np.nextafter(mid, np.float32(-np.inf))]
+    vals.append(np.array([65504, 65505, 65519, 65520, 65536, 1e9, 2.0**-24, 2.0**-25, 2.0**-26, 3 * 2.0**-26,
+                          0.0, 6.1e-5, 6.0e-5], np.float32))
+    v = np.concatenate(vals).astype(np.float32)
+    return np.concatenate([v, -v])
+
+
+def test_f16_round_nearest_even_matches_numpy():
+    x = _conversion_probe_values()
+    ref = x.astype(np.float16).view(np.uint16)
+    got = np.array([oracle.f16_from_f32_rne(float(v)) for v in x], np.uint16)
+    assert np.array_equal(got, ref)
+
+
+def test_f16_round_up_is_the_binary16_ceiling():
+    x = _conversion_probe_values()
+    x = x[np.abs(x) <= 65504]
+    for v in x:
+        h = np.uint16(oracle.f16_from_f32_ru(float(v)))
+        hv = np.float64(h.view(np.float16))
+        assert hv >= float(v)
+        below = np.float64(np.nextafter(h.view(np.float16), np.float16(-np.inf)))
+        assert below < float(v)
+
+
+# ----------------------------------------------------------------------------- quantizer pins
+def test_worked_example_minus_0p1_to_3p0():
+    g = json.load(open(os.path.join(GOLDEN, "quant_worked_example.json")))
+    x = _f16(g["inputs"])
+    for c in g["cases"]:
+        s, z = oracle.quant_params(x, c["bits"])
+        assert s == int(c["scale_f16"], 16)
+        assert z == int(c["zp_f16"], 16)
+        u = oracle.quantize_values(x, c["bits"], s, z)
+        assert u.tolist() == c["u"]
+
+
+def test_round_half_to_even_ties():
+    g = json.load(open(os.path.join(GOLDEN, "quant_ties.json")))
+    for c in g["cases"]:
+        x = _f16(c["x"])
+        s, z = oracle.quant_params(x, c["bits"])
+        assert (s, z) == (int(c["scale_f16"], 16), int(c["zp_f16"], 16))
+        assert oracle.quantize_values(x, c["bits"], s, z).tolist() == c["u"]
+
+
+def test_int_ranges():
+    # int8 [-128, 127] and int4 [-8, 7] as printed; int2 read as [-2, 1]
+    assert (oracle.qmin(8), oracle.qmax(8)) == (-128, 127)
+    assert (oracle.qmin(4), oracle.qmax(4)) == (-8, 7)
+    assert (oracle.qmin(2), oracle.qmax(2)) == (-2, 1)
+
+
+def test_identity_case_int8():
+    x = _f16(np.arange(-128, 128))
+    np.random.default_rng(0).shuffle(x)
+    s, z = oracle.quant_params(x, 8)
+    assert np.uint16(s).view(np.float16) == 1.0
+    assert np.uint16(z).view(np.float16) == 0.0
+    u = oracle.quantize_values(x, 8, s, z)
+    assert np.array_equal(u.astype(np.int32) - 128, x.astype(np.int32))
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_on_grid_round_trip_is_exact(bits):
+    rng = np.random.default_rng(bits)
+    qmin, qmax = oracle.qmin(bits), oracle.qmax(bits)
+    for trial in range(200):
+        s = 2.0 ** int(rng.integers(-8, 4))
+        zp = int(rng.integers(-40, 41))
+        n = int(rng.integers(2, 130))
+        q = rng.integers(qmin, qmax + 1, n)
+        q[0], q[-1] = qmin, qmax
+        x = (s * (q - zp)).astype(np.float64)
+        xh = _f16(x)
+        assert np.array_equal(xh.astype(np.float64), x)  # on the binary16 grid
+        sh, zh = oracle.quant_params(xh, bits)
+        assert np.uint16(sh).view(np.float16) == s
+        assert np.uint16(zh).view(np.float16) == zp
+        u = oracle.quantize_values(xh, bits, sh, zh)
+        assert np.array_equal(u.astype(np.int64), q - qmin)
+        back = np.array([oracle.dequantize_value(int(v), bits, sh, zh) for v in u], np.float32)
+        assert np.array_equal(back.view(np.uint32), x.astype(np.float32).view(np.uint32))
+
+
+def _groups(rng, n_groups, size):
+    out = []
+    for i in range(n_groups):
+        kind = i % 5
+        if kind == 0:
+            x = rng.standard_normal(size)
+        elif kind == 1:
+            x = rng.uniform(-0.1, 3.0, size)  # lopsided, as in the pages' example
+        elif kind == 2:
+            x = rng.standard_normal(size) * 20 + 5  # an outlier channel
+        elif kind == 3:
+            x = rng.standard_normal(size) * 1e-3 + 7.0  # far from zero, narrow
+        else:
+            x = rng.standard_normal(size) * 300.0
+        out.append(_f16(x))
+    return out
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_error_bound_half_step(bits):
+    """|x - x_hat| <= scale/2 ("KV Cache Quantization — 8-bit and 4-bit", § Integer quantization in one screen)."""
+    rng = np.random.default_rng(100 + bits)
+    qmin, qmax = oracle.qmin(bits), oracle.qmax(bits)
+    for x in _groups(rng, 300, 32) + _groups(rng, 50, 128):
+        sh, zh = oracle.quant_params(x, bits)
+        s = float(np.uint16(sh).view(np.float16))
+        u = oracle.quantize_values(x, bits, sh, zh)
+        assert u.max() <= qmax - qmin
+        xd = x.astype(np.float64)
+        xhat = np.array([oracle.dequantize_value(int(v), bits, sh, zh) for v in u], np.float64)
+        err = np.abs(xd - xhat)
+        zp = float(np.uint16(zh).view(np.float16))
+        if abs(zp) <= 2048:
+            if xd.max() > xd.min():  # (a constant group is widened to include 0)
+                assert u[int(np.argmin(xd))] == 0  # the smallest value lands on q_min
+            assert err.max() <= s / 2 * (1 + 2.0**-20) + 1e-30, (bits, err.max(), s)
+        else:
+            # binary16 holds integers exactly only up to 2048: the stored zero point may be
+            # one step off, which moves one end of the group into the clamp (see below)
+            # stored zero point off by up to half its binary16 spacing: self-consistency only
+            assert np.array_equal(xhat, (np.float32(s) * (u.astype(np.float32) + qmin - np.float32(zp))).astype(np.float64))
+
+
+def test_zero_point_beyond_binary16_integers():
+    """A narrow group far from zero needs |zero_point| > 2048, which binary16 stores
+    only to the nearest even integer; quantization then stays self-consistent with
+    the stored value (x_hat = scale * (q - zp_h)) and within one step and a half."""
+    x = _f16(7.0 + 2.0**-8 * np.array([-1, 0, 1, 1, 0, -1, 0, 1]))  # three neighbouring binary16 values
+    sh, zh = oracle.quant_params(x, 2)
+    s = float(np.uint16(sh).view(np.float16))
+    zp = float(np.uint16(zh).view(np.float16))
+    assert abs(zp) > 2048 and zp % 2 == 0
+    u = oracle.quantize_values(x, 2, sh, zh)
+    for xi, ui in zip(x.astype(np.float64), u):
+        xhat = oracle.dequantize_value(int(ui), 2, sh, zh)
+        assert xhat == np.float32(s) * np.float32(int(ui) - 2 - zp)
+        assert abs(xhat - xi) <= 1.5 * s
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_scale_is_range_over_levels_rounded_up(bits):
+    """scale = (x_max - x_min)/(q_max - q_min), stored in binary16 rounded up."""
+    rng = np.random.default_rng(200 + bits)
+    N = oracle.qmax(bits) - oracle.qmin(bits)
+    for x in _groups(rng, 200, 64):
+        xd = x.astype(np.float64)
+        if xd.max() == xd.min():
+            continue  # constant groups follow the widening rule (test_degenerate_groups)
+        exact = (xd.max() - xd.min()) / N
+        sh, _ = oracle.quant_params(x, bits)
+        s = np.uint16(sh).view(np.float16)
+        below = np.float64(np.nextafter(s, np.float16(-np.inf)))
+        # rounded up from a binary32 quotient: within one binary16 step above, never a step below
+        assert float(s) >= exact * (1 - 2.0**-22)
+        assert below < exact * (1 + 2.0**-22)
+
+
+def test_degenerate_groups():
+    for bits in (2, 4, 8):
+        z = _f16(np.zeros(16))
+        sh, zh = oracle.quant_params(z, bits)
+        assert sh == 0x3C00
+        u = oracle.quantize_values(z, bits, sh, zh)
+        assert all(oracle.dequantize_value(int(v), bits, sh, zh) == 0.0 for v in u)
+        for c in (2.0, -3.5, 1e-3, 60000.0):
+            x = _f16(np.full(8, c))
+            sh, zh = oracle.quant_params(x, bits)
+            s = float(np.uint16(sh).view(np.float16))
+            u = oracle.quantize_values(x, bits, sh, zh)
+            xhat = oracle.dequantize_value(int(u[0]), bits, sh, zh)
+            assert abs(xhat - float(x[0])) <= s / 2 * (1 + 2.0**-20)
+
+
+# ----------------------------------------------------------------------------- bytes accounting
+def test_bytes_formula_worked_example():
+    g = json.load(open(os.path.join(GOLDEN, "kv_bytes_examples.json")))["worked_example"]
+    L, H, d, S = g["L"], g["n_kv"], g["d_head"], g["S"]
+    assert oracle.kv_bytes(L, H, d, 1, 16) == g["fp16_bytes_per_token"]
+    assert oracle.kv_bytes(L, H, d, 1, 8) == g["elements_per_token"]  # one byte per element
+    assert round(oracle.kv_bytes(L, H, d, S, 16) / 1e9, 1) == g["gb_fp16_approx"]
+    assert round(oracle.kv_bytes(L, H, d, S, 8) / 1e9, 1) == g["gb_int8_approx"]
+    assert round(oracle.kv_bytes(L, H, d, S, 4) / 1e9, 1) == g["gb_int4_approx"]
+
+
+def test_bytes_per_token_table():
+    g = json.load(open(os.path.join(GOLDEN, "kv_bytes_examples.json")))["per_token_table"]
+    # the model's (L, n_kv, d) product is fixed by the fp16 row: 160 KiB = 2 * 2 B * L*n_kv*d
+    prod = g["fp16_kib_per_token"] * 1024 // 4
+    for row in g["rows"]:
+        per_tok = oracle.kv_bytes(1, 1, prod, 1, row["bits"])
+        assert per_tok == row["kib_per_token"] * 1024
+        turn = oracle.kv_bytes(1, 1, prod, g["turn_tokens"], row["bits"]) / 2**30
+        assert round(turn, 2) == row["gib_per_turn"]
+
+
+def test_block_scale_overhead_64k():
+    g = json.load(open(os.path.join(GOLDEN, "kv_bytes_examples.json")))["block_scale_64k"]
+    prod = g["fp16_kib_per_token"] * 1024 // 4
+    T = g["tokens"]
+    assert oracle.kv_bytes(1, 1, prod, T, 16) / 2**30 == g["fp16_gib"]
+    kib8 = oracle.kv_bytes(1, 1, prod, 1, 8, g["meta_bytes"], g["group_elems"]) / 1024
+    lo, hi = g["int8_kib_per_token_range"]
+    assert lo <= kib8 <= hi and kib8 == hi
+    assert round(oracle.kv_bytes(1, 1, prod, T, 8, g["meta_bytes"], g["group_elems"]) / 2**30) == g["int8_gib_approx"]
+    kib4 = oracle.kv_bytes(1, 1, prod, 1, 4, g["meta_bytes"], g["group_elems"]) / 1024
+    assert kib4 == g["int4_kib_per_token"]
+    gib4 = oracle.kv_bytes(1, 1, prod, T, 4, g["meta_bytes"], g["group_elems"]) / 2**30
+    assert gib4 == 1.125 and abs(gib4 - g["int4_gib_approx"]) <= 0.005  # printed to two places
+
+
+# ----------------------------------------------------------------------------- attention pins
+def _sdpa64(q, k, v, scale):
+    q = torch.as_tensor(np.asarray(q, np.float64))[None, :, None, :]  # [1, r, 1, d]
+    k = torch.as_tensor(np.asarray(k, np.float64))[None, None].expand(1, q.shape[1], -1, -1)
+    v = torch.as_tensor(np.asarray(v, np.float64))[None, None].expand(1, q.shape[1], -1, -1)
+    o = torch.nn.functional.scaled_dot_product_attention(q, k, v, scale=scale)
+    return o[0, :, 0, :].numpy()
+
+
+@pytest.mark.parametrize("T,d,r", [(1, 8, 1), (5, 8, 2), (37, 16, 4), (300, 128, 8)])
+def test_attention_matches_torch_float64(T, d, r):
+    rng = np.random.default_rng(T * 7 + d)
+    q = _f16(rng.standard_normal((r, d)))
+    k = rng.standard_normal((T, d)).astype(np.float32) * 3
+    v = rng.standard_normal((T, d)).astype(np.float32)
+    scale = 1 / math.sqrt(d)
+    got = oracle.attention(q, k, v, scale)
+    ref = _sdpa64(q.astype(np.float64), k, v, scale)
+    assert np.abs(got - ref).max() < 1e-6
+
+
+def test_attention_invariants():
+    rng = np.random.default_rng(5)
+    T, d = 64, 16
+    k = rng.standard_normal((T, d)).astype(np.float32)
+    v = rng.standard_normal((T, d)).astype(np.float32)
+    # zero query: uniform weights -> the mean of the values
+    o = oracle.attention(np.zeros((1, d), np.float16), k, v, 0.25)
+    assert np.abs(o[0] - v.astype(np.float64).mean(0)).max() < 1e-6
+    # one dominant score -> that token's value
+    kk = np.zeros((T, d), np.float32)
+    kk[17, 0] = 100.0
+    q = np.zeros((1, d), np.float16)
+    q[0, 0] = 1.0
+    o = oracle.attention(q, kk, v, 1.0)
+    assert np.abs(o[0] - v[17]).max() < 1e-6
+
+
+@pytest.mark.parametrize("bits,G,Gv,R", [(8, 32, 128, 0), (4, 128, 64, 128), (2, 32, 32, 128)])
+def test_on_grid_cache_attention_equals_textbook(bits, G, Gv, R):
+    """Keys and values on each group's grid quantize exactly, so attention over the
+    quantized cache equals torch's float64 attention over the raw binary16 inputs."""
+    rng = np.random.default_rng(bits)
+    d, T, r = 128, 300, 4
+    qmin, qmax = oracle.qmin(bits), oracle.qmax(bits)
+    R_eff = R if R > 0 else G
+    Tq = (T // R_eff) * R_eff
+    k = np.zeros((T, d))
+    for g in range(T // G):
+        for c in range(d):
+            s = 2.0 ** int(rng.integers(-6, 0))
+            zp = int(rng.integers(-3, 4))
+            qs = rng.integers(qmin, qmax + 1, G)
+            qs[0], qs[-1] = qmin, qmax
+            k[g * G:(g + 1) * G, c] = s * (qs - zp)
+    k[(T // G) * G:] = rng.standard_normal((T - (T // G) * G, d))
+    v = np.zeros((T, d))
+    for t in range(T):
+        for j in range(d // Gv):
+            s = 2.0 ** int(rng.integers(-6, 0))
+            zp = int(rng.integers(-3, 4))
+            qs = rng.integers(qmin, qmax + 1, Gv)
+            qs[0], qs[-1] = qmin, qmax
+            v[t, j * Gv:(j + 1) * Gv] = s * (qs - zp)
+    k16, v16 = _f16(k), _f16(v)
+    assert np.array_equal(k16[:Tq].astype(np.float64), k[:Tq])
+    st = oracle.cache_state(k16, v16, d=d, bits=bits, G=G, Gv=Gv, R=R)
+    kh, vh = oracle.dequantize_state(st, d=d, bits=bits, G=G, Gv=Gv, R=R)
+    assert np.array_equal(kh, k16.astype(np.float32))
+    assert np.array_equal(vh, v16.astype(np.float32))
+    q = _f16(rng.standard_normal((r, d)))
+    got = oracle.attention(q, kh, vh, 1 / math.sqrt(d))
+    ref = _sdpa64(q.astype(np.float64), k16.astype(np.float64), v16.astype(np.float64), 1 / math.sqrt(d))
+    assert np.abs(got - ref).max() < 1e-6
+
+
+# ----------------------------------------------------------------------------- quantization axes
+def test_keys_per_channel_values_per_token():
+    """Keys are grouped along tokens per channel, values along channels per token
+    ("Sub-8-Bit KV Cache Quantization Is Not a Free Lever for an RDNA4 Agent Swarm",
+    § The cache is two distributions, not one). A huge key channel and a huge value
+    token must not spoil the other channels / tokens."""
+    rng = np.random.default_rng(9)
+    d, T, G, Gv, bits = 128, 64, 32, 128, 8
+    k = rng.standard_normal((T, d))
+    k[:, 5] *= 1000.0  # outlier key channel
+    v = rng.standard_normal((T, d)) * 0.5
+    v[7, :] *= 1000.0  # outlier value token
+    k16, v16 = _f16(k), _f16(v)
+    st = oracle.cache_state(k16, v16, d=d, bits=bits, G=G, Gv=Gv, R=0)
+    kh, vh = oracle.dequantize_state(st, d=d, bits=bits, G=G, Gv=Gv, R=0)
+    ek = np.abs(kh - k16.astype(np.float32))
+    ev = np.abs(vh - v16.astype(np.float32))
+    assert np.delete(ek, 5, axis=1).max() < 0.02  # ordinary channels keep a fine step
+    assert ek[:, 5].max() > 0.5  # the outlier channel has its own coarse one
+    assert np.delete(ev, 7, axis=0).max() < 0.01
+    assert ev[7].max() > 0.5
+    # every key group's metadata is per channel: G tokens share one (scale, zp) per channel
+    assert st.k_meta.shape == (T // G, d, 2)
+    assert st.v_meta.shape == (T, d // Gv, 2)
+
+
+def test_residual_window_keeps_newest_tokens_in_f16():
+    rng = np.random.default_rng(11)
+    d, T, G, Gv, R, bits = 128, 300, 32, 64, 128, 4
+    k16 = _f16(rng.standard_normal((T, d)))
+    v16 = _f16(rng.standard_normal((T, d)))
+    st = oracle.cache_state(k16, v16, d=d, bits=bits, G=G, Gv=Gv, R=R)
+    assert st.Tq == 256 and st.k_codes.shape[0] == 256
+    for t in range(256, T):
+        assert np.array_equal(st.k_resid[t % R], k16[t].view(np.uint16))
+    kh, _ = oracle.dequantize_state(st, d=d, bits=bits, G=G, Gv=Gv, R=R)
+    assert np.array_equal(kh[256:], k16[256:].astype(np.float32))
+    # R = 0: the residual holds T mod G tokens
+    st0 = oracle.cache_state(k16, v16, d=d, bits=bits, G=G, Gv=Gv, R=0)
+    assert st0.Tq == (T // G) * G
+
+
+# ----------------------------------------------------------------------------- layout self-consistency (parity unpinned)
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_layout_pack_unpack_round_trip(bits):
+    d = 128
+    rng = np.random.default_rng(bits)
+    assert sorted(oracle.v_pos(d, c) for c in range(d)) == list(range(d))
+    for _ in range(20):
+        u = rng.integers(0, 2**bits, d).astype(np.uint8)
+        assert np.array_equal(oracle.unpack_k_row(oracle.pack_k_row(u, d, bits), d, bits), u)
+        pairs = np.zeros(4 * d * bits // 8, np.uint8)
+        u2 = rng.integers(0, 2**bits, d).astype(np.uint8)
+        oracle.pack_v_token(u, d, bits, 2, pairs)
+        oracle.pack_v_token(u2, d, bits, 3, pairs)
+        assert np.array_equal(oracle.unpack_v_token(pairs, d, bits, 2), u)
+        assert np.array_equal(oracle.unpack_v_token(pairs, d, bits, 3), u2)
+        assert not pairs[: 2 * d * bits // 8].any()
+
+
+def test_cache_state_codes_agree_with_group_quantizer():
+    rng = np.random.default_rng(12)
+    d, T, G, Gv, bits = 128, 96, 32, 32, 2
+    k16 = _f16(rng.standard_normal((T, d)))
+    v16 = _f16(rng.standard_normal((T, d)))
+    st = oracle.cache_state(k16, v16, d=d, bits=bits, G=G, Gv=Gv, R=0)
+    for t in range(T):
+        assert np.array_equal(oracle.unpack_v_token(st.v_codes, d, bits, t), st.v_u[t])
+    for t in range(st.Tq):
+        assert np.array_equal(oracle.unpack_k_row(st.k_codes[t], d, bits), st.k_u[t])
+    # one key group by hand through the scalar quantizer
+    g, c = 1, 77
+    col = k16[g * G:(g + 1) * G, c]
+    sh, zh = oracle.quant_params(col, bits)
+    assert (st.k_meta[g, c, 0], st.k_meta[g, c, 1]) == (sh, zh)
+    assert np.array_equal(st.k_u[g * G:(g + 1) * G, c], oracle.quantize_values(col, bits, sh, zh))
