@@ -1,0 +1,252 @@
+// kvq_api.cu — the C ABI of libkvq (declared in include/kvq.h): argument checks,
+// geometry, split-K planning and kernel dispatch. Host code only; every check runs
+// before any launch, and a failed check launches nothing.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "kvq_common.cuh"
+#include "kvq_kernels.h"
+
+using kvq::Geometry;
+
+namespace {
+
+bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+kvq_status check_buffers(const kvq_buffers* b) {
+  if (!b) return KVQ_ERR_INVALID_ARG;
+  const void* ps[5] = {b->k_codes, b->k_meta, b->k_resid, b->v_codes, b->v_meta};
+  for (const void* p : ps)
+    if (!aligned16(p)) return KVQ_ERR_INVALID_ARG;
+  return KVQ_OK;
+}
+
+// Layer-0-relative pointers of one layer.
+struct LayerPtrs {
+  uint8_t* k_codes;
+  __half2* k_meta;
+  __half* k_resid;
+  uint8_t* v_codes;
+  __half2* v_meta;
+};
+
+LayerPtrs layer_ptrs(const Geometry& g, const kvq_buffers* b, int layer) {
+  const int64_t s0 = (int64_t)layer * g.B * g.H;  // first slice of the layer
+  LayerPtrs p;
+  p.k_codes = static_cast<uint8_t*>(b->k_codes) + s0 * g.k_codes_slice;
+  p.k_meta = reinterpret_cast<__half2*>(static_cast<uint8_t*>(b->k_meta) + s0 * g.k_meta_slice);
+  p.k_resid = reinterpret_cast<__half*>(static_cast<uint8_t*>(b->k_resid) + s0 * g.k_resid_slice);
+  p.v_codes = static_cast<uint8_t*>(b->v_codes) + s0 * g.v_codes_slice;
+  p.v_meta = reinterpret_cast<__half2*>(static_cast<uint8_t*>(b->v_meta) + s0 * g.v_meta_slice);
+  return p;
+}
+
+int device_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+// Split-K plan: enough CTAs to cover the SMs several times, at least one 128-token
+// tile per split, never more than the device-independent workspace bound.
+void plan_splits(const Geometry& g, int64_t T, int ctas_per_sm, int64_t* n_split, int64_t* chunk) {
+  int sms = device_sm_count();
+  if (sms <= 0) sms = 152;
+  const int64_t units = (int64_t)g.B * g.H;
+  const int64_t tiles = (T + 127) / 128;
+  int64_t s = ((int64_t)sms * ctas_per_sm + units - 1) / units;
+  if (s > tiles) s = tiles;
+  const int64_t cap = kvq::max_splits(g, T);
+  if (s > cap) s = cap;
+  if (s < 1) s = 1;
+  int64_t c = (T + s - 1) / s;
+  c = (c + 127) / 128 * 128;
+  *chunk = c;
+  *n_split = (T + c - 1) / c;
+}
+
+constexpr int kSimtCtasPerSm = 4;
+
+}  // namespace
+
+extern "C" {
+
+const char* kvq_status_string(kvq_status s) {
+  switch (s) {
+    case KVQ_OK: return "ok";
+    case KVQ_ERR_INVALID_ARG: return "invalid argument";
+    case KVQ_ERR_UNSUPPORTED: return "unsupported configuration";
+    case KVQ_ERR_CAPACITY: return "cache capacity exceeded";
+    case KVQ_ERR_WORKSPACE: return "workspace missing or too small";
+    case KVQ_ERR_CUDA: return "CUDA launch error";
+  }
+  return "unknown status";
+}
+
+const char* kvq_version(void) { return "kvq 0.1.0 sm_103a"; }
+
+kvq_status kvq_buffer_sizes(const kvq_config* cfg, size_t bytes[KVQ_NUM_BUFFERS]) {
+  if (!bytes) return KVQ_ERR_INVALID_ARG;
+  Geometry g;
+  kvq_status st = kvq::make_geometry(cfg, &g);
+  if (st != KVQ_OK) return st;
+  bytes[KVQ_BUF_K_CODES] = (size_t)(g.n_slices * g.k_codes_slice);
+  bytes[KVQ_BUF_K_META] = (size_t)(g.n_slices * g.k_meta_slice);
+  bytes[KVQ_BUF_K_RESID] = (size_t)(g.n_slices * g.k_resid_slice);
+  bytes[KVQ_BUF_V_CODES] = (size_t)(g.n_slices * g.v_codes_slice);
+  bytes[KVQ_BUF_V_META] = (size_t)(g.n_slices * g.v_meta_slice);
+  return KVQ_OK;
+}
+
+kvq_status kvq_quantize_append(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur,
+                               int64_t n_new, const void* k_f16, const void* v_f16, void* stream) {
+  Geometry g;
+  kvq_status st = kvq::make_geometry(cfg, &g);
+  if (st != KVQ_OK) return st;
+  if ((st = check_buffers(bufs)) != KVQ_OK) return st;
+  if (layer < 0 || layer >= g.L || s_cur < 0 || n_new < 1) return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(k_f16) || !aligned16(v_f16)) return KVQ_ERR_INVALID_ARG;
+  if (s_cur + n_new > g.S_max) return KVQ_ERR_CAPACITY;
+  const int64_t T = s_cur + n_new;
+  const int64_t A0 = (s_cur / g.R_eff) * g.R_eff;
+  const int64_t A1 = (T / g.R_eff) * g.R_eff;
+  const LayerPtrs lp = layer_ptrs(g, bufs, layer);
+  kvq::AppendParams p;
+  p.k_codes = lp.k_codes;
+  p.k_meta = lp.k_meta;
+  p.k_resid = lp.k_resid;
+  p.v_codes = lp.v_codes;
+  p.v_meta = lp.v_meta;
+  p.k_in = static_cast<const __half*>(k_f16);
+  p.v_in = static_cast<const __half*>(v_f16);
+  p.s_cur = s_cur;
+  p.n_new = n_new;
+  p.A1 = A1;
+  p.group0 = A0 / g.G;
+  p.n_groups = (int)((A1 - A0) / g.G);
+  p.B = g.B;
+  p.H = g.H;
+  p.G = g.G;
+  p.Gv = g.Gv;
+  p.R_eff = g.R_eff;
+  p.n_vg = g.n_vg;
+  p.S_pad = g.S_pad;
+  p.rowK = g.rowK;
+  p.rowV = g.rowV;
+  p.k_codes_slice = g.k_codes_slice;
+  p.v_codes_slice = g.v_codes_slice;
+  cudaError_t e = kvq::launch_append(p, g.bits, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+kvq_status kvq_dequantize(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur, float* k_out,
+                          float* v_out, void* stream) {
+  Geometry g;
+  kvq_status st = kvq::make_geometry(cfg, &g);
+  if (st != KVQ_OK) return st;
+  if ((st = check_buffers(bufs)) != KVQ_OK) return st;
+  if (layer < 0 || layer >= g.L || s_cur < 1) return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(k_out) || !aligned16(v_out)) return KVQ_ERR_INVALID_ARG;
+  if (s_cur > g.S_max) return KVQ_ERR_CAPACITY;
+  const LayerPtrs lp = layer_ptrs(g, bufs, layer);
+  kvq::DequantParams p;
+  p.k_codes = lp.k_codes;
+  p.k_meta = lp.k_meta;
+  p.k_resid = lp.k_resid;
+  p.v_codes = lp.v_codes;
+  p.v_meta = lp.v_meta;
+  p.k_out = k_out;
+  p.v_out = v_out;
+  p.T = s_cur;
+  p.Tq = kvq::quantized_keys(g, s_cur);
+  p.B = g.B;
+  p.H = g.H;
+  p.G = g.G;
+  p.Gv = g.Gv;
+  p.R_eff = g.R_eff;
+  p.n_vg = g.n_vg;
+  p.S_pad = g.S_pad;
+  p.rowK = g.rowK;
+  p.rowV = g.rowV;
+  p.k_codes_slice = g.k_codes_slice;
+  p.v_codes_slice = g.v_codes_slice;
+  cudaError_t e = kvq::launch_dequant(p, g.bits, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+size_t kvq_decode_workspace_size(const kvq_config* cfg, int64_t s_cur) {
+  Geometry g;
+  if (kvq::make_geometry(cfg, &g) != KVQ_OK || s_cur < 1) return 0;
+  return kvq::workspace_layout(g, s_cur).total;
+}
+
+int32_t kvq_decode_num_splits(const kvq_config* cfg, int64_t s_cur) {
+  Geometry g;
+  if (kvq::make_geometry(cfg, &g) != KVQ_OK || s_cur < 1) return 0;
+  int64_t n, c;
+  plan_splits(g, s_cur, kSimtCtasPerSm, &n, &c);
+  return (int32_t)n;
+}
+
+kvq_status kvq_decode_attention_impl(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur,
+                                     const void* q_f16, float softmax_scale, float* out, void* ws,
+                                     size_t ws_bytes, void* stream, kvq_decode_impl impl) {
+  Geometry g;
+  kvq_status st = kvq::make_geometry(cfg, &g);
+  if (st != KVQ_OK) return st;
+  if ((st = check_buffers(bufs)) != KVQ_OK) return st;
+  if (layer < 0 || layer >= g.L || s_cur < 1) return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(q_f16) || !aligned16(out)) return KVQ_ERR_INVALID_ARG;
+  if (!(softmax_scale == softmax_scale) || softmax_scale == __builtin_inff() || softmax_scale == -__builtin_inff())
+    return KVQ_ERR_INVALID_ARG;
+  if (impl != KVQ_DECODE_AUTO && impl != KVQ_DECODE_SIMT && impl != KVQ_DECODE_MMA) return KVQ_ERR_INVALID_ARG;
+  if (s_cur > g.S_max) return KVQ_ERR_CAPACITY;
+  const kvq::WorkspaceLayout wl = kvq::workspace_layout(g, s_cur);
+  if (!aligned16(ws) || ws_bytes < wl.total) return KVQ_ERR_WORKSPACE;
+  const LayerPtrs lp = layer_ptrs(g, bufs, layer);
+  kvq::DecodeParams p;
+  p.k_codes = lp.k_codes;
+  p.k_meta = lp.k_meta;
+  p.k_resid = lp.k_resid;
+  p.v_codes = lp.v_codes;
+  p.v_meta = lp.v_meta;
+  p.q = static_cast<const __half*>(q_f16);
+  p.out = out;
+  p.tickets = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + wl.tickets_off);
+  p.ws_ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) + wl.ml_off);
+  p.ws_o = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + wl.o_off);
+  p.T = s_cur;
+  p.Tq = kvq::quantized_keys(g, s_cur);
+  p.cap = (int)wl.cap;
+  p.B = g.B;
+  p.H = g.H;
+  p.r = g.r;
+  p.G = g.G;
+  p.Gv = g.Gv;
+  p.R_eff = g.R_eff;
+  p.n_vg = g.n_vg;
+  p.S_pad = g.S_pad;
+  p.rowK = g.rowK;
+  p.rowV = g.rowV;
+  p.k_codes_slice = g.k_codes_slice;
+  p.v_codes_slice = g.v_codes_slice;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  int64_t n_split, chunk;
+  plan_splits(g, s_cur, kSimtCtasPerSm, &n_split, &chunk);
+  p.n_split = (int)n_split;
+  p.chunk = chunk;
+  if (impl == KVQ_DECODE_MMA) return KVQ_ERR_UNSUPPORTED;
+  cudaError_t e = kvq::launch_decode_simt(p, g.bits, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+kvq_status kvq_decode_attention(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur,
+                                const void* q_f16, float softmax_scale, float* out, void* ws, size_t ws_bytes,
+                                void* stream) {
+  return kvq_decode_attention_impl(cfg, bufs, layer, s_cur, q_f16, softmax_scale, out, ws, ws_bytes, stream,
+                                   KVQ_DECODE_AUTO);
+}
+
+}  // extern "C"

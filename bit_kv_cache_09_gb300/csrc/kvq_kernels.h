@@ -1,0 +1,68 @@
+// kvq_kernels.h — kernel parameter blocks and launchers (library-internal).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace kvq {
+
+// All pointers are already offset to the layer's first slice (layer, batch 0, head 0).
+struct AppendParams {
+  uint8_t* k_codes;
+  __half2* k_meta;
+  __half* k_resid;
+  uint8_t* v_codes;
+  __half2* v_meta;
+  const __half* k_in;  // [B][n_new][H][d]
+  const __half* v_in;  // [B][n_new][H][d]
+  int64_t s_cur, n_new;
+  int64_t A1;      // first token of the residual window after the call
+  int64_t group0;  // first key group quantized by this call
+  int n_groups;    // key groups quantized by this call
+  int B, H, G, Gv, R_eff, n_vg;
+  int64_t S_pad, rowK, rowV;
+  int64_t k_codes_slice, v_codes_slice;
+};
+
+struct DequantParams {
+  const uint8_t* k_codes;
+  const __half2* k_meta;
+  const __half* k_resid;
+  const uint8_t* v_codes;
+  const __half2* v_meta;
+  float* k_out;  // [B][H][T][d]
+  float* v_out;
+  int64_t T, Tq;
+  int B, H, G, Gv, R_eff, n_vg;
+  int64_t S_pad, rowK, rowV;
+  int64_t k_codes_slice, v_codes_slice;
+};
+
+struct DecodeParams {
+  const uint8_t* k_codes;
+  const __half2* k_meta;
+  const __half* k_resid;
+  const uint8_t* v_codes;
+  const __half2* v_meta;
+  const __half* q;  // [B][H*r][d]
+  float* out;       // [B][H*r][d]
+  uint32_t* tickets;  // [B*H]
+  float2* ws_ml;      // [B][H*r][cap] (running max in log2 units, denominator)
+  float* ws_o;        // [B][H*r][cap][d]
+  int64_t T, Tq;
+  int64_t chunk;      // tokens per split (multiple of 128)
+  int n_split, cap;
+  int B, H, r, G, Gv, R_eff, n_vg;
+  int64_t S_pad, rowK, rowV;
+  int64_t k_codes_slice, v_codes_slice;
+  float scale_log2;   // softmax_scale * log2(e)
+};
+
+cudaError_t launch_append(const AppendParams& p, int bits, cudaStream_t stream);
+cudaError_t launch_dequant(const DequantParams& p, int bits, cudaStream_t stream);
+cudaError_t launch_decode_simt(const DecodeParams& p, int bits, cudaStream_t stream);
+cudaError_t launch_decode_mma(const DecodeParams& p, int bits, cudaStream_t stream);
+
+}  // namespace kvq

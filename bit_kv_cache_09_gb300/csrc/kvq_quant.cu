@@ -1,0 +1,299 @@
+// kvq_quant.cu — quantize / pack / append and dequantize kernels (sm_103a).
+//
+// The quantizer is the affine scheme of the page "KV Cache Quantization — 8-bit and
+// 4-bit", § Integer quantization in one screen, applied per channel over groups of G
+// tokens for keys and per token over groups of Gv channels for values ("Sub-8-Bit KV
+// Cache Quantization Is Not a Free Lever for an RDNA4 Agent Swarm", § The cache is
+// two distributions, not one). Every floating-point step is one explicitly rounded
+// binary32 intrinsic (this file is also compiled with -fmad=false), so codes, scales
+// and zero points are reproducible bit for bit:
+//   s_h = binary16_round_up((x_max - x_min) / (q_max - q_min))
+//   zp  = clamp(q_min - rint(x_min / s_h), +-65504) -> binary16 (nearest even)
+//   u   = clamp(rint(x / s_h) + zp, q_min, q_max) - q_min
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "kvq_common.cuh"
+#include "kvq_kernels.h"
+
+namespace kvq {
+namespace {
+
+template <int BITS>
+struct Q {
+  static constexpr float qmin = -(float)(1 << (BITS - 1));
+  static constexpr float qmax = (float)((1 << (BITS - 1)) - 1);
+};
+
+// Group parameters from the (exact) binary32 min and max of binary16 inputs.
+template <int BITS>
+__device__ __forceinline__ void group_params(float xmin, float xmax, __half& s_h, __half& z_h, float& s, float& zp) {
+  if (xmax == xmin) {  // a constant group is widened to include 0
+    if (xmin > 0.0f) xmin = 0.0f;
+    if (xmax < 0.0f) xmax = 0.0f;
+  }
+  if (xmax == xmin) {
+    s_h = __float2half_rn(1.0f);  // all zeros: scale 1
+  } else {
+    const float range = __fsub_rn(xmax, xmin);
+    s_h = __float2half_ru(__fdiv_rn(range, __fsub_rn(Q<BITS>::qmax, Q<BITS>::qmin)));
+  }
+  s = __half2float(s_h);
+  float z = __fsub_rn(Q<BITS>::qmin, rintf(__fdiv_rn(xmin, s)));
+  z = fminf(fmaxf(z, -65504.0f), 65504.0f);
+  z_h = __float2half_rn(z);
+  zp = __half2float(z_h);
+}
+
+template <int BITS>
+__device__ __forceinline__ uint32_t quant_code(float x, float s, float zp) {
+  float q = __fadd_rn(rintf(__fdiv_rn(x, s)), zp);
+  q = fminf(fmaxf(q, Q<BITS>::qmin), Q<BITS>::qmax);
+  return (uint32_t)(int)__fsub_rn(q, Q<BITS>::qmin);
+}
+
+__device__ __forceinline__ void load4(const __half* p, float* x) {
+  const uint2 raw = *reinterpret_cast<const uint2*>(p);
+  const __half2 a = *reinterpret_cast<const __half2*>(&raw.x);
+  const __half2 b = *reinterpret_cast<const __half2*>(&raw.y);
+  x[0] = __low2float(a);
+  x[1] = __high2float(a);
+  x[2] = __low2float(b);
+  x[3] = __high2float(b);
+}
+
+// Store the 4 codes of channels [4*lane, 4*lane+4) into a key row (natural order).
+template <int BITS>
+__device__ __forceinline__ void store_k4(uint8_t* row, int lane, const uint32_t* u) {
+  if (BITS == 8) {
+    reinterpret_cast<uint32_t*>(row)[lane] = u[0] | (u[1] << 8) | (u[2] << 16) | (u[3] << 24);
+  } else if (BITS == 4) {
+    reinterpret_cast<uint16_t*>(row)[lane] = (uint16_t)(u[0] | (u[1] << 4) | (u[2] << 8) | (u[3] << 12));
+  } else {
+    row[lane] = (uint8_t)(u[0] | (u[1] << 2) | (u[2] << 4) | (u[3] << 6));
+  }
+}
+
+// Channel stored at value-row position p (inverse of pos(c) = 16*(c%8) + 2*(c/16) + (c/8)%2, d = 128).
+__device__ __forceinline__ int v_channel_of_pos(int p) {
+  const int g = p >> 4, i = p & 15;
+  return 16 * (i >> 1) + 8 * (i & 1) + g;
+}
+
+// ---------------------------------------------------------------------------
+// Keys: one CTA per (group, kv head, batch row); 8 warps, warp w holds tokens
+// w, w+8, ... of the group, lane l holds channels [4l, 4l+4). Token rows come from
+// the residual window (tokens < s_cur) or from the appended input.
+// ---------------------------------------------------------------------------
+template <int BITS, int G>
+__global__ void __launch_bounds__(256) k_group_kernel(AppendParams p) {
+  constexpr int PER_WARP = G / 8;
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t g = p.group0 + blockIdx.x;
+  const int64_t t0 = g * G;
+  const int64_t slice = (int64_t)b * p.H + h;
+
+  __shared__ float red_min[8][kHeadDim];
+  __shared__ float red_max[8][kHeadDim];
+  __shared__ float s_sc[kHeadDim];
+  __shared__ float s_zp[kHeadDim];
+
+  float x[PER_WARP][4];
+  float mn[4], mx[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    mn[e] = __int_as_float(0x7f800000);
+    mx[e] = -__int_as_float(0x7f800000);
+  }
+  const __half* resid = p.k_resid + slice * (int64_t)p.R_eff * kHeadDim;
+#pragma unroll
+  for (int k = 0; k < PER_WARP; ++k) {
+    const int64_t t = t0 + warp + 8 * k;
+    const __half* row = (t < p.s_cur) ? resid + (t % p.R_eff) * kHeadDim
+                                      : p.k_in + (((int64_t)b * p.n_new + (t - p.s_cur)) * p.H + h) * kHeadDim;
+    load4(row + 4 * lane, x[k]);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      mn[e] = fminf(mn[e], x[k][e]);
+      mx[e] = fmaxf(mx[e], x[k][e]);
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    red_min[warp][4 * lane + e] = mn[e];
+    red_max[warp][4 * lane + e] = mx[e];
+  }
+  __syncthreads();
+  if (threadIdx.x < kHeadDim) {
+    const int c = threadIdx.x;
+    float a = red_min[0][c], z = red_max[0][c];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) {
+      a = fminf(a, red_min[w][c]);
+      z = fmaxf(z, red_max[w][c]);
+    }
+    __half s_h, z_h;
+    float s, zp;
+    group_params<BITS>(a, z, s_h, z_h, s, zp);
+    s_sc[c] = s;
+    s_zp[c] = zp;
+    p.k_meta[(slice * (p.S_pad / G) + g) * kHeadDim + c] = __halves2half2(s_h, z_h);
+  }
+  __syncthreads();
+  float s[4], zp[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    s[e] = s_sc[4 * lane + e];
+    zp[e] = s_zp[4 * lane + e];
+  }
+  uint8_t* codes = p.k_codes + slice * p.k_codes_slice;
+#pragma unroll
+  for (int k = 0; k < PER_WARP; ++k) {
+    const int64_t t = t0 + warp + 8 * k;
+    uint32_t u[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) u[e] = quant_code<BITS>(x[k][e], s[e], zp[e]);
+    store_k4<BITS>(codes + t * p.rowK, lane, u);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Values (and the key residual copy): one warp per appended (batch row, token,
+// kv head) row, in the input's own order. Lane l holds channels [4l, 4l+4).
+// ---------------------------------------------------------------------------
+template <int BITS>
+__global__ void __launch_bounds__(256) v_token_kernel(AppendParams p, int64_t n_rows) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t w = (int64_t)blockIdx.x * 8 + warp;
+  __shared__ uint8_t codes_s[8][kHeadDim];
+  if (w >= n_rows) return;  // whole warps only: the warp-level code below stays converged
+  const int h = (int)(w % p.H);
+  const int64_t bt = w / p.H;
+  const int64_t t = p.s_cur + bt % p.n_new;
+  const int b = (int)(bt / p.n_new);
+  const int64_t slice = (int64_t)b * p.H + h;
+
+  float x[4];
+  load4(p.v_in + w * kHeadDim + 4 * lane, x);
+  float mn = fminf(fminf(x[0], x[1]), fminf(x[2], x[3]));
+  float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+  const int lanes_per_group = p.Gv / 4;  // 8, 16 or 32
+  for (int off = 1; off < lanes_per_group; off <<= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  }
+  __half s_h, z_h;
+  float s, zp;
+  group_params<BITS>(mn, mx, s_h, z_h, s, zp);
+  if (lane % lanes_per_group == 0) {
+    const int j = lane / lanes_per_group;
+    p.v_meta[(slice * p.S_pad + t) * p.n_vg + j] = __halves2half2(s_h, z_h);
+  }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) codes_s[warp][4 * lane + e] = (uint8_t)quant_code<BITS>(x[e], s, zp);
+  __syncwarp();
+  // Assemble 16-bit units of the token's row (positions in stored order) and write
+  // them into the token's half of its pair row.
+  constexpr int PER_UNIT = 16 / BITS;
+  constexpr int UNITS = kHeadDim * BITS / 16;
+  uint16_t* pair = reinterpret_cast<uint16_t*>(p.v_codes + slice * p.v_codes_slice + (t >> 1) * 2 * p.rowV);
+  for (int k = lane; k < UNITS; k += 32) {
+    uint32_t unit = 0;
+#pragma unroll
+    for (int i = 0; i < PER_UNIT; ++i) unit |= (uint32_t)codes_s[warp][v_channel_of_pos(k * PER_UNIT + i)] << (i * BITS);
+    pair[2 * k + (int)(t & 1)] = (uint16_t)unit;
+  }
+  // Keys of tokens past the last full residual window go to the residual.
+  if (t >= p.A1) {
+    const uint2 raw = *reinterpret_cast<const uint2*>(p.k_in + w * kHeadDim + 4 * lane);
+    __half* dst = p.k_resid + (slice * p.R_eff + t % p.R_eff) * kHeadDim;
+    *reinterpret_cast<uint2*>(dst + 4 * lane) = raw;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Dequantize the first T tokens: one warp per (batch row, kv head, token).
+// x_hat = s * (u + q_min - zp), one binary32 product.
+// ---------------------------------------------------------------------------
+template <int BITS>
+__global__ void __launch_bounds__(256) dequant_kernel(DequantParams p, int64_t n_rows) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t w = (int64_t)blockIdx.x * 8 + warp;
+  if (w >= n_rows) return;
+  const int64_t t = w % p.T;
+  const int64_t slice = w / p.T;  // b * H + h
+  const int c0 = 4 * lane;
+  float kx[4], vx[4];
+  if (t < p.Tq) {
+    const uint8_t* row = p.k_codes + slice * p.k_codes_slice + t * p.rowK;
+    const __half2* meta = p.k_meta + (slice * (p.S_pad / p.G) + t / p.G) * kHeadDim;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int c = c0 + e;
+      const uint32_t u = (row[(c * BITS) >> 3] >> ((c * BITS) & 7)) & ((1u << BITS) - 1u);
+      const __half2 m = meta[c];
+      kx[e] = __fmul_rn(__low2float(m), __fsub_rn((float)((int)u + (int)Q<BITS>::qmin), __high2float(m)));
+    }
+  } else {
+    load4(p.k_resid + (slice * p.R_eff + t % p.R_eff) * kHeadDim + c0, kx);
+  }
+  {
+    const uint16_t* pair = reinterpret_cast<const uint16_t*>(p.v_codes + slice * p.v_codes_slice + (t >> 1) * 2 * p.rowV);
+    const __half2* meta = p.v_meta + (slice * p.S_pad + t) * p.n_vg;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int c = c0 + e;
+      const int pos = 16 * (c & 7) + 2 * (c >> 4) + ((c >> 3) & 1);
+      const int bit = pos * BITS;
+      const uint32_t unit = pair[2 * (bit >> 4) + (int)(t & 1)];
+      const uint32_t u = (unit >> (bit & 15)) & ((1u << BITS) - 1u);
+      const __half2 m = meta[c / p.Gv];
+      vx[e] = __fmul_rn(__low2float(m), __fsub_rn((float)((int)u + (int)Q<BITS>::qmin), __high2float(m)));
+    }
+  }
+  *reinterpret_cast<float4*>(p.k_out + w * kHeadDim + c0) = make_float4(kx[0], kx[1], kx[2], kx[3]);
+  *reinterpret_cast<float4*>(p.v_out + w * kHeadDim + c0) = make_float4(vx[0], vx[1], vx[2], vx[3]);
+}
+
+template <int BITS>
+cudaError_t launch_append_bits(const AppendParams& p, cudaStream_t stream) {
+  if (p.n_groups > 0) {
+    dim3 grid((unsigned)p.n_groups, (unsigned)p.H, (unsigned)p.B);
+    switch (p.G) {
+      case 32: k_group_kernel<BITS, 32><<<grid, 256, 0, stream>>>(p); break;
+      case 64: k_group_kernel<BITS, 64><<<grid, 256, 0, stream>>>(p); break;
+      default: k_group_kernel<BITS, 128><<<grid, 256, 0, stream>>>(p); break;
+    }
+  }
+  const int64_t rows = (int64_t)p.B * p.n_new * p.H;
+  v_token_kernel<BITS><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(p, rows);
+  return cudaGetLastError();
+}
+
+template <int BITS>
+cudaError_t launch_dequant_bits(const DequantParams& p, cudaStream_t stream) {
+  const int64_t rows = (int64_t)p.B * p.H * p.T;
+  dequant_kernel<BITS><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(p, rows);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_append(const AppendParams& p, int bits, cudaStream_t stream) {
+  switch (bits) {
+    case 8: return launch_append_bits<8>(p, stream);
+    case 4: return launch_append_bits<4>(p, stream);
+    default: return launch_append_bits<2>(p, stream);
+  }
+}
+
+cudaError_t launch_dequant(const DequantParams& p, int bits, cudaStream_t stream) {
+  switch (bits) {
+    case 8: return launch_dequant_bits<8>(p, stream);
+    case 4: return launch_dequant_bits<4>(p, stream);
+    default: return launch_dequant_bits<2>(p, stream);
+  }
+}
+
+}  // namespace kvq

@@ -1,0 +1,174 @@
+/*
+ * kvq.h — C ABI of the quantized KV cache and its fused-dequant decode attention
+ * (libkvq.so, CUDA, sm_103a).
+ *
+ * What it computes
+ *   Asymmetric affine quantization of the attention KV cache, as in the page
+ *   "KV Cache Quantization — 8-bit and 4-bit", § Integer quantization in one screen:
+ *       scale      = (x_max - x_min) / (q_max - q_min)
+ *       zero_point = q_min - round(x_min / scale)
+ *       q          = round(x / scale) + zero_point          (clamped to [q_min, q_max])
+ *       x_hat      = scale * (q - zero_point)
+ *   with int8 [-128, 127], int4 [-8, 7] and int2 [-2, 1] codes. Keys are quantized
+ *   per channel over groups of k_group consecutive tokens, values per token over
+ *   groups of v_group consecutive channels (page "Sub-8-Bit KV Cache Quantization Is
+ *   Not a Free Lever for an RDNA4 Agent Swarm", § The cache is two distributions, not
+ *   one; and "KV Cache Quantization — 8-bit and 4-bit", § Granularity and § Why keys
+ *   and values want different treatment). The newest keys that do not yet fill the
+ *   residual window stay binary16 ("Sub-8-Bit …", § What the low-bit numbers actually
+ *   cost: a small full-precision residual for the most recent tokens). Decode
+ *   attention reads the packed integers and dequantizes them on the fly ("KV Cache
+ *   Quantization — 8-bit and 4-bit", § Decode is memory-bound, so smaller is also
+ *   faster), with softmax(scale * q . k_hat) . v_hat over every cached token.
+ *
+ * Arithmetic (bit-exact contract of the quantizer)
+ *   All of it in IEEE binary32, round to nearest even, no contraction:
+ *   range = x_max - x_min; s32 = range / (q_max - q_min); the stored scale is
+ *   binary16(s32) rounded toward +infinity; zp = q_min - rint(x_min / scale), clamped to
+ *   +-65504 and stored as binary16 (nearest even); q = clamp(rint(x / scale) + zp).
+ *   A group whose values are all equal is widened to include 0; an all-zero group
+ *   gets scale 1. Codes are stored as u = q - q_min (unsigned, b bits).
+ *
+ * State after T tokens of one (layer, batch row, kv head)
+ *   R_eff = residual_len, or k_group when residual_len == 0.
+ *   Keys of tokens [0, Tq), Tq = floor(T / R_eff) * R_eff, are quantized; keys of
+ *   tokens [Tq, T) are binary16 copies in residual slot (t mod R_eff). Values of all
+ *   T tokens are quantized. The state depends only on the token history, never on
+ *   how the tokens were split into append calls.
+ *
+ * Memory (all device memory, owned by the caller; this library allocates nothing)
+ *   S_pad = max_seq_len rounded up to a multiple of 128; LBH = n_layers*batch*n_kv_heads;
+ *   slices are ordered [layer][batch][kv head]. Per slice:
+ *     k_codes : S_pad rows of d*b/8 bytes. Channel c occupies bits [c*b, c*b+b) of its
+ *               row (little-endian bytes, low bits first).
+ *     k_meta  : (S_pad / k_group) groups x d channels x {scale, zero_point} binary16.
+ *     k_resid : R_eff rows of d binary16.
+ *     v_codes : S_pad/2 pair rows of 2*d*b/8 bytes. Channel c of a token sits at
+ *               position pos(c) = (d/8)*(c%8) + 2*(c/16) + (c/8)%2 of that token's
+ *               d*b/8-byte row; the rows of tokens 2p and 2p+1 are interleaved in
+ *               16-bit units (32-bit word k of pair row p = unit k of token 2p in the
+ *               low half, unit k of token 2p+1 in the high half).
+ *     v_meta  : S_pad tokens x (d / v_group) groups x {scale, zero_point} binary16.
+ *   Every buffer must be 256-byte aligned (torch and cudaMalloc allocations are) and
+ *   zero-filled before the first append.
+ *
+ * Calls
+ *   Every call checks its arguments on the host first and launches nothing when they
+ *   are wrong. Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is
+ *   the legacy default stream); nothing synchronizes. Functions keep no state and are
+ *   reentrant; calls that touch the same buffers must be ordered by the caller.
+ *   A launch failure is reported as KVQ_ERR_CUDA (cudaGetLastError after the launch).
+ */
+#ifndef KVQ_H_
+#define KVQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KVQ_OK = 0,
+  KVQ_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad layer, s_cur/n_new out of order */
+  KVQ_ERR_UNSUPPORTED = 2, /* a configuration this build does not implement */
+  KVQ_ERR_CAPACITY = 3,    /* s_cur + n_new > max_seq_len */
+  KVQ_ERR_WORKSPACE = 4,   /* decode workspace missing or too small */
+  KVQ_ERR_CUDA = 5         /* a CUDA launch reported an error */
+} kvq_status;
+
+/* Cache shape and quantizer settings; the names follow the pages' problem
+ * statement ("KV Cache Quantization — 8-bit and 4-bit", § The bytes-per-token
+ * formula: L, n_kv, d_head, S). Supported: d_head == 128; bits in {2, 4, 8};
+ * k_group and v_group in {32, 64, 128}; residual_len == 0 or a multiple of k_group
+ * up to 1024; 1 <= gqa_ratio <= 8; n_kv_heads <= 255; batch <= 4095;
+ * 1 <= max_seq_len <= 2^24. */
+typedef struct {
+  int32_t n_layers;     /* L */
+  int32_t batch;        /* B: sequences; all share one length */
+  int32_t n_kv_heads;   /* n_kv */
+  int32_t gqa_ratio;    /* r: query heads per kv head; query head i reads kv head i / r */
+  int32_t d_head;       /* d */
+  int32_t max_seq_len;  /* capacity in tokens */
+  int32_t bits;         /* b: code width for keys and values */
+  int32_t k_group;      /* G: tokens per key group (keys are quantized per channel) */
+  int32_t v_group;      /* Gv: channels per value group (values are quantized per token) */
+  int32_t residual_len; /* R: binary16 key residual capacity; 0 means k_group */
+} kvq_config;
+
+/* Device pointers to the five cache buffers of all layers (layout above). */
+typedef struct {
+  void* k_codes;
+  void* k_meta;
+  void* k_resid;
+  void* v_codes;
+  void* v_meta;
+} kvq_buffers;
+
+enum { KVQ_BUF_K_CODES = 0, KVQ_BUF_K_META = 1, KVQ_BUF_K_RESID = 2, KVQ_BUF_V_CODES = 3, KVQ_BUF_V_META = 4,
+       KVQ_NUM_BUFFERS = 5 };
+
+/* Sizes in bytes of the five buffers for `cfg` (layout above), so that the caller can
+ * allocate them. Returns KVQ_ERR_INVALID_ARG / KVQ_ERR_UNSUPPORTED for a bad config. */
+kvq_status kvq_buffer_sizes(const kvq_config* cfg, size_t bytes[KVQ_NUM_BUFFERS]);
+
+/* Append n_new >= 1 tokens of one layer after the s_cur tokens already cached
+ * (s_cur + n_new <= max_seq_len). k_f16 and v_f16 are device binary16 arrays
+ * [batch][n_new][n_kv_heads][d_head] (16-byte aligned). Values are quantized per token;
+ * keys go to the residual window and every residual window that fills is quantized
+ * per channel (its R_eff / k_group groups at once). A prefill is s_cur = 0,
+ * n_new = prompt length; a decode step is n_new = 1. */
+kvq_status kvq_quantize_append(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur,
+                               int64_t n_new, const void* k_f16, const void* v_f16, void* stream);
+
+/* Dequantize the first s_cur tokens of one layer into binary32 arrays
+ * k_out, v_out [batch][n_kv_heads][s_cur][d_head] (device, 16-byte aligned):
+ * x_hat = scale * (q - zero_point) as one binary32 product; residual keys are copied.
+ * For tests and inspection: the decode path never materializes these. */
+kvq_status kvq_dequantize(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur,
+                          float* k_out, float* v_out, void* stream);
+
+/* Bytes of device workspace kvq_decode_attention needs for s_cur cached tokens
+ * (0 for a bad config). The workspace holds split-K partials and per-(batch, kv head)
+ * counters; zero-fill it once before its first use: every call leaves the counters
+ * at zero again. */
+size_t kvq_decode_workspace_size(const kvq_config* cfg, int64_t s_cur);
+
+/* Decode attention of one layer over its s_cur >= 1 cached tokens (the token just
+ * appended included). q_f16 [batch][n_kv_heads*gqa_ratio][d_head] binary16, out the
+ * same shape in binary32 (device, 16-byte aligned):
+ *   out[b][i] = sum_t softmax_t(softmax_scale * q[b][i] . k_hat[t]) * v_hat[t]
+ * with k_hat / v_hat of kv head i / gqa_ratio, dequantized on the fly. ws/ws_bytes:
+ * workspace of at least kvq_decode_workspace_size(cfg, s_cur) bytes. */
+kvq_status kvq_decode_attention(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur,
+                                const void* q_f16, float softmax_scale, float* out, void* ws, size_t ws_bytes,
+                                void* stream);
+
+/* Kernel choice for kvq_decode_attention_impl. AUTO is what kvq_decode_attention uses. */
+typedef enum {
+  KVQ_DECODE_AUTO = 0,
+  KVQ_DECODE_SIMT = 1, /* binary32 CUDA-core dot products */
+  KVQ_DECODE_MMA = 2   /* tensor-core m16n8k16 products over exact integer codes */
+} kvq_decode_impl;
+
+/* kvq_decode_attention with an explicit kernel choice (for comparison runs). */
+kvq_status kvq_decode_attention_impl(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur,
+                                     const void* q_f16, float softmax_scale, float* out, void* ws,
+                                     size_t ws_bytes, void* stream, kvq_decode_impl impl);
+
+/* Number of split-K partitions kvq_decode_attention uses for s_cur tokens (>= 1),
+ * or 0 for a bad config. */
+int32_t kvq_decode_num_splits(const kvq_config* cfg, int64_t s_cur);
+
+/* Human-readable name of a status code (static string). */
+const char* kvq_status_string(kvq_status status);
+
+/* Library version, e.g. "kvq 0.1.0 sm_103a". */
+const char* kvq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H_ */

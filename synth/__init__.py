@@ -99,20 +99,19 @@ def _to_f16(x32: np.ndarray) -> np.ndarray:
     return x32.astype(np.float32).astype(np.float16)
 
 
-def gen_k(seed, layer, batches, tokens, n_kv, d, n_out, a, shift=5.0) -> np.ndarray:
-    """Keys [len(batches)][len(tokens)][n_kv][d] binary16."""
+def gen_k(seed, layer, batches, tokens, n_kv, d, n_out, a, shift=5.0, heads=None) -> np.ndarray:
+    """Keys [len(batches)][len(tokens)][len(heads)][d] binary16 (heads default: all n_kv)."""
+    heads = np.arange(n_kv, dtype=np.int64) if heads is None else np.asarray(heads, np.int64)
     b = np.asarray(batches, np.int64)[:, None, None, None]
     t = np.asarray(tokens, np.int64)[None, :, None, None]
-    h = np.arange(n_kv, dtype=np.int64)[None, None, :, None]
+    h = heads[None, None, :, None]
     c = np.arange(d, dtype=np.int64)[None, None, None, :]
     m = normal_m(seed, counter(STREAM_K, layer, h, c, b, t))
-    z = (m.astype(np.float32) * np.float32(2.0**-16))  # exact
-    out = np.broadcast_to(np.array(0, np.float32), m.shape).copy()
-    out[...] = z
+    out = m.astype(np.float32) * np.float32(2.0**-16)  # exact
     if n_out > 0:
-        mask = np.zeros((n_kv, d), bool)
-        for hh in range(n_kv):
-            mask[hh, outlier_channels(seed, layer, hh, n_out, d)] = True
+        mask = np.zeros((len(heads), d), bool)
+        for j, hh in enumerate(heads):
+            mask[j, outlier_channels(seed, layer, int(hh), n_out, d)] = True
         mask = np.broadcast_to(mask[None, None], m.shape)
         ai = int(a)
         assert ai == a, "outlier gain must be an integer"
@@ -121,11 +120,12 @@ def gen_k(seed, layer, batches, tokens, n_kv, d, n_out, a, shift=5.0) -> np.ndar
     return _to_f16(out)
 
 
-def gen_v(seed, layer, batches, tokens, n_kv, d) -> np.ndarray:
-    """Values [len(batches)][len(tokens)][n_kv][d] binary16, sigma 0.5."""
+def gen_v(seed, layer, batches, tokens, n_kv, d, heads=None) -> np.ndarray:
+    """Values [len(batches)][len(tokens)][len(heads)][d] binary16, sigma 0.5."""
+    heads = np.arange(n_kv, dtype=np.int64) if heads is None else np.asarray(heads, np.int64)
     b = np.asarray(batches, np.int64)[:, None, None, None]
     t = np.asarray(tokens, np.int64)[None, :, None, None]
-    h = np.arange(n_kv, dtype=np.int64)[None, None, :, None]
+    h = heads[None, None, :, None]
     c = np.arange(d, dtype=np.int64)[None, None, None, :]
     m = normal_m(seed, counter(STREAM_V, layer, h, c, b, t))
     return _to_f16(m.astype(np.float32) * np.float32(2.0**-17))
@@ -203,13 +203,13 @@ WORKLOADS: dict[str, Workload] = {
 
 def k_slice(w: Workload, layer: int, b: int, h: int, tokens) -> np.ndarray:
     """Keys of one (batch row, kv head) over ``tokens``: [len(tokens)][d] binary16."""
-    full = gen_k(w.seed, layer, [b], tokens, w.n_kv, w.d_head, w.n_out, w.gain, w.shift)
-    return np.ascontiguousarray(full[0, :, h, :])
+    full = gen_k(w.seed, layer, [b], tokens, w.n_kv, w.d_head, w.n_out, w.gain, w.shift, heads=[h])
+    return np.ascontiguousarray(full[0, :, 0, :])
 
 
 def v_slice(w: Workload, layer: int, b: int, h: int, tokens) -> np.ndarray:
-    full = gen_v(w.seed, layer, [b], tokens, w.n_kv, w.d_head)
-    return np.ascontiguousarray(full[0, :, h, :])
+    full = gen_v(w.seed, layer, [b], tokens, w.n_kv, w.d_head, heads=[h])
+    return np.ascontiguousarray(full[0, :, 0, :])
 
 
 def q_rows(w: Workload, layer: int, b: int, h: int, step_token: int) -> np.ndarray:

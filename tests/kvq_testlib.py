@@ -1,0 +1,94 @@
+"""Shared helpers of the parity tests: slices of the GPU cache buffers, oracle
+states of the same slices, and element-by-element comparisons.
+
+Inputs come from the seeded generator (host numpy side for the oracle, device
+side or host copies for the CUDA side); expected values come from ``oracle`` only.
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+import oracle
+import synth
+
+ATOL = 2e-3  # decode attention: max-abs error against the oracle's attention over x_hat
+
+
+def cfg_dims(cache):
+    c = cache.cfg
+    R_eff = c.residual_len if c.residual_len > 0 else c.k_group
+    S_pad = (c.max_seq_len + 127) // 128 * 128
+    row = c.d_head * c.bits // 8
+    return dict(L=c.n_layers, B=c.batch, H=c.n_kv_heads, r=c.gqa_ratio, d=c.d_head, bits=c.bits, G=c.k_group,
+                Gv=c.v_group, R=c.residual_len, R_eff=R_eff, S_pad=S_pad, row=row, n_vg=c.d_head // c.v_group)
+
+
+def gpu_slice_state(cache, layer: int, b: int, h: int, T: int):
+    """The five buffers of one (layer, b, h) slice, cut to the valid part for T tokens (numpy)."""
+    import torch  # noqa: F401
+
+    g = cfg_dims(cache)
+    sl = (layer * g["B"] + b) * g["H"] + h
+    Tq = (T // g["R_eff"]) * g["R_eff"]
+
+    def part(name, slice_bytes, nbytes):
+        buf = cache.buffer(name)
+        return buf[sl * slice_bytes: sl * slice_bytes + nbytes].cpu().numpy()
+
+    kc = part("k_codes", g["S_pad"] * g["row"], Tq * g["row"]).reshape(Tq, g["row"])
+    km = part("k_meta", (g["S_pad"] // g["G"]) * g["d"] * 4, (Tq // g["G"]) * g["d"] * 4).view(np.uint16)
+    km = km.reshape(Tq // g["G"], g["d"], 2)
+    kr = part("k_resid", g["R_eff"] * g["d"] * 2, (T - Tq) * g["d"] * 2).view(np.uint16).reshape(T - Tq, g["d"])
+    npairs = (T + 1) // 2
+    vc = part("v_codes", g["S_pad"] * g["row"], npairs * 2 * g["row"]).reshape(npairs, 2 * g["row"])
+    vm = part("v_meta", g["S_pad"] * g["n_vg"] * 4, T * g["n_vg"] * 4).view(np.uint16).reshape(T, g["n_vg"], 2)
+    return dict(k_codes=kc, k_meta=km, k_resid=kr, v_codes=vc, v_meta=vm, Tq=Tq)
+
+
+def oracle_slice_state(k_hist, v_hist, cache):
+    g = cfg_dims(cache)
+    return oracle.cache_state(k_hist, v_hist, d=g["d"], bits=g["bits"], G=g["G"], Gv=g["Gv"], R=g["R"])
+
+
+def assert_slice_equal(gpu: dict, st: oracle.OracleState, where: str = ""):
+    T = st.T
+    assert gpu["Tq"] == st.Tq
+    for name in ("k_codes", "k_meta", "v_codes", "v_meta"):
+        a, e = gpu[name], getattr(st, name)
+        assert a.shape == e.shape, (where, name, a.shape, e.shape)
+        if not np.array_equal(a, e):
+            bad = np.argwhere(a != e)
+            raise AssertionError(f"{where} {name}: {len(bad)} mismatches, first at {bad[:3].tolist()}")
+    n_res = T - st.Tq
+    R_eff = st.k_resid.shape[0]
+    # residual slot (t mod R_eff) of tokens [Tq, T); with Tq a multiple of R_eff that is t - Tq
+    exp_res = st.k_resid[:n_res] if n_res <= R_eff else None
+    assert exp_res is not None
+    if not np.array_equal(gpu["k_resid"], exp_res):
+        raise AssertionError(f"{where} k_resid mismatch")
+
+
+def oracle_attention(st: oracle.OracleState, q_rows, cache, softmax_scale):
+    g = cfg_dims(cache)
+    kh, vh = oracle.dequantize_state(st, d=g["d"], bits=g["bits"], G=g["G"], Gv=g["Gv"], R=g["R"])
+    return oracle.attention(q_rows, kh, vh, softmax_scale)
+
+
+def small_workload(name="small", *, L=1, H=2, r=4, B=2, S=600, steps=8, bits=4, G=32, Gv=64, R=128, n_out=2,
+                   gain=20, seed=777):
+    return synth.Workload(name, L, H, r, 128, B, S, steps, bits, G, Gv, R, n_out, gain, seed)
+
+
+def host_layer_inputs(w, layer, t0, nt):
+    """Keys and values [B][nt][H][d] of tokens [t0, t0+nt) from the host generator."""
+    toks = np.arange(t0, t0 + nt)
+    k = synth.gen_k(w.seed, layer, range(w.batch), toks, w.n_kv, w.d_head, w.n_out, w.gain, w.shift)
+    v = synth.gen_v(w.seed, layer, range(w.batch), toks, w.n_kv, w.d_head)
+    return k, v
+
+
+def softmax_scale(w):
+    return 1.0 / math.sqrt(w.d_head)

@@ -1,0 +1,114 @@
+"""The C-ABI library without a GPU: it loads, exports every declared entry point,
+and rejects bad arguments on the host before any launch."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+from bit_kv_cache_09_gb300 import build as kvq_build
+from bit_kv_cache_09_gb300 import kvq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kvq_build.build()
+    return kvq.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvq_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in kvq.EXPORTED
+    assert kvq.kvq_version().startswith("kvq ")
+
+
+def good_cfg(**kw):
+    base = dict(n_layers=2, batch=3, n_kv_heads=2, gqa_ratio=4, d_head=128, max_seq_len=1000, bits=4, k_group=32,
+                v_group=64, residual_len=128)
+    base.update(kw)
+    return kvq.make_config(**base)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(bits=3), 2), (dict(bits=16), 2), (dict(d_head=64), 2), (dict(k_group=48), 2), (dict(v_group=16), 2),
+    (dict(residual_len=100), 1), (dict(residual_len=2048), 2), (dict(gqa_ratio=9), 2), (dict(batch=0), 1),
+    (dict(max_seq_len=0), 1), (dict(n_kv_heads=256), 2),
+])
+def test_bad_configs_are_rejected(lib, kw, status):
+    sizes = (ctypes.c_size_t * 5)()
+    assert lib.kvq_buffer_sizes(ctypes.byref(good_cfg(**kw)), sizes) == status
+    assert kvq.kvq_decode_workspace_size(good_cfg(**kw), 10) == 0
+
+
+def test_buffer_sizes_follow_the_bytes_formula(lib):
+    """Code bytes are the pages' 2*L*n_kv*d*S*bits/8 (batch rows count as extra
+    sequences); metadata adds one (scale, zero) binary16 pair per group."""
+    for bits, G, Gv, R in [(8, 32, 128, 0), (4, 128, 64, 128), (2, 32, 32, 128)]:
+        L, B, H, S = 3, 2, 4, 1024
+        cfg = good_cfg(n_layers=L, batch=B, n_kv_heads=H, max_seq_len=S, bits=bits, k_group=G, v_group=Gv,
+                       residual_len=R)
+        kc, km, kr, vc, vm = kvq.kvq_buffer_sizes(cfg)
+        assert kc + vc == oracle.kv_bytes(L, H * B, 128, S, bits)
+        assert km == oracle.kv_bytes(L, H * B, 128, S, 0, 4, G) / 2
+        assert vm == oracle.kv_bytes(L, H * B, 128, S, 0, 4, Gv) / 2
+        R_eff = R or G
+        assert kr == L * B * H * R_eff * 128 * 2
+
+
+def _bufs(ptr=4096):
+    return kvq.make_buffers([ptr, ptr + 4096, ptr + 8192, ptr + 12288, ptr + 16384])
+
+
+def test_append_argument_checks(lib):
+    cfg = good_cfg()
+    B = ctypes.byref
+    bufs = _bufs()
+    # wrong layer, negative s_cur, empty append, capacity, null/misaligned inputs: nothing launches
+    assert lib.kvq_quantize_append(B(cfg), B(bufs), 2, 0, 1, 4096, 4096, None) == 1
+    assert lib.kvq_quantize_append(B(cfg), B(bufs), 0, -1, 1, 4096, 4096, None) == 1
+    assert lib.kvq_quantize_append(B(cfg), B(bufs), 0, 0, 0, 4096, 4096, None) == 1
+    assert lib.kvq_quantize_append(B(cfg), B(bufs), 0, 999, 2, 4096, 4096, None) == 3
+    assert lib.kvq_quantize_append(B(cfg), B(bufs), 0, 0, 1, None, 4096, None) == 1
+    assert lib.kvq_quantize_append(B(cfg), B(bufs), 0, 0, 1, 4098, 4096, None) == 1
+    assert lib.kvq_quantize_append(B(cfg), B(_bufs(4100)), 0, 0, 1, 4096, 4096, None) == 1
+    assert lib.kvq_quantize_append(B(cfg), None, 0, 0, 1, 4096, 4096, None) == 1
+    assert lib.kvq_quantize_append(None, B(bufs), 0, 0, 1, 4096, 4096, None) == 1
+
+
+def test_decode_argument_checks(lib):
+    cfg = good_cfg()
+    B = ctypes.byref
+    bufs = _bufs()
+    need = kvq.kvq_decode_workspace_size(cfg, 500)
+    assert need > 0
+    args = lambda layer, s, q, out, ws, wsb, scale=0.088: (B(cfg), B(bufs), layer, s, q, ctypes.c_float(scale), out,  # noqa: E731
+                                                           ws, wsb, None)
+    assert lib.kvq_decode_attention(*args(0, 0, 4096, 4096, 4096, need)) == 1  # no tokens
+    assert lib.kvq_decode_attention(*args(0, 1001, 4096, 4096, 4096, need)) == 3
+    assert lib.kvq_decode_attention(*args(0, 500, 4096, 4096, 4096, need - 1)) == 4
+    assert lib.kvq_decode_attention(*args(0, 500, 4096, 4096, None, need)) == 4
+    assert lib.kvq_decode_attention(*args(0, 500, 4100, 4096, 4096, need)) == 1
+    assert lib.kvq_decode_attention(*args(0, 500, 4096, 4096, 4096, need, float("nan"))) == 1
+    assert lib.kvq_decode_attention(*args(5, 500, 4096, 4096, 4096, need)) == 1
+    assert lib.kvq_dequantize(B(cfg), B(bufs), 0, 0, 4096, 4096, None) == 1
+    assert lib.kvq_dequantize(B(cfg), B(bufs), 0, 1001, 4096, 4096, None) == 3
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert kvq.kvq_status_string(s)
+    with pytest.raises(kvq.KVQError):
+        kvq.kvq_buffer_sizes(good_cfg(bits=5))

@@ -1,0 +1,163 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Codes, scales, zero points and the residual window must match bit for bit;
+dequantized values bit for bit; decode attention within 2e-3 max-abs.
+"""
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+import synth  # noqa: E402
+from kvq_testlib import (ATOL, assert_slice_equal, gpu_slice_state, host_layer_inputs,  # noqa: E402
+                         oracle_attention, oracle_slice_state, small_workload, softmax_scale)
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+from bit_kv_cache_09_gb300 import kvq  # noqa: E402
+from bit_kv_cache_09_gb300.cache import QuantizedKVCache  # noqa: E402
+
+IMPLS = [kvq.DECODE_SIMT]
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _history(w, layer, b, h, T):
+    return synth.k_slice(w, layer, b, h, range(T)), synth.v_slice(w, layer, b, h, range(T))
+
+
+def _check_all_slices(cache, w, layer, T, k_host, v_host):
+    """Bit-exact state of every (b, h) slice after T tokens; k_host/v_host [B][T][H][d]."""
+    for b in range(w.batch):
+        for h in range(w.n_kv):
+            st = oracle_slice_state(k_host[b, :T, h], v_host[b, :T, h], cache)
+            assert_slice_equal(gpu_slice_state(cache, layer, b, h, T), st, f"b={b} h={h} T={T}")
+
+
+def _check_attention(cache, w, layer, T, k_host, v_host, q_host, impl):
+    q = _dev(q_host)
+    out = cache.attention(layer, T, q, softmax_scale(w), impl=impl).cpu().numpy()
+    worst = 0.0
+    for b in range(w.batch):
+        for h in range(w.n_kv):
+            st = oracle_slice_state(k_host[b, :T, h], v_host[b, :T, h], cache)
+            ref = oracle_attention(st, q_host[b, h * w.gqa:(h + 1) * w.gqa], cache, softmax_scale(w))
+            got = out[b, h * w.gqa:(h + 1) * w.gqa]
+            worst = max(worst, float(np.abs(got - ref).max()))
+    assert worst <= ATOL, worst
+    return worst
+
+
+def test_device_generator_matches_host():
+    from synth.device import DeviceGenerator
+
+    for name in ("tiny-int8", "kivi-int2", "long-int4-16k"):
+        w = synth.WORKLOADS[name]
+        gen = DeviceGenerator(w)
+        k, v = gen.kv(layer=3 % w.n_layers, t0=1000, nt=40, b0=0, nb=2)
+        kh = synth.gen_k(w.seed, 3 % w.n_layers, [0, 1], range(1000, 1040), w.n_kv, w.d_head, w.n_out, w.gain)
+        vh = synth.gen_v(w.seed, 3 % w.n_layers, [0, 1], range(1000, 1040), w.n_kv, w.d_head)
+        assert np.array_equal(k.cpu().numpy().view(np.uint16), kh.view(np.uint16))
+        assert np.array_equal(v.cpu().numpy().view(np.uint16), vh.view(np.uint16))
+        q = gen.q(layer=0, step_token=w.seq + 5, b0=1, nb=1)
+        qh = synth.gen_q(w.seed, 0, [1], w.seq + 5, w.n_q, w.d_head)
+        assert np.array_equal(q.cpu().numpy().view(np.uint16), qh.view(np.uint16))
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_tiny_workload_full_parity(impl):
+    """One layer, one kv head, GQA 4, int8, K groups of 32, no residual; prefill of 256
+    tokens and one decode step: every byte of the cache, every dequantized value and
+    every attention output."""
+    w = synth.WORKLOADS["tiny-int8"]
+    cache = QuantizedKVCache.for_workload(w)
+    k_host, v_host = host_layer_inputs(w, 0, 0, w.seq + w.steps)
+    cache.append(0, 0, _dev(k_host[:, :w.seq]), _dev(v_host[:, :w.seq]))
+    _check_all_slices(cache, w, 0, w.seq, k_host, v_host)
+    q0 = synth.gen_q(w.seed, 0, range(w.batch), w.seq - 1, w.n_q, w.d_head)
+    _check_attention(cache, w, 0, w.seq, k_host, v_host, q0, impl)
+    for s in range(w.steps):
+        T = w.seq + s
+        cache.append(0, T, _dev(k_host[:, T:T + 1]), _dev(v_host[:, T:T + 1]))
+        _check_all_slices(cache, w, 0, T + 1, k_host, v_host)
+        q = synth.gen_q(w.seed, 0, range(w.batch), T, w.n_q, w.d_head)
+        _check_attention(cache, w, 0, T + 1, k_host, v_host, q, impl)
+    # dequantize: bit-exact against the oracle's binary32 x_hat
+    T = w.seq + w.steps
+    kd, vd = cache.dequantize(0, T)
+    st = oracle_slice_state(k_host[0, :T, 0], v_host[0, :T, 0], cache)
+    kh, vh = oracle.dequantize_state(st, d=128, bits=w.bits, G=w.k_group, Gv=w.v_group, R=w.residual)
+    assert np.array_equal(kd[0, 0].cpu().numpy().view(np.uint32), kh.view(np.uint32))
+    assert np.array_equal(vd[0, 0].cpu().numpy().view(np.uint32), vh.view(np.uint32))
+
+
+CONFIGS = [
+    # bits, G, Gv, R, r
+    (8, 32, 128, 0, 4),
+    (8, 128, 128, 0, 4),
+    (4, 128, 64, 128, 4),
+    (2, 32, 32, 128, 4),
+    (4, 128, 128, 128, 8),
+    (4, 64, 32, 256, 3),
+    (2, 128, 64, 0, 1),
+]
+
+
+@pytest.mark.parametrize("bits,G,Gv,R,r", CONFIGS)
+@pytest.mark.parametrize("impl", IMPLS)
+def test_ragged_prefill_decode_and_flush(bits, G, Gv, R, r, impl):
+    """Prefill of a ragged length, then decode steps that cross a residual flush."""
+    R_eff = R if R > 0 else G
+    off = min(37, R_eff - 5)
+    S = 3 * R_eff + off  # ragged: several tiles plus a partial residual
+    steps = R_eff - off + 3  # crosses the next flush
+    w = small_workload(bits=bits, G=G, Gv=Gv, R=R, r=r, B=2, H=2, S=S, steps=steps, seed=1000 + bits * 10 + r)
+    cache = QuantizedKVCache.for_workload(w)
+    k_host, v_host = host_layer_inputs(w, 0, 0, w.max_seq)
+    cache.append(0, 0, _dev(k_host[:, :S]), _dev(v_host[:, :S]))
+    _check_all_slices(cache, w, 0, S, k_host, v_host)
+    for s in range(steps):
+        T = S + s
+        cache.append(0, T, _dev(k_host[:, T:T + 1]), _dev(v_host[:, T:T + 1]))
+        if s in (0, steps - 4, steps - 3, steps - 1):
+            _check_all_slices(cache, w, 0, T + 1, k_host, v_host)
+            q = synth.gen_q(w.seed, 0, range(w.batch), T, w.n_q, w.d_head)
+            _check_attention(cache, w, 0, T + 1, k_host, v_host, q, impl)
+
+
+def test_chunked_appends_equal_one_shot():
+    """The cache state depends only on the token history, not on how it was appended."""
+    w = small_workload(bits=4, G=32, Gv=64, R=128, B=2, H=3, S=650, steps=0, seed=4242)
+    k_host, v_host = host_layer_inputs(w, 0, 0, w.seq)
+    rng = np.random.default_rng(0)
+    cache = QuantizedKVCache.for_workload(w)
+    T = 0
+    while T < w.seq:
+        n = int(min(w.seq - T, rng.integers(1, 150)))
+        cache.append(0, T, _dev(k_host[:, T:T + n]), _dev(v_host[:, T:T + n]))
+        T += n
+        if rng.random() < 0.3:
+            _check_all_slices(cache, w, 0, T, k_host, v_host)
+    _check_all_slices(cache, w, 0, T, k_host, v_host)
+
+
+def test_layers_are_independent():
+    w = small_workload(L=3, bits=2, G=32, Gv=32, R=128, B=1, H=2, S=300, steps=0, seed=99)
+    cache = QuantizedKVCache.for_workload(w)
+    ins = {}
+    for layer in (2, 0):
+        k_host, v_host = host_layer_inputs(w, layer, 0, w.seq)
+        ins[layer] = (k_host, v_host)
+        cache.append(layer, 0, _dev(k_host), _dev(v_host))
+    for layer in (0, 2):
+        _check_all_slices(cache, w, layer, w.seq, *ins[layer])
+    g = cache.buffer("k_codes")
+    n = g.numel() // 3
+    assert not g[n:2 * n].any()  # layer 1 untouched
