@@ -237,8 +237,8 @@ kvq_status kvq_decode_attention_impl(const kvq_config* cfg, const kvq_buffers* b
   plan_splits(g, s_cur, kSimtCtasPerSm, &n_split, &chunk);
   p.n_split = (int)n_split;
   p.chunk = chunk;
-  if (impl == KVQ_DECODE_MMA) return KVQ_ERR_UNSUPPORTED;
-  cudaError_t e = kvq::launch_decode_simt(p, g.bits, static_cast<cudaStream_t>(stream));
+  cudaError_t e = (impl == KVQ_DECODE_SIMT) ? kvq::launch_decode_simt(p, g.bits, static_cast<cudaStream_t>(stream))
+                                            : kvq::launch_decode_mma(p, g.bits, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 

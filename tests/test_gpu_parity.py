@@ -22,7 +22,7 @@ if not torch.cuda.is_available():
 from bit_kv_cache_09_gb300 import kvq  # noqa: E402
 from bit_kv_cache_09_gb300.cache import QuantizedKVCache  # noqa: E402
 
-IMPLS = [kvq.DECODE_SIMT]
+IMPLS = [kvq.DECODE_SIMT, kvq.DECODE_MMA]
 
 
 def _dev(a):
