@@ -3,6 +3,7 @@
 // before any launch, and a failed check launches nothing.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "kvq_common.cuh"
@@ -49,25 +50,55 @@ int device_sm_count() {
   return n;
 }
 
-// Split-K plan: enough CTAs to cover the SMs several times, at least one 128-token
-// tile per split, never more than the device-independent workspace bound.
-void plan_splits(const Geometry& g, int64_t T, int ctas_per_sm, int64_t* n_split, int64_t* chunk) {
+// Resident CTAs per SM of the decode kernel that `impl` selects (cached per device).
+int decode_occupancy(const Geometry& g, kvq_decode_impl impl) {
+  static std::atomic<int> cache[16][2][3][2][3];  // device, impl, bits, r class, value groups
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) dev = 0;
+  const int ii = impl == KVQ_DECODE_SIMT ? 0 : 1;
+  const int bi = g.bits == 8 ? 0 : (g.bits == 4 ? 1 : 2);
+  const int ri = g.r <= 4 ? 0 : 1;
+  const int vi = g.n_vg == 1 ? 0 : (g.n_vg == 2 ? 1 : 2);
+  std::atomic<int>& slot = cache[dev][ii][bi][ri][vi];
+  int n = slot.load(std::memory_order_relaxed);
+  if (n <= 0) {
+    n = ii == 0 ? kvq::occupancy_decode_simt(g.bits) : kvq::occupancy_decode_mma(g.bits, g.r, g.n_vg);
+    if (n > 0) slot.store(n, std::memory_order_relaxed);
+  }
+  return n > 0 ? n : 1;
+}
+
+// Split-K plan: the number of splits per (batch row, kv head) is chosen so that the
+// grid fills whole waves of resident CTAs (>= 92% of the slots busy when possible),
+// every split has at least 64 tokens, and the workspace bound holds. Chunks are a
+// multiple of `align` tokens.
+void plan_splits(const Geometry& g, int64_t T, kvq_decode_impl impl, int64_t* n_split, int64_t* chunk) {
   int sms = device_sm_count();
   if (sms <= 0) sms = 152;
+  const int64_t slots = (int64_t)sms * decode_occupancy(g, impl);
+  const int64_t align = impl == KVQ_DECODE_SIMT ? 128 : 32;
   const int64_t units = (int64_t)g.B * g.H;
-  const int64_t tiles = (T + 127) / 128;
-  int64_t s = ((int64_t)sms * ctas_per_sm + units - 1) / units;
-  if (s > tiles) s = tiles;
-  const int64_t cap = kvq::max_splits(g, T);
-  if (s > cap) s = cap;
-  if (s < 1) s = 1;
-  int64_t c = (T + s - 1) / s;
-  c = (c + 127) / 128 * 128;
+  int64_t max_k = kvq::max_splits(g, T);
+  const int64_t by_len = (T + 63) / 64;
+  if (max_k > by_len) max_k = by_len;
+  if (max_k < 1) max_k = 1;
+  int64_t best_k = 1;
+  double best_eff = 0.0;
+  for (int64_t k = 1; k <= max_k; ++k) {
+    const int64_t ctas = units * k;
+    const int64_t waves = (ctas + slots - 1) / slots;
+    const double eff = (double)ctas / (double)(waves * slots);
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best_k = k;
+    }
+    if (eff >= 0.92) break;
+  }
+  int64_t c = (T + best_k - 1) / best_k;
+  c = (c + align - 1) / align * align;
   *chunk = c;
   *n_split = (T + c - 1) / c;
 }
-
-constexpr int kSimtCtasPerSm = 4;
 
 }  // namespace
 
@@ -186,7 +217,7 @@ int32_t kvq_decode_num_splits(const kvq_config* cfg, int64_t s_cur) {
   Geometry g;
   if (kvq::make_geometry(cfg, &g) != KVQ_OK || s_cur < 1) return 0;
   int64_t n, c;
-  plan_splits(g, s_cur, kSimtCtasPerSm, &n, &c);
+  plan_splits(g, s_cur, KVQ_DECODE_MMA, &n, &c);
   return (int32_t)n;
 }
 
@@ -214,6 +245,7 @@ kvq_status kvq_decode_attention_impl(const kvq_config* cfg, const kvq_buffers* b
   p.v_meta = lp.v_meta;
   p.q = static_cast<const __half*>(q_f16);
   p.out = out;
+  p.err = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + wl.err_off);
   p.tickets = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + wl.tickets_off);
   p.ws_ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) + wl.ml_off);
   p.ws_o = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + wl.o_off);
@@ -224,6 +256,7 @@ kvq_status kvq_decode_attention_impl(const kvq_config* cfg, const kvq_buffers* b
   p.H = g.H;
   p.r = g.r;
   p.G = g.G;
+  p.log2G = g.G == 32 ? 5 : (g.G == 64 ? 6 : 7);
   p.Gv = g.Gv;
   p.R_eff = g.R_eff;
   p.n_vg = g.n_vg;
@@ -233,11 +266,12 @@ kvq_status kvq_decode_attention_impl(const kvq_config* cfg, const kvq_buffers* b
   p.k_codes_slice = g.k_codes_slice;
   p.v_codes_slice = g.v_codes_slice;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  const kvq_decode_impl use = impl == KVQ_DECODE_SIMT ? KVQ_DECODE_SIMT : KVQ_DECODE_MMA;
   int64_t n_split, chunk;
-  plan_splits(g, s_cur, kSimtCtasPerSm, &n_split, &chunk);
+  plan_splits(g, s_cur, use, &n_split, &chunk);
   p.n_split = (int)n_split;
   p.chunk = chunk;
-  cudaError_t e = (impl == KVQ_DECODE_SIMT) ? kvq::launch_decode_simt(p, g.bits, static_cast<cudaStream_t>(stream))
+  cudaError_t e = (use == KVQ_DECODE_SIMT) ? kvq::launch_decode_simt(p, g.bits, static_cast<cudaStream_t>(stream))
                                             : kvq::launch_decode_mma(p, g.bits, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }

@@ -79,14 +79,15 @@ inline int64_t max_splits(const Geometry& g, int64_t T) {
   int64_t units = (int64_t)g.B * g.H;
   int64_t by_units = (2048 + units - 1) / units;
   int64_t m = by_len < by_units ? by_len : by_units;
+  if (m > 256) m = 256;
   return m < 1 ? 1 : m;
 }
 
-// Workspace layout: tickets [B*H] u32 (padded to 256 B), then (m, l) float2
-// [B][n_q][cap], then o float [B][n_q][cap][d].
+// Workspace layout: error word (u32) at offset 0, tickets [B*H] u32 at 256, then
+// (m, l) float2 [B][n_q][cap], then o float [B][n_q][cap][d].
 struct WorkspaceLayout {
   int64_t cap;
-  size_t tickets_off, ml_off, o_off, total;
+  size_t err_off, tickets_off, ml_off, o_off, total;
 };
 
 inline WorkspaceLayout workspace_layout(const Geometry& g, int64_t T) {
@@ -94,8 +95,9 @@ inline WorkspaceLayout workspace_layout(const Geometry& g, int64_t T) {
   w.cap = max_splits(g, T);
   const int64_t nq = (int64_t)g.H * g.r;
   auto up = [](size_t v) { return (v + 255) / 256 * 256; };
-  w.tickets_off = 0;
-  w.ml_off = up((size_t)g.B * g.H * 4);
+  w.err_off = 0;
+  w.tickets_off = 256;
+  w.ml_off = w.tickets_off + up((size_t)g.B * g.H * 4);
   w.o_off = w.ml_off + up((size_t)g.B * nq * w.cap * 8);
   w.total = w.o_off + up((size_t)g.B * nq * w.cap * g.d * 4);
   return w;

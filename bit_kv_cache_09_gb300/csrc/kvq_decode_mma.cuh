@@ -1,0 +1,683 @@
+// kvq_decode_mma.cuh — split-K decode attention with tensor-core products over the
+// exact integer codes (mma.sync m16n8k16, binary16 operands, binary32 accumulation).
+//
+// Decode streams the whole packed cache once per step and reads integers that it
+// dequantizes on the fly ("KV Cache Quantization — 8-bit and 4-bit", § Decode is
+// memory-bound, so smaller is also faster); keys carry per-channel scales and values
+// per-token scales inside the same loop ("Sub-8-Bit KV Cache Quantization Is Not a
+// Free Lever for an RDNA4 Agent Swarm", § The RDNA4 kernel angle). With r = 4..8
+// query heads per kv head the binary32 CUDA-core FMA work (2*r*d per token) exceeds
+// what the FP32 pipe sustains at HBM speed for 4- and 2-bit codes, so both products
+// run on the tensor cores:
+//
+//   scores  S[i][t] = sum_c (q_ic s_gc) u_tc + sum_c q_ic s_gc (q_min - zp_gc)
+//           A = folded query (rows: query heads, hi and lo binary16 halves of a
+//               per-row power-of-two-normalised binary32 value), B = key codes.
+//   output  O[c][i] = sum_t u_tc (p_it s_tj) + sum_t p_it s_tj (q_min - zp_tj)
+//           A = value codes (rows: channels), B = weights p*s (hi and lo halves).
+//
+// Codes enter the MMA as binary16 subnormals: the 16-bit pattern u IS the value
+// u * 2^-24, so unpacking is a mask (and a byte permute for 8-bit codes), and the
+// 2^24 factor is restored on the binary32 results. The zero-point sums are plain
+// binary32 FMAs. Packed layouts are chosen so that every lane's fragment comes from
+// one contiguous chunk (see include/kvq.h): key row chunk j of a lane holds channels
+// [32j, 32j+32); value pair-row chunk g holds channels {16m + g, 16m + g + 8}.
+//
+// Staging: every warp streams its own contiguous run of 16-token slabs through a
+// ring of NS shared-memory stages filled by bulk asynchronous copies (cp.async.bulk
+// on the TMA engine), one mbarrier per stage, with bounded waits. A CTA (4 warps)
+// merges its warps; splits merge through the workspace (last CTA, atomic ticket).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "kvq_common.cuh"
+#include "kvq_kernels.h"
+#include "kvq_merge.cuh"
+
+namespace kvq {
+namespace mma {
+
+constexpr int kWarps = 4;
+constexpr int kSlab = 16;
+
+__device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(0u), "r"(sel));
+  return d;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+
+// hi = binary16(x), lo = binary16(x - hi) for a pair, packed as half2 bit patterns.
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(x0, x1);
+  const float2 hf = __half22float2(h);
+  hi = h2_bits(h);
+  lo = h2_bits(__floats2half2_rn(x0 - hf.x, x1 - hf.y));
+}
+
+// Words of one lane's chunk of a key row / value pair row (rowK/4 bytes).
+template <int BITS>
+struct Chunk {
+  static constexpr int WORDS = BITS * 128 / 8 / 4 / 4;  // 8, 4, 2
+};
+
+// Key codes: pair pi (0..15) of lane chunk j -> half2 of channels (ca, cb) as binary16
+// subnormals. A code may be left shifted inside its 16-bit half as long as the pattern
+// stays below 0x400 (the subnormal range): the value is then u * 2^-24 * k_scale(pi),
+// and the matching query entries are divided by k_scale(pi). This saves the shifts.
+template <int BITS>
+__device__ __forceinline__ uint32_t k_pair(const uint32_t* w, int pi) {
+  if (BITS == 8) return prmt(w[pi >> 1], (pi & 1) ? 0x4342u : 0x4140u);
+  if (BITS == 4) {
+    const int s = pi & 3;
+    const uint32_t x = (s < 2) ? w[pi >> 2] : (w[pi >> 2] >> 8);
+    return x & ((s & 1) ? 0x00F000F0u : 0x000F000Fu);
+  }
+  const int s = pi & 7;
+  const uint32_t x = (s < 5) ? w[pi >> 3] : (w[pi >> 3] >> 10);
+  return x & (0x00030003u << (2 * (s < 5 ? s : s - 5)));
+}
+
+// Scale k_pair leaves on pair pi (a power of two; 1 for 8-bit codes).
+template <int BITS>
+__device__ __forceinline__ constexpr float k_scale(int pi) {
+  return BITS == 8 ? 1.0f
+                   : (BITS == 4 ? (((pi & 3) & 1) ? 16.0f : 1.0f)
+                                : (float)(1 << (2 * ((pi & 7) < 5 ? (pi & 7) : (pi & 7) - 5))));
+}
+
+// Local channel indices (within the lane's 32 channels) of key pair pi.
+template <int BITS>
+__device__ __forceinline__ int k_pair_ca(int pi) {
+  if (BITS == 8) return 4 * (pi >> 1) + 2 * (pi & 1);
+  if (BITS == 4) return 8 * (pi >> 2) + (pi & 3);
+  return 16 * (pi >> 3) + (pi & 7);
+}
+template <int BITS>
+__device__ __forceinline__ int k_pair_cb(int pi) {
+  return k_pair_ca<BITS>(pi) + (BITS == 8 ? 1 : (BITS == 4 ? 4 : 8));
+}
+
+// Value codes: position i (0..15) of lane chunk g in a pair row -> half2(token 2p, token 2p+1),
+// left in place inside the 16-bit halves like k_pair (scale v_scale(i), undone per channel).
+template <int BITS>
+__device__ __forceinline__ uint32_t v_pair(const uint32_t* w, int i) {
+  if (BITS == 8) return prmt(w[i >> 1], (i & 1) ? 0x4341u : 0x4240u);
+  if (BITS == 4) {
+    const int s = i & 3;
+    const uint32_t x = (s < 2) ? w[i >> 2] : (w[i >> 2] >> 8);
+    return x & ((s & 1) ? 0x00F000F0u : 0x000F000Fu);
+  }
+  const int s = i & 7;
+  const uint32_t x = (s < 5) ? w[i >> 3] : (w[i >> 3] >> 10);
+  return x & (0x00030003u << (2 * (s < 5 ? s : s - 5)));
+}
+
+template <int BITS>
+__device__ __forceinline__ constexpr float v_scale(int i) {
+  return k_scale<BITS>(i);
+}
+
+// One stage = one iteration of 32 tokens (two 16-token halves):
+//   [key codes 32*rowK][value pair rows 32*rowV][value meta 32*4*NVG B][key-group meta 512 B]
+template <int BITS, int NVG>
+struct Stage {
+  static constexpr int KB = 32 * BITS * 128 / 8;  // key codes of 32 tokens
+  static constexpr int VB = KB;                   // value codes of 32 tokens
+  static constexpr int VM = 32 * 4 * NVG;         // value meta of 32 tokens
+  static constexpr int KM = 512;                  // one key group's meta
+  static constexpr int BYTES = KB + VB + VM + KM;
+  static constexpr int NS = BITS == 8 ? 2 : (BITS == 4 ? 3 : 4);
+  static constexpr int WARP_BYTES = NS * BYTES;
+  static constexpr int SMEM = kWarps * WARP_BYTES;
+  static_assert(SMEM >= 20480 + 4 * kMergeScratchFloats, "merge scratch must fit in the stage rings");
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred P;\n mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\n selp.u32 %0, 1, 0, P;\n}\n"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for a stage's copies; gives up after ~2 s (returns false) instead of spinning forever.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (true) {
+    for (int k = 0; k < 64; ++k)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > 2000000000ull) return false;
+  }
+}
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+template <int BITS>
+__device__ __forceinline__ void lds_chunk(const uint8_t* p, uint32_t* w) {
+  if (BITS == 8) {
+    const uint4 a = reinterpret_cast<const uint4*>(p)[0];
+    const uint4 b = reinterpret_cast<const uint4*>(p)[1];
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+  } else if (BITS == 4) {
+    const uint4 a = reinterpret_cast<const uint4*>(p)[0];
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+  } else {
+    const uint2 a = reinterpret_cast<const uint2*>(p)[0];
+    w[0] = a.x; w[1] = a.y;
+  }
+}
+
+// value meta (scale, zero) of tokens tl and tl + 1 for every group: 2 * NVG half2
+template <int NVG>
+__device__ __forceinline__ void lds_vmeta(const __half2* p, __half2* m) {
+  if (NVG == 1) {
+    const uint2 a = *reinterpret_cast<const uint2*>(p);
+    m[0] = *reinterpret_cast<const __half2*>(&a.x);
+    m[1] = *reinterpret_cast<const __half2*>(&a.y);
+  } else if (NVG == 2) {
+    const uint4 a = *reinterpret_cast<const uint4*>(p);
+    m[0] = *reinterpret_cast<const __half2*>(&a.x);
+    m[1] = *reinterpret_cast<const __half2*>(&a.y);
+    m[2] = *reinterpret_cast<const __half2*>(&a.z);
+    m[3] = *reinterpret_cast<const __half2*>(&a.w);
+  } else {
+    const uint4 a = reinterpret_cast<const uint4*>(p)[0];
+    const uint4 b = reinterpret_cast<const uint4*>(p)[1];
+    m[0] = *reinterpret_cast<const __half2*>(&a.x);
+    m[1] = *reinterpret_cast<const __half2*>(&a.y);
+    m[2] = *reinterpret_cast<const __half2*>(&a.z);
+    m[3] = *reinterpret_cast<const __half2*>(&a.w);
+    m[4] = *reinterpret_cast<const __half2*>(&b.x);
+    m[5] = *reinterpret_cast<const __half2*>(&b.y);
+    m[6] = *reinterpret_cast<const __half2*>(&b.z);
+    m[7] = *reinterpret_cast<const __half2*>(&b.w);
+  }
+}
+
+template <int NT>
+constexpr int min_blocks() {
+  return NT == 1 ? 3 : 2;
+}
+
+// BITS: code width; NT: PV n-tiles (1: r <= 4, hi/lo halves share one tile;
+// 2: r <= 8, hi tile + lo tile); NVG: value groups per token (d / Gv).
+template <int BITS, int NT, int NVG>
+__global__ void __launch_bounds__(kWarps * 32, min_blocks<NT>()) decode_mma_kernel(DecodeParams p) {
+  using St = Stage<BITS, NVG>;
+  constexpr int NS = St::NS;
+  constexpr int kTok = 32;  // tokens per iteration
+  constexpr float qmin = -(float)(1 << (BITS - 1));
+  constexpr int CW = Chunk<BITS>::WORDS;
+  constexpr int ROW = BITS * 128 / 8;  // bytes per key row / value row
+  constexpr float kTwo24 = 16777216.0f;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bars[kWarps][NS];
+  __shared__ __align__(16) float q_s[kMaxGqa][kHeadDim];
+
+  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, j = lane & 3;
+  const int r = p.r;
+  const int qi = (NT == 1) ? ((g & 3) % r) : (g % r);  // query head of QK row g / PV column g
+  const bool lo_lane = (NT == 1) && (g >= 4);            // supplies the lo half of p in the PV tile
+  const int64_t slice = (int64_t)b * p.H + h;
+  const int64_t qrow0 = (int64_t)b * p.H * r + (int64_t)h * r;
+
+  const int T = (int)p.T, Tq = (int)p.Tq;
+  const int t_begin = split * (int)p.chunk;  // chunk is a multiple of 32
+  const int t_end = min(t_begin + (int)p.chunk, T);
+  const int n_it = (t_end - t_begin + kTok - 1) / kTok;
+  const int ipw = (n_it + kWarps - 1) / kWarps;
+  const int it0 = warp * ipw;
+  const int n_mine = max(0, min(n_it, it0 + ipw) - it0);
+  const int ts0 = t_begin + it0 * kTok;  // first token of this warp (a multiple of 32)
+
+  uint8_t* wbase = smem + warp * St::WARP_BYTES;
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < NS; ++s) mbar_init(smem_u32(&bars[warp][s]));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+
+  // sources of the warp's first iteration; iteration i adds 32*i tokens
+  const uint8_t* k_src = p.k_codes + slice * p.k_codes_slice + (int64_t)ts0 * ROW;
+  const uint8_t* v_src = p.v_codes + slice * p.v_codes_slice + (int64_t)ts0 * ROW;
+  const uint8_t* vm_src = reinterpret_cast<const uint8_t*>(p.v_meta + (slice * p.S_pad + ts0) * NVG);
+  const __half2* km_base = p.k_meta + slice * (p.S_pad >> p.log2G) * kHeadDim;
+
+  // Copies of the warp's iteration i into stage i % NS (lane 0 only).
+  auto issue = [&](int i, int sidx) {
+    const int ts = ts0 + i * kTok;
+    uint8_t* st = wbase + sidx * St::BYTES;
+    const uint32_t bar = smem_u32(&bars[warp][sidx]);
+    const bool quant = ts < Tq;
+    const bool newgrp = quant && (i == 0 || (ts & (p.G - 1)) == 0);
+    const uint32_t bytes = St::VB + St::VM + (quant ? St::KB : 0) + (newgrp ? St::KM : 0);
+    const size_t off = (size_t)i * St::KB;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_expect_tx(bar, bytes);
+    if (quant) bulk_g2s(smem_u32(st), k_src + off, St::KB, bar);
+    bulk_g2s(smem_u32(st + St::KB), v_src + off, St::VB, bar);
+    bulk_g2s(smem_u32(st + St::KB + St::VB), vm_src + (size_t)i * St::VM, St::VM, bar);
+    if (newgrp) bulk_g2s(smem_u32(st + St::KB + St::VB + St::VM), km_base + ((ts >> p.log2G) << 7), St::KM, bar);
+  };
+  if (lane == 0)
+    for (int i = 0; i < min(NS, n_mine); ++i) issue(i, i);
+
+  // query rows of this kv head, binary32, in shared memory
+  for (int idx = threadIdx.x; idx < r * kHeadDim; idx += kWarps * 32)
+    q_s[idx >> 7][idx & 127] = __half2float(p.q[qrow0 * kHeadDim + idx]);
+  __syncthreads();
+
+  // online softmax state of query qi (identical in the 4 lanes of row g)
+  float m_run = -__int_as_float(0x7f800000), l_run = 0.0f;
+  float o[8][NT][4];
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[mt][nt][e] = 0.0f;
+  float beta[NVG];  // zero-point sums per value group
+#pragma unroll
+  for (int k = 0; k < NVG; ++k) beta[k] = 0.0f;
+
+  uint32_t qa[8][4];  // QK A fragments of the current key group (or of the raw query for residual keys)
+  float qscale = 0.0f, qbias = 0.0f;
+  bool resid_frags = false;
+  const float* qrow = &q_s[qi][32 * j];
+
+  // Scores of iteration i (stage st) as MMA accumulators, with the (scale, bias) that
+  // turn them into log2-unit scores: s = acc * sc + bi.
+  auto qk = [&](int i, const uint8_t* st, float (&acc)[2][2][4], float& sc, float& bi) {
+    const int ts = ts0 + i * kTok;
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[hf][nt][e] = 0.0f;
+    if (ts < Tq) {
+      if (i == 0 || (ts & (p.G - 1)) == 0) {
+        resid_frags = false;
+        // folded query of this group: x_c = q_c * s_c, bias = sum_c x_c (q_min - zp_c)
+        const uint4* mp = reinterpret_cast<const uint4*>(st + St::KB + St::VB + St::VM) + 8 * j;
+        float x[32];
+        float amax = 0.0f, bias = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint4 v = mp[k];
+          const float4 qv = reinterpret_cast<const float4*>(qrow)[k];
+          const float qq[4] = {qv.x, qv.y, qv.z, qv.w};
+          const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 sz = __half22float2(*reinterpret_cast<const __half2*>(&ws[e]));
+            const int c = 4 * k + e;
+            x[c] = qq[e] * sz.x;
+            bias = fmaf(x[c], qmin - sz.y, bias);
+            amax = fmaxf(amax, fabsf(x[c]));
+          }
+        }
+        bias += __shfl_xor_sync(0xffffffffu, bias, 1);
+        bias += __shfl_xor_sync(0xffffffffu, bias, 2);
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        // power-of-two normalisation: amax * 2^E in [2^14, 2^15)
+        int E = 0;
+        if (amax > 0.0f) E = 14 - (((__float_as_int(amax) >> 23) & 0xFF) - 127);
+        E = max(-100, min(100, E));
+        const float up = __int_as_float((127 + E) << 23);    // 2^E, exact
+        const float down = __int_as_float((127 - E) << 23);  // 2^-E, exact
+        qscale = kTwo24 * down * p.scale_log2;
+        qbias = bias * p.scale_log2;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const float u0 = up / k_scale<BITS>(2 * ks), u1 = up / k_scale<BITS>(2 * ks + 1);
+          split2(x[k_pair_ca<BITS>(2 * ks)] * u0, x[k_pair_cb<BITS>(2 * ks)] * u0, qa[ks][0], qa[ks][1]);
+          split2(x[k_pair_ca<BITS>(2 * ks + 1)] * u1, x[k_pair_cb<BITS>(2 * ks + 1)] * u1, qa[ks][2], qa[ks][3]);
+        }
+      }
+      uint32_t kw[2][2][CW];
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) lds_chunk<BITS>(st + (16 * hf + 8 * nt + g) * ROW + j * (ROW / 4), kw[hf][nt]);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+            mma16816(acc[hf][nt], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], k_pair<BITS>(kw[hf][nt], 2 * ks),
+                     k_pair<BITS>(kw[hf][nt], 2 * ks + 1));
+    } else {
+      if (!resid_frags) {
+        resid_frags = true;  // raw query fragments for binary16 residual keys: natural channel pairs
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const float4 qv = reinterpret_cast<const float4*>(qrow)[ks];
+          qa[ks][0] = h2_bits(__floats2half2_rn(qv.x, qv.y));
+          qa[ks][2] = h2_bits(__floats2half2_rn(qv.z, qv.w));
+          qa[ks][1] = 0u;
+          qa[ks][3] = 0u;
+        }
+        qscale = p.scale_log2;
+        qbias = 0.0f;
+      }
+      const __half* kr = p.k_resid + slice * (int64_t)p.R_eff * kHeadDim;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          // residual slots of tokens [Tq, T) are t - Tq (Tq is a multiple of the window)
+          const uint4* rp = reinterpret_cast<const uint4*>(kr + (ts - Tq + 16 * hf + 8 * nt + g) * kHeadDim + 32 * j);
+          uint32_t kw[16];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint4 v = __ldg(rp + k);
+            kw[4 * k] = v.x; kw[4 * k + 1] = v.y; kw[4 * k + 2] = v.z; kw[4 * k + 3] = v.w;
+          }
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            mma16816(acc[hf][nt], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], kw[2 * ks], kw[2 * ks + 1]);
+        }
+    }
+    sc = qscale;
+    bi = qbias;
+  };
+
+  // Online softmax and P.V of iteration i (stage st) from its score accumulators.
+  auto softmax_pv = [&](int i, const uint8_t* st, const float (&acc)[2][2][4], float sc, float bi) {
+    const int ts = ts0 + i * kTok;
+    // scores (log2 units) of tokens ts + 16hf + {2j, 2j+1, 8+2j, 9+2j} for query qi
+    float s[2][4];
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) s[hf][2 * nt + e] = fmaf(acc[hf][nt][e] + acc[hf][nt][e + 2], sc, bi);
+    if (ts + kTok > t_end) {  // ragged last iteration
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (ts + 16 * hf + (k >> 1) * 8 + 2 * j + (k & 1) >= t_end) s[hf][k] = -__int_as_float(0x7f800000);
+    }
+    float mx = fmaxf(fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[0][2], s[0][3])),
+                     fmaxf(fmaxf(s[1][0], s[1][1]), fmaxf(s[1][2], s[1][3])));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float m_new = fmaxf(m_run, mx);
+    if (__any_sync(0xffffffffu, m_new > m_run)) {
+      const float alpha = ex2(m_run - m_new);  // 0 on the first iteration (m_run = -inf)
+      l_run *= alpha;
+#pragma unroll
+      for (int k = 0; k < NVG; ++k) beta[k] *= alpha;
+      // PV column n holds the query of row n: alphas of columns 2j, 2j+1 live in rows 2j, 2j+1
+      const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * j);
+      const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * j + 4);
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          o[mt][nt][0] *= a0; o[mt][nt][1] *= a1; o[mt][nt][2] *= a0; o[mt][nt][3] *= a1;
+        }
+      m_run = m_new;
+    }
+    float pr[2][4];
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        pr[hf][k] = ex2(s[hf][k] - m_run);
+        l_run += pr[hf][k];
+      }
+    // values: weights p * s per value group, split into binary16 halves
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      uint32_t vw[2][CW];
+#pragma unroll
+      for (int pi = 0; pi < 2; ++pi)
+        lds_chunk<BITS>(st + St::KB + (8 * hf + 4 * pi + j) * (2 * ROW) + g * (ROW / 4), vw[pi]);
+      const __half2* vms = reinterpret_cast<const __half2*>(st + St::KB + St::VB) + 16 * hf * NVG;
+      __half2 mlo[2 * NVG], mhi[2 * NVG];  // tokens (2j, 2j+1) and (8+2j, 9+2j)
+      lds_vmeta<NVG>(vms + (2 * j) * NVG, mlo);
+      lds_vmeta<NVG>(vms + (8 + 2 * j) * NVG, mhi);
+      uint32_t bf[NVG][NT][2];
+#pragma unroll
+      for (int vg = 0; vg < NVG; ++vg) {
+        const float2 z0 = __half22float2(mlo[vg]), z1 = __half22float2(mlo[NVG + vg]);
+        const float2 z2 = __half22float2(mhi[vg]), z3 = __half22float2(mhi[NVG + vg]);
+        const float w0 = pr[hf][0] * z0.x, w1 = pr[hf][1] * z1.x, w2 = pr[hf][2] * z2.x, w3 = pr[hf][3] * z3.x;
+        beta[vg] = fmaf(w0, qmin - z0.y, beta[vg]);
+        beta[vg] = fmaf(w1, qmin - z1.y, beta[vg]);
+        beta[vg] = fmaf(w2, qmin - z2.y, beta[vg]);
+        beta[vg] = fmaf(w3, qmin - z3.y, beta[vg]);
+        uint32_t hi0, lo0, hi1, lo1;
+        split2(w0, w1, hi0, lo0);
+        split2(w2, w3, hi1, lo1);
+        if (NT == 1) {
+          bf[vg][0][0] = lo_lane ? lo0 : hi0;
+          bf[vg][0][1] = lo_lane ? lo1 : hi1;
+        } else {
+          bf[vg][0][0] = hi0; bf[vg][0][1] = hi1;
+          bf[vg][NT - 1][0] = lo0; bf[vg][NT - 1][1] = lo1;
+        }
+      }
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        const int vg = (mt * NVG) / 8;  // compile-time after unrolling
+        const uint32_t a0 = v_pair<BITS>(vw[0], 2 * mt), a1 = v_pair<BITS>(vw[0], 2 * mt + 1);
+        const uint32_t a2 = v_pair<BITS>(vw[1], 2 * mt), a3 = v_pair<BITS>(vw[1], 2 * mt + 1);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma16816(o[mt][nt], a0, a1, a2, a3, bf[vg][nt][0], bf[vg][nt][1]);
+      }
+    }
+  };
+
+  // Software pipeline: the products of iteration i+1 are issued before the softmax and
+  // P.V of iteration i, so the two independent chains overlap.
+  int failed_at = -1;
+  int sidx = 0;
+  uint32_t phase = 0;
+  float accA[2][2][4], accB[2][2][4];
+  float scA = 0.f, biA = 0.f, scB = 0.f, biB = 0.f;
+  auto step = [&](int i, float (&acc_cur)[2][2][4], float sc_cur, float bi_cur, float (&acc_nxt)[2][2][4],
+                  float& sc_nxt, float& bi_nxt) -> bool {
+    const int sn = (sidx + 1 == NS) ? 0 : sidx + 1;
+    const uint32_t pn = (sn == 0) ? (phase ^ 1u) : phase;
+    if (i + 1 < n_mine) {
+      if (!mbar_wait(smem_u32(&bars[warp][sn]), pn)) {
+        failed_at = i + 1;
+        return false;
+      }
+      qk(i + 1, wbase + sn * St::BYTES, acc_nxt, sc_nxt, bi_nxt);
+    }
+    softmax_pv(i, wbase + sidx * St::BYTES, acc_cur, sc_cur, bi_cur);
+    __syncwarp();  // every lane is done with stage sidx
+    if (lane == 0 && i + NS < n_mine) issue(i + NS, sidx);
+    sidx = sn;
+    phase = pn;
+    return true;
+  };
+  if (n_mine > 0) {
+    if (!mbar_wait(smem_u32(&bars[warp][0]), 0u)) failed_at = 0;
+    else qk(0, wbase, accA, scA, biA);
+  }
+  if (failed_at < 0) {
+    for (int i = 0; i < n_mine; i += 2) {
+      if (!step(i, accA, scA, biA, accB, scB, biB)) break;
+      if (i + 1 < n_mine && !step(i + 1, accB, scB, biB, accA, scA, biA)) break;
+    }
+  }
+
+  if (failed_at >= 0) {
+    // a stage never completed: flag it and drain (bounded) what is still in flight
+    if (lane == 0) atomicOr(p.err, 1u);
+    for (int i = failed_at; i < min(n_mine, failed_at + NS); ++i)
+      mbar_wait(smem_u32(&bars[warp][i % NS]), (uint32_t)((i / NS) & 1));
+  }
+  __syncwarp();
+
+  // ---------------- per-warp results -> shared memory (the stage rings are drained)
+  __syncthreads();
+  float* o_s = reinterpret_cast<float*>(smem);  // [kWarps][kMaxGqa][kHeadDim]
+  float* m_s = o_s + kWarps * kMaxGqa * kHeadDim;
+  float* l_s = m_s + kWarps * kMaxGqa;
+  float* beta_s = l_s + kWarps * kMaxGqa;  // [kWarps][kMaxGqa][NVG]
+  l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+  l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+#pragma unroll
+  for (int k = 0; k < NVG; ++k) {
+    beta[k] += __shfl_xor_sync(0xffffffffu, beta[k], 1);
+    beta[k] += __shfl_xor_sync(0xffffffffu, beta[k], 2);
+  }
+  if (j == 0 && g < r) {  // row g holds query g for g < r
+    m_s[warp * kMaxGqa + g] = m_run;
+    l_s[warp * kMaxGqa + g] = l_run;
+#pragma unroll
+    for (int k = 0; k < NVG; ++k) beta_s[(warp * kMaxGqa + g) * NVG + k] = beta[k];
+  }
+  // PV columns: NT == 1: cols 0..3 hi / 4..7 lo of queries 0..3; NT == 2: tile 0 hi, tile 1 lo of queries 0..7
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    float v[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      v[e] = o[mt][0][e];
+      if (NT == 2) v[e] += o[mt][NT - 1][e];
+    }
+    if (NT == 1) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[e] += __shfl_xor_sync(0xffffffffu, v[e], 2);  // lo columns j+2 -> j
+    }
+    const float sc0 = 1.0f / v_scale<BITS>(2 * mt), sc1 = 1.0f / v_scale<BITS>(2 * mt + 1);
+    v[0] *= sc0; v[1] *= sc0; v[2] *= sc1; v[3] *= sc1;
+    if ((NT == 2) || (j < 2)) {
+      const int i0 = 2 * j, i1 = 2 * j + 1;
+      const int c0 = 16 * mt + g, c1 = c0 + 8;
+      if (i0 < r) { o_s[(warp * kMaxGqa + i0) * kHeadDim + c0] = v[0]; o_s[(warp * kMaxGqa + i0) * kHeadDim + c1] = v[2]; }
+      if (i1 < r) { o_s[(warp * kMaxGqa + i1) * kHeadDim + c0] = v[1]; o_s[(warp * kMaxGqa + i1) * kHeadDim + c1] = v[3]; }
+    }
+  }
+  __syncthreads();
+
+  // ---------------- CTA merge of the warps; thread = channel (128 threads)
+  const int c = threadIdx.x;
+  const int vgc = (c * NVG) / kHeadDim;
+  for (int i = 0; i < r; ++i) {
+    float M = -__int_as_float(0x7f800000);
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w)
+      if (w * ipw < n_it) M = fmaxf(M, m_s[w * kMaxGqa + i]);
+    float L = 0.0f, acc = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      if (w * ipw >= n_it) continue;  // warp had no tokens
+      const float wt = ex2(m_s[w * kMaxGqa + i] - M);
+      L += wt * l_s[w * kMaxGqa + i];
+      acc += wt * fmaf(o_s[(w * kMaxGqa + i) * kHeadDim + c], kTwo24, beta_s[(w * kMaxGqa + i) * NVG + vgc]);
+    }
+    if (p.n_split == 1) {
+      p.out[(qrow0 + i) * kHeadDim + c] = acc / L;
+    } else {
+      p.ws_o[((qrow0 + i) * p.cap + split) * kHeadDim + c] = acc;
+      if (c == 0) p.ws_ml[(qrow0 + i) * p.cap + split] = make_float2(M, L);
+    }
+  }
+  if (p.n_split == 1) return;
+  merge_if_last(p, slice, qrow0, reinterpret_cast<float*>(smem + 20480));
+}
+
+template <int BITS, int NT, int NVG>
+cudaError_t launch_cfg(const DecodeParams& p, cudaStream_t stream) {
+  constexpr int smem = Stage<BITS, NVG>::SMEM;
+  cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<BITS, NT, NVG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)p.n_split, (unsigned)p.H, (unsigned)p.B);
+  decode_mma_kernel<BITS, NT, NVG><<<grid, kWarps * 32, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int BITS, int NT, int NVG>
+int occupancy_cfg() {
+  constexpr int smem = Stage<BITS, NVG>::SMEM;
+  if (cudaFuncSetAttribute(decode_mma_kernel<BITS, NT, NVG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+      cudaSuccess)
+    return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<BITS, NT, NVG>, kWarps * 32, smem) !=
+      cudaSuccess)
+    return 0;
+  return n;
+}
+
+template <int BITS>
+cudaError_t launch_bits(const DecodeParams& p, cudaStream_t stream) {
+  if (p.r <= 4) {
+    if (p.n_vg == 1) return launch_cfg<BITS, 1, 1>(p, stream);
+    if (p.n_vg == 2) return launch_cfg<BITS, 1, 2>(p, stream);
+    return launch_cfg<BITS, 1, 4>(p, stream);
+  }
+  if (p.n_vg == 1) return launch_cfg<BITS, 2, 1>(p, stream);
+  if (p.n_vg == 2) return launch_cfg<BITS, 2, 2>(p, stream);
+  return launch_cfg<BITS, 2, 4>(p, stream);
+}
+
+template <int BITS>
+int occupancy_bits(int r, int n_vg) {
+  if (r <= 4) {
+    if (n_vg == 1) return occupancy_cfg<BITS, 1, 1>();
+    if (n_vg == 2) return occupancy_cfg<BITS, 1, 2>();
+    return occupancy_cfg<BITS, 1, 4>();
+  }
+  if (n_vg == 1) return occupancy_cfg<BITS, 2, 1>();
+  if (n_vg == 2) return occupancy_cfg<BITS, 2, 2>();
+  return occupancy_cfg<BITS, 2, 4>();
+}
+
+}  // namespace mma
+}  // namespace kvq

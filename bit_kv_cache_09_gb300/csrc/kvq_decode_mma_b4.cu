@@ -1,0 +1,10 @@
+// kvq_decode_mma_b4.cu — instantiations of the tensor-core decode attention for 4-bit codes.
+#include "kvq_decode_mma.cuh"
+
+namespace kvq {
+
+cudaError_t launch_decode_mma_b4(const DecodeParams& p, cudaStream_t stream) { return mma::launch_bits<4>(p, stream); }
+
+int occupancy_decode_mma_b4(int r, int n_vg) { return mma::occupancy_bits<4>(r, n_vg); }
+
+}  // namespace kvq

@@ -18,6 +18,7 @@
 
 #include "kvq_common.cuh"
 #include "kvq_kernels.h"
+#include "kvq_merge.cuh"
 
 namespace kvq {
 namespace {
@@ -44,7 +45,6 @@ __global__ void __launch_bounds__(128) decode_simt_kernel(DecodeParams p) {
   __shared__ __align__(16) uint32_t v_s[kTile * kHeadDim * BITS / 8 / 4];  // value pair rows of the tile
   __shared__ __half2 vm_s[kTile * 4];                        // value metadata of the tile
   __shared__ float m_s[kRM], l_s[kRM], a_s[kRM];
-  __shared__ int last_s;
 
   // query of the r heads of this kv head (zero for unused heads)
   for (int idx = tid; idx < kHeadDim * kRM; idx += blockDim.x) {
@@ -232,32 +232,18 @@ __global__ void __launch_bounds__(128) decode_simt_kernel(DecodeParams p) {
   }
   for (int i = 0; i < p.r; ++i) p.ws_o[((qrow0 + i) * p.cap + split) * kHeadDim + c_own] = o[i];
   if (tid < p.r) p.ws_ml[(qrow0 + tid) * p.cap + split] = make_float2(m_s[tid], l_s[tid]);
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const uint32_t ticket = atomicAdd(&p.tickets[slice], 1u);
-    last_s = (ticket == (uint32_t)(p.n_split - 1));
-  }
-  __syncthreads();
-  if (!last_s) return;
-  __threadfence();
-  for (int i = 0; i < p.r; ++i) {
-    const float2* ml = p.ws_ml + (qrow0 + i) * p.cap;
-    float M = -__int_as_float(0x7f800000);
-    for (int s = 0; s < p.n_split; ++s) M = fmaxf(M, __ldcg(&ml[s]).x);
-    float L = 0.0f, acc = 0.0f;
-    for (int s = 0; s < p.n_split; ++s) {
-      const float2 v = __ldcg(&ml[s]);
-      const float w = exp2f(v.x - M);
-      L += w * v.y;
-      acc += w * __ldcg(&p.ws_o[((qrow0 + i) * p.cap + s) * kHeadDim + c_own]);
-    }
-    p.out[(qrow0 + i) * kHeadDim + c_own] = acc / L;
-  }
-  if (tid == 0) p.tickets[slice] = 0u;  // ready for the next call
+  merge_if_last(p, slice, qrow0, &qk_s[0][0][0]);  // the folded-query buffer is free now
 }
 
 }  // namespace
+
+int occupancy_decode_simt(int bits) {
+  int n = 0;
+  cudaError_t e = bits == 8 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_simt_kernel<8>, 128, 0)
+                  : bits == 4 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_simt_kernel<4>, 128, 0)
+                              : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_simt_kernel<2>, 128, 0);
+  return e == cudaSuccess ? n : 0;
+}
 
 cudaError_t launch_decode_simt(const DecodeParams& p, int bits, cudaStream_t stream) {
   dim3 grid((unsigned)p.n_split, (unsigned)p.H, (unsigned)p.B);

@@ -48,6 +48,7 @@ struct DecodeParams {
   const __half2* v_meta;
   const __half* q;  // [B][H*r][d]
   float* out;       // [B][H*r][d]
+  uint32_t* err;      // error word: bit 0 = a wait for staged data timed out
   uint32_t* tickets;  // [B*H]
   float2* ws_ml;      // [B][H*r][cap] (running max in log2 units, denominator)
   float* ws_o;        // [B][H*r][cap][d]
@@ -55,6 +56,7 @@ struct DecodeParams {
   int64_t chunk;      // tokens per split (multiple of 128)
   int n_split, cap;
   int B, H, r, G, Gv, R_eff, n_vg;
+  int log2G;          // G is a power of two
   int64_t S_pad, rowK, rowV;
   int64_t k_codes_slice, v_codes_slice;
   float scale_log2;   // softmax_scale * log2(e)
@@ -64,5 +66,7 @@ cudaError_t launch_append(const AppendParams& p, int bits, cudaStream_t stream);
 cudaError_t launch_dequant(const DequantParams& p, int bits, cudaStream_t stream);
 cudaError_t launch_decode_simt(const DecodeParams& p, int bits, cudaStream_t stream);
 cudaError_t launch_decode_mma(const DecodeParams& p, int bits, cudaStream_t stream);
+int occupancy_decode_mma(int bits, int r, int n_vg);  // resident CTAs per SM (0 on error)
+int occupancy_decode_simt(int bits);
 
 }  // namespace kvq
