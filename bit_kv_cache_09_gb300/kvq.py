@@ -23,7 +23,7 @@ BUFFER_NAMES = ("k_codes", "k_meta", "k_resid", "v_codes", "v_meta")
 DECODE_AUTO, DECODE_SIMT, DECODE_MMA = 0, 1, 2
 EXPORTED = ("kvq_buffer_sizes", "kvq_quantize_append", "kvq_dequantize", "kvq_decode_workspace_size",
             "kvq_decode_attention", "kvq_decode_attention_impl", "kvq_decode_num_splits", "kvq_status_string",
-            "kvq_version")
+            "kvq_version", "kvq_decode_attention_noalloc")
 
 
 class KVQError(RuntimeError):
@@ -69,6 +69,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.kvq_decode_attention.restype = ctypes.c_int
         L.kvq_decode_attention_impl.argtypes = L.kvq_decode_attention.argtypes + [ctypes.c_int]
         L.kvq_decode_attention_impl.restype = ctypes.c_int
+        L.kvq_decode_attention_noalloc.argtypes = [cfgp, bufp, ctypes.c_int32, ctypes.c_int64, vp, ctypes.c_float,
+                                                   vp, vp]
+        L.kvq_decode_attention_noalloc.restype = ctypes.c_int
         L.kvq_decode_num_splits.argtypes = [cfgp, ctypes.c_int64]
         L.kvq_decode_num_splits.restype = ctypes.c_int32
         L.kvq_status_string.argtypes = [ctypes.c_int]
@@ -141,3 +144,12 @@ def kvq_decode_attention_impl(cfg: kvq_config, bufs: kvq_buffers, layer: int, s_
     _check("kvq_decode_attention_impl",
            load().kvq_decode_attention_impl(ctypes.byref(cfg), ctypes.byref(bufs), layer, s_cur, q_f16, softmax_scale,
                                             out, ws, ws_bytes, stream, impl))
+
+
+def kvq_decode_attention_noalloc(cfg: kvq_config, bufs: kvq_buffers, layer: int, s_cur: int, q_f16: int,
+                                 softmax_scale: float, out: int, stream: int = 0) -> None:
+    """Decode attention with the library's static 16 MiB device scratch instead of a
+    caller workspace (for callers that cannot allocate; calls must not overlap)."""
+    _check("kvq_decode_attention_noalloc",
+           load().kvq_decode_attention_noalloc(ctypes.byref(cfg), ctypes.byref(bufs), layer, s_cur, q_f16,
+                                               softmax_scale, out, stream))

@@ -157,6 +157,23 @@ kvq_status kvq_decode_attention_impl(const kvq_config* cfg, const kvq_buffers* b
                                      const void* q_f16, float softmax_scale, float* out, void* ws,
                                      size_t ws_bytes, void* stream, kvq_decode_impl impl);
 
+/* kvq_decode_attention without a caller-supplied workspace, for callers that cannot
+ * allocate device memory at the call site (code embedded in a framework whose allocator
+ * owns all device memory, or a decode loop where an allocation's implicit device
+ * synchronisation is not acceptable). No counterpart in the pages: it is a deployment
+ * convenience of this library. The split-K scratch is one file-scope __device__ array
+ * of 16 MiB that every GPU loading the library keeps until the process exits; a
+ * configuration whose kvq_decode_workspace_size(cfg, s_cur) exceeds 16 MiB is rejected
+ * with KVQ_ERR_WORKSPACE. The function allocates nothing (no cudaMalloc/cudaFree, no
+ * allocating library call). Its first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture. Every call on a device shares the one array: it clears the
+ * array's counters on `stream` and then runs the same kernels as kvq_decode_attention,
+ * so calls whose executions overlap on the GPU (other streams, other threads) race and
+ * must be ordered by the caller. */
+kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur,
+                                        const void* q_f16, float softmax_scale, float* out, void* stream);
+
 /* Number of split-K partitions kvq_decode_attention uses for s_cur tokens (>= 1),
  * or 0 for a bad config. */
 int32_t kvq_decode_num_splits(const kvq_config* cfg, int64_t s_cur);
