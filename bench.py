@@ -68,6 +68,49 @@ def step_launches(w, s_cur: int) -> int:
 
 
 # ----------------------------------------------------------------------------- helpers
+def max_over_ranks(value: float, dist=None, device="cpu") -> float:
+    """The largest value over all ranks (the slowest rank's time); identity on one rank."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(value)
+    import torch
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, seconds: float) -> float:
+    """Replicas: every rank processes the same work, so the job rate is world x units / max time."""
+    return units_per_rank * world / seconds
+
+
+DECODE_SOURCES = ("bit_kv_cache_09_gb300/csrc/kvq_decode_mma.cuh", "bit_kv_cache_09_gb300/csrc/kvq_merge.cuh")
+
+
+def decode_source_hash() -> str:
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in DECODE_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str):
+    """DRAM bytes per decode-attention launch from the committed ncu capture, or None
+    when there is none for this workload or the kernel source changed since."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            e = json.load(f).get(workload)
+    except Exception:
+        return None
+    if not e or e.get("kernel_src_sha") != decode_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -327,16 +370,12 @@ def main():
             launches += step_launches(w, S + s)
         e1.record()
         torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
-    if dist:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
     clocks = clk.summary()
     nbytes = sum(L * (attn_bytes_per_layer(w, S + s + 1) + append_bytes_per_layer(w, S + s)) for s in range(W, W + K))
     ms_step = ms / K
-    gbs = nbytes * world / (ms / 1e3) / 1e9
-    tok_s = w.batch * K * world / (ms / 1e3)
+    gbs = whole_job_rate(nbytes, world, ms / 1e3) / 1e9
+    tok_s = whole_job_rate(w.batch * K, world, ms / 1e3)
     peak, peak_kind = measured_peaks()
 
     # dominant kernel alone: decode attention over all layers back to back (one graph), same T
@@ -357,14 +396,7 @@ def main():
     attn_us = a0.elapsed_time(a1) * 1e3 / (reps * L)
     attn_b = attn_bytes_per_layer(w, T_k)
     achieved = attn_b / (attn_us * 1e-6) / 1e9
-    traffic = None
-    prof_path = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(prof_path):
-        try:
-            with open(prof_path) as f:
-                traffic = json.load(f).get(w.name, {}).get("dram_bytes_per_launch")
-        except Exception:
-            traffic = None
+    traffic = measured_traffic(w.name)
 
     # end to end through the public API: pinned host inputs in, outputs back, every step
     e2e = None
