@@ -68,36 +68,80 @@ int decode_occupancy(const Geometry& g, kvq_decode_impl impl) {
   return n > 0 ? n : 1;
 }
 
-// Split-K plan: the number of splits per (batch row, kv head) is chosen so that the
-// grid fills whole waves of resident CTAs (>= 92% of the slots busy when possible),
-// every split has at least 64 tokens, and the workspace bound holds. Chunks are a
-// multiple of `align` tokens.
-void plan_splits(const Geometry& g, int64_t T, kvq_decode_impl impl, int64_t* n_split, int64_t* chunk) {
+// Largest power-of-two cluster size <= 16 whose clusters can all be resident for
+// `units` (batch row, kv head) pairs (cached per device and kernel shape).
+int decode_cluster_size(const Geometry& g, int64_t units) {
+  static std::atomic<int> cache[16][3][2][3][5];  // device, bits, r class, value groups, log2 size
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) dev = 0;
+  const int bi = g.bits == 8 ? 0 : (g.bits == 4 ? 1 : 2);
+  const int ri = g.r <= 4 ? 0 : 1;
+  const int vi = g.n_vg == 1 ? 0 : (g.n_vg == 2 ? 1 : 2);
+  for (int lg = 4; lg >= 1; --lg) {
+    std::atomic<int>& slot = cache[dev][bi][ri][vi][lg];
+    int n = slot.load(std::memory_order_relaxed);
+    if (n == 0) {
+      n = kvq::max_clusters_decode_mma(g.bits, g.r, g.n_vg, 1 << lg);
+      if (n <= 0) n = -1;
+      slot.store(n, std::memory_order_relaxed);
+    }
+    if (n >= units) return 1 << lg;
+  }
+  return 1;
+}
+
+// Split-K plan.
+// Large grids (many (batch row, kv head) pairs): the number of splits per pair is chosen
+// so that the grid fills whole waves of resident CTAs (>= 92% of the slots busy when
+// possible); partials merge through the workspace (last CTA, atomic ticket).
+// Small grids (at most 1/32 of the slots per pair): latency-bound, so each pair gets a
+// cluster of up to 16 CTAs, small enough that every warp's stages are all in flight at
+// once, merged through distributed shared memory without touching the workspace.
+struct Plan {
+  int64_t n_split, chunk;
+  int cluster, n_parts;
+};
+
+Plan plan_splits(const Geometry& g, int64_t T, kvq_decode_impl impl) {
   int sms = device_sm_count();
   if (sms <= 0) sms = 152;
   const int64_t slots = (int64_t)sms * decode_occupancy(g, impl);
   const int64_t align = impl == KVQ_DECODE_SIMT ? 128 : 32;
   const int64_t units = (int64_t)g.B * g.H;
+  Plan pl;
+  if (impl != KVQ_DECODE_SIMT && units * 32 <= slots) {
+    const int cs = decode_cluster_size(g, units);
+    int64_t c = (T + cs - 1) / cs;
+    c = (c + align - 1) / align * align;
+    pl.n_split = cs;  // trailing splits may be empty; they merge with weight 0
+    pl.chunk = c;
+    pl.cluster = cs;
+    pl.n_parts = 1;
+    return pl;
+  }
   int64_t max_k = kvq::max_splits(g, T);
-  const int64_t by_len = (T + 63) / 64;
+  const int64_t by_len = (T + align - 1) / align;
   if (max_k > by_len) max_k = by_len;
   if (max_k < 1) max_k = 1;
-  int64_t best_k = 1;
+  int64_t k = 1;
   double best_eff = 0.0;
-  for (int64_t k = 1; k <= max_k; ++k) {
-    const int64_t ctas = units * k;
+  for (int64_t c = 1; c <= max_k; ++c) {
+    const int64_t ctas = units * c;
     const int64_t waves = (ctas + slots - 1) / slots;
     const double eff = (double)ctas / (double)(waves * slots);
     if (eff > best_eff + 1e-9) {
       best_eff = eff;
-      best_k = k;
+      k = c;
     }
     if (eff >= 0.92) break;
   }
-  int64_t c = (T + best_k - 1) / best_k;
+  int64_t c = (T + k - 1) / k;
   c = (c + align - 1) / align * align;
-  *chunk = c;
-  *n_split = (T + c - 1) / c;
+  pl.n_split = (T + c - 1) / c;
+  pl.chunk = c;
+  pl.cluster = 1;
+  pl.n_parts = (int)pl.n_split;
+  return pl;
 }
 
 }  // namespace
@@ -216,9 +260,7 @@ size_t kvq_decode_workspace_size(const kvq_config* cfg, int64_t s_cur) {
 int32_t kvq_decode_num_splits(const kvq_config* cfg, int64_t s_cur) {
   Geometry g;
   if (kvq::make_geometry(cfg, &g) != KVQ_OK || s_cur < 1) return 0;
-  int64_t n, c;
-  plan_splits(g, s_cur, KVQ_DECODE_MMA, &n, &c);
-  return (int32_t)n;
+  return (int32_t)plan_splits(g, s_cur, KVQ_DECODE_MMA).n_split;
 }
 
 kvq_status kvq_decode_attention_impl(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur,
@@ -267,10 +309,11 @@ kvq_status kvq_decode_attention_impl(const kvq_config* cfg, const kvq_buffers* b
   p.v_codes_slice = g.v_codes_slice;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   const kvq_decode_impl use = impl == KVQ_DECODE_SIMT ? KVQ_DECODE_SIMT : KVQ_DECODE_MMA;
-  int64_t n_split, chunk;
-  plan_splits(g, s_cur, use, &n_split, &chunk);
-  p.n_split = (int)n_split;
-  p.chunk = chunk;
+  const Plan pl = plan_splits(g, s_cur, use);
+  p.n_split = (int)pl.n_split;
+  p.chunk = pl.chunk;
+  p.cluster = pl.cluster;
+  p.n_parts = pl.n_parts;
   cudaError_t e = (use == KVQ_DECODE_SIMT) ? kvq::launch_decode_simt(p, g.bits, static_cast<cudaStream_t>(stream))
                                             : kvq::launch_decode_mma(p, g.bits, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;

@@ -10,6 +10,9 @@ cudaError_t launch_decode_mma_b2(const DecodeParams& p, cudaStream_t stream);
 int occupancy_decode_mma_b8(int r, int n_vg);
 int occupancy_decode_mma_b4(int r, int n_vg);
 int occupancy_decode_mma_b2(int r, int n_vg);
+int max_clusters_decode_mma_b8(int r, int n_vg, int cs);
+int max_clusters_decode_mma_b4(int r, int n_vg, int cs);
+int max_clusters_decode_mma_b2(int r, int n_vg, int cs);
 
 cudaError_t launch_decode_mma(const DecodeParams& p, int bits, cudaStream_t stream) {
   switch (bits) {
@@ -24,6 +27,14 @@ int occupancy_decode_mma(int bits, int r, int n_vg) {
     case 8: return occupancy_decode_mma_b8(r, n_vg);
     case 4: return occupancy_decode_mma_b4(r, n_vg);
     default: return occupancy_decode_mma_b2(r, n_vg);
+  }
+}
+
+int max_clusters_decode_mma(int bits, int r, int n_vg, int cs) {
+  switch (bits) {
+    case 8: return max_clusters_decode_mma_b8(r, n_vg, cs);
+    case 4: return max_clusters_decode_mma_b4(r, n_vg, cs);
+    default: return max_clusters_decode_mma_b2(r, n_vg, cs);
   }
 }
 

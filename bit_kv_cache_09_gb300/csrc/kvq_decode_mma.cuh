@@ -29,6 +29,7 @@
 // merges its warps; splits merge through the workspace (last CTA, atomic ticket).
 #pragma once
 
+#include <cooperative_groups.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -38,6 +39,8 @@
 
 namespace kvq {
 namespace mma {
+
+namespace cg = cooperative_groups;
 
 constexpr int kWarps = 4;
 constexpr int kSlab = 16;
@@ -143,10 +146,11 @@ struct Stage {
   static constexpr int VM = 32 * 4 * NVG;         // value meta of 32 tokens
   static constexpr int KM = 512;                  // one key group's meta
   static constexpr int BYTES = KB + VB + VM + KM;
-  static constexpr int NS = BITS == 8 ? 2 : (BITS == 4 ? 3 : 4);
+  static constexpr int NS = BITS == 8 ? 3 : (BITS == 4 ? 2 : 3);
   static constexpr int WARP_BYTES = NS * BYTES;
-  static constexpr int SMEM = kWarps * WARP_BYTES;
-  static_assert(SMEM >= 20480 + 4 * kMergeScratchFloats, "merge scratch must fit in the stage rings");
+  // the stage rings are reused after the loop for the merges (at most 24 KB + scratch)
+  static constexpr int kEpilogueBytes = 24576 + 4 * kMergeScratchFloats;
+  static constexpr int SMEM = kWarps * WARP_BYTES > kEpilogueBytes ? kWarps * WARP_BYTES : kEpilogueBytes;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -236,7 +240,7 @@ __device__ __forceinline__ void lds_vmeta(const __half2* p, __half2* m) {
 
 template <int NT>
 constexpr int min_blocks() {
-  return NT == 1 ? 3 : 2;
+  return NT == 1 ? 4 : 2;
 }
 
 // BITS: code width; NT: PV n-tiles (1: r <= 4, hi/lo halves share one tile;
@@ -266,10 +270,10 @@ __global__ void __launch_bounds__(kWarps * 32, min_blocks<NT>()) decode_mma_kern
   const int T = (int)p.T, Tq = (int)p.Tq;
   const int t_begin = split * (int)p.chunk;  // chunk is a multiple of 32
   const int t_end = min(t_begin + (int)p.chunk, T);
-  const int n_it = (t_end - t_begin + kTok - 1) / kTok;
-  const int ipw = (n_it + kWarps - 1) / kWarps;
-  const int it0 = warp * ipw;
-  const int n_mine = max(0, min(n_it, it0 + ipw) - it0);
+  const int n_it = max(0, (t_end - t_begin + kTok - 1) / kTok);  // 0 for a trailing empty split
+  // balanced contiguous runs of iterations per warp (warp w: [w*n_it/4, (w+1)*n_it/4))
+  const int it0 = (warp * n_it) / kWarps;
+  const int n_mine = ((warp + 1) * n_it) / kWarps - it0;
   const int ts0 = t_begin + it0 * kTok;  // first token of this warp (a multiple of 32)
 
   uint8_t* wbase = smem + warp * St::WARP_BYTES;
@@ -518,39 +522,24 @@ __global__ void __launch_bounds__(kWarps * 32, min_blocks<NT>()) decode_mma_kern
     }
   };
 
-  // Software pipeline: the products of iteration i+1 are issued before the softmax and
-  // P.V of iteration i, so the two independent chains overlap.
   int failed_at = -1;
   int sidx = 0;
   uint32_t phase = 0;
-  float accA[2][2][4], accB[2][2][4];
-  float scA = 0.f, biA = 0.f, scB = 0.f, biB = 0.f;
-  auto step = [&](int i, float (&acc_cur)[2][2][4], float sc_cur, float bi_cur, float (&acc_nxt)[2][2][4],
-                  float& sc_nxt, float& bi_nxt) -> bool {
-    const int sn = (sidx + 1 == NS) ? 0 : sidx + 1;
-    const uint32_t pn = (sn == 0) ? (phase ^ 1u) : phase;
-    if (i + 1 < n_mine) {
-      if (!mbar_wait(smem_u32(&bars[warp][sn]), pn)) {
-        failed_at = i + 1;
-        return false;
-      }
-      qk(i + 1, wbase + sn * St::BYTES, acc_nxt, sc_nxt, bi_nxt);
+  for (int i = 0; i < n_mine; ++i) {
+    if (!mbar_wait(smem_u32(&bars[warp][sidx]), phase)) {
+      failed_at = i;
+      break;
     }
-    softmax_pv(i, wbase + sidx * St::BYTES, acc_cur, sc_cur, bi_cur);
+    const uint8_t* st = wbase + sidx * St::BYTES;
+    float acc[2][2][4];
+    float sc, bi;
+    qk(i, st, acc, sc, bi);
+    softmax_pv(i, st, acc, sc, bi);
     __syncwarp();  // every lane is done with stage sidx
     if (lane == 0 && i + NS < n_mine) issue(i + NS, sidx);
-    sidx = sn;
-    phase = pn;
-    return true;
-  };
-  if (n_mine > 0) {
-    if (!mbar_wait(smem_u32(&bars[warp][0]), 0u)) failed_at = 0;
-    else qk(0, wbase, accA, scA, biA);
-  }
-  if (failed_at < 0) {
-    for (int i = 0; i < n_mine; i += 2) {
-      if (!step(i, accA, scA, biA, accB, scB, biB)) break;
-      if (i + 1 < n_mine && !step(i + 1, accB, scB, biB, accA, scA, biA)) break;
+    if (++sidx == NS) {
+      sidx = 0;
+      phase ^= 1u;
     }
   }
 
@@ -608,37 +597,117 @@ __global__ void __launch_bounds__(kWarps * 32, min_blocks<NT>()) decode_mma_kern
   // ---------------- CTA merge of the warps; thread = channel (128 threads)
   const int c = threadIdx.x;
   const int vgc = (c * NVG) / kHeadDim;
+  // per-CTA partial (max, denominator, unnormalised output) for the cluster merge
+  float* cm_s = reinterpret_cast<float*>(smem + 20480);  // [kMaxGqa]
+  float* cl_s = cm_s + kMaxGqa;                           // [kMaxGqa]
+  float* co_s = cl_s + kMaxGqa;                           // [kMaxGqa][kHeadDim]
   for (int i = 0; i < r; ++i) {
     float M = -__int_as_float(0x7f800000);
 #pragma unroll
     for (int w = 0; w < kWarps; ++w)
-      if (w * ipw < n_it) M = fmaxf(M, m_s[w * kMaxGqa + i]);
+      if (((w + 1) * n_it) / kWarps > (w * n_it) / kWarps) M = fmaxf(M, m_s[w * kMaxGqa + i]);
     float L = 0.0f, acc = 0.0f;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
-      if (w * ipw >= n_it) continue;  // warp had no tokens
+      if (((w + 1) * n_it) / kWarps == (w * n_it) / kWarps) continue;  // warp had no tokens
       const float wt = ex2(m_s[w * kMaxGqa + i] - M);
       L += wt * l_s[w * kMaxGqa + i];
       acc += wt * fmaf(o_s[(w * kMaxGqa + i) * kHeadDim + c], kTwo24, beta_s[(w * kMaxGqa + i) * NVG + vgc]);
     }
-    if (p.n_split == 1) {
-      p.out[(qrow0 + i) * kHeadDim + c] = acc / L;
-    } else {
-      p.ws_o[((qrow0 + i) * p.cap + split) * kHeadDim + c] = acc;
-      if (c == 0) p.ws_ml[(qrow0 + i) * p.cap + split] = make_float2(M, L);
+    if (p.cluster == 1) {  // no cluster: this CTA's partial is the split's partial
+      if (p.n_parts == 1) {
+        p.out[(qrow0 + i) * kHeadDim + c] = acc / L;
+      } else {
+        p.ws_o[((qrow0 + i) * p.cap + split) * kHeadDim + c] = acc;
+        if (c == 0) p.ws_ml[(qrow0 + i) * p.cap + split] = make_float2(M, L);
+      }
+      continue;
+    }
+    co_s[i * kHeadDim + c] = acc;
+    if (c == 0) {
+      cm_s[i] = M;
+      cl_s[i] = L;
     }
   }
-  if (p.n_split == 1) return;
-  merge_if_last(p, slice, qrow0, reinterpret_cast<float*>(smem + 20480));
+  if (p.cluster == 1) {
+    if (p.n_parts > 1) merge_if_last(p, slice, qrow0, reinterpret_cast<float*>(smem + 24576));
+    return;
+  }
+  // ---------------- merge of the splits of one cluster through distributed shared memory.
+  // The cluster's CTAs are co-resident and the barriers are hardware cluster barriers.
+  // CTA rank R merges channels [R*S, R*S + S) (S = 128 / cluster size) of every query
+  // head, reading all partials of the cluster with independent remote loads.
+  cg::cluster_group cluster = cg::this_cluster();
+  cluster.sync();
+  {
+    const int cs = p.cluster;  // a power of two <= 16
+    const int rank = (int)cluster.block_rank();
+    const int S = kHeadDim / cs;
+    const int part = split / cs;
+    for (int o_idx = threadIdx.x; o_idx < r * S; o_idx += kWarps * 32) {
+      const int i = o_idx / S;
+      const int cc = rank * S + (o_idx % S);
+      float mq[16], lq[16], oq[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        if (q < cs) {
+          mq[q] = *cluster.map_shared_rank(cm_s + i, q);
+          lq[q] = *cluster.map_shared_rank(cl_s + i, q);
+          oq[q] = *cluster.map_shared_rank(co_s + i * kHeadDim + cc, q);
+        }
+      }
+      float M = -__int_as_float(0x7f800000);
+#pragma unroll
+      for (int q = 0; q < 16; ++q)
+        if (q < cs) M = fmaxf(M, mq[q]);
+      float L = 0.0f, acc = 0.0f;
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        if (q < cs && mq[q] != -__int_as_float(0x7f800000)) {  // CTAs without tokens weigh 0
+          const float wt = ex2(mq[q] - M);
+          L += wt * lq[q];
+          acc += wt * oq[q];
+        }
+      }
+      if (p.n_parts == 1) {
+        p.out[(qrow0 + i) * kHeadDim + cc] = acc / L;
+      } else {
+        p.ws_o[((qrow0 + i) * p.cap + part) * kHeadDim + cc] = acc;
+        if (rank == 0 && o_idx % S == 0) p.ws_ml[(qrow0 + i) * p.cap + part] = make_float2(M, L);
+      }
+    }
+    if (p.n_parts > 1) __threadfence();  // slices visible device-wide before the ticket
+  }
+  cluster.sync();  // the other CTAs keep their shared memory until every rank has read it
+  if (p.n_parts > 1 && cluster.block_rank() == 0) merge_if_last(p, slice, qrow0, reinterpret_cast<float*>(smem + 24576));
 }
 
 template <int BITS, int NT, int NVG>
 cudaError_t launch_cfg(const DecodeParams& p, cudaStream_t stream) {
   constexpr int smem = Stage<BITS, NVG>::SMEM;
-  cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<BITS, NT, NVG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  auto* kern = decode_mma_kernel<BITS, NT, NVG>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)p.n_split, (unsigned)p.H, (unsigned)p.B);
-  decode_mma_kernel<BITS, NT, NVG><<<grid, kWarps * 32, smem, stream>>>(p);
+  if (p.cluster < 1 || p.cluster > 16 || (p.cluster & (p.cluster - 1)) || p.n_split != p.cluster * p.n_parts)
+    return cudaErrorInvalidConfiguration;
+  if (p.cluster > 8) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.n_split, (unsigned)p.H, (unsigned)p.B);
+  cfg.blockDim = dim3(kWarps * 32, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)p.cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -653,6 +722,41 @@ int occupancy_cfg() {
       cudaSuccess)
     return 0;
   return n;
+}
+
+// Clusters of `cs` CTAs that can be resident at once (0 if such a cluster cannot launch).
+template <int BITS, int NT, int NVG>
+int max_clusters_cfg(int cs) {
+  constexpr int smem = Stage<BITS, NVG>::SMEM;
+  auto* kern = decode_mma_kernel<BITS, NT, NVG>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
+  if (cs > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)cs, 1, 1);
+  cfg.blockDim = dim3(kWarps * 32, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return 0;
+  return n;
+}
+
+template <int BITS>
+int max_clusters_bits(int r, int n_vg, int cs) {
+  if (r <= 4) {
+    if (n_vg == 1) return max_clusters_cfg<BITS, 1, 1>(cs);
+    if (n_vg == 2) return max_clusters_cfg<BITS, 1, 2>(cs);
+    return max_clusters_cfg<BITS, 1, 4>(cs);
+  }
+  if (n_vg == 1) return max_clusters_cfg<BITS, 2, 1>(cs);
+  if (n_vg == 2) return max_clusters_cfg<BITS, 2, 2>(cs);
+  return max_clusters_cfg<BITS, 2, 4>(cs);
 }
 
 template <int BITS>

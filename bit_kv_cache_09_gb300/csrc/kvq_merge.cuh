@@ -1,6 +1,6 @@
 // kvq_merge.cuh — split-K merge of decode-attention partials (library-internal).
 //
-// Every split s of a (batch row, kv head) leaves, per query head i, its running max
+// Every part s (a split, or a cluster of splits) of a (batch row, kv head) leaves, per query head i, its running max
 // m_s (log2 units), its denominator l_s and its unnormalised output o_s[c]. The
 // exact softmax over all tokens is the log-sum-exp combination
 //   M = max_s m_s,  out[c] = sum_s 2^(m_s - M) o_s[c] / sum_s 2^(m_s - M) l_s.
@@ -31,7 +31,7 @@ __device__ __forceinline__ void merge_if_last(const DecodeParams& p, int64_t sli
   __syncthreads();
   if (threadIdx.x == 0) {
     const uint32_t ticket = atomicAdd(&p.tickets[slice], 1u);
-    last_s = (ticket == (uint32_t)(p.n_split - 1));
+    last_s = (ticket == (uint32_t)(p.n_parts - 1));
   }
   __syncthreads();
   if (!last_s) return;
@@ -45,7 +45,7 @@ __device__ __forceinline__ void merge_if_last(const DecodeParams& p, int64_t sli
 #pragma unroll
     for (int k = 0; k < kMaxSplits / 32; ++k) {
       const int s = lane + 32 * k;
-      v[k] = (s < p.n_split) ? __ldcg(&ml[s]) : make_float2(-__int_as_float(0x7f800000), 0.0f);
+      v[k] = (s < p.n_parts) ? __ldcg(&ml[s]) : make_float2(-__int_as_float(0x7f800000), 0.0f);
       M = fmaxf(M, v[k].x);
     }
 #pragma unroll
@@ -54,7 +54,7 @@ __device__ __forceinline__ void merge_if_last(const DecodeParams& p, int64_t sli
 #pragma unroll
     for (int k = 0; k < kMaxSplits / 32; ++k) {
       const int s = lane + 32 * k;
-      if (s < p.n_split) {
+      if (s < p.n_parts) {
         const float wt = exp2f(v[k].x - M);
         w_s[i][s] = wt;
         L += wt * v[k].y;
@@ -70,20 +70,20 @@ __device__ __forceinline__ void merge_if_last(const DecodeParams& p, int64_t sli
   float acc[kMaxGqa];
 #pragma unroll
   for (int i = 0; i < kMaxGqa; ++i) acc[i] = 0.0f;
-  for (int s0 = 0; s0 < p.n_split; s0 += 4) {
+  for (int s0 = 0; s0 < p.n_parts; s0 += 4) {
     float ov[kMaxGqa][4];
 #pragma unroll
     for (int i = 0; i < kMaxGqa; ++i)
 #pragma unroll
       for (int u = 0; u < 4; ++u)
-        ov[i][u] = (i < p.r && s0 + u < p.n_split)
+        ov[i][u] = (i < p.r && s0 + u < p.n_parts)
                        ? __ldcg(p.ws_o + ((qrow0 + i) * p.cap + s0 + u) * kHeadDim + c)
                        : 0.0f;
 #pragma unroll
     for (int i = 0; i < kMaxGqa; ++i)
 #pragma unroll
       for (int u = 0; u < 4; ++u)
-        if (i < p.r && s0 + u < p.n_split) acc[i] = fmaf(w_s[i][s0 + u], ov[i][u], acc[i]);
+        if (i < p.r && s0 + u < p.n_parts) acc[i] = fmaf(w_s[i][s0 + u], ov[i][u], acc[i]);
   }
 #pragma unroll
   for (int i = 0; i < kMaxGqa; ++i)
