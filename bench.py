@@ -61,9 +61,13 @@ def append_bytes_per_layer(w, s_cur: int, n_new: int = 1) -> int:
     return w.batch * w.n_kv * per
 
 
-def step_launches(w, s_cur: int) -> int:
+def step_launches(w, s_cur: int, fused: bool = True) -> int:
+    """Kernels one decode step launches: per layer one fused append+attention launch, or
+    (separate calls, or a step that fills a residual window) append (+ key groups) and attention."""
     R = w.r_eff
     flush = ((s_cur + 1) // R) > (s_cur // R)
+    if fused and not flush:
+        return w.n_layers
     return w.n_layers * (2 + (1 if flush else 0))
 
 
@@ -334,8 +338,11 @@ def main():
     def step(s):
         T = S + s
         for layer in range(L):
-            cache.append(layer, T, kin[s, layer], vin[s, layer])
-            cache.attention(layer, T + 1, qin[s, layer], scale, out=out[layer], impl=impl)
+            if impl == kvq.DECODE_SIMT:
+                cache.append(layer, T, kin[s, layer], vin[s, layer])
+                cache.attention(layer, T + 1, qin[s, layer], scale, out=out[layer], impl=impl)
+            else:  # append fused into the attention launch
+                cache.decode_step(layer, T, kin[s, layer], vin[s, layer], qin[s, layer], scale, out=out[layer])
 
     use_graph = not args.no_graph
     graphs = {}
@@ -367,7 +374,7 @@ def main():
         e0.record()
         for s in range(W, W + K):
             run(s)
-            launches += step_launches(w, S + s)
+            launches += step_launches(w, S + s, fused=impl != kvq.DECODE_SIMT)
         e1.record()
         torch.cuda.synchronize()
     ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
@@ -416,18 +423,38 @@ def main():
             vd.copy_(vh[i], non_blocking=True)
             qd.copy_(qh[i], non_blocking=True)
             for layer in range(L):
-                cache.append(layer, T, kd[layer], vd[layer])
-                cache.attention(layer, T + 1, qd[layer], scale, out=out[layer], impl=impl)
+                if impl == kvq.DECODE_SIMT:
+                    cache.append(layer, T, kd[layer], vd[layer])
+                    cache.attention(layer, T + 1, qd[layer], scale, out=out[layer], impl=impl)
+                else:
+                    cache.decode_step(layer, T, kd[layer], vd[layer], qd[layer], scale, out=out[layer])
             oh[i].copy_(out, non_blocking=True)
 
+        # one graph per step: host->device copies of the step's inputs (pinned), the
+        # decode step of every layer, and the device->host copy of the outputs
+        e2e_graphs = {}
+        if use_graph:
+            for i in range(WE + KE):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    e2e_step(i)
+                e2e_graphs[i] = g
+            torch.cuda.synchronize()
+
+        def e2e_run(i):
+            if use_graph:
+                e2e_graphs[i].replay()
+            else:
+                e2e_step(i)
+
         for i in range(WE):
-            e2e_step(i)
+            e2e_run(i)
         torch.cuda.synchronize()
         b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t_host = time.perf_counter()
         b0.record()
         for i in range(WE, WE + KE):
-            e2e_step(i)
+            e2e_run(i)
         b1.record()
         torch.cuda.synchronize()
         t_host = time.perf_counter() - t_host
@@ -438,7 +465,7 @@ def main():
         d2h = out.numel() * 4
         e2e = {"value": round(e_bytes * world / (e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
                "tokens_per_s": round(w.batch * KE * world / (e_ms / 1e3), 1),
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": KE, "eager": True}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": KE, "cuda_graph": use_graph}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -64,3 +64,14 @@ class QuantizedKVCache:
         kvq.kvq_decode_attention_impl(self.cfg, self.bufs, layer, s_cur, q.data_ptr(), softmax_scale, out.data_ptr(),
                                       self.ws.data_ptr(), self.ws.numel(), self._stream(), impl)
         return out
+
+    def decode_step(self, layer: int, s_cur: int, k: torch.Tensor, v: torch.Tensor, q: torch.Tensor,
+                    softmax_scale: float, out: torch.Tensor = None) -> torch.Tensor:
+        """Append one token ([batch][1][n_kv][d] float16) and attend over s_cur + 1 tokens."""
+        assert k.dtype == torch.float16 and v.dtype == torch.float16 and q.dtype == torch.float16
+        assert k.is_contiguous() and v.is_contiguous() and q.is_contiguous() and k.shape[1] == 1
+        if out is None:
+            out = torch.empty(q.shape, dtype=torch.float32, device=self.device)
+        kvq.kvq_decode_step(self.cfg, self.bufs, layer, s_cur, k.data_ptr(), v.data_ptr(), q.data_ptr(), softmax_scale,
+                            out.data_ptr(), self.ws.data_ptr(), self.ws.numel(), self._stream())
+        return out

@@ -263,9 +263,15 @@ int32_t kvq_decode_num_splits(const kvq_config* cfg, int64_t s_cur) {
   return (int32_t)plan_splits(g, s_cur, KVQ_DECODE_MMA).n_split;
 }
 
-kvq_status kvq_decode_attention_impl(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur,
-                                     const void* q_f16, float softmax_scale, float* out, void* ws,
-                                     size_t ws_bytes, void* stream, kvq_decode_impl impl) {
+}  // extern "C"
+
+namespace {
+
+// Checks and launches decode attention over s_cur tokens; when k_new/v_new are given
+// (tensor-core kernel only) the kernel first appends token s_cur - 1 itself.
+kvq_status decode_launch(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur,
+                         const void* q_f16, float softmax_scale, float* out, void* ws, size_t ws_bytes, void* stream,
+                         kvq_decode_impl impl, const void* k_new, const void* v_new) {
   Geometry g;
   kvq_status st = kvq::make_geometry(cfg, &g);
   if (st != KVQ_OK) return st;
@@ -286,6 +292,11 @@ kvq_status kvq_decode_attention_impl(const kvq_config* cfg, const kvq_buffers* b
   p.v_codes = lp.v_codes;
   p.v_meta = lp.v_meta;
   p.q = static_cast<const __half*>(q_f16);
+  p.k_new = static_cast<const __half*>(k_new);
+  p.v_new = static_cast<const __half*>(v_new);
+  p.k_resid_w = lp.k_resid;
+  p.v_codes_w = lp.v_codes;
+  p.v_meta_w = lp.v_meta;
   p.out = out;
   p.err = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + wl.err_off);
   p.tickets = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + wl.tickets_off);
@@ -309,6 +320,7 @@ kvq_status kvq_decode_attention_impl(const kvq_config* cfg, const kvq_buffers* b
   p.v_codes_slice = g.v_codes_slice;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   const kvq_decode_impl use = impl == KVQ_DECODE_SIMT ? KVQ_DECODE_SIMT : KVQ_DECODE_MMA;
+  if (use == KVQ_DECODE_SIMT && (k_new || v_new)) return KVQ_ERR_UNSUPPORTED;
   const Plan pl = plan_splits(g, s_cur, use);
   p.n_split = (int)pl.n_split;
   p.chunk = pl.chunk;
@@ -317,6 +329,38 @@ kvq_status kvq_decode_attention_impl(const kvq_config* cfg, const kvq_buffers* b
   cudaError_t e = (use == KVQ_DECODE_SIMT) ? kvq::launch_decode_simt(p, g.bits, static_cast<cudaStream_t>(stream))
                                             : kvq::launch_decode_mma(p, g.bits, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+kvq_status kvq_decode_attention_impl(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur,
+                                     const void* q_f16, float softmax_scale, float* out, void* ws,
+                                     size_t ws_bytes, void* stream, kvq_decode_impl impl) {
+  return decode_launch(cfg, bufs, layer, s_cur, q_f16, softmax_scale, out, ws, ws_bytes, stream, impl, nullptr,
+                       nullptr);
+}
+
+kvq_status kvq_decode_step(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur,
+                           const void* k_f16, const void* v_f16, const void* q_f16, float softmax_scale, float* out,
+                           void* ws, size_t ws_bytes, void* stream) {
+  Geometry g;
+  kvq_status st = kvq::make_geometry(cfg, &g);
+  if (st != KVQ_OK) return st;
+  if ((st = check_buffers(bufs)) != KVQ_OK) return st;
+  if (layer < 0 || layer >= g.L || s_cur < 0) return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(k_f16) || !aligned16(v_f16)) return KVQ_ERR_INVALID_ARG;
+  if (s_cur + 1 > g.S_max) return KVQ_ERR_CAPACITY;
+  const int64_t T = s_cur + 1;
+  if (T % g.R_eff == 0) {  // the append fills a residual window: quantize it with the append kernels
+    st = kvq_quantize_append(cfg, bufs, layer, s_cur, 1, k_f16, v_f16, stream);
+    if (st != KVQ_OK) return st;
+    return decode_launch(cfg, bufs, layer, T, q_f16, softmax_scale, out, ws, ws_bytes, stream, KVQ_DECODE_AUTO,
+                         nullptr, nullptr);
+  }
+  return decode_launch(cfg, bufs, layer, T, q_f16, softmax_scale, out, ws, ws_bytes, stream, KVQ_DECODE_AUTO, k_f16,
+                       v_f16);
 }
 
 kvq_status kvq_decode_attention(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur,

@@ -36,6 +36,7 @@
 #include "kvq_common.cuh"
 #include "kvq_kernels.h"
 #include "kvq_merge.cuh"
+#include "kvq_quantizer.cuh"
 
 namespace kvq {
 namespace mma {
@@ -306,6 +307,22 @@ __global__ void __launch_bounds__(kWarps * 32, min_blocks<NT>()) decode_mma_kern
     bulk_g2s(smem_u32(st + St::KB + St::VB), vm_src + (size_t)i * St::VM, St::VM, bar);
     if (newgrp) bulk_g2s(smem_u32(st + St::KB + St::VB + St::VM), km_base + ((ts >> p.log2G) << 7), St::KM, bar);
   };
+  // Fused decode step: the CTA whose range holds the new token T-1 appends it first
+  // (value row quantized per group into its half of the pair row, key row into its
+  // residual slot), then makes those global writes visible to the bulk copies.
+  if (p.v_new != nullptr && t_begin <= T - 1 && T - 1 < t_end) {
+    if (warp == 0) {
+      const int t_new = T - 1;
+      const int64_t row = (int64_t)b * p.H + h;  // [B][1][H][d]
+      uint16_t* pair = reinterpret_cast<uint16_t*>(p.v_codes_w + slice * p.v_codes_slice + (int64_t)(t_new >> 1) * 2 * ROW);
+      quant::quantize_value_row<BITS>(p.v_new + row * kHeadDim, pair, t_new & 1,
+                                      p.v_meta_w + (slice * p.S_pad + t_new) * NVG, p.Gv, lane, smem);
+      const uint2 kv = *reinterpret_cast<const uint2*>(p.k_new + row * kHeadDim + 4 * lane);
+      *reinterpret_cast<uint2*>(p.k_resid_w + (slice * p.R_eff + t_new % p.R_eff) * kHeadDim + 4 * lane) = kv;
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
+    __syncthreads();
+  }
   if (lane == 0)
     for (int i = 0; i < min(NS, n_mine); ++i) issue(i, i);
 
@@ -420,7 +437,7 @@ __global__ void __launch_bounds__(kWarps * 32, min_blocks<NT>()) decode_mma_kern
           uint32_t kw[16];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const uint4 v = __ldg(rp + k);
+            const uint4 v = rp[k];  // plain load: the fused step may have written this row
             kw[4 * k] = v.x; kw[4 * k + 1] = v.y; kw[4 * k + 2] = v.z; kw[4 * k + 3] = v.w;
           }
 #pragma unroll

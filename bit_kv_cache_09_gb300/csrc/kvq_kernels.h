@@ -47,6 +47,13 @@ struct DecodeParams {
   const uint8_t* v_codes;
   const __half2* v_meta;
   const __half* q;  // [B][H*r][d]
+  // fused decode step (tensor-core kernel only): when k_new/v_new are set, the CTA that
+  // owns token T-1 first appends it (value quantized per group, key into the residual)
+  const __half* k_new;  // [B][1][H][d] or null
+  const __half* v_new;  // [B][1][H][d] or null
+  __half* k_resid_w;
+  uint8_t* v_codes_w;
+  __half2* v_meta_w;
   float* out;       // [B][H*r][d]
   uint32_t* err;      // error word: bit 0 = a wait for staged data timed out
   uint32_t* tickets;  // [B*H]

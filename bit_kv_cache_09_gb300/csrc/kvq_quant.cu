@@ -15,52 +15,12 @@
 
 #include "kvq_common.cuh"
 #include "kvq_kernels.h"
+#include "kvq_quantizer.cuh"
 
 namespace kvq {
 namespace {
 
-template <int BITS>
-struct Q {
-  static constexpr float qmin = -(float)(1 << (BITS - 1));
-  static constexpr float qmax = (float)((1 << (BITS - 1)) - 1);
-};
-
-// Group parameters from the (exact) binary32 min and max of binary16 inputs.
-template <int BITS>
-__device__ __forceinline__ void group_params(float xmin, float xmax, __half& s_h, __half& z_h, float& s, float& zp) {
-  if (xmax == xmin) {  // a constant group is widened to include 0
-    if (xmin > 0.0f) xmin = 0.0f;
-    if (xmax < 0.0f) xmax = 0.0f;
-  }
-  if (xmax == xmin) {
-    s_h = __float2half_rn(1.0f);  // all zeros: scale 1
-  } else {
-    const float range = __fsub_rn(xmax, xmin);
-    s_h = __float2half_ru(__fdiv_rn(range, __fsub_rn(Q<BITS>::qmax, Q<BITS>::qmin)));
-  }
-  s = __half2float(s_h);
-  float z = __fsub_rn(Q<BITS>::qmin, rintf(__fdiv_rn(xmin, s)));
-  z = fminf(fmaxf(z, -65504.0f), 65504.0f);
-  z_h = __float2half_rn(z);
-  zp = __half2float(z_h);
-}
-
-template <int BITS>
-__device__ __forceinline__ uint32_t quant_code(float x, float s, float zp) {
-  float q = __fadd_rn(rintf(__fdiv_rn(x, s)), zp);
-  q = fminf(fmaxf(q, Q<BITS>::qmin), Q<BITS>::qmax);
-  return (uint32_t)(int)__fsub_rn(q, Q<BITS>::qmin);
-}
-
-__device__ __forceinline__ void load4(const __half* p, float* x) {
-  const uint2 raw = *reinterpret_cast<const uint2*>(p);
-  const __half2 a = *reinterpret_cast<const __half2*>(&raw.x);
-  const __half2 b = *reinterpret_cast<const __half2*>(&raw.y);
-  x[0] = __low2float(a);
-  x[1] = __high2float(a);
-  x[2] = __low2float(b);
-  x[3] = __high2float(b);
-}
+using namespace quant;
 
 // Store the 4 codes of channels [4*lane, 4*lane+4) into a key row (natural order).
 template <int BITS>
@@ -72,12 +32,6 @@ __device__ __forceinline__ void store_k4(uint8_t* row, int lane, const uint32_t*
   } else {
     row[lane] = (uint8_t)(u[0] | (u[1] << 2) | (u[2] << 4) | (u[3] << 6));
   }
-}
-
-// Channel stored at value-row position p (inverse of pos(c) = 16*(c%8) + 2*(c/16) + (c/8)%2, d = 128).
-__device__ __forceinline__ int v_channel_of_pos(int p) {
-  const int g = p >> 4, i = p & 15;
-  return 16 * (i >> 1) + 8 * (i & 1) + g;
 }
 
 // ---------------------------------------------------------------------------
@@ -174,36 +128,9 @@ __global__ void __launch_bounds__(256) v_token_kernel(AppendParams p, int64_t n_
   const int b = (int)(bt / p.n_new);
   const int64_t slice = (int64_t)b * p.H + h;
 
-  float x[4];
-  load4(p.v_in + w * kHeadDim + 4 * lane, x);
-  float mn = fminf(fminf(x[0], x[1]), fminf(x[2], x[3]));
-  float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-  const int lanes_per_group = p.Gv / 4;  // 8, 16 or 32
-  for (int off = 1; off < lanes_per_group; off <<= 1) {
-    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-  }
-  __half s_h, z_h;
-  float s, zp;
-  group_params<BITS>(mn, mx, s_h, z_h, s, zp);
-  if (lane % lanes_per_group == 0) {
-    const int j = lane / lanes_per_group;
-    p.v_meta[(slice * p.S_pad + t) * p.n_vg + j] = __halves2half2(s_h, z_h);
-  }
-#pragma unroll
-  for (int e = 0; e < 4; ++e) codes_s[warp][4 * lane + e] = (uint8_t)quant_code<BITS>(x[e], s, zp);
-  __syncwarp();
-  // Assemble 16-bit units of the token's row (positions in stored order) and write
-  // them into the token's half of its pair row.
-  constexpr int PER_UNIT = 16 / BITS;
-  constexpr int UNITS = kHeadDim * BITS / 16;
   uint16_t* pair = reinterpret_cast<uint16_t*>(p.v_codes + slice * p.v_codes_slice + (t >> 1) * 2 * p.rowV);
-  for (int k = lane; k < UNITS; k += 32) {
-    uint32_t unit = 0;
-#pragma unroll
-    for (int i = 0; i < PER_UNIT; ++i) unit |= (uint32_t)codes_s[warp][v_channel_of_pos(k * PER_UNIT + i)] << (i * BITS);
-    pair[2 * k + (int)(t & 1)] = (uint16_t)unit;
-  }
+  quantize_value_row<BITS>(p.v_in + w * kHeadDim, pair, (int)(t & 1), p.v_meta + (slice * p.S_pad + t) * p.n_vg, p.Gv,
+                           lane, codes_s[warp]);
   // Keys of tokens past the last full residual window go to the residual.
   if (t >= p.A1) {
     const uint2 raw = *reinterpret_cast<const uint2*>(p.k_in + w * kHeadDim + 4 * lane);

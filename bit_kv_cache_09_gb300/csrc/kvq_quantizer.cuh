@@ -1,0 +1,107 @@
+// kvq_quantizer.cuh — the bit-exact affine quantizer shared by the append kernels and
+// the fused decode step (library-internal).
+//
+// The quantizer is the affine scheme of the page "KV Cache Quantization — 8-bit and
+// 4-bit", § Integer quantization in one screen. Every floating-point step is one
+// explicitly rounded binary32 intrinsic, so no compiler contraction can change a
+// result and codes, scales and zero points are reproducible bit for bit:
+//   s_h = binary16_round_up((x_max - x_min) / (q_max - q_min))
+//   zp  = clamp(q_min - rint(x_min / s_h), +-65504) -> binary16 (nearest even)
+//   u   = clamp(rint(x / s_h) + zp, q_min, q_max) - q_min
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "kvq_common.cuh"
+
+namespace kvq {
+namespace quant {
+
+template <int BITS>
+struct Q {
+  static constexpr float qmin = -(float)(1 << (BITS - 1));
+  static constexpr float qmax = (float)((1 << (BITS - 1)) - 1);
+};
+
+// Group parameters from the (exact) binary32 min and max of binary16 inputs.
+template <int BITS>
+__device__ __forceinline__ void group_params(float xmin, float xmax, __half& s_h, __half& z_h, float& s, float& zp) {
+  if (xmax == xmin) {  // a constant group is widened to include 0
+    if (xmin > 0.0f) xmin = 0.0f;
+    if (xmax < 0.0f) xmax = 0.0f;
+  }
+  if (xmax == xmin) {
+    s_h = __float2half_rn(1.0f);  // all zeros: scale 1
+  } else {
+    const float range = __fsub_rn(xmax, xmin);
+    s_h = __float2half_ru(__fdiv_rn(range, __fsub_rn(Q<BITS>::qmax, Q<BITS>::qmin)));
+  }
+  s = __half2float(s_h);
+  float z = __fsub_rn(Q<BITS>::qmin, rintf(__fdiv_rn(xmin, s)));
+  z = fminf(fmaxf(z, -65504.0f), 65504.0f);
+  z_h = __float2half_rn(z);
+  zp = __half2float(z_h);
+}
+
+template <int BITS>
+__device__ __forceinline__ uint32_t quant_code(float x, float s, float zp) {
+  float q = __fadd_rn(rintf(__fdiv_rn(x, s)), zp);
+  q = fminf(fmaxf(q, Q<BITS>::qmin), Q<BITS>::qmax);
+  return (uint32_t)(int)__fsub_rn(q, Q<BITS>::qmin);
+}
+
+__device__ __forceinline__ void load4(const __half* p, float* x) {
+  const uint2 raw = *reinterpret_cast<const uint2*>(p);
+  const __half2 a = *reinterpret_cast<const __half2*>(&raw.x);
+  const __half2 b = *reinterpret_cast<const __half2*>(&raw.y);
+  x[0] = __low2float(a);
+  x[1] = __high2float(a);
+  x[2] = __low2float(b);
+  x[3] = __high2float(b);
+}
+
+// Channel stored at value-row position p (inverse of pos(c) = 16*(c%8) + 2*(c/16) + (c/8)%2, d = 128).
+__device__ __forceinline__ int v_channel_of_pos(int p) {
+  const int g = p >> 4, i = p & 15;
+  return 16 * (i >> 1) + 8 * (i & 1) + g;
+}
+
+// One warp quantizes one value row (binary16, 128 channels; lane l holds channels
+// [4l, 4l+4)) per group of Gv channels, writes its (scale, zero point) pairs to
+// meta[0 .. d/Gv) and its codes, in stored-position order, into half `half_sel` of
+// the 16-bit units of its pair row. codes_s: 128 bytes of warp-private shared memory.
+template <int BITS>
+__device__ __forceinline__ void quantize_value_row(const __half* v_row, uint16_t* pair_row, int half_sel, __half2* meta,
+                                                   int Gv, int lane, uint8_t* codes_s) {
+  float x[4];
+  load4(v_row + 4 * lane, x);
+  float mn = fminf(fminf(x[0], x[1]), fminf(x[2], x[3]));
+  float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+  const int lanes_per_group = Gv / 4;  // 8, 16 or 32
+  for (int off = 1; off < lanes_per_group; off <<= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  }
+  __half s_h, z_h;
+  float s, zp;
+  group_params<BITS>(mn, mx, s_h, z_h, s, zp);
+  if (lane % lanes_per_group == 0) meta[lane / lanes_per_group] = __halves2half2(s_h, z_h);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) codes_s[4 * lane + e] = (uint8_t)quant_code<BITS>(x[e], s, zp);
+  __syncwarp();
+  constexpr int PER_UNIT = 16 / BITS;
+  constexpr int UNITS = kHeadDim * BITS / 16;
+  for (int k = lane; k < UNITS; k += 32) {
+    uint32_t unit = 0;
+#pragma unroll
+    for (int i = 0; i < PER_UNIT; ++i) unit |= (uint32_t)codes_s[v_channel_of_pos(k * PER_UNIT + i)] << (i * BITS);
+    pair_row[2 * k + half_sel] = (uint16_t)unit;
+  }
+  __syncwarp();
+}
+
+}  // namespace quant
+}  // namespace kvq

@@ -23,7 +23,7 @@ BUFFER_NAMES = ("k_codes", "k_meta", "k_resid", "v_codes", "v_meta")
 DECODE_AUTO, DECODE_SIMT, DECODE_MMA = 0, 1, 2
 EXPORTED = ("kvq_buffer_sizes", "kvq_quantize_append", "kvq_dequantize", "kvq_decode_workspace_size",
             "kvq_decode_attention", "kvq_decode_attention_impl", "kvq_decode_num_splits", "kvq_status_string",
-            "kvq_version", "kvq_decode_attention_noalloc")
+            "kvq_version", "kvq_decode_attention_noalloc", "kvq_decode_step")
 
 
 class KVQError(RuntimeError):
@@ -72,6 +72,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.kvq_decode_attention_noalloc.argtypes = [cfgp, bufp, ctypes.c_int32, ctypes.c_int64, vp, ctypes.c_float,
                                                    vp, vp]
         L.kvq_decode_attention_noalloc.restype = ctypes.c_int
+        L.kvq_decode_step.argtypes = [cfgp, bufp, ctypes.c_int32, ctypes.c_int64, vp, vp, vp, ctypes.c_float, vp, vp,
+                                      ctypes.c_size_t, vp]
+        L.kvq_decode_step.restype = ctypes.c_int
         L.kvq_decode_num_splits.argtypes = [cfgp, ctypes.c_int64]
         L.kvq_decode_num_splits.restype = ctypes.c_int32
         L.kvq_status_string.argtypes = [ctypes.c_int]
@@ -144,6 +147,12 @@ def kvq_decode_attention_impl(cfg: kvq_config, bufs: kvq_buffers, layer: int, s_
     _check("kvq_decode_attention_impl",
            load().kvq_decode_attention_impl(ctypes.byref(cfg), ctypes.byref(bufs), layer, s_cur, q_f16, softmax_scale,
                                             out, ws, ws_bytes, stream, impl))
+
+
+def kvq_decode_step(cfg: kvq_config, bufs: kvq_buffers, layer: int, s_cur: int, k_f16: int, v_f16: int, q_f16: int,
+                    softmax_scale: float, out: int, ws: int, ws_bytes: int, stream: int = 0) -> None:
+    _check("kvq_decode_step", load().kvq_decode_step(ctypes.byref(cfg), ctypes.byref(bufs), layer, s_cur, k_f16, v_f16,
+                                                     q_f16, softmax_scale, out, ws, ws_bytes, stream))
 
 
 def kvq_decode_attention_noalloc(cfg: kvq_config, bufs: kvq_buffers, layer: int, s_cur: int, q_f16: int,

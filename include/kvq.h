@@ -145,6 +145,18 @@ kvq_status kvq_decode_attention(const kvq_config* cfg, const kvq_buffers* bufs, 
                                 const void* q_f16, float softmax_scale, float* out, void* ws, size_t ws_bytes,
                                 void* stream);
 
+/* One decode step of one layer: exactly kvq_quantize_append(cfg, bufs, layer, s_cur, 1,
+ * k_f16, v_f16, stream) followed by kvq_decode_attention over s_cur + 1 tokens, in one
+ * kernel launch when the new token does not fill a residual window (the CTA whose
+ * token range holds the new token appends it before reading its stages), and in the
+ * two launches otherwise. k_f16, v_f16: [batch][1][n_kv_heads][d_head] binary16
+ * (16-byte aligned). Same cache state and outputs as the two calls ("KV Cache
+ * Quantization — 8-bit and 4-bit", § Decode is memory-bound, so smaller is also
+ * faster: one pass over the cache per step). */
+kvq_status kvq_decode_step(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur,
+                           const void* k_f16, const void* v_f16, const void* q_f16, float softmax_scale, float* out,
+                           void* ws, size_t ws_bytes, void* stream);
+
 /* Kernel choice for kvq_decode_attention_impl. AUTO is what kvq_decode_attention uses. */
 typedef enum {
   KVQ_DECODE_AUTO = 0,

@@ -161,3 +161,31 @@ def test_layers_are_independent():
     g = cache.buffer("k_codes")
     n = g.numel() // 3
     assert not g[n:2 * n].any()  # layer 1 untouched
+
+
+@pytest.mark.parametrize("bits,G,Gv,R,r", [(8, 128, 128, 0, 4), (4, 128, 64, 128, 4), (2, 32, 32, 128, 4),
+                                          (4, 128, 128, 128, 8), (4, 64, 32, 256, 3)])
+def test_fused_decode_step(bits, G, Gv, R, r):
+    """kvq_decode_step (append fused into the attention launch) leaves the same cache
+    state as the oracle and gives the same outputs as the two separate calls, across a
+    residual flush (where it takes the two-launch path)."""
+    R_eff = R if R > 0 else G
+    S = 2 * R_eff + 7
+    steps = R_eff - 7 + 4
+    w = small_workload(bits=bits, G=G, Gv=Gv, R=R, r=r, B=3, H=2, S=S, steps=steps, seed=2000 + bits + r)
+    fused = QuantizedKVCache.for_workload(w)
+    split = QuantizedKVCache.for_workload(w)
+    k_host, v_host = host_layer_inputs(w, 0, 0, w.max_seq)
+    for c in (fused, split):
+        c.append(0, 0, _dev(k_host[:, :S]), _dev(v_host[:, :S]))
+    for s in range(steps):
+        T = S + s
+        q_host = synth.gen_q(w.seed, 0, range(w.batch), T, w.n_q, w.d_head)
+        kd, vd, qd = _dev(k_host[:, T:T + 1]), _dev(v_host[:, T:T + 1]), _dev(q_host)
+        out_f = fused.decode_step(0, T, kd, vd, qd, softmax_scale(w))
+        split.append(0, T, kd, vd)
+        out_s = split.attention(0, T + 1, qd, softmax_scale(w))
+        assert torch.equal(out_f, out_s), (s, (out_f - out_s).abs().max().item())
+        if s in (0, 1, steps - 5, steps - 4, steps - 1):
+            _check_all_slices(fused, w, 0, T + 1, k_host, v_host)
+            _check_attention(fused, w, 0, T + 1, k_host, v_host, q_host, kvq.DECODE_AUTO)
