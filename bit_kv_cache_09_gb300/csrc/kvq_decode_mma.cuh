@@ -284,6 +284,7 @@ __global__ void __launch_bounds__(kWarps * 32, min_blocks<NT>()) decode_mma_kern
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncwarp();
+  pdl_wait();  // everything above touched shared memory only
 
   // sources of the warp's first iteration; iteration i adds 32*i tokens
   const uint8_t* k_src = p.k_codes + slice * p.k_codes_slice + (int64_t)ts0 * ROW;
@@ -560,6 +561,7 @@ __global__ void __launch_bounds__(kWarps * 32, min_blocks<NT>()) decode_mma_kern
     }
   }
 
+  pdl_allow_dependents();  // the next kernel of the stream may start its prologue
   if (failed_at >= 0) {
     // a stage never completed: flag it and drain (bounded) what is still in flight
     if (lane == 0) atomicOr(p.err, 1u);
@@ -716,13 +718,15 @@ cudaError_t launch_cfg(const DecodeParams& p, cudaStream_t stream) {
   cfg.blockDim = dim3(kWarps * 32, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)p.cluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, kern, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -71,6 +71,28 @@ struct DecodeParams {
   float scale_log2;   // softmax_scale * log2(e)
 };
 
+// Programmatic dependent launch: a kernel launched with the attribute may start while
+// the previous kernel of the stream finishes; it runs pdl_wait() before touching any
+// global memory, which blocks until that kernel has completed and its writes are visible.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 cudaError_t launch_append(const AppendParams& p, int bits, cudaStream_t stream);
 cudaError_t launch_dequant(const DequantParams& p, int bits, cudaStream_t stream);
 cudaError_t launch_decode_simt(const DecodeParams& p, int bits, cudaStream_t stream);

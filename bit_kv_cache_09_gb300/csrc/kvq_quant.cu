@@ -42,6 +42,8 @@ __device__ __forceinline__ void store_k4(uint8_t* row, int lane, const uint32_t*
 template <int BITS, int G>
 __global__ void __launch_bounds__(256) k_group_kernel(AppendParams p) {
   constexpr int PER_WARP = G / 8;
+  pdl_wait();
+  pdl_allow_dependents();
   const int h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t g = p.group0 + blockIdx.x;
@@ -121,6 +123,8 @@ __global__ void __launch_bounds__(256) v_token_kernel(AppendParams p, int64_t n_
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t w = (int64_t)blockIdx.x * 8 + warp;
   __shared__ uint8_t codes_s[8][kHeadDim];
+  pdl_wait();
+  pdl_allow_dependents();
   if (w >= n_rows) return;  // whole warps only: the warp-level code below stays converged
   const int h = (int)(w % p.H);
   const int64_t bt = w / p.H;
@@ -187,14 +191,17 @@ template <int BITS>
 cudaError_t launch_append_bits(const AppendParams& p, cudaStream_t stream) {
   if (p.n_groups > 0) {
     dim3 grid((unsigned)p.n_groups, (unsigned)p.H, (unsigned)p.B);
+    cudaError_t e;
     switch (p.G) {
-      case 32: k_group_kernel<BITS, 32><<<grid, 256, 0, stream>>>(p); break;
-      case 64: k_group_kernel<BITS, 64><<<grid, 256, 0, stream>>>(p); break;
-      default: k_group_kernel<BITS, 128><<<grid, 256, 0, stream>>>(p); break;
+      case 32: e = launch_pdl(k_group_kernel<BITS, 32>, grid, dim3(256), 0, stream, p); break;
+      case 64: e = launch_pdl(k_group_kernel<BITS, 64>, grid, dim3(256), 0, stream, p); break;
+      default: e = launch_pdl(k_group_kernel<BITS, 128>, grid, dim3(256), 0, stream, p); break;
     }
+    if (e != cudaSuccess) return e;
   }
   const int64_t rows = (int64_t)p.B * p.n_new * p.H;
-  v_token_kernel<BITS><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(p, rows);
+  cudaError_t e = launch_pdl(v_token_kernel<BITS>, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, stream, p, rows);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
