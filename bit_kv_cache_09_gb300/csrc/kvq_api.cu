@@ -123,20 +123,25 @@ Plan plan_splits(const Geometry& g, int64_t T, kvq_decode_impl impl) {
   const int64_t by_len = (T + align - 1) / align;
   if (max_k > by_len) max_k = by_len;
   if (max_k < 1) max_k = 1;
-  int64_t k = 1;
-  double best_eff = 0.0;
-  for (int64_t c = 1; c <= max_k; ++c) {
-    const int64_t ctas = units * c;
-    const int64_t waves = (ctas + slots - 1) / slots;
-    const double eff = (double)ctas / (double)(waves * slots);
-    if (eff > best_eff + 1e-9) {
-      best_eff = eff;
-      k = c;
+  // Cost model: the CTAs of a split run in rounds of `slots` co-resident CTAs; a round
+  // lasts as long as one CTA: a fixed cost (prologue, pipeline fill, merge; about four
+  // loop iterations of a warp, measured) plus its loop iterations (each of the 4 warps
+  // takes 32 tokens per iteration). Ties go to fewer splits.
+  const int64_t per_it = 128;
+  const int64_t fixed_it = 4;
+  int64_t best_cost = -1, best_chunk = align;
+  for (int64_t k = 1; k <= max_k; ++k) {
+    int64_t c = (T + k - 1) / k;
+    c = (c + align - 1) / align * align;
+    const int64_t n = (T + c - 1) / c;
+    const int64_t rounds = (units * n + slots - 1) / slots;
+    const int64_t cost = rounds * (fixed_it + (c + per_it - 1) / per_it);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best_chunk = c;
     }
-    if (eff >= 0.92) break;
   }
-  int64_t c = (T + k - 1) / k;
-  c = (c + align - 1) / align * align;
+  const int64_t c = best_chunk;
   pl.n_split = (T + c - 1) / c;
   pl.chunk = c;
   pl.cluster = 1;

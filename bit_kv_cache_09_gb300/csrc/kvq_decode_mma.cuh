@@ -67,6 +67,45 @@ __device__ __forceinline__ float ex2(float x) {
 
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
+// Byte permute of two words (selector nibbles 0..7 pick bytes of {b, a}).
+__device__ __forceinline__ uint32_t prmt2(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// Packed binary16 arithmetic with one IEEE rounding each (.rn keeps the compiler from
+// contracting a product into a later add).
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t hmax2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// a*b split into binary16 halves: hi = fl(a*b), lo = fl(a*b - hi) (the residual is exact
+// when it is representable, so hi + lo carries ~22 bits of the product).
+__device__ __forceinline__ uint32_t hneg2(uint32_t a) {
+  uint32_t d;
+  asm("neg.f16x2 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+__device__ __forceinline__ void hmul2_split(uint32_t a, uint32_t b, uint32_t& hi, uint32_t& lo) {
+  hi = hmul2(a, b);
+  lo = hfma2(a, b, hneg2(hi));
+}
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }  // e in [-126, 127]
+
+constexpr uint32_t kOne2 = 0x3C003C00u;  // half2(1, 1)
+
 // hi = binary16(x), lo = binary16(x - hi) for a pair, packed as half2 bit patterns.
 __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
   const __half2 h = __floats2half2_rn(x0, x1);
@@ -104,6 +143,13 @@ __device__ __forceinline__ constexpr float k_scale(int pi) {
   return BITS == 8 ? 1.0f
                    : (BITS == 4 ? (((pi & 3) & 1) ? 16.0f : 1.0f)
                                 : (float)(1 << (2 * ((pi & 7) < 5 ? (pi & 7) : (pi & 7) - 5))));
+}
+
+// half2 bit pattern of k_scale(pi) * 2^-8 (a normal binary16 power of two).
+template <int BITS>
+__device__ __forceinline__ constexpr uint32_t kc_bits(int pi) {
+  const int sh = BITS == 8 ? 0 : (BITS == 4 ? 4 * (pi & 1) : 2 * ((pi & 7) < 5 ? (pi & 7) : (pi & 7) - 5));
+  return (uint32_t)(sh + 7) << 10 | (uint32_t)(sh + 7) << 26;
 }
 
 // Local channel indices (within the lane's 32 channels) of key pair pi.
@@ -147,7 +193,7 @@ struct Stage {
   static constexpr int VM = 32 * 4 * NVG;         // value meta of 32 tokens
   static constexpr int KM = 512;                  // one key group's meta
   static constexpr int BYTES = KB + VB + VM + KM;
-  static constexpr int NS = BITS == 8 ? 3 : (BITS == 4 ? 2 : 3);
+  static constexpr int NS = BITS == 2 ? 3 : 2;
   static constexpr int WARP_BYTES = NS * BYTES;
   // the stage rings are reused after the loop for the merges (at most 24 KB + scratch)
   static constexpr int kEpilogueBytes = 24576 + 4 * kMergeScratchFloats;
@@ -258,6 +304,11 @@ __global__ void __launch_bounds__(kWarps * 32, min_blocks<NT>()) decode_mma_kern
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bars[kWarps][NS];
   __shared__ __align__(16) float q_s[kMaxGqa][kHeadDim];
+  // query row i in key-pair order of lane chunk c, pre-divided by k_scale and scaled
+  // by 2^qe_s[i] (so that |entry| < 2^8), as binary16 pairs
+  __shared__ __align__(16) uint32_t q2_s[kMaxGqa][4][16];
+  __shared__ int qe_s[kMaxGqa];
+  __shared__ __align__(16) uint32_t qa_s[kWarps][(NT == 1) ? 16 : 32][36];  // padded rows: no bank conflicts
 
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -331,6 +382,22 @@ __global__ void __launch_bounds__(kWarps * 32, min_blocks<NT>()) decode_mma_kern
   for (int idx = threadIdx.x; idx < r * kHeadDim; idx += kWarps * 32)
     q_s[idx >> 7][idx & 127] = __half2float(p.q[qrow0 * kHeadDim + idx]);
   __syncthreads();
+  // per-row power-of-two normalisation: qmax * 2^qe in [2^7, 2^8)
+  for (int i = warp; i < r; i += kWarps) {
+    float a = fmaxf(fmaxf(fabsf(q_s[i][lane]), fabsf(q_s[i][lane + 32])),
+                    fmaxf(fabsf(q_s[i][lane + 64]), fabsf(q_s[i][lane + 96])));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    if (lane == 0) qe_s[i] = a > 0.0f ? 7 - (((__float_as_int(a) >> 23) & 0xFF) - 127) : 0;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < r * 64; idx += kWarps * 32) {
+    const int i = idx >> 6, c = (idx >> 4) & 3, pi = idx & 15;
+    const float f = pow2f(qe_s[i]) / k_scale<BITS>(pi);  // exact: powers of two
+    q2_s[i][c][pi] = h2_bits(__floats2half2_rn(q_s[i][32 * c + k_pair_ca<BITS>(pi)] * f,
+                                               q_s[i][32 * c + k_pair_cb<BITS>(pi)] * f));
+  }
+  __syncthreads();
 
   // online softmax state of query qi (identical in the 4 lanes of row g)
   float m_run = -__int_as_float(0x7f800000), l_run = 0.0f;
@@ -341,11 +408,24 @@ __global__ void __launch_bounds__(kWarps * 32, min_blocks<NT>()) decode_mma_kern
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) o[mt][nt][e] = 0.0f;
-  float beta[NVG];  // zero-point sums per value group
+  // zero-point sums per value group on the tensor cores: in an extra PV tile rows 0..7
+  // are ones and rows 8..15 the tokens' zero points, so every lane accumulates
+  // sum_t w_t (registers 0, 1) and sum_t zp_t w_t (registers 2, 3) of its two columns
+  float bacc[NVG][NT][4];
 #pragma unroll
-  for (int k = 0; k < NVG; ++k) beta[k] = 0.0f;
+  for (int k = 0; k < NVG; ++k)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) bacc[k][nt][e] = 0.0f;
+  const int qe_mine = qe_s[qi];
 
-  uint32_t qa[8][4];  // QK A fragments of the current key group (or of the raw query for residual keys)
+  // QK A fragments of the current key group (or of the raw query for residual keys) in
+  // shared memory, one padded row per (query, lane chunk): word 4ks + e is fragment
+  // register e of k-step ks. With r <= 4 the lanes g and g + 4 share a row and each
+  // computes half of it (k-steps 4h .. 4h + 3, h = g / 4).
+  uint32_t* qa_row = &qa_s[warp][(NT == 1) ? ((g & 3) * 4 + j) : lane][0];
+  const int hh = (NT == 1) ? (g >> 2) : 0;  // first half this lane folds
   float qscale = 0.0f, qbias = 0.0f;
   bool resid_frags = false;
   const float* qrow = &q_s[qi][32 * j];
@@ -363,43 +443,91 @@ __global__ void __launch_bounds__(kWarps * 32, min_blocks<NT>()) decode_mma_kern
     if (ts < Tq) {
       if (i == 0 || (ts & (p.G - 1)) == 0) {
         resid_frags = false;
-        // folded query of this group: x_c = q_c * s_c, bias = sum_c x_c (q_min - zp_c)
+        // Folded query of this key group, x_c = q_c s_c, as binary16 hi/lo pairs computed
+        // with packed half arithmetic: q2_s holds q_c 2^qe / k_scale, the scales are
+        // scaled by 2^Es so that the largest is in [2^7, 2^8) (no overflow, products
+        // below 2^16); hi = fl(q s), lo = fl(q s - hi). Pairs 8h .. 8h + 7 of a lane
+        // chunk cover its local channels [16h, 16h + 16) for every code width.
+        constexpr int NH = (NT == 1) ? 1 : 2;  // halves folded by this lane
         const uint4* mp = reinterpret_cast<const uint4*>(st + St::KB + St::VB + St::VM) + 8 * j;
-        float x[32];
-        float amax = 0.0f, bias = 0.0f;
+        uint32_t mw[NH][16];  // (scale, zero point) of the lane's channels of each half it folds
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint4 v = mp[k];
-          const float4 qv = reinterpret_cast<const float4*>(qrow)[k];
-          const float qq[4] = {qv.x, qv.y, qv.z, qv.w};
-          const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
+        for (int u = 0; u < NH; ++u)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 sz = __half22float2(*reinterpret_cast<const __half2*>(&ws[e]));
-            const int c = 4 * k + e;
-            x[c] = qq[e] * sz.x;
-            bias = fmaf(x[c], qmin - sz.y, bias);
-            amax = fmaxf(amax, fabsf(x[c]));
+          for (int k = 0; k < 4; ++k) {
+            const uint4 v = mp[4 * (hh + u) + k];
+            mw[u][4 * k] = v.x; mw[u][4 * k + 1] = v.y; mw[u][4 * k + 2] = v.z; mw[u][4 * k + 3] = v.w;
+          }
+        uint32_t s2[NH][8];
+        uint32_t mx = 0u;
+#pragma unroll
+        for (int u = 0; u < NH; ++u) {
+#pragma unroll
+          for (int pl = 0; pl < 8; ++pl)
+            s2[u][pl] = prmt2(mw[u][k_pair_ca<BITS>(pl)], mw[u][k_pair_cb<BITS>(pl)], 0x5410u);
+          const uint32_t m01 = hmax2(s2[u][0], s2[u][1]), m23 = hmax2(s2[u][2], s2[u][3]);
+          const uint32_t m45 = hmax2(s2[u][4], s2[u][5]), m67 = hmax2(s2[u][6], s2[u][7]);
+          const uint32_t m = hmax2(hmax2(m01, m23), hmax2(m45, m67));
+          mx = (u == 0) ? m : hmax2(mx, m);
+        }
+        if (NT == 1) mx = hmax2(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        mx = hmax2(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = hmax2(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        // scales are positive: the larger bit pattern is the larger value
+        const uint32_t smax = max(mx & 0xFFFFu, mx >> 16);
+        const int Es = min(15, 7 - (max((int)(smax >> 10), 1) - 15));  // in [-8, 15]
+        const uint32_t pe = (uint32_t)(Es + 15) << 10;
+        const uint32_t p2 = pe | (pe << 16);  // half2(2^Es, 2^Es)
+        // bias = sum_c x_c (q_min - zp_c) on the tensor cores, from the fragments just
+        // computed: an extra key tile whose column 0 is k_scale 2^-8 (ones, lane g = 0)
+        // and column 1 zp_c k_scale 2^-8 (lane g = 1). With r <= 4, rows g < 4 run on
+        // the first half of the channels and rows g >= 4 on the second in the same MMA,
+        // so lane g = 5 supplies the second half's zero points in column 5 and a query's
+        // bias adds rows q and q + 4.
+        float bt[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        const uint32_t ones_col = (g == 0) ? kOne2 : 0u;
+        const uint32_t zsel = (g == 1 || (NT == 1 && g == 5)) ? kOne2 : 0u;
+#pragma unroll
+        for (int u = 0; u < NH; ++u) {
+          const int h = hh + u;
+          const uint4* qp = reinterpret_cast<const uint4*>(&q2_s[qi][j][8 * h]);
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {  // k-steps 4h + 2k, 4h + 2k + 1
+            const uint4 qv = qp[k];
+            const uint32_t qq[4] = {qv.x, qv.y, qv.z, qv.w};
+            uint32_t f[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) hmul2_split(qq[e], hmul2(s2[u][4 * k + e], p2), f[2 * e], f[2 * e + 1]);
+            reinterpret_cast<uint4*>(qa_row)[4 * h + 2 * k] = make_uint4(f[0], f[1], f[2], f[3]);
+            reinterpret_cast<uint4*>(qa_row)[4 * h + 2 * k + 1] = make_uint4(f[4], f[5], f[6], f[7]);
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+              uint32_t bz[2];
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int pl = 4 * k + 2 * kk + e;
+                const uint32_t z2 = prmt2(mw[u][k_pair_ca<BITS>(pl)], mw[u][k_pair_cb<BITS>(pl)], 0x7632u);
+                bz[e] = hmul2(hfma2(z2, zsel, ones_col), kc_bits<BITS>(pl));
+              }
+              mma16816(bt, f[4 * kk], f[4 * kk + 1], f[4 * kk + 2], f[4 * kk + 3], bz[0], bz[1]);
+            }
           }
         }
-        bias += __shfl_xor_sync(0xffffffffu, bias, 1);
-        bias += __shfl_xor_sync(0xffffffffu, bias, 2);
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        // power-of-two normalisation: amax * 2^E in [2^14, 2^15)
-        int E = 0;
-        if (amax > 0.0f) E = 14 - (((__float_as_int(amax) >> 23) & 0xFF) - 127);
-        E = max(-100, min(100, E));
-        const float up = __int_as_float((127 + E) << 23);    // 2^E, exact
-        const float down = __int_as_float((127 - E) << 23);  // 2^-E, exact
-        qscale = kTwo24 * down * p.scale_log2;
-        qbias = bias * p.scale_log2;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const float u0 = up / k_scale<BITS>(2 * ks), u1 = up / k_scale<BITS>(2 * ks + 1);
-          split2(x[k_pair_ca<BITS>(2 * ks)] * u0, x[k_pair_cb<BITS>(2 * ks)] * u0, qa[ks][0], qa[ks][1]);
-          split2(x[k_pair_ca<BITS>(2 * ks + 1)] * u1, x[k_pair_cb<BITS>(2 * ks + 1)] * u1, qa[ks][2], qa[ks][3]);
+        __syncwarp();
+        // lanes j = 0 hold columns 0 and 1 of rows g (hi) and g + 8 (lo), lanes j = 2 column 5
+        const float t0 = bt[0] + bt[2], tz = bt[1] + bt[3];
+        float bsum;
+        if (NT == 1) {
+          const int q = g & 3;
+          const float ones = __shfl_sync(0xffffffffu, t0, 4 * q) + __shfl_sync(0xffffffffu, t0, 4 * q + 16);
+          const float zz = __shfl_sync(0xffffffffu, tz, 4 * q) + __shfl_sync(0xffffffffu, tz, 4 * q + 18);
+          bsum = qmin * ones - zz;
+        } else {
+          bsum = __shfl_sync(0xffffffffu, qmin * t0 - tz, lane & ~3);
         }
+        const int E = qe_mine + Es;
+        qscale = pow2f(24 - E) * p.scale_log2;
+        qbias = bsum * pow2f(8 - E) * p.scale_log2;
       }
       uint32_t kw[2][2][CW];
 #pragma unroll
@@ -407,24 +535,26 @@ __global__ void __launch_bounds__(kWarps * 32, min_blocks<NT>()) decode_mma_kern
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) lds_chunk<BITS>(st + (16 * hf + 8 * nt + g) * ROW + j * (ROW / 4), kw[hf][nt]);
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks)
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint4 a = reinterpret_cast<const uint4*>(qa_row)[ks];
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt)
-            mma16816(acc[hf][nt], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], k_pair<BITS>(kw[hf][nt], 2 * ks),
+            mma16816(acc[hf][nt], a.x, a.y, a.z, a.w, k_pair<BITS>(kw[hf][nt], 2 * ks),
                      k_pair<BITS>(kw[hf][nt], 2 * ks + 1));
+      }
     } else {
       if (!resid_frags) {
         resid_frags = true;  // raw query fragments for binary16 residual keys: natural channel pairs
+        __syncwarp();
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const float4 qv = reinterpret_cast<const float4*>(qrow)[ks];
-          qa[ks][0] = h2_bits(__floats2half2_rn(qv.x, qv.y));
-          qa[ks][2] = h2_bits(__floats2half2_rn(qv.z, qv.w));
-          qa[ks][1] = 0u;
-          qa[ks][3] = 0u;
+          reinterpret_cast<uint4*>(qa_row)[ks] = make_uint4(h2_bits(__floats2half2_rn(qv.x, qv.y)), 0u,
+                                                            h2_bits(__floats2half2_rn(qv.z, qv.w)), 0u);
         }
+        __syncwarp();
         qscale = p.scale_log2;
         qbias = 0.0f;
       }
@@ -442,8 +572,10 @@ __global__ void __launch_bounds__(kWarps * 32, min_blocks<NT>()) decode_mma_kern
             kw[4 * k] = v.x; kw[4 * k + 1] = v.y; kw[4 * k + 2] = v.z; kw[4 * k + 3] = v.w;
           }
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            mma16816(acc[hf][nt], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], kw[2 * ks], kw[2 * ks + 1]);
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint4 a = reinterpret_cast<const uint4*>(qa_row)[ks];
+            mma16816(acc[hf][nt], a.x, a.y, a.z, a.w, kw[2 * ks], kw[2 * ks + 1]);
+          }
         }
     }
     sc = qscale;
@@ -476,8 +608,6 @@ __global__ void __launch_bounds__(kWarps * 32, min_blocks<NT>()) decode_mma_kern
     if (__any_sync(0xffffffffu, m_new > m_run)) {
       const float alpha = ex2(m_run - m_new);  // 0 on the first iteration (m_run = -inf)
       l_run *= alpha;
-#pragma unroll
-      for (int k = 0; k < NVG; ++k) beta[k] *= alpha;
       // PV column n holds the query of row n: alphas of columns 2j, 2j+1 live in rows 2j, 2j+1
       const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * j);
       const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * j + 4);
@@ -486,6 +616,12 @@ __global__ void __launch_bounds__(kWarps * 32, min_blocks<NT>()) decode_mma_kern
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           o[mt][nt][0] *= a0; o[mt][nt][1] *= a1; o[mt][nt][2] *= a0; o[mt][nt][3] *= a1;
+        }
+#pragma unroll
+      for (int k = 0; k < NVG; ++k)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          bacc[k][nt][0] *= a0; bacc[k][nt][1] *= a1; bacc[k][nt][2] *= a0; bacc[k][nt][3] *= a1;
         }
       m_run = m_new;
     }
@@ -508,26 +644,33 @@ __global__ void __launch_bounds__(kWarps * 32, min_blocks<NT>()) decode_mma_kern
       __half2 mlo[2 * NVG], mhi[2 * NVG];  // tokens (2j, 2j+1) and (8+2j, 9+2j)
       lds_vmeta<NVG>(vms + (2 * j) * NVG, mlo);
       lds_vmeta<NVG>(vms + (8 + 2 * j) * NVG, mhi);
+      // p of the token pairs (2j, 2j+1) and (8+2j, 9+2j) as binary16 hi/lo halves
+      uint32_t ph[2], pl[2];
+      split2(pr[hf][0], pr[hf][1], ph[0], pl[0]);
+      split2(pr[hf][2], pr[hf][3], ph[1], pl[1]);
       uint32_t bf[NVG][NT][2];
 #pragma unroll
       for (int vg = 0; vg < NVG; ++vg) {
-        const float2 z0 = __half22float2(mlo[vg]), z1 = __half22float2(mlo[NVG + vg]);
-        const float2 z2 = __half22float2(mhi[vg]), z3 = __half22float2(mhi[NVG + vg]);
-        const float w0 = pr[hf][0] * z0.x, w1 = pr[hf][1] * z1.x, w2 = pr[hf][2] * z2.x, w3 = pr[hf][3] * z3.x;
-        beta[vg] = fmaf(w0, qmin - z0.y, beta[vg]);
-        beta[vg] = fmaf(w1, qmin - z1.y, beta[vg]);
-        beta[vg] = fmaf(w2, qmin - z2.y, beta[vg]);
-        beta[vg] = fmaf(w3, qmin - z3.y, beta[vg]);
-        uint32_t hi0, lo0, hi1, lo1;
-        split2(w0, w1, hi0, lo0);
-        split2(w2, w3, hi1, lo1);
-        if (NT == 1) {
-          bf[vg][0][0] = lo_lane ? lo0 : hi0;
-          bf[vg][0][1] = lo_lane ? lo1 : hi1;
-        } else {
-          bf[vg][0][0] = hi0; bf[vg][0][1] = hi1;
-          bf[vg][NT - 1][0] = lo0; bf[vg][NT - 1][1] = lo1;
+        uint32_t za[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const uint32_t m0 = h2_bits(e ? mhi[vg] : mlo[vg]), m1 = h2_bits(e ? mhi[NVG + vg] : mlo[NVG + vg]);
+          // weights w = p * s with packed half arithmetic: hi = fl(p_hi s),
+          // lo = fl(p_lo s + fl(p_hi s - hi))
+          const uint32_t s2 = prmt2(m0, m1, 0x5410u);
+          uint32_t whi, wlo;
+          hmul2_split(ph[e], s2, whi, wlo);
+          wlo = hfma2(pl[e], s2, wlo);
+          if (NT == 1) {
+            bf[vg][0][e] = lo_lane ? wlo : whi;
+          } else {
+            bf[vg][0][e] = whi;
+            bf[vg][NT - 1][e] = wlo;
+          }
+          za[e] = prmt2(m0, m1, 0x7632u);  // zero points of the token pair
         }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma16816(bacc[vg][nt], kOne2, za[0], kOne2, za[1], bf[vg][nt][0], bf[vg][nt][1]);
       }
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
@@ -578,16 +721,25 @@ __global__ void __launch_bounds__(kWarps * 32, min_blocks<NT>()) decode_mma_kern
   float* beta_s = l_s + kWarps * kMaxGqa;  // [kWarps][kMaxGqa][NVG]
   l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
   l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
-#pragma unroll
-  for (int k = 0; k < NVG; ++k) {
-    beta[k] += __shfl_xor_sync(0xffffffffu, beta[k], 1);
-    beta[k] += __shfl_xor_sync(0xffffffffu, beta[k], 2);
-  }
   if (j == 0 && g < r) {  // row g holds query g for g < r
     m_s[warp * kMaxGqa + g] = m_run;
     l_s[warp * kMaxGqa + g] = l_run;
+  }
+  // zero-point terms beta = q_min * sum_t w_t - sum_t zp_t w_t of queries 2j and 2j+1
+  // (columns 2j, 2j+1); NT == 1 adds the lo columns 4..7 (lanes j + 2), NT == 2 the lo tile
 #pragma unroll
-    for (int k = 0; k < NVG; ++k) beta_s[(warp * kMaxGqa + g) * NVG + k] = beta[k];
+  for (int k = 0; k < NVG; ++k) {
+    float t[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      t[e] = bacc[k][0][e];
+      if (NT == 2) t[e] += bacc[k][NT - 1][e];
+      else t[e] += __shfl_xor_sync(0xffffffffu, t[e], 2);
+    }
+    if (g == 0 && (NT == 2 || j < 2)) {
+      if (2 * j < r) beta_s[(warp * kMaxGqa + 2 * j) * NVG + k] = qmin * t[0] - t[2];
+      if (2 * j + 1 < r) beta_s[(warp * kMaxGqa + 2 * j + 1) * NVG + k] = qmin * t[1] - t[3];
+    }
   }
   // PV columns: NT == 1: cols 0..3 hi / 4..7 lo of queries 0..3; NT == 2: tile 0 hi, tile 1 lo of queries 0..7
 #pragma unroll
