@@ -11,22 +11,28 @@
 // run on the tensor cores:
 //
 //   scores  S[i][t] = sum_c (q_ic s_gc) u_tc + sum_c q_ic s_gc (q_min - zp_gc)
-//           A = folded query (rows: query heads, hi and lo binary16 halves of a
-//               per-row power-of-two-normalised binary32 value), B = key codes.
+//           A = folded query x = q*s (rows: query heads, hi and lo binary16 halves,
+//               formed with packed half multiply/fma after power-of-two scaling of
+//               the query row and of the group's scales), B = key codes. The bias
+//               term is one more MMA tile per key group whose B columns hold ones
+//               and the group's zero points.
 //   output  O[c][i] = sum_t u_tc (p_it s_tj) + sum_t p_it s_tj (q_min - zp_tj)
-//           A = value codes (rows: channels), B = weights p*s (hi and lo halves).
+//           A = value codes (rows: channels), B = weights w = p*s (hi and lo halves,
+//           packed half arithmetic). The zero-point sums sum_t w and sum_t zp_t w run
+//           as one more MMA tile per value group (A rows: ones and zero points).
 //
 // Codes enter the MMA as binary16 subnormals: the 16-bit pattern u IS the value
 // u * 2^-24, so unpacking is a mask (and a byte permute for 8-bit codes), and the
-// 2^24 factor is restored on the binary32 results. The zero-point sums are plain
-// binary32 FMAs. Packed layouts are chosen so that every lane's fragment comes from
-// one contiguous chunk (see include/kvq.h): key row chunk j of a lane holds channels
-// [32j, 32j+32); value pair-row chunk g holds channels {16m + g, 16m + g + 8}.
+// 2^24 factor is restored on the binary32 results. Packed layouts are chosen so that
+// every lane's fragment comes from one contiguous chunk (see include/kvq.h): key row
+// chunk j of a lane holds channels [32j, 32j+32); value pair-row chunk g holds
+// channels {16m + g, 16m + g + 8}.
 //
-// Staging: every warp streams its own contiguous run of 16-token slabs through a
-// ring of NS shared-memory stages filled by bulk asynchronous copies (cp.async.bulk
-// on the TMA engine), one mbarrier per stage, with bounded waits. A CTA (4 warps)
-// merges its warps; splits merge through the workspace (last CTA, atomic ticket).
+// Staging: every warp streams its own contiguous run of 32-token iterations through a
+// ring of NS shared-memory stages filled by per-lane 16-byte asynchronous copies
+// (cp.async, completion counted on one mbarrier per stage), with bounded waits. A CTA
+// (4 warps) merges its warps; splits merge through the workspace (last CTA, atomic
+// ticket) or, for small grids, through distributed shared memory of a cluster.
 #pragma once
 
 #include <cooperative_groups.h>
@@ -202,12 +208,10 @@ struct Stage {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
+// A stage barrier completes a phase when all 32 lanes of the warp have seen their
+// copies of the stage land (cp.async.mbarrier.arrive.noinc, one arrival per lane).
 __device__ __forceinline__ void mbar_init(uint32_t bar) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 32;" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
@@ -237,10 +241,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
+// 16-byte asynchronous global -> shared copy (L2 only), per thread.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// Arrive on `bar` once this thread's earlier cp.async copies have completed.
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 template <int BITS>
@@ -343,25 +350,31 @@ __global__ void __launch_bounds__(kWarps * 32, min_blocks<NT>()) decode_mma_kern
   const uint8_t* vm_src = reinterpret_cast<const uint8_t*>(p.v_meta + (slice * p.S_pad + ts0) * NVG);
   const __half2* km_base = p.k_meta + slice * (p.S_pad >> p.log2G) * kHeadDim;
 
-  // Copies of the warp's iteration i into stage i % NS (lane 0 only).
+  // Copies of the warp's iteration i into stage sidx: every lane moves 16-byte pieces
+  // (piece lane + 32c of each block) with cp.async and arrives on the stage barrier
+  // when its pieces have landed. Plain per-thread copies keep the issue cost at a
+  // few instructions per lane and iteration.
+  const uint32_t wbase_s = smem_u32(wbase) + 16 * lane;
   auto issue = [&](int i, int sidx) {
+    constexpr int CK = St::KB / 512;  // pieces per lane of the key / value codes
     const int ts = ts0 + i * kTok;
-    uint8_t* st = wbase + sidx * St::BYTES;
-    const uint32_t bar = smem_u32(&bars[warp][sidx]);
+    const uint32_t dst = wbase_s + sidx * St::BYTES;
     const bool quant = ts < Tq;
     const bool newgrp = quant && (i == 0 || (ts & (p.G - 1)) == 0);
-    const uint32_t bytes = St::VB + St::VM + (quant ? St::KB : 0) + (newgrp ? St::KM : 0);
-    const size_t off = (size_t)i * St::KB;
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    mbar_expect_tx(bar, bytes);
-    if (quant) bulk_g2s(smem_u32(st), k_src + off, St::KB, bar);
-    bulk_g2s(smem_u32(st + St::KB), v_src + off, St::VB, bar);
-    bulk_g2s(smem_u32(st + St::KB + St::VB), vm_src + (size_t)i * St::VM, St::VM, bar);
-    if (newgrp) bulk_g2s(smem_u32(st + St::KB + St::VB + St::VM), km_base + ((ts >> p.log2G) << 7), St::KM, bar);
+    const size_t off = (size_t)i * St::KB + 16 * lane;
+    if (quant) {
+#pragma unroll
+      for (int c = 0; c < CK; ++c) cp_async16(dst + 512 * c, k_src + off + 512 * c);
+    }
+#pragma unroll
+    for (int c = 0; c < CK; ++c) cp_async16(dst + St::KB + 512 * c, v_src + off + 512 * c);
+    if (16 * lane < St::VM) cp_async16(dst + St::KB + St::VB, vm_src + (size_t)i * St::VM + 16 * lane);
+    if (newgrp) cp_async16(dst + St::KB + St::VB + St::VM, km_base + ((ts >> p.log2G) << 7) + 4 * lane);
+    cp_async_arrive(smem_u32(&bars[warp][sidx]));
   };
   // Fused decode step: the CTA whose range holds the new token T-1 appends it first
   // (value row quantized per group into its half of the pair row, key row into its
-  // residual slot), then makes those global writes visible to the bulk copies.
+  // residual slot); the barrier orders those global writes before the copies.
   if (p.v_new != nullptr && t_begin <= T - 1 && T - 1 < t_end) {
     if (warp == 0) {
       const int t_new = T - 1;
@@ -371,12 +384,10 @@ __global__ void __launch_bounds__(kWarps * 32, min_blocks<NT>()) decode_mma_kern
                                       p.v_meta_w + (slice * p.S_pad + t_new) * NVG, p.Gv, lane, smem);
       const uint2 kv = *reinterpret_cast<const uint2*>(p.k_new + row * kHeadDim + 4 * lane);
       *reinterpret_cast<uint2*>(p.k_resid_w + (slice * p.R_eff + t_new % p.R_eff) * kHeadDim + 4 * lane) = kv;
-      asm volatile("fence.proxy.async.global;" ::: "memory");
     }
     __syncthreads();
   }
-  if (lane == 0)
-    for (int i = 0; i < min(NS, n_mine); ++i) issue(i, i);
+  for (int i = 0; i < min(NS, n_mine); ++i) issue(i, i);
 
   // query rows of this kv head, binary32, in shared memory
   for (int idx = threadIdx.x; idx < r * kHeadDim; idx += kWarps * 32)
@@ -697,7 +708,7 @@ __global__ void __launch_bounds__(kWarps * 32, min_blocks<NT>()) decode_mma_kern
     qk(i, st, acc, sc, bi);
     softmax_pv(i, st, acc, sc, bi);
     __syncwarp();  // every lane is done with stage sidx
-    if (lane == 0 && i + NS < n_mine) issue(i + NS, sidx);
+    if (i + NS < n_mine) issue(i + NS, sidx);
     if (++sidx == NS) {
       sidx = 0;
       phase ^= 1u;
@@ -710,6 +721,7 @@ __global__ void __launch_bounds__(kWarps * 32, min_blocks<NT>()) decode_mma_kern
     if (lane == 0) atomicOr(p.err, 1u);
     for (int i = failed_at; i < min(n_mine, failed_at + NS); ++i)
       mbar_wait(smem_u32(&bars[warp][i % NS]), (uint32_t)((i / NS) & 1));
+    asm volatile("cp.async.wait_all;" ::: "memory");  // no copy may land after the CTA exits
   }
   __syncwarp();
 
