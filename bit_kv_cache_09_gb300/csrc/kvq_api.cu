@@ -70,30 +70,38 @@ int decode_occupancy(const Geometry& g, kvq_decode_impl impl) {
 
 // Largest power-of-two cluster size <= 16 whose clusters can all be resident for
 // `units` (batch row, kv head) pairs (cached per device and kernel shape).
-int decode_cluster_size(const Geometry& g, int64_t units) {
+// Clusters of `cs` CTAs (a power of two, 2..16) of the tensor-core kernel that can be
+// resident at once on this device (<= 0: such a cluster cannot launch); cached.
+int resident_clusters(const Geometry& g, int cs) {
   static std::atomic<int> cache[16][3][2][3][5];  // device, bits, r class, value groups, log2 size
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) dev = 0;
   const int bi = g.bits == 8 ? 0 : (g.bits == 4 ? 1 : 2);
   const int ri = g.r <= 4 ? 0 : 1;
   const int vi = g.n_vg == 1 ? 0 : (g.n_vg == 2 ? 1 : 2);
-  for (int lg = 4; lg >= 1; --lg) {
-    std::atomic<int>& slot = cache[dev][bi][ri][vi][lg];
-    int n = slot.load(std::memory_order_relaxed);
-    if (n == 0) {
-      n = kvq::max_clusters_decode_mma(g.bits, g.r, g.n_vg, 1 << lg);
-      if (n <= 0) n = -1;
-      slot.store(n, std::memory_order_relaxed);
-    }
-    if (n >= units) return 1 << lg;
+  int lg = 0;
+  while ((1 << lg) < cs) ++lg;
+  std::atomic<int>& slot = cache[dev][bi][ri][vi][lg];
+  int n = slot.load(std::memory_order_relaxed);
+  if (n == 0) {
+    n = kvq::max_clusters_decode_mma(g.bits, g.r, g.n_vg, cs);
+    if (n <= 0) n = -1;
+    slot.store(n, std::memory_order_relaxed);
   }
+  return n;
+}
+
+int decode_cluster_size(const Geometry& g, int64_t units) {
+  for (int lg = 4; lg >= 1; --lg)
+    if (resident_clusters(g, 1 << lg) >= units) return 1 << lg;
   return 1;
 }
 
 // Split-K plan.
-// Large grids (many (batch row, kv head) pairs): the number of splits per pair is chosen
-// so that the grid fills whole waves of resident CTAs (>= 92% of the slots busy when
-// possible); partials merge through the workspace (last CTA, atomic ticket).
+// Large grids (many (batch row, kv head) pairs): the number of splits per pair minimises
+// a cost model (rounds of resident CTAs x per-CTA time); 2, 4 or 8 splits of a pair run
+// as one cluster and merge through distributed shared memory, other counts merge
+// through the workspace (last CTA, atomic ticket).
 // Small grids (at most 1/32 of the slots per pair): latency-bound, so each pair gets a
 // cluster of up to 16 CTAs, small enough that every warp's stages are all in flight at
 // once, merged through distributed shared memory without touching the workspace.
@@ -146,6 +154,11 @@ Plan plan_splits(const Geometry& g, int64_t T, kvq_decode_impl impl) {
   pl.chunk = c;
   pl.cluster = 1;
   pl.n_parts = (int)pl.n_split;
+  if (impl != KVQ_DECODE_SIMT && (pl.n_split == 2 || pl.n_split == 4 || pl.n_split == 8) &&
+      resident_clusters(g, (int)pl.n_split) > 0) {
+    pl.cluster = (int)pl.n_split;
+    pl.n_parts = 1;
+  }
   return pl;
 }
 
