@@ -61,6 +61,16 @@ def append_bytes_per_layer(w, s_cur: int, n_new: int = 1) -> int:
     return w.batch * w.n_kv * per
 
 
+def prefill_bytes_per_layer(w, S: int) -> int:
+    """Algorithmic bytes of quantizing an S-token prompt of one layer: binary16 keys and
+    values read; key codes + group metadata, residual keys, value codes + metadata written."""
+    d, b = w.d_head, w.bits
+    Tq = (S // w.r_eff) * w.r_eff
+    per = S * 2 * d * 2 + Tq * (d * b // 8) + (Tq // w.k_group) * d * 4 + (S - Tq) * 2 * d
+    per += S * (d * b // 8) + S * (d // w.v_group) * 4
+    return w.batch * w.n_kv * per
+
+
 def step_launches(w, s_cur: int, fused: bool = True) -> int:
     """Kernels one decode step launches: per layer one fused append+attention launch, or
     (separate calls, or a step that fills a residual window) append (+ key groups) and attention."""
@@ -314,15 +324,23 @@ def main():
     stream = torch.cuda.current_stream()
     S, L = w.seq, w.n_layers
 
-    # prefill every layer (untimed), in chunks to bound the fp16 staging memory
+    # prefill every layer, in chunks to bound the fp16 staging memory; the quantize-append
+    # calls (not the input generator) are timed with CUDA events for the prefill line
     chunk = max(128, min(S, (1 << 28) // (w.batch * w.n_kv * w.d_head * 2) // 128 * 128))
+    pre_ms = 0.0
     for layer in range(L):
         t = 0
         while t < S:
             n = min(chunk, S - t)
             k, v = gen.kv(layer, t, n)
+            p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            p0.record()
             cache.append(layer, t, k, v)
+            p1.record()
+            p1.synchronize()
+            pre_ms += p0.elapsed_time(p1)
             t += n
+    pre_bytes = L * prefill_bytes_per_layer(w, S)
     # inputs of every decode step, resident on the device
     kin = torch.empty((n_steps, L, w.batch, 1, w.n_kv, w.d_head), dtype=torch.float16, device=dev)
     vin = torch.empty_like(kin)
@@ -488,6 +506,10 @@ def main():
                              "frac": round(achieved / peak, 4), "traffic": traffic,
                              "kernel": "decode attention", "us_per_launch": round(attn_us, 3),
                              "bytes_per_launch": attn_b, "peak_kind": f"{peak_kind} hbm_gbs"},
+                "prefill": {"what": f"quantize-append of the {S}-token prompt, all layers, chunks of {chunk} tokens "
+                                    "(key-group and value-token kernels), CUDA events around each call",
+                            "gbs": round(pre_bytes / (pre_ms / 1e3) / 1e9, 1), "frac": round(pre_bytes / (pre_ms / 1e3) / 1e9 / peak, 4),
+                            "ms": round(pre_ms, 3), "bytes": pre_bytes},
                 "gpu_launches": launches, "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu}
         print(json.dumps(line), flush=True)
     if dist:

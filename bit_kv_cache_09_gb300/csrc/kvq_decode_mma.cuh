@@ -616,7 +616,12 @@ __global__ void __launch_bounds__(kWarps * 32, min_blocks<NT>()) decode_mma_kern
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
     const float m_new = fmaxf(m_run, mx);
-    if (__any_sync(0xffffffffu, m_new > m_run)) {
+    // Lazy rescale: the running max is only moved when a score exceeds it by more than
+    // kTau (log2 units), so p = 2^(s - m_run) <= 2^kTau. kTau keeps every binary16
+    // weight p*s finite for any binary16 value group: the largest value scale is
+    // 131008 / (2^b - 1) rounded up (514, 8734, 43669 for b = 8, 4, 2).
+    constexpr float kTau = BITS == 8 ? 6.0f : (BITS == 4 ? 2.0f : 0.5f);
+    if (__any_sync(0xffffffffu, m_new > m_run + kTau)) {
       const float alpha = ex2(m_run - m_new);  // 0 on the first iteration (m_run = -inf)
       l_run *= alpha;
       // PV column n holds the query of row n: alphas of columns 2j, 2j+1 live in rows 2j, 2j+1

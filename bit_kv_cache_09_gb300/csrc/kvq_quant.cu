@@ -53,6 +53,7 @@ __global__ void __launch_bounds__(256) k_group_kernel(AppendParams p) {
   __shared__ float red_min[8][kHeadDim];
   __shared__ float red_max[8][kHeadDim];
   __shared__ float s_sc[kHeadDim];
+  __shared__ float s_rs[kHeadDim];
   __shared__ float s_zp[kHeadDim];
 
   float x[PER_WARP][4];
@@ -93,14 +94,16 @@ __global__ void __launch_bounds__(256) k_group_kernel(AppendParams p) {
     float s, zp;
     group_params<BITS>(a, z, s_h, z_h, s, zp);
     s_sc[c] = s;
+    s_rs[c] = __frcp_rn(s);
     s_zp[c] = zp;
     p.k_meta[(slice * (p.S_pad / G) + g) * kHeadDim + c] = __halves2half2(s_h, z_h);
   }
   __syncthreads();
-  float s[4], zp[4];
+  float s[4], rs[4], zp[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     s[e] = s_sc[4 * lane + e];
+    rs[e] = s_rs[4 * lane + e];
     zp[e] = s_zp[4 * lane + e];
   }
   uint8_t* codes = p.k_codes + slice * p.k_codes_slice;
@@ -109,7 +112,7 @@ __global__ void __launch_bounds__(256) k_group_kernel(AppendParams p) {
     const int64_t t = t0 + warp + 8 * k;
     uint32_t u[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) u[e] = quant_code<BITS>(x[k][e], s[e], zp[e]);
+    for (int e = 0; e < 4; ++e) u[e] = quant_code<BITS>(x[k][e], s[e], rs[e], zp[e]);
     store_k4<BITS>(codes + t * p.rowK, lane, u);
   }
 }

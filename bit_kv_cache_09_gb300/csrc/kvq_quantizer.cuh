@@ -46,9 +46,25 @@ __device__ __forceinline__ void group_params(float xmin, float xmax, __half& s_h
   zp = __half2float(z_h);
 }
 
+// Correctly rounded binary32 quotient x / s for binary16 operands x and s, from the
+// correctly rounded reciprocal rs = RN(1/s), by Markstein's fma correction (P. W.
+// Markstein, "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Dev. 34(1), 1990): q0 = RN(x * rs) lies within 1.5 ulp of
+// x/s; the remainder x - s*q0 is then a multiple of ulp(s)*ulp(q0) below 2^12 of them,
+// so one fma computes it exactly; and q0 + remainder*rs = x/s + e with
+// |e| <= 1.5 * 2^-24 ulp. A quotient of two 11-bit binary16 numbers that is not itself
+// a binary32 number lies at least 2^-12 ulp away from every rounding midpoint, so the
+// final fma returns RN(x/s), the same value as an IEEE division.
+__device__ __forceinline__ float div_rn_f16(float x, float s, float rs) {
+  const float q0 = __fmul_rn(x, rs);
+  const float r = __fmaf_rn(-s, q0, x);
+  return __fmaf_rn(r, rs, q0);
+}
+
+// Code of x in a group with binary16 scale s (rs = RN(1/s)) and zero point zp.
 template <int BITS>
-__device__ __forceinline__ uint32_t quant_code(float x, float s, float zp) {
-  float q = __fadd_rn(rintf(__fdiv_rn(x, s)), zp);
+__device__ __forceinline__ uint32_t quant_code(float x, float s, float rs, float zp) {
+  float q = __fadd_rn(rintf(div_rn_f16(x, s, rs)), zp);
   q = fminf(fmaxf(q, Q<BITS>::qmin), Q<BITS>::qmax);
   return (uint32_t)(int)__fsub_rn(q, Q<BITS>::qmin);
 }
@@ -90,7 +106,9 @@ __device__ __forceinline__ void quantize_value_row(const __half* v_row, uint16_t
   group_params<BITS>(mn, mx, s_h, z_h, s, zp);
   if (lane % lanes_per_group == 0) meta[lane / lanes_per_group] = __halves2half2(s_h, z_h);
 #pragma unroll
-  for (int e = 0; e < 4; ++e) codes_s[4 * lane + e] = (uint8_t)quant_code<BITS>(x[e], s, zp);
+  const float rs = __frcp_rn(s);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) codes_s[4 * lane + e] = (uint8_t)quant_code<BITS>(x[e], s, rs, zp);
   __syncwarp();
   constexpr int PER_UNIT = 16 / BITS;
   constexpr int UNITS = kHeadDim * BITS / 16;

@@ -189,3 +189,67 @@ def test_fused_decode_step(bits, G, Gv, R, r):
         if s in (0, 1, steps - 5, steps - 4, steps - 1):
             _check_all_slices(fused, w, 0, T + 1, k_host, v_host)
             _check_attention(fused, w, 0, T + 1, k_host, v_host, q_host, kvq.DECODE_AUTO)
+
+
+def _all_f16_values():
+    """Every finite binary16 value, as float64, sorted, with its bit pattern."""
+    bits = np.arange(0x10000, dtype=np.uint32).astype(np.uint16)
+    vals = bits.view(np.float16).astype(np.float64)
+    ok = np.isfinite(vals)
+    order = np.argsort(vals[ok], kind="stable")
+    return vals[ok][order], bits[ok][order]
+
+
+def _near_midpoints(lo, hi, s, n, vals, bits):
+    """n binary16 values strictly inside (lo, hi) whose quotient by s is closest to a
+    half-integer (where a wrongly rounded division would change the code)."""
+    a, b = np.searchsorted(vals, lo, side="right"), np.searchsorted(vals, hi, side="left")
+    cand_v, cand_b = vals[a:b], bits[a:b]
+    if cand_v.size == 0:
+        return np.zeros(0, np.uint16)
+    t = cand_v / s
+    dist = np.abs(t - np.floor(t) - 0.5)
+    return cand_b[np.argsort(dist, kind="stable")[:n]]
+
+
+@pytest.mark.parametrize("bits", [8, 4, 2])
+def test_quantize_near_rounding_midpoints(bits):
+    """Inputs planted where x / scale is as close as binary16 allows to a half-integer:
+    the kernels' fma-corrected division must give the same codes as the oracle's IEEE
+    division (prefill through the key-group and value-token kernels, then decode steps
+    through the fused append)."""
+    G = Gv = 32
+    w = small_workload(bits=bits, G=G, Gv=Gv, R=0, r=4, B=1, H=1, S=64, steps=6, seed=4100 + bits)
+    vals, pats = _all_f16_values()
+    k_host, v_host = host_layer_inputs(w, 0, 0, w.max_seq)
+    k_host, v_host = k_host.copy(), v_host.copy()
+    kb, vb = k_host.view(np.uint16), v_host.view(np.uint16)
+    rng = np.random.default_rng(bits)
+    # keys: per group of G tokens and channel, overwrite 8 tokens that are neither the min nor the max
+    for g0 in range(0, 64, G):
+        for c in range(128):
+            col = k_host[0, g0:g0 + G, 0, c].astype(np.float64)
+            s_h, _ = oracle.quant_params(k_host[0, g0:g0 + G, 0, c], bits)
+            s = float(np.array([s_h], np.uint16).view(np.float16)[0])
+            pick = _near_midpoints(col.min(), col.max(), s, 8, vals, pats)
+            inner = [t for t in rng.permutation(G) if col[t] != col.min() and col[t] != col.max()][:pick.size]
+            for t, pb in zip(inner, pick):
+                kb[0, g0 + t, 0, c] = pb
+    # values: per token and group of Gv channels, overwrite 6 inner channels
+    for t in range(w.max_seq):
+        for g0 in range(0, 128, Gv):
+            row = v_host[0, t, 0, g0:g0 + Gv].astype(np.float64)
+            s_h, _ = oracle.quant_params(v_host[0, t, 0, g0:g0 + Gv], bits)
+            s = float(np.array([s_h], np.uint16).view(np.float16)[0])
+            pick = _near_midpoints(row.min(), row.max(), s, 6, vals, pats)
+            inner = [c for c in rng.permutation(Gv) if row[c] != row.min() and row[c] != row.max()][:pick.size]
+            for c, pb in zip(inner, pick):
+                vb[0, t, 0, g0 + c] = pb
+    cache = QuantizedKVCache.for_workload(w)
+    cache.append(0, 0, _dev(k_host[:, :64]), _dev(v_host[:, :64]))
+    _check_all_slices(cache, w, 0, 64, k_host, v_host)
+    for s in range(w.steps):
+        T = 64 + s
+        q = _dev(synth.gen_q(w.seed, 0, range(w.batch), T, w.n_q, w.d_head))
+        cache.decode_step(0, T, _dev(k_host[:, T:T + 1]), _dev(v_host[:, T:T + 1]), q, softmax_scale(w))
+    _check_all_slices(cache, w, 0, 64 + w.steps, k_host, v_host)
