@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(256) k_group_kernel(AppendParams p) {
     group_params<BITS>(a, z, s_h, z_h, s, zp);
     s_sc[c] = s;
     s_rs[c] = __frcp_rn(s);
-    s_zp[c] = zp;
+    s_zp[c] = __fsub_rn(zp, Q<BITS>::qmin);
     p.k_meta[(slice * (p.S_pad / G) + g) * kHeadDim + c] = __halves2half2(s_h, z_h);
   }
   __syncthreads();
@@ -118,31 +118,113 @@ __global__ void __launch_bounds__(256) k_group_kernel(AppendParams p) {
 }
 
 // ---------------------------------------------------------------------------
-// Values (and the key residual copy): one warp per appended (batch row, token,
-// kv head) row, in the input's own order. Lane l holds channels [4l, 4l+4).
+// Values (and the key residual copy): each warp quantizes four appended (batch row,
+// token, kv head) rows, in the input's own order; lanes 8r .. 8r+7 hold row r, lane
+// 8r + l its channels [16l, 16l + 16). A value group of Gv channels spans Gv/16 lanes.
+// In the pair-row layout channel 16l + i sits at position 16(i % 8) + 2l + i / 8, so
+// 8-bit codes fill their 16-bit units within a lane, 4-bit units take two lanes and
+// 2-bit units four.
 // ---------------------------------------------------------------------------
 template <int BITS>
 __global__ void __launch_bounds__(256) v_token_kernel(AppendParams p, int64_t n_rows) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t w = (int64_t)blockIdx.x * 8 + warp;
-  __shared__ uint8_t codes_s[8][kHeadDim];
+  const int sl = lane & 7;
+  const int64_t w_raw = ((int64_t)blockIdx.x * 8 + warp) * 4 + (lane >> 3);
   pdl_wait();
   pdl_allow_dependents();
-  if (w >= n_rows) return;  // whole warps only: the warp-level code below stays converged
+  const bool valid = w_raw < n_rows;
+  const int64_t w = valid ? w_raw : n_rows - 1;  // lanes past the end read a real row and store nothing
   const int h = (int)(w % p.H);
   const int64_t bt = w / p.H;
   const int64_t t = p.s_cur + bt % p.n_new;
   const int b = (int)(bt / p.n_new);
   const int64_t slice = (int64_t)b * p.H + h;
 
-  uint16_t* pair = reinterpret_cast<uint16_t*>(p.v_codes + slice * p.v_codes_slice + (t >> 1) * 2 * p.rowV);
-  quantize_value_row<BITS>(p.v_in + w * kHeadDim, pair, (int)(t & 1), p.v_meta + (slice * p.S_pad + t) * p.n_vg, p.Gv,
-                           lane, codes_s[warp]);
+  float x[16];
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(p.v_in + w * kHeadDim + 16 * sl);
+    const uint4 a = src[0], c = src[1];
+    const uint32_t wd[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wd[k]));
+      x[2 * k] = f.x;
+      x[2 * k + 1] = f.y;
+    }
+  }
+  float mn = x[0], mx = x[0];
+#pragma unroll
+  for (int i = 1; i < 16; ++i) {
+    mn = fminf(mn, x[i]);
+    mx = fmaxf(mx, x[i]);
+  }
+  const int lpg = p.Gv >> 4;  // lanes per value group: 2, 4 or 8
+  for (int off = 1; off < lpg; off <<= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  }
+  __half s_h, z_h;
+  float s, zp;
+  group_params<BITS>(mn, mx, s_h, z_h, s, zp);
+  if (valid && sl % lpg == 0) p.v_meta[(slice * p.S_pad + t) * p.n_vg + sl / lpg] = __halves2half2(s_h, z_h);
+  const float rs = __frcp_rn(s), zpu = __fsub_rn(zp, Q<BITS>::qmin);
+  uint32_t u[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) u[i] = quant_code<BITS>(x[i], s, rs, zpu);
+
+  uint16_t* pair = reinterpret_cast<uint16_t*>(p.v_codes + slice * p.v_codes_slice + (t >> 1) * 2 * p.rowV) + (t & 1);
+  if (BITS == 8) {
+    // unit 8m + l = (channel 16l + m, channel 16l + m + 8)
+    if (valid) {
+#pragma unroll
+      for (int m = 0; m < 8; ++m) pair[2 * (8 * m + sl)] = (uint16_t)(u[m] | (u[m + 8] << 8));
+    }
+  } else if (BITS == 4) {
+    // unit 4m + l/2: bytes of lanes 2(l/2) (low) and 2(l/2) + 1 (high); byte m of a lane
+    // holds channels 16l + m and 16l + m + 8. Even lanes store m = 0..3, odd lanes 4..7.
+    uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      w0 |= (u[m] | (u[m + 8] << 4)) << (8 * m);
+      w1 |= (u[m + 4] | (u[m + 12] << 4)) << (8 * m);
+    }
+    const bool odd = sl & 1;
+    const uint32_t recv = __shfl_xor_sync(0xffffffffu, odd ? w0 : w1, 1);
+    const uint32_t lo = odd ? recv : w0, hi = odd ? w1 : recv;
+    if (valid) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int m = odd ? 4 + j : j;
+        pair[2 * (4 * m + (sl >> 1))] = (uint16_t)__byte_perm(lo, hi, (unsigned)(j | ((4 + j) << 4)));
+      }
+    }
+  } else {
+    // unit 2m + l/4: 4-bit pieces of the four lanes 4(l/4) .. 4(l/4) + 3 (lane q at bit 4q);
+    // piece m of a lane holds channels 16l + m and 16l + m + 8. Lane q stores m = 2q, 2q+1.
+    uint32_t wd = 0;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) wd |= (u[m] | (u[m + 8] << 2)) << (4 * m);
+    const int base = lane & ~3, q = sl & 3;
+    uint32_t wq[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) wq[k] = __shfl_sync(0xffffffffu, wd, base + k);
+    if (valid) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int m = 2 * q + e;
+        uint32_t unit = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) unit |= ((wq[k] >> (4 * m)) & 0xFu) << (4 * k);
+        pair[2 * (2 * m + (sl >> 2))] = (uint16_t)unit;
+      }
+    }
+  }
   // Keys of tokens past the last full residual window go to the residual.
-  if (t >= p.A1) {
-    const uint2 raw = *reinterpret_cast<const uint2*>(p.k_in + w * kHeadDim + 4 * lane);
-    __half* dst = p.k_resid + (slice * p.R_eff + t % p.R_eff) * kHeadDim;
-    *reinterpret_cast<uint2*>(dst + 4 * lane) = raw;
+  if (valid && t >= p.A1) {
+    const uint4* ks = reinterpret_cast<const uint4*>(p.k_in + w * kHeadDim + 16 * sl);
+    uint4* kd = reinterpret_cast<uint4*>(p.k_resid + (slice * p.R_eff + t % p.R_eff) * kHeadDim + 16 * sl);
+    kd[0] = ks[0];
+    kd[1] = ks[1];
   }
 }
 
@@ -203,7 +285,7 @@ cudaError_t launch_append_bits(const AppendParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
   }
   const int64_t rows = (int64_t)p.B * p.n_new * p.H;
-  cudaError_t e = launch_pdl(v_token_kernel<BITS>, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, stream, p, rows);
+  cudaError_t e = launch_pdl(v_token_kernel<BITS>, dim3((unsigned)((rows + 31) / 32)), dim3(256), 0, stream, p, rows);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -61,12 +61,14 @@ __device__ __forceinline__ float div_rn_f16(float x, float s, float rs) {
   return __fmaf_rn(r, rs, q0);
 }
 
-// Code of x in a group with binary16 scale s (rs = RN(1/s)) and zero point zp.
+// Code u = clamp(rint(x/s) + zp, q_min, q_max) - q_min of x in a group with binary16
+// scale s (rs = RN(1/s)); zpu = zp - q_min (an integer-valued binary32, so the shift
+// by q_min is exact and the clamp bounds become [0, 2^b - 1]).
 template <int BITS>
-__device__ __forceinline__ uint32_t quant_code(float x, float s, float rs, float zp) {
-  float q = __fadd_rn(rintf(div_rn_f16(x, s, rs)), zp);
-  q = fminf(fmaxf(q, Q<BITS>::qmin), Q<BITS>::qmax);
-  return (uint32_t)(int)__fsub_rn(q, Q<BITS>::qmin);
+__device__ __forceinline__ uint32_t quant_code(float x, float s, float rs, float zpu) {
+  float q = __fadd_rn(rintf(div_rn_f16(x, s, rs)), zpu);
+  q = fminf(fmaxf(q, 0.0f), (float)((1 << BITS) - 1));
+  return (uint32_t)(int)q;
 }
 
 __device__ __forceinline__ void load4(const __half* p, float* x) {
@@ -106,9 +108,9 @@ __device__ __forceinline__ void quantize_value_row(const __half* v_row, uint16_t
   group_params<BITS>(mn, mx, s_h, z_h, s, zp);
   if (lane % lanes_per_group == 0) meta[lane / lanes_per_group] = __halves2half2(s_h, z_h);
 #pragma unroll
-  const float rs = __frcp_rn(s);
+  const float rs = __frcp_rn(s), zpu = __fsub_rn(zp, Q<BITS>::qmin);
 #pragma unroll
-  for (int e = 0; e < 4; ++e) codes_s[4 * lane + e] = (uint8_t)quant_code<BITS>(x[e], s, rs, zp);
+  for (int e = 0; e < 4; ++e) codes_s[4 * lane + e] = (uint8_t)quant_code<BITS>(x[e], s, rs, zpu);
   __syncwarp();
   constexpr int PER_UNIT = 16 / BITS;
   constexpr int UNITS = kHeadDim * BITS / 16;
