@@ -37,10 +37,10 @@ __device__ __forceinline__ void store_k4(uint8_t* row, int lane, const uint32_t*
 // ---------------------------------------------------------------------------
 // Keys: one CTA per (group, kv head, batch row); 8 warps, warp w holds tokens
 // w, w+8, ... of the group, lane l holds channels [4l, 4l+4). Token rows come from
-// the residual window (tokens < s_cur) or from the appended input.
+// the residual window (tokens < s_cur) or from the appended input. 4 CTAs per SM.
 // ---------------------------------------------------------------------------
 template <int BITS, int G>
-__global__ void __launch_bounds__(256) k_group_kernel(AppendParams p) {
+__global__ void __launch_bounds__(256, 4) k_group_kernel(AppendParams p) {
   constexpr int PER_WARP = G / 8;
   pdl_wait();
   pdl_allow_dependents();
@@ -56,26 +56,28 @@ __global__ void __launch_bounds__(256) k_group_kernel(AppendParams p) {
   __shared__ float s_rs[kHeadDim];
   __shared__ float s_zp[kHeadDim];
 
-  float x[PER_WARP][4];
-  float mn[4], mx[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    mn[e] = __int_as_float(0x7f800000);
-    mx[e] = -__int_as_float(0x7f800000);
-  }
+  // rows are kept as binary16 pairs (half the registers of binary32): the group
+  // min/max of binary16 values is exact in binary16
+  uint2 x[PER_WARP];
+  __half2 mn2[2], mx2[2];
   const __half* resid = p.k_resid + slice * (int64_t)p.R_eff * kHeadDim;
 #pragma unroll
   for (int k = 0; k < PER_WARP; ++k) {
     const int64_t t = t0 + warp + 8 * k;
     const __half* row = (t < p.s_cur) ? resid + (t % p.R_eff) * kHeadDim
                                       : p.k_in + (((int64_t)b * p.n_new + (t - p.s_cur)) * p.H + h) * kHeadDim;
-    load4(row + 4 * lane, x[k]);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      mn[e] = fminf(mn[e], x[k][e]);
-      mx[e] = fmaxf(mx[e], x[k][e]);
+    x[k] = *reinterpret_cast<const uint2*>(row + 4 * lane);
+    const __half2 a = *reinterpret_cast<const __half2*>(&x[k].x), c = *reinterpret_cast<const __half2*>(&x[k].y);
+    if (k == 0) {
+      mn2[0] = a; mx2[0] = a; mn2[1] = c; mx2[1] = c;
+    } else {
+      mn2[0] = __hmin2(mn2[0], a); mx2[0] = __hmax2(mx2[0], a);
+      mn2[1] = __hmin2(mn2[1], c); mx2[1] = __hmax2(mx2[1], c);
     }
   }
+  float mn[4], mx[4];
+  mn[0] = __low2float(mn2[0]); mn[1] = __high2float(mn2[0]); mn[2] = __low2float(mn2[1]); mn[3] = __high2float(mn2[1]);
+  mx[0] = __low2float(mx2[0]); mx[1] = __high2float(mx2[0]); mx[2] = __low2float(mx2[1]); mx[3] = __high2float(mx2[1]);
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     red_min[warp][4 * lane + e] = mn[e];
@@ -110,9 +112,11 @@ __global__ void __launch_bounds__(256) k_group_kernel(AppendParams p) {
 #pragma unroll
   for (int k = 0; k < PER_WARP; ++k) {
     const int64_t t = t0 + warp + 8 * k;
+    float xf[4];
+    load4(reinterpret_cast<const __half*>(&x[k]), xf);
     uint32_t u[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) u[e] = quant_code<BITS>(x[k][e], s[e], rs[e], zp[e]);
+    for (int e = 0; e < 4; ++e) u[e] = quant_code<BITS>(xf[e], s[e], rs[e], zp[e]);
     store_k4<BITS>(codes + t * p.rowK, lane, u);
   }
 }
