@@ -68,12 +68,11 @@ int decode_occupancy(const Geometry& g, kvq_decode_impl impl) {
   return n > 0 ? n : 1;
 }
 
-// Largest power-of-two cluster size <= 16 whose clusters can all be resident for
-// `units` (batch row, kv head) pairs (cached per device and kernel shape).
-// Clusters of `cs` CTAs (a power of two, 2..16) of the tensor-core kernel that can be
-// resident at once on this device (<= 0: such a cluster cannot launch); cached.
-int resident_clusters(const Geometry& g, int cs) {
-  static std::atomic<int> cache[16][3][2][3][5];  // device, bits, r class, value groups, log2 size
+// Clusters of `cs` CTAs (a power of two, 2..16) of `nw` warps of the tensor-core
+// kernel that can be resident at once on this device (<= 0: such a cluster cannot
+// launch); cached per device and kernel shape.
+int resident_clusters(const Geometry& g, int cs, int nw) {
+  static std::atomic<int> cache[16][3][2][3][5][2];  // device, bits, r class, value groups, log2 size, warps
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) dev = 0;
   const int bi = g.bits == 8 ? 0 : (g.bits == 4 ? 1 : 2);
@@ -81,19 +80,21 @@ int resident_clusters(const Geometry& g, int cs) {
   const int vi = g.n_vg == 1 ? 0 : (g.n_vg == 2 ? 1 : 2);
   int lg = 0;
   while ((1 << lg) < cs) ++lg;
-  std::atomic<int>& slot = cache[dev][bi][ri][vi][lg];
+  std::atomic<int>& slot = cache[dev][bi][ri][vi][lg][nw == 8 ? 1 : 0];
   int n = slot.load(std::memory_order_relaxed);
   if (n == 0) {
-    n = kvq::max_clusters_decode_mma(g.bits, g.r, g.n_vg, cs);
+    n = kvq::max_clusters_decode_mma(g.bits, g.r, g.n_vg, cs, nw);
     if (n <= 0) n = -1;
     slot.store(n, std::memory_order_relaxed);
   }
   return n;
 }
 
-int decode_cluster_size(const Geometry& g, int64_t units) {
+// Largest power-of-two cluster size <= 16 whose clusters of nw-warp CTAs can all be
+// resident for `units` (batch row, kv head) pairs (1: none).
+int decode_cluster_size(const Geometry& g, int64_t units, int nw) {
   for (int lg = 4; lg >= 1; --lg)
-    if (resident_clusters(g, 1 << lg) >= units) return 1 << lg;
+    if (resident_clusters(g, 1 << lg, nw) >= units) return 1 << lg;
   return 1;
 }
 
@@ -104,10 +105,12 @@ int decode_cluster_size(const Geometry& g, int64_t units) {
 // through the workspace (last CTA, atomic ticket).
 // Small grids (at most 1/32 of the slots per pair): latency-bound, so each pair gets a
 // cluster of up to 16 CTAs, small enough that every warp's stages are all in flight at
-// once, merged through distributed shared memory without touching the workspace.
+// once, merged through distributed shared memory without touching the workspace; CTAs
+// of 8 warps are used when that shortens the longest warp's run of iterations.
 struct Plan {
   int64_t n_split, chunk;
   int cluster, n_parts;
+  int warps = 4;
 };
 
 Plan plan_splits(const Geometry& g, int64_t T, kvq_decode_impl impl) {
@@ -118,13 +121,22 @@ Plan plan_splits(const Geometry& g, int64_t T, kvq_decode_impl impl) {
   const int64_t units = (int64_t)g.B * g.H;
   Plan pl;
   if (impl != KVQ_DECODE_SIMT && units * 32 <= slots) {
-    const int cs = decode_cluster_size(g, units);
-    int64_t c = (T + cs - 1) / cs;
-    c = (c + align - 1) / align * align;
-    pl.n_split = cs;  // trailing splits may be empty; they merge with weight 0
-    pl.chunk = c;
-    pl.cluster = cs;
-    pl.n_parts = 1;
+    int64_t best_run = -1;
+    for (int nw = 4; nw <= 8; nw += 4) {
+      const int cs = decode_cluster_size(g, units, nw);
+      if (nw == 8 && cs < 2) continue;
+      int64_t c = (T + cs - 1) / cs;
+      c = (c + align - 1) / align * align;
+      const int64_t run = (c / 32 + nw - 1) / nw;  // iterations of the busiest warp
+      if (best_run < 0 || run < best_run) {
+        best_run = run;
+        pl.n_split = cs;  // trailing splits may be empty; they merge with weight 0
+        pl.chunk = c;
+        pl.cluster = cs;
+        pl.n_parts = 1;
+        pl.warps = nw;
+      }
+    }
     return pl;
   }
   int64_t max_k = kvq::max_splits(g, T);
@@ -155,7 +167,7 @@ Plan plan_splits(const Geometry& g, int64_t T, kvq_decode_impl impl) {
   pl.cluster = 1;
   pl.n_parts = (int)pl.n_split;
   if (impl != KVQ_DECODE_SIMT && (pl.n_split == 2 || pl.n_split == 4 || pl.n_split == 8) &&
-      resident_clusters(g, (int)pl.n_split) > 0) {
+      resident_clusters(g, (int)pl.n_split, 4) > 0) {
     pl.cluster = (int)pl.n_split;
     pl.n_parts = 1;
   }
@@ -344,6 +356,7 @@ kvq_status decode_launch(const kvq_config* cfg, const kvq_buffers* bufs, int32_t
   p.chunk = pl.chunk;
   p.cluster = pl.cluster;
   p.n_parts = pl.n_parts;
+  p.warps = pl.warps;
   cudaError_t e = (use == KVQ_DECODE_SIMT) ? kvq::launch_decode_simt(p, g.bits, static_cast<cudaStream_t>(stream))
                                             : kvq::launch_decode_mma(p, g.bits, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;

@@ -10,9 +10,9 @@ cudaError_t launch_decode_mma_b2(const DecodeParams& p, cudaStream_t stream);
 int occupancy_decode_mma_b8(int r, int n_vg);
 int occupancy_decode_mma_b4(int r, int n_vg);
 int occupancy_decode_mma_b2(int r, int n_vg);
-int max_clusters_decode_mma_b8(int r, int n_vg, int cs);
-int max_clusters_decode_mma_b4(int r, int n_vg, int cs);
-int max_clusters_decode_mma_b2(int r, int n_vg, int cs);
+int max_clusters_decode_mma_b8(int r, int n_vg, int cs, int nw);
+int max_clusters_decode_mma_b4(int r, int n_vg, int cs, int nw);
+int max_clusters_decode_mma_b2(int r, int n_vg, int cs, int nw);
 
 cudaError_t launch_decode_mma(const DecodeParams& p, int bits, cudaStream_t stream) {
   switch (bits) {
@@ -30,11 +30,11 @@ int occupancy_decode_mma(int bits, int r, int n_vg) {
   }
 }
 
-int max_clusters_decode_mma(int bits, int r, int n_vg, int cs) {
+int max_clusters_decode_mma(int bits, int r, int n_vg, int cs, int nw) {
   switch (bits) {
-    case 8: return max_clusters_decode_mma_b8(r, n_vg, cs);
-    case 4: return max_clusters_decode_mma_b4(r, n_vg, cs);
-    default: return max_clusters_decode_mma_b2(r, n_vg, cs);
+    case 8: return max_clusters_decode_mma_b8(r, n_vg, cs, nw);
+    case 4: return max_clusters_decode_mma_b4(r, n_vg, cs, nw);
+    default: return max_clusters_decode_mma_b2(r, n_vg, cs, nw);
   }
 }
 

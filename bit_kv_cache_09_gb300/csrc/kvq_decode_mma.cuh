@@ -49,7 +49,6 @@ namespace mma {
 
 namespace cg = cooperative_groups;
 
-constexpr int kWarps = 4;
 constexpr int kSlab = 16;
 
 __device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
@@ -192,7 +191,10 @@ __device__ __forceinline__ constexpr float v_scale(int i) {
 
 // One stage = one iteration of 32 tokens (two 16-token halves):
 //   [key codes 32*rowK][value pair rows 32*rowV][value meta 32*4*NVG B][key-group meta 512 B]
-template <int BITS, int NVG>
+// NW warps per CTA each own a ring of NS stages. After the loop the rings are reused
+// for the merges: per-warp partials (o, m, l, beta), the CTA partial read by the
+// cluster merge (cm, cl, co), then the scratch of the workspace merge.
+template <int BITS, int NVG, int NW>
 struct Stage {
   static constexpr int KB = 32 * BITS * 128 / 8;  // key codes of 32 tokens
   static constexpr int VB = KB;                   // value codes of 32 tokens
@@ -201,9 +203,13 @@ struct Stage {
   static constexpr int BYTES = KB + VB + VM + KM;
   static constexpr int NS = BITS == 2 ? 3 : 2;
   static constexpr int WARP_BYTES = NS * BYTES;
-  // the stage rings are reused after the loop for the merges (at most 24 KB + scratch)
-  static constexpr int kEpilogueBytes = 24576 + 4 * kMergeScratchFloats;
-  static constexpr int SMEM = kWarps * WARP_BYTES > kEpilogueBytes ? kWarps * WARP_BYTES : kEpilogueBytes;
+  static constexpr int EP_M = NW * kMaxGqa * kHeadDim * 4;
+  static constexpr int EP_L = EP_M + NW * kMaxGqa * 4;
+  static constexpr int EP_BETA = EP_L + NW * kMaxGqa * 4;
+  static constexpr int EP_CM = EP_BETA + NW * kMaxGqa * NVG * 4;
+  static constexpr int EP_SCRATCH = (EP_CM + (2 * kMaxGqa + kMaxGqa * kHeadDim) * 4 + 15) / 16 * 16;
+  static constexpr int kEpilogueBytes = EP_SCRATCH + 4 * kMergeScratchFloats;
+  static constexpr int SMEM = NW * WARP_BYTES > kEpilogueBytes ? NW * WARP_BYTES : kEpilogueBytes;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -298,10 +304,13 @@ constexpr int min_blocks() {
 }
 
 // BITS: code width; NT: PV n-tiles (1: r <= 4, hi/lo halves share one tile;
-// 2: r <= 8, hi tile + lo tile); NVG: value groups per token (d / Gv).
-template <int BITS, int NT, int NVG>
-__global__ void __launch_bounds__(kWarps * 32, min_blocks<NT>()) decode_mma_kernel(DecodeParams p) {
-  using St = Stage<BITS, NVG>;
+// 2: r <= 8, hi tile + lo tile); NVG: value groups per token (d / Gv); NW: warps per
+// CTA (4; 8 for small cluster-merged grids, where one CTA per SM is resident anyway and
+// twice the warps halve the iterations on the critical path).
+template <int BITS, int NT, int NVG, int NW>
+__global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : 1) decode_mma_kernel(DecodeParams p) {
+  constexpr int kWarps = NW;
+  using St = Stage<BITS, NVG, NW>;
   constexpr int NS = St::NS;
   constexpr int kTok = 32;  // tokens per iteration
   constexpr float qmin = -(float)(1 << (BITS - 1));
@@ -330,7 +339,7 @@ __global__ void __launch_bounds__(kWarps * 32, min_blocks<NT>()) decode_mma_kern
   const int t_begin = split * (int)p.chunk;  // chunk is a multiple of 32
   const int t_end = min(t_begin + (int)p.chunk, T);
   const int n_it = max(0, (t_end - t_begin + kTok - 1) / kTok);  // 0 for a trailing empty split
-  // balanced contiguous runs of iterations per warp (warp w: [w*n_it/4, (w+1)*n_it/4))
+  // balanced contiguous runs of iterations per warp (warp w: [w*n_it/NW, (w+1)*n_it/NW))
   const int it0 = (warp * n_it) / kWarps;
   const int n_mine = ((warp + 1) * n_it) / kWarps - it0;
   const int ts0 = t_begin + it0 * kTok;  // first token of this warp (a multiple of 32)
@@ -782,14 +791,14 @@ __global__ void __launch_bounds__(kWarps * 32, min_blocks<NT>()) decode_mma_kern
   }
   __syncthreads();
 
-  // ---------------- CTA merge of the warps; thread = channel (128 threads)
+  // ---------------- CTA merge of the warps; thread = channel (threads 0..127)
   const int c = threadIdx.x;
-  const int vgc = (c * NVG) / kHeadDim;
+  const int vgc = ((c & (kHeadDim - 1)) * NVG) / kHeadDim;
   // per-CTA partial (max, denominator, unnormalised output) for the cluster merge
-  float* cm_s = reinterpret_cast<float*>(smem + 20480);  // [kMaxGqa]
+  float* cm_s = reinterpret_cast<float*>(smem + St::EP_CM);  // [kMaxGqa]
   float* cl_s = cm_s + kMaxGqa;                           // [kMaxGqa]
   float* co_s = cl_s + kMaxGqa;                           // [kMaxGqa][kHeadDim]
-  for (int i = 0; i < r; ++i) {
+  for (int i = 0; i < (c < kHeadDim ? r : 0); ++i) {
     float M = -__int_as_float(0x7f800000);
 #pragma unroll
     for (int w = 0; w < kWarps; ++w)
@@ -818,7 +827,10 @@ __global__ void __launch_bounds__(kWarps * 32, min_blocks<NT>()) decode_mma_kern
     }
   }
   if (p.cluster == 1) {
-    if (p.n_parts > 1) merge_if_last(p, slice, qrow0, reinterpret_cast<float*>(smem + 24576));
+    // the workspace merge runs with 4-warp CTAs only (the host never plans NW = 8 with parts)
+    if constexpr (NW == 4) {
+      if (p.n_parts > 1) merge_if_last(p, slice, qrow0, reinterpret_cast<float*>(smem + St::EP_SCRATCH));
+    }
     return;
   }
   // ---------------- merge of the splits of one cluster through distributed shared memory.
@@ -867,13 +879,16 @@ __global__ void __launch_bounds__(kWarps * 32, min_blocks<NT>()) decode_mma_kern
     if (p.n_parts > 1) __threadfence();  // slices visible device-wide before the ticket
   }
   cluster.sync();  // the other CTAs keep their shared memory until every rank has read it
-  if (p.n_parts > 1 && cluster.block_rank() == 0) merge_if_last(p, slice, qrow0, reinterpret_cast<float*>(smem + 24576));
+  if constexpr (NW == 4) {
+    if (p.n_parts > 1 && cluster.block_rank() == 0)
+      merge_if_last(p, slice, qrow0, reinterpret_cast<float*>(smem + St::EP_SCRATCH));
+  }
 }
 
-template <int BITS, int NT, int NVG>
+template <int BITS, int NT, int NVG, int NW>
 cudaError_t launch_cfg(const DecodeParams& p, cudaStream_t stream) {
-  constexpr int smem = Stage<BITS, NVG>::SMEM;
-  auto* kern = decode_mma_kernel<BITS, NT, NVG>;
+  constexpr int smem = Stage<BITS, NVG, NW>::SMEM;
+  auto* kern = decode_mma_kernel<BITS, NT, NVG, NW>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   if (p.cluster < 1 || p.cluster > 16 || (p.cluster & (p.cluster - 1)) || p.n_split != p.cluster * p.n_parts)
@@ -884,7 +899,7 @@ cudaError_t launch_cfg(const DecodeParams& p, cudaStream_t stream) {
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.n_split, (unsigned)p.H, (unsigned)p.B);
-  cfg.blockDim = dim3(kWarps * 32, 1, 1);
+  cfg.blockDim = dim3(NW * 32, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
@@ -903,27 +918,27 @@ cudaError_t launch_cfg(const DecodeParams& p, cudaStream_t stream) {
 
 template <int BITS, int NT, int NVG>
 int occupancy_cfg() {
-  constexpr int smem = Stage<BITS, NVG>::SMEM;
-  if (cudaFuncSetAttribute(decode_mma_kernel<BITS, NT, NVG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+  constexpr int smem = Stage<BITS, NVG, 4>::SMEM;
+  if (cudaFuncSetAttribute(decode_mma_kernel<BITS, NT, NVG, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess)
     return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<BITS, NT, NVG>, kWarps * 32, smem) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<BITS, NT, NVG, 4>, 4 * 32, smem) !=
       cudaSuccess)
     return 0;
   return n;
 }
 
 // Clusters of `cs` CTAs that can be resident at once (0 if such a cluster cannot launch).
-template <int BITS, int NT, int NVG>
+template <int BITS, int NT, int NVG, int NW>
 int max_clusters_cfg(int cs) {
-  constexpr int smem = Stage<BITS, NVG>::SMEM;
-  auto* kern = decode_mma_kernel<BITS, NT, NVG>;
+  constexpr int smem = Stage<BITS, NVG, NW>::SMEM;
+  auto* kern = decode_mma_kernel<BITS, NT, NVG, NW>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
   if (cs > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)cs, 1, 1);
-  cfg.blockDim = dim3(kWarps * 32, 1, 1);
+  cfg.blockDim = dim3(NW * 32, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -937,28 +952,42 @@ int max_clusters_cfg(int cs) {
   return n;
 }
 
-template <int BITS>
-int max_clusters_bits(int r, int n_vg, int cs) {
+template <int BITS, int NW>
+int max_clusters_nw(int r, int n_vg, int cs) {
   if (r <= 4) {
-    if (n_vg == 1) return max_clusters_cfg<BITS, 1, 1>(cs);
-    if (n_vg == 2) return max_clusters_cfg<BITS, 1, 2>(cs);
-    return max_clusters_cfg<BITS, 1, 4>(cs);
+    if (n_vg == 1) return max_clusters_cfg<BITS, 1, 1, NW>(cs);
+    if (n_vg == 2) return max_clusters_cfg<BITS, 1, 2, NW>(cs);
+    return max_clusters_cfg<BITS, 1, 4, NW>(cs);
   }
-  if (n_vg == 1) return max_clusters_cfg<BITS, 2, 1>(cs);
-  if (n_vg == 2) return max_clusters_cfg<BITS, 2, 2>(cs);
-  return max_clusters_cfg<BITS, 2, 4>(cs);
+  if (n_vg == 1) return max_clusters_cfg<BITS, 2, 1, NW>(cs);
+  if (n_vg == 2) return max_clusters_cfg<BITS, 2, 2, NW>(cs);
+  return max_clusters_cfg<BITS, 2, 4, NW>(cs);
+}
+
+template <int BITS>
+int max_clusters_bits(int r, int n_vg, int cs, int nw) {
+  return nw == 8 ? max_clusters_nw<BITS, 8>(r, n_vg, cs) : max_clusters_nw<BITS, 4>(r, n_vg, cs);
+}
+
+template <int BITS, int NW>
+cudaError_t launch_nw(const DecodeParams& p, cudaStream_t stream) {
+  if (p.r <= 4) {
+    if (p.n_vg == 1) return launch_cfg<BITS, 1, 1, NW>(p, stream);
+    if (p.n_vg == 2) return launch_cfg<BITS, 1, 2, NW>(p, stream);
+    return launch_cfg<BITS, 1, 4, NW>(p, stream);
+  }
+  if (p.n_vg == 1) return launch_cfg<BITS, 2, 1, NW>(p, stream);
+  if (p.n_vg == 2) return launch_cfg<BITS, 2, 2, NW>(p, stream);
+  return launch_cfg<BITS, 2, 4, NW>(p, stream);
 }
 
 template <int BITS>
 cudaError_t launch_bits(const DecodeParams& p, cudaStream_t stream) {
-  if (p.r <= 4) {
-    if (p.n_vg == 1) return launch_cfg<BITS, 1, 1>(p, stream);
-    if (p.n_vg == 2) return launch_cfg<BITS, 1, 2>(p, stream);
-    return launch_cfg<BITS, 1, 4>(p, stream);
+  if (p.warps == 8) {
+    if (p.n_parts != 1) return cudaErrorInvalidConfiguration;  // 8-warp CTAs merge in clusters only
+    return launch_nw<BITS, 8>(p, stream);
   }
-  if (p.n_vg == 1) return launch_cfg<BITS, 2, 1>(p, stream);
-  if (p.n_vg == 2) return launch_cfg<BITS, 2, 2>(p, stream);
-  return launch_cfg<BITS, 2, 4>(p, stream);
+  return launch_nw<BITS, 4>(p, stream);
 }
 
 template <int BITS>

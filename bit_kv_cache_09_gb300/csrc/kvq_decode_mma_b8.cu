@@ -7,6 +7,6 @@ cudaError_t launch_decode_mma_b8(const DecodeParams& p, cudaStream_t stream) { r
 
 int occupancy_decode_mma_b8(int r, int n_vg) { return mma::occupancy_bits<8>(r, n_vg); }
 
-int max_clusters_decode_mma_b8(int r, int n_vg, int cs) { return mma::max_clusters_bits<8>(r, n_vg, cs); }
+int max_clusters_decode_mma_b8(int r, int n_vg, int cs, int nw) { return mma::max_clusters_bits<8>(r, n_vg, cs, nw); }
 
 }  // namespace kvq

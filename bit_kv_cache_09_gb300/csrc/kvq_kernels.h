@@ -63,6 +63,7 @@ struct DecodeParams {
   int64_t chunk;      // tokens per split (multiple of 128)
   int n_split, cap;
   int cluster;        // CTAs per cluster (splits merged through distributed shared memory)
+  int warps;          // warps per CTA of the tensor-core kernel: 4, or 8 (cluster merges only)
   int n_parts;        // partials merged through the workspace: n_split / cluster
   int B, H, r, G, Gv, R_eff, n_vg;
   int log2G;          // G is a power of two
@@ -98,7 +99,7 @@ cudaError_t launch_dequant(const DequantParams& p, int bits, cudaStream_t stream
 cudaError_t launch_decode_simt(const DecodeParams& p, int bits, cudaStream_t stream);
 cudaError_t launch_decode_mma(const DecodeParams& p, int bits, cudaStream_t stream);
 int occupancy_decode_mma(int bits, int r, int n_vg);  // resident CTAs per SM (0 on error)
-int max_clusters_decode_mma(int bits, int r, int n_vg, int cs);  // resident clusters of cs CTAs
+int max_clusters_decode_mma(int bits, int r, int n_vg, int cs, int nw);  // resident clusters of cs CTAs of nw warps
 int occupancy_decode_simt(int bits);
 
 }  // namespace kvq
