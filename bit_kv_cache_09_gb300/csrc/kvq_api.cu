@@ -242,6 +242,8 @@ kvq_status kvq_quantize_append(const kvq_config* cfg, const kvq_buffers* bufs, i
   p.rowV = g.rowV;
   p.k_codes_slice = g.k_codes_slice;
   p.v_codes_slice = g.v_codes_slice;
+  p.fd_H = kvq::make_fast_div((uint32_t)g.H);
+  p.rows_32 = n_new * g.H < (int64_t(1) << 31);
   cudaError_t e = kvq::launch_append(p, g.bits, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }

@@ -9,6 +9,31 @@
 namespace kvq {
 
 // All pointers are already offset to the layer's first slice (layer, batch 0, head 0).
+// Division by an invariant 32-bit divisor d of dividends below 2^31 (Granlund and
+// Montgomery, "Division by invariant integers using multiplication", PLDI 1994):
+// with l = ceil(log2 d), mul = ceil(2^(31+l) / d) < 2^32 and x < 2^31,
+// floor(x / d) = umulhi(x, mul) >> (l - 1) (the excess of mul*d over 2^(31+l) is below d,
+// so it moves x*mul / 2^(31+l) above x/d by less than 1/d). mul = 0 encodes d = 1.
+struct FastDiv {
+  uint32_t mul, shift;
+};
+
+inline FastDiv make_fast_div(uint32_t d) {
+  FastDiv f{0u, 0u};
+  if (d <= 1) return f;
+  uint32_t l = 0;
+  while ((1ull << l) < d) ++l;
+  f.mul = (uint32_t)(((1ull << (31 + l)) + d - 1) / d);
+  f.shift = l - 1;
+  return f;
+}
+
+#ifdef __CUDACC__
+__device__ __forceinline__ uint32_t fast_div(uint32_t x, FastDiv f) {
+  return f.mul ? (__umulhi(x, f.mul) >> f.shift) : x;
+}
+#endif
+
 struct AppendParams {
   uint8_t* k_codes;
   __half2* k_meta;
@@ -24,6 +49,8 @@ struct AppendParams {
   int B, H, G, Gv, R_eff, n_vg;
   int64_t S_pad, rowK, rowV;
   int64_t k_codes_slice, v_codes_slice;
+  FastDiv fd_H;     // division by H of value-row indices below 2^31
+  int rows_32;      // n_new * H < 2^31: value-row indices fit the fast division
 };
 
 struct DequantParams {

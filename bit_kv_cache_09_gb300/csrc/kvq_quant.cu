@@ -60,12 +60,16 @@ __global__ void __launch_bounds__(256, 4) k_group_kernel(AppendParams p) {
   // min/max of binary16 values is exact in binary16
   uint2 x[PER_WARP];
   __half2 mn2[2], mx2[2];
-  const __half* resid = p.k_resid + slice * (int64_t)p.R_eff * kHeadDim;
+  // token t < s_cur is a residual row (slot t - A0, where A0 = group0 * G is the start
+  // of the flushed window, a multiple of the window), token t >= s_cur input row
+  // (b, t - s_cur, h)
+  const __half* resid = p.k_resid + (slice * (int64_t)p.R_eff - p.group0 * G) * kHeadDim;
+  const __half* in = p.k_in + (((int64_t)b * p.n_new - p.s_cur) * p.H + h) * kHeadDim;
+  const int64_t in_stride = (int64_t)p.H * kHeadDim;
 #pragma unroll
   for (int k = 0; k < PER_WARP; ++k) {
     const int64_t t = t0 + warp + 8 * k;
-    const __half* row = (t < p.s_cur) ? resid + (t % p.R_eff) * kHeadDim
-                                      : p.k_in + (((int64_t)b * p.n_new + (t - p.s_cur)) * p.H + h) * kHeadDim;
+    const __half* row = (t < p.s_cur) ? resid + t * kHeadDim : in + t * in_stride;
     x[k] = *reinterpret_cast<const uint2*>(row + 4 * lane);
     const __half2 a = *reinterpret_cast<const __half2*>(&x[k].x), c = *reinterpret_cast<const __half2*>(&x[k].y);
     if (k == 0) {
@@ -93,10 +97,10 @@ __global__ void __launch_bounds__(256, 4) k_group_kernel(AppendParams p) {
       z = fmaxf(z, red_max[w][c]);
     }
     __half s_h, z_h;
-    float s, zp;
-    group_params<BITS>(a, z, s_h, z_h, s, zp);
+    float s, rs, zp;
+    group_params<BITS>(a, z, s_h, z_h, s, rs, zp);
     s_sc[c] = s;
-    s_rs[c] = __frcp_rn(s);
+    s_rs[c] = rs;
     s_zp[c] = __fsub_rn(zp, Q<BITS>::qmin);
     p.k_meta[(slice * (p.S_pad / G) + g) * kHeadDim + c] = __halves2half2(s_h, z_h);
   }
@@ -130,18 +134,28 @@ __global__ void __launch_bounds__(256, 4) k_group_kernel(AppendParams p) {
 // 2-bit units four.
 // ---------------------------------------------------------------------------
 template <int BITS>
-__global__ void __launch_bounds__(256) v_token_kernel(AppendParams p, int64_t n_rows) {
+__global__ void __launch_bounds__(256) v_token_kernel(AppendParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sl = lane & 7;
-  const int64_t w_raw = ((int64_t)blockIdx.x * 8 + warp) * 4 + (lane >> 3);
+  // rows of batch row b = blockIdx.y in the input's order (token, kv head)
+  const int64_t nb = p.n_new * p.H;
+  const int64_t wb_raw = ((int64_t)blockIdx.x * 8 + warp) * 4 + (lane >> 3);
   pdl_wait();
   pdl_allow_dependents();
-  const bool valid = w_raw < n_rows;
-  const int64_t w = valid ? w_raw : n_rows - 1;  // lanes past the end read a real row and store nothing
-  const int h = (int)(w % p.H);
-  const int64_t bt = w / p.H;
-  const int64_t t = p.s_cur + bt % p.n_new;
-  const int b = (int)(bt / p.n_new);
+  const bool valid = wb_raw < nb;
+  const int64_t wb = valid ? wb_raw : nb - 1;  // lanes past the end read a real row and store nothing
+  int64_t tt;
+  int h;
+  if (p.rows_32) {
+    tt = fast_div((uint32_t)wb, p.fd_H);
+    h = (int)(wb - tt * p.H);
+  } else {
+    tt = wb / p.H;
+    h = (int)(wb % p.H);
+  }
+  const int b = blockIdx.y;
+  const int64_t w = (int64_t)b * nb + wb;
+  const int64_t t = p.s_cur + tt;
   const int64_t slice = (int64_t)b * p.H + h;
 
   float x[16];
@@ -168,10 +182,10 @@ __global__ void __launch_bounds__(256) v_token_kernel(AppendParams p, int64_t n_
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
   }
   __half s_h, z_h;
-  float s, zp;
-  group_params<BITS>(mn, mx, s_h, z_h, s, zp);
+  float s, rs, zp;
+  group_params<BITS>(mn, mx, s_h, z_h, s, rs, zp);
   if (valid && sl % lpg == 0) p.v_meta[(slice * p.S_pad + t) * p.n_vg + sl / lpg] = __halves2half2(s_h, z_h);
-  const float rs = __frcp_rn(s), zpu = __fsub_rn(zp, Q<BITS>::qmin);
+  const float zpu = __fsub_rn(zp, Q<BITS>::qmin);
   uint32_t u[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) u[i] = quant_code<BITS>(x[i], s, rs, zpu);
@@ -226,7 +240,7 @@ __global__ void __launch_bounds__(256) v_token_kernel(AppendParams p, int64_t n_
   // Keys of tokens past the last full residual window go to the residual.
   if (valid && t >= p.A1) {
     const uint4* ks = reinterpret_cast<const uint4*>(p.k_in + w * kHeadDim + 16 * sl);
-    uint4* kd = reinterpret_cast<uint4*>(p.k_resid + (slice * p.R_eff + t % p.R_eff) * kHeadDim + 16 * sl);
+    uint4* kd = reinterpret_cast<uint4*>(p.k_resid + (slice * p.R_eff + (t - p.A1)) * kHeadDim + 16 * sl);
     kd[0] = ks[0];
     kd[1] = ks[1];
   }
@@ -288,8 +302,9 @@ cudaError_t launch_append_bits(const AppendParams& p, cudaStream_t stream) {
     }
     if (e != cudaSuccess) return e;
   }
-  const int64_t rows = (int64_t)p.B * p.n_new * p.H;
-  cudaError_t e = launch_pdl(v_token_kernel<BITS>, dim3((unsigned)((rows + 31) / 32)), dim3(256), 0, stream, p, rows);
+  const int64_t rows = p.n_new * p.H;  // per batch row
+  cudaError_t e = launch_pdl(v_token_kernel<BITS>, dim3((unsigned)((rows + 31) / 32), (unsigned)p.B), dim3(256), 0,
+                             stream, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

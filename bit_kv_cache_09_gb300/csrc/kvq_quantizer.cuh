@@ -26,9 +26,39 @@ struct Q {
   static constexpr float qmax = (float)((1 << (BITS - 1)) - 1);
 };
 
-// Group parameters from the (exact) binary32 min and max of binary16 inputs.
+// Correctly rounded binary32 quotient a / b from the correctly rounded reciprocal
+// rb = RN(1/b), by Markstein's fma correction (P. W. Markstein, "Computation of
+// elementary functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1),
+// 1990): q0 = RN(a * rb) lies within 1.5 ulp of a/b, the remainder a - b*q0 is exactly
+// representable (one fma computes it), and q0 + remainder*rb = a/b + e with
+// |e| <= 1.5 * 2^-24 ulp, so the final fma returns RN(a/b) whenever a/b, if it is not a
+// binary32 number, lies farther than that from every rounding midpoint (a = -0 gives
+// +0; every use rounds the quotient to an integer and adds one, so the sign of a zero
+// quotient never shows). The two uses:
+//  * a and b binary16 values (11-bit significands; the quantizer's x/s and x_min/s):
+//    the remainder is a multiple of ulp(b)*ulp(q0) below 2^12 of them, and such a
+//    quotient lies at least 2^-12 ulp from every midpoint;
+//  * a any positive binary32 and b = 2^bits - 1 (odd, at most 8 bits; the scale's
+//    range/levels): the remainder is an integer multiple of ulp(a/b) below 2^9 of them,
+//    and a - m*b is an odd multiple of ulp(a/b)/2 for every midpoint m, so the quotient
+//    lies at least 2^-9 ulp from every midpoint.
+__device__ __forceinline__ float div_rn(float a, float b, float rb) {
+  const float q0 = __fmul_rn(a, rb);
+  const float r = __fmaf_rn(-b, q0, a);
+  return __fmaf_rn(r, rb, q0);
+}
+
+// RN(1 / (2^BITS - 1)) as binary32 bit patterns.
 template <int BITS>
-__device__ __forceinline__ void group_params(float xmin, float xmax, __half& s_h, __half& z_h, float& s, float& zp) {
+__device__ __forceinline__ float inv_levels() {
+  return __int_as_float(BITS == 8 ? 0x3B808081 : (BITS == 4 ? 0x3D888889 : 0x3EAAAAAB));
+}
+
+// Group parameters from the (exact) binary32 min and max of binary16 inputs:
+// binary16 scale s_h and zero point z_h, and as binary32 s, rs = RN(1/s), zp.
+template <int BITS>
+__device__ __forceinline__ void group_params(float xmin, float xmax, __half& s_h, __half& z_h, float& s, float& rs,
+                                             float& zp) {
   if (xmax == xmin) {  // a constant group is widened to include 0
     if (xmin > 0.0f) xmin = 0.0f;
     if (xmax < 0.0f) xmax = 0.0f;
@@ -37,28 +67,14 @@ __device__ __forceinline__ void group_params(float xmin, float xmax, __half& s_h
     s_h = __float2half_rn(1.0f);  // all zeros: scale 1
   } else {
     const float range = __fsub_rn(xmax, xmin);
-    s_h = __float2half_ru(__fdiv_rn(range, __fsub_rn(Q<BITS>::qmax, Q<BITS>::qmin)));
+    s_h = __float2half_ru(div_rn(range, __fsub_rn(Q<BITS>::qmax, Q<BITS>::qmin), inv_levels<BITS>()));
   }
   s = __half2float(s_h);
-  float z = __fsub_rn(Q<BITS>::qmin, rintf(__fdiv_rn(xmin, s)));
+  rs = __frcp_rn(s);
+  float z = __fsub_rn(Q<BITS>::qmin, rintf(div_rn(xmin, s, rs)));
   z = fminf(fmaxf(z, -65504.0f), 65504.0f);
   z_h = __float2half_rn(z);
   zp = __half2float(z_h);
-}
-
-// Correctly rounded binary32 quotient x / s for binary16 operands x and s, from the
-// correctly rounded reciprocal rs = RN(1/s), by Markstein's fma correction (P. W.
-// Markstein, "Computation of elementary functions on the IBM RISC System/6000
-// processor", IBM J. Res. Dev. 34(1), 1990): q0 = RN(x * rs) lies within 1.5 ulp of
-// x/s; the remainder x - s*q0 is then a multiple of ulp(s)*ulp(q0) below 2^12 of them,
-// so one fma computes it exactly; and q0 + remainder*rs = x/s + e with
-// |e| <= 1.5 * 2^-24 ulp. A quotient of two 11-bit binary16 numbers that is not itself
-// a binary32 number lies at least 2^-12 ulp away from every rounding midpoint, so the
-// final fma returns RN(x/s), the same value as an IEEE division.
-__device__ __forceinline__ float div_rn_f16(float x, float s, float rs) {
-  const float q0 = __fmul_rn(x, rs);
-  const float r = __fmaf_rn(-s, q0, x);
-  return __fmaf_rn(r, rs, q0);
 }
 
 // Code u = clamp(rint(x/s) + zp, q_min, q_max) - q_min of x in a group with binary16
@@ -66,7 +82,7 @@ __device__ __forceinline__ float div_rn_f16(float x, float s, float rs) {
 // by q_min is exact and the clamp bounds become [0, 2^b - 1]).
 template <int BITS>
 __device__ __forceinline__ uint32_t quant_code(float x, float s, float rs, float zpu) {
-  float q = __fadd_rn(rintf(div_rn_f16(x, s, rs)), zpu);
+  float q = __fadd_rn(rintf(div_rn(x, s, rs)), zpu);
   q = fminf(fmaxf(q, 0.0f), (float)((1 << BITS) - 1));
   return (uint32_t)(int)q;
 }
@@ -104,11 +120,10 @@ __device__ __forceinline__ void quantize_value_row(const __half* v_row, uint16_t
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
   }
   __half s_h, z_h;
-  float s, zp;
-  group_params<BITS>(mn, mx, s_h, z_h, s, zp);
+  float s, rs, zp;
+  group_params<BITS>(mn, mx, s_h, z_h, s, rs, zp);
   if (lane % lanes_per_group == 0) meta[lane / lanes_per_group] = __halves2half2(s_h, z_h);
-#pragma unroll
-  const float rs = __frcp_rn(s), zpu = __fsub_rn(zp, Q<BITS>::qmin);
+  const float zpu = __fsub_rn(zp, Q<BITS>::qmin);
 #pragma unroll
   for (int e = 0; e < 4; ++e) codes_s[4 * lane + e] = (uint8_t)quant_code<BITS>(x[e], s, rs, zpu);
   __syncwarp();
