@@ -398,24 +398,54 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : 1) decod
   }
   for (int i = 0; i < min(NS, n_mine); ++i) issue(i, i);
 
-  // query rows of this kv head, binary32, in shared memory
-  for (int idx = threadIdx.x; idx < r * kHeadDim; idx += kWarps * 32)
-    q_s[idx >> 7][idx & 127] = __half2float(p.q[qrow0 * kHeadDim + idx]);
-  __syncthreads();
-  // per-row power-of-two normalisation: qmax * 2^qe in [2^7, 2^8)
+  // Query rows of this kv head: warp w takes rows w, w + NW, ...; lane l holds channels
+  // [4l, 4l+4). Each row goes to q_s (binary32, for residual keys) and, normalised by
+  // 2^qe (qmax * 2^qe in [2^7, 2^8)) and divided by k_scale, to q2_s in key-pair order:
+  // pair pi of chunk c = l/8 joins channels ca(pi) and cb(pi), which lie in this lane
+  // (8-bit codes) or in the lane 1 (4-bit) or 2 (2-bit) above it.
   for (int i = warp; i < r; i += kWarps) {
-    float a = fmaxf(fmaxf(fabsf(q_s[i][lane]), fabsf(q_s[i][lane + 32])),
-                    fmaxf(fabsf(q_s[i][lane + 64]), fabsf(q_s[i][lane + 96])));
+    const uint2 raw = *reinterpret_cast<const uint2*>(p.q + (qrow0 + i) * kHeadDim + 4 * lane);
+    float xq[4];
+    {
+      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+      const float2 c2 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+      xq[0] = a.x; xq[1] = a.y; xq[2] = c2.x; xq[3] = c2.y;
+    }
+    reinterpret_cast<float4*>(&q_s[i][0])[lane] = make_float4(xq[0], xq[1], xq[2], xq[3]);
+    float a = fmaxf(fmaxf(fabsf(xq[0]), fabsf(xq[1])), fmaxf(fabsf(xq[2]), fabsf(xq[3])));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-    if (lane == 0) qe_s[i] = a > 0.0f ? 7 - (((__float_as_int(a) >> 23) & 0xFF) - 127) : 0;
-  }
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < r * 64; idx += kWarps * 32) {
-    const int i = idx >> 6, c = (idx >> 4) & 3, pi = idx & 15;
-    const float f = pow2f(qe_s[i]) / k_scale<BITS>(pi);  // exact: powers of two
-    q2_s[i][c][pi] = h2_bits(__floats2half2_rn(q_s[i][32 * c + k_pair_ca<BITS>(pi)] * f,
-                                               q_s[i][32 * c + k_pair_cb<BITS>(pi)] * f));
+    const int qe = a > 0.0f ? 7 - (((__float_as_int(a) >> 23) & 0xFF) - 127) : 0;
+    if (lane == 0) qe_s[i] = qe;
+    const float f = pow2f(qe);  // exact scaling by a power of two
+    float v[4], w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) v[k] = xq[k] * f;
+    constexpr int D = BITS == 8 ? 0 : (BITS == 4 ? 1 : 2);  // lane distance of a pair's second channel
+#pragma unroll
+    for (int k = 0; k < 4; ++k) w[k] = D ? __shfl_down_sync(0xffffffffu, v[k], D) : v[k];
+    const int lc = lane & 7, c = lane >> 3;  // lane within its chunk, chunk
+    if (BITS == 8) {  // pairs 2lc (channels 4lc, 4lc+1) and 2lc+1 (4lc+2, 4lc+3)
+      q2_s[i][c][2 * lc] = h2_bits(__floats2half2_rn(v[0], v[1]));
+      q2_s[i][c][2 * lc + 1] = h2_bits(__floats2half2_rn(v[2], v[3]));
+    } else if (BITS == 4) {  // even lc: pairs 4m + e join channels 8m + e and 8m + e + 4 (m = lc/2)
+      if ((lc & 1) == 0) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float ks = k_scale<BITS>(e);
+          q2_s[i][c][2 * lc + e] = h2_bits(__floats2half2_rn(v[e] / ks, w[e] / ks));
+        }
+      }
+    } else {  // lc % 4 < 2: pairs 8m + 4(lc & 1) + k join channels 16m + 4(lc & 1) + k and + 8
+      if ((lc & 3) < 2) {
+        const int pi0 = 8 * (lc >> 2) + 4 * (lc & 1);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float ks = (lc & 1) ? k_scale<BITS>(4 + k) : k_scale<BITS>(k);
+          q2_s[i][c][pi0 + k] = h2_bits(__floats2half2_rn(v[k] / ks, w[k] / ks));
+        }
+      }
+    }
   }
   __syncthreads();
 

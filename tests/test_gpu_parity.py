@@ -194,7 +194,8 @@ def test_fused_decode_step(bits, G, Gv, R, r):
 def _all_f16_values():
     """Every finite binary16 value, as float64, sorted, with its bit pattern."""
     bits = np.arange(0x10000, dtype=np.uint32).astype(np.uint16)
-    vals = bits.view(np.float16).astype(np.float64)
+    with np.errstate(invalid="ignore"):
+        vals = bits.view(np.float16).astype(np.float64)
     ok = np.isfinite(vals)
     order = np.argsort(vals[ok], kind="stable")
     return vals[ok][order], bits[ok][order]
