@@ -254,3 +254,26 @@ def test_quantize_near_rounding_midpoints(bits):
         q = _dev(synth.gen_q(w.seed, 0, range(w.batch), T, w.n_q, w.d_head))
         cache.decode_step(0, T, _dev(k_host[:, T:T + 1]), _dev(v_host[:, T:T + 1]), q, softmax_scale(w))
     _check_all_slices(cache, w, 0, 64 + w.steps, k_host, v_host)
+
+
+@pytest.mark.parametrize("bits,G,Gv,R,r", [(8, 128, 128, 0, 4), (4, 128, 64, 128, 8), (2, 32, 32, 128, 3)])
+def test_small_grid_long_sequence(bits, G, Gv, R, r):
+    """Two (batch row, kv head) pairs over ~4k tokens: the plan runs each pair as one
+    16-CTA cluster of 8-warp CTAs (each warp then owns one 32-token iteration), through
+    both the attention call and the fused decode step."""
+    w = small_workload(bits=bits, G=G, Gv=Gv, R=R, r=r, B=1, H=2, S=3900, steps=3, seed=5000 + bits + r)
+    cache = QuantizedKVCache.for_workload(w)
+    k_host, v_host = host_layer_inputs(w, 0, 0, w.max_seq)
+    cache.append(0, 0, _dev(k_host[:, :w.seq]), _dev(v_host[:, :w.seq]))
+    q0 = synth.gen_q(w.seed, 0, range(w.batch), w.seq - 1, w.n_q, w.d_head)
+    _check_attention(cache, w, 0, w.seq, k_host, v_host, q0, kvq.DECODE_MMA)
+    for s in range(w.steps):
+        T = w.seq + s
+        q_host = synth.gen_q(w.seed, 0, range(w.batch), T, w.n_q, w.d_head)
+        out = cache.decode_step(0, T, _dev(k_host[:, T:T + 1]), _dev(v_host[:, T:T + 1]), _dev(q_host),
+                                softmax_scale(w)).cpu().numpy()
+        for h in range(w.n_kv):
+            st = oracle_slice_state(k_host[0, :T + 1, h], v_host[0, :T + 1, h], cache)
+            ref = oracle_attention(st, q_host[0, h * w.gqa:(h + 1) * w.gqa], cache, softmax_scale(w))
+            assert float(np.abs(out[0, h * w.gqa:(h + 1) * w.gqa] - ref).max()) <= ATOL
+    _check_all_slices(cache, w, 0, w.max_seq, k_host, v_host)
