@@ -51,18 +51,24 @@ int device_sm_count() {
 }
 
 // Resident CTAs per SM of the decode kernel that `impl` selects (cached per device).
+// Index of the (key, value) code widths: 8/8, 4/4, 2/2, 8/4.
+int width_index(const Geometry& g) {
+  if (g.vbits != g.bits) return 3;
+  return g.bits == 8 ? 0 : (g.bits == 4 ? 1 : 2);
+}
+
 int decode_occupancy(const Geometry& g, kvq_decode_impl impl) {
-  static std::atomic<int> cache[16][2][3][2][3];  // device, impl, bits, r class, value groups
+  static std::atomic<int> cache[16][2][4][2][3];  // device, impl, code widths, r class, value groups
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) dev = 0;
   const int ii = impl == KVQ_DECODE_SIMT ? 0 : 1;
-  const int bi = g.bits == 8 ? 0 : (g.bits == 4 ? 1 : 2);
+  const int bi = width_index(g);
   const int ri = g.r <= 4 ? 0 : 1;
   const int vi = g.n_vg == 1 ? 0 : (g.n_vg == 2 ? 1 : 2);
   std::atomic<int>& slot = cache[dev][ii][bi][ri][vi];
   int n = slot.load(std::memory_order_relaxed);
   if (n <= 0) {
-    n = ii == 0 ? kvq::occupancy_decode_simt(g.bits) : kvq::occupancy_decode_mma(g.bits, g.r, g.n_vg);
+    n = ii == 0 ? kvq::occupancy_decode_simt(g.bits) : kvq::occupancy_decode_mma(g.bits, g.vbits, g.r, g.n_vg);
     if (n > 0) slot.store(n, std::memory_order_relaxed);
   }
   return n > 0 ? n : 1;
@@ -72,10 +78,10 @@ int decode_occupancy(const Geometry& g, kvq_decode_impl impl) {
 // kernel that can be resident at once on this device (<= 0: such a cluster cannot
 // launch); cached per device and kernel shape.
 int resident_clusters(const Geometry& g, int cs, int nw) {
-  static std::atomic<int> cache[16][3][2][3][5][2];  // device, bits, r class, value groups, log2 size, warps
+  static std::atomic<int> cache[16][4][2][3][5][2];  // device, code widths, r class, value groups, log2 size, warps
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) dev = 0;
-  const int bi = g.bits == 8 ? 0 : (g.bits == 4 ? 1 : 2);
+  const int bi = width_index(g);
   const int ri = g.r <= 4 ? 0 : 1;
   const int vi = g.n_vg == 1 ? 0 : (g.n_vg == 2 ? 1 : 2);
   int lg = 0;
@@ -83,7 +89,7 @@ int resident_clusters(const Geometry& g, int cs, int nw) {
   std::atomic<int>& slot = cache[dev][bi][ri][vi][lg][nw == 8 ? 1 : 0];
   int n = slot.load(std::memory_order_relaxed);
   if (n == 0) {
-    n = kvq::max_clusters_decode_mma(g.bits, g.r, g.n_vg, cs, nw);
+    n = kvq::max_clusters_decode_mma(g.bits, g.vbits, g.r, g.n_vg, cs, nw);
     if (n <= 0) n = -1;
     slot.store(n, std::memory_order_relaxed);
   }
@@ -244,7 +250,7 @@ kvq_status kvq_quantize_append(const kvq_config* cfg, const kvq_buffers* bufs, i
   p.v_codes_slice = g.v_codes_slice;
   p.fd_H = kvq::make_fast_div((uint32_t)g.H);
   p.rows_32 = n_new * g.H < (int64_t(1) << 31);
-  cudaError_t e = kvq::launch_append(p, g.bits, static_cast<cudaStream_t>(stream));
+  cudaError_t e = kvq::launch_append(p, g.bits, g.vbits, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
@@ -279,7 +285,7 @@ kvq_status kvq_dequantize(const kvq_config* cfg, const kvq_buffers* bufs, int32_
   p.rowV = g.rowV;
   p.k_codes_slice = g.k_codes_slice;
   p.v_codes_slice = g.v_codes_slice;
-  cudaError_t e = kvq::launch_dequant(p, g.bits, static_cast<cudaStream_t>(stream));
+  cudaError_t e = kvq::launch_dequant(p, g.bits, g.vbits, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
@@ -353,6 +359,7 @@ kvq_status decode_launch(const kvq_config* cfg, const kvq_buffers* bufs, int32_t
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   const kvq_decode_impl use = impl == KVQ_DECODE_SIMT ? KVQ_DECODE_SIMT : KVQ_DECODE_MMA;
   if (use == KVQ_DECODE_SIMT && (k_new || v_new)) return KVQ_ERR_UNSUPPORTED;
+  if (use == KVQ_DECODE_SIMT && g.vbits != g.bits) return KVQ_ERR_UNSUPPORTED;  // CUDA-core kernel: equal widths
   const Plan pl = plan_splits(g, s_cur, use);
   p.n_split = (int)pl.n_split;
   p.chunk = pl.chunk;
@@ -360,7 +367,7 @@ kvq_status decode_launch(const kvq_config* cfg, const kvq_buffers* bufs, int32_t
   p.n_parts = pl.n_parts;
   p.warps = pl.warps;
   cudaError_t e = (use == KVQ_DECODE_SIMT) ? kvq::launch_decode_simt(p, g.bits, static_cast<cudaStream_t>(stream))
-                                            : kvq::launch_decode_mma(p, g.bits, static_cast<cudaStream_t>(stream));
+                                            : kvq::launch_decode_mma(p, g.bits, g.vbits, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 

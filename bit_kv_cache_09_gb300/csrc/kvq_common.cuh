@@ -22,7 +22,7 @@ constexpr int kMaxGqa = 8;        // query heads per kv head handled by one CTA
 constexpr int kMaxResidual = 1024;
 
 struct Geometry {
-  int L, B, H, r, d, S_max, bits, G, Gv, R, R_eff;
+  int L, B, H, r, d, S_max, bits, vbits, G, Gv, R, R_eff;  // bits: keys, vbits: values
   int64_t S_pad;
   int64_t rowK, rowV;  // bytes per token row of key / value codes
   int n_vg;            // value groups per token (d / Gv)
@@ -37,6 +37,9 @@ inline kvq_status make_geometry(const kvq_config* c, Geometry* g) {
       c->max_seq_len < 1 || c->k_group < 1 || c->v_group < 1 || c->residual_len < 0)
     return KVQ_ERR_INVALID_ARG;
   if (c->bits != 2 && c->bits != 4 && c->bits != 8) return KVQ_ERR_UNSUPPORTED;
+  const int vbits = c->v_bits == 0 ? c->bits : c->v_bits;
+  if (vbits != 2 && vbits != 4 && vbits != 8) return KVQ_ERR_UNSUPPORTED;
+  if (vbits != c->bits && !(c->bits == 8 && vbits == 4)) return KVQ_ERR_UNSUPPORTED;  // mixed: 8-bit keys, 4-bit values
   if (c->d_head != kHeadDim) return KVQ_ERR_UNSUPPORTED;
   if (c->k_group != 32 && c->k_group != 64 && c->k_group != 128) return KVQ_ERR_UNSUPPORTED;
   if (c->v_group != 32 && c->v_group != 64 && c->v_group != 128) return KVQ_ERR_UNSUPPORTED;
@@ -52,13 +55,14 @@ inline kvq_status make_geometry(const kvq_config* c, Geometry* g) {
   x.d = c->d_head;
   x.S_max = c->max_seq_len;
   x.bits = c->bits;
+  x.vbits = vbits;
   x.G = c->k_group;
   x.Gv = c->v_group;
   x.R = c->residual_len;
   x.R_eff = c->residual_len > 0 ? c->residual_len : c->k_group;
   x.S_pad = ((int64_t)c->max_seq_len + kSeqAlign - 1) / kSeqAlign * kSeqAlign;
   x.rowK = (int64_t)x.d * x.bits / 8;
-  x.rowV = x.rowK;
+  x.rowV = (int64_t)x.d * x.vbits / 8;
   x.n_vg = x.d / x.Gv;
   x.k_codes_slice = x.S_pad * x.rowK;
   x.k_meta_slice = (x.S_pad / x.G) * x.d * 4;

@@ -194,10 +194,10 @@ __device__ __forceinline__ constexpr float v_scale(int i) {
 // NW warps per CTA each own a ring of NS stages. After the loop the rings are reused
 // for the merges: per-warp partials (o, m, l, beta), the CTA partial read by the
 // cluster merge (cm, cl, co), then the scratch of the workspace merge.
-template <int BITS, int NVG, int NW>
+template <int BITS, int VBITS, int NVG, int NW>
 struct Stage {
-  static constexpr int KB = 32 * BITS * 128 / 8;  // key codes of 32 tokens
-  static constexpr int VB = KB;                   // value codes of 32 tokens
+  static constexpr int KB = 32 * BITS * 128 / 8;   // key codes of 32 tokens
+  static constexpr int VB = 32 * VBITS * 128 / 8;  // value codes of 32 tokens
   static constexpr int VM = 32 * 4 * NVG;         // value meta of 32 tokens
   static constexpr int KM = 512;                  // one key group's meta
   static constexpr int BYTES = KB + VB + VM + KM;
@@ -303,19 +303,22 @@ constexpr int min_blocks() {
   return NT == 1 ? 4 : 2;
 }
 
-// BITS: code width; NT: PV n-tiles (1: r <= 4, hi/lo halves share one tile;
+// BITS, VBITS: key and value code widths; NT: PV n-tiles (1: r <= 4, hi/lo halves share one tile;
 // 2: r <= 8, hi tile + lo tile); NVG: value groups per token (d / Gv); NW: warps per
 // CTA (4; 8 for small cluster-merged grids, where one CTA per SM is resident anyway and
 // twice the warps halve the iterations on the critical path).
-template <int BITS, int NT, int NVG, int NW>
+template <int BITS, int VBITS, int NT, int NVG, int NW>
 __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : 1) decode_mma_kernel(DecodeParams p) {
   constexpr int kWarps = NW;
-  using St = Stage<BITS, NVG, NW>;
+  using St = Stage<BITS, VBITS, NVG, NW>;
   constexpr int NS = St::NS;
   constexpr int kTok = 32;  // tokens per iteration
-  constexpr float qmin = -(float)(1 << (BITS - 1));
+  constexpr float qmin = -(float)(1 << (BITS - 1));     // keys
+  constexpr float qmin_v = -(float)(1 << (VBITS - 1));  // values
   constexpr int CW = Chunk<BITS>::WORDS;
-  constexpr int ROW = BITS * 128 / 8;  // bytes per key row / value row
+  constexpr int CWV = Chunk<VBITS>::WORDS;
+  constexpr int ROW = BITS * 128 / 8;    // bytes per key row
+  constexpr int ROWV = VBITS * 128 / 8;  // bytes per value row
   constexpr float kTwo24 = 16777216.0f;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bars[kWarps][NS];
@@ -355,7 +358,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : 1) decod
 
   // sources of the warp's first iteration; iteration i adds 32*i tokens
   const uint8_t* k_src = p.k_codes + slice * p.k_codes_slice + (int64_t)ts0 * ROW;
-  const uint8_t* v_src = p.v_codes + slice * p.v_codes_slice + (int64_t)ts0 * ROW;
+  const uint8_t* v_src = p.v_codes + slice * p.v_codes_slice + (int64_t)ts0 * ROWV;
   const uint8_t* vm_src = reinterpret_cast<const uint8_t*>(p.v_meta + (slice * p.S_pad + ts0) * NVG);
   const __half2* km_base = p.k_meta + slice * (p.S_pad >> p.log2G) * kHeadDim;
 
@@ -365,18 +368,18 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : 1) decod
   // few instructions per lane and iteration.
   const uint32_t wbase_s = smem_u32(wbase) + 16 * lane;
   auto issue = [&](int i, int sidx) {
-    constexpr int CK = St::KB / 512;  // pieces per lane of the key / value codes
+    constexpr int CK = St::KB / 512, CKV = St::VB / 512;  // pieces per lane of the key / value codes
     const int ts = ts0 + i * kTok;
     const uint32_t dst = wbase_s + sidx * St::BYTES;
     const bool quant = ts < Tq;
     const bool newgrp = quant && (i == 0 || (ts & (p.G - 1)) == 0);
-    const size_t off = (size_t)i * St::KB + 16 * lane;
+    const size_t off = (size_t)i * St::KB + 16 * lane, offv = (size_t)i * St::VB + 16 * lane;
     if (quant) {
 #pragma unroll
       for (int c = 0; c < CK; ++c) cp_async16(dst + 512 * c, k_src + off + 512 * c);
     }
 #pragma unroll
-    for (int c = 0; c < CK; ++c) cp_async16(dst + St::KB + 512 * c, v_src + off + 512 * c);
+    for (int c = 0; c < CKV; ++c) cp_async16(dst + St::KB + 512 * c, v_src + offv + 512 * c);
     if (16 * lane < St::VM) cp_async16(dst + St::KB + St::VB, vm_src + (size_t)i * St::VM + 16 * lane);
     if (newgrp) cp_async16(dst + St::KB + St::VB + St::VM, km_base + ((ts >> p.log2G) << 7) + 4 * lane);
     cp_async_arrive(smem_u32(&bars[warp][sidx]));
@@ -388,8 +391,8 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : 1) decod
     if (warp == 0) {
       const int t_new = T - 1;
       const int64_t row = (int64_t)b * p.H + h;  // [B][1][H][d]
-      uint16_t* pair = reinterpret_cast<uint16_t*>(p.v_codes_w + slice * p.v_codes_slice + (int64_t)(t_new >> 1) * 2 * ROW);
-      quant::quantize_value_row<BITS>(p.v_new + row * kHeadDim, pair, t_new & 1,
+      uint16_t* pair = reinterpret_cast<uint16_t*>(p.v_codes_w + slice * p.v_codes_slice + (int64_t)(t_new >> 1) * 2 * ROWV);
+      quant::quantize_value_row<VBITS>(p.v_new + row * kHeadDim, pair, t_new & 1,
                                       p.v_meta_w + (slice * p.S_pad + t_new) * NVG, p.Gv, lane, smem);
       const uint2 kv = *reinterpret_cast<const uint2*>(p.k_new + row * kHeadDim + 4 * lane);
       *reinterpret_cast<uint2*>(p.k_resid_w + (slice * p.R_eff + t_new % p.R_eff) * kHeadDim + 4 * lane) = kv;
@@ -659,7 +662,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : 1) decod
     // kTau (log2 units), so p = 2^(s - m_run) <= 2^kTau. kTau keeps every binary16
     // weight p*s finite for any binary16 value group: the largest value scale is
     // 131008 / (2^b - 1) rounded up (514, 8734, 43669 for b = 8, 4, 2).
-    constexpr float kTau = BITS == 8 ? 6.0f : (BITS == 4 ? 2.0f : 0.5f);
+    constexpr float kTau = VBITS == 8 ? 6.0f : (VBITS == 4 ? 2.0f : 0.5f);
     if (__any_sync(0xffffffffu, m_new > m_run + kTau)) {
       const float alpha = ex2(m_run - m_new);  // 0 on the first iteration (m_run = -inf)
       l_run *= alpha;
@@ -691,10 +694,10 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : 1) decod
     // values: weights p * s per value group, split into binary16 halves
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
-      uint32_t vw[2][CW];
+      uint32_t vw[2][CWV];
 #pragma unroll
       for (int pi = 0; pi < 2; ++pi)
-        lds_chunk<BITS>(st + St::KB + (8 * hf + 4 * pi + j) * (2 * ROW) + g * (ROW / 4), vw[pi]);
+        lds_chunk<VBITS>(st + St::KB + (8 * hf + 4 * pi + j) * (2 * ROWV) + g * (ROWV / 4), vw[pi]);
       const __half2* vms = reinterpret_cast<const __half2*>(st + St::KB + St::VB) + 16 * hf * NVG;
       __half2 mlo[2 * NVG], mhi[2 * NVG];  // tokens (2j, 2j+1) and (8+2j, 9+2j)
       lds_vmeta<NVG>(vms + (2 * j) * NVG, mlo);
@@ -730,8 +733,8 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : 1) decod
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         const int vg = (mt * NVG) / 8;  // compile-time after unrolling
-        const uint32_t a0 = v_pair<BITS>(vw[0], 2 * mt), a1 = v_pair<BITS>(vw[0], 2 * mt + 1);
-        const uint32_t a2 = v_pair<BITS>(vw[1], 2 * mt), a3 = v_pair<BITS>(vw[1], 2 * mt + 1);
+        const uint32_t a0 = v_pair<VBITS>(vw[0], 2 * mt), a1 = v_pair<VBITS>(vw[0], 2 * mt + 1);
+        const uint32_t a2 = v_pair<VBITS>(vw[1], 2 * mt), a3 = v_pair<VBITS>(vw[1], 2 * mt + 1);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) mma16816(o[mt][nt], a0, a1, a2, a3, bf[vg][nt][0], bf[vg][nt][1]);
       }
@@ -793,8 +796,8 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : 1) decod
       else t[e] += __shfl_xor_sync(0xffffffffu, t[e], 2);
     }
     if (g == 0 && (NT == 2 || j < 2)) {
-      if (2 * j < r) beta_s[(warp * kMaxGqa + 2 * j) * NVG + k] = qmin * t[0] - t[2];
-      if (2 * j + 1 < r) beta_s[(warp * kMaxGqa + 2 * j + 1) * NVG + k] = qmin * t[1] - t[3];
+      if (2 * j < r) beta_s[(warp * kMaxGqa + 2 * j) * NVG + k] = qmin_v * t[0] - t[2];
+      if (2 * j + 1 < r) beta_s[(warp * kMaxGqa + 2 * j + 1) * NVG + k] = qmin_v * t[1] - t[3];
     }
   }
   // PV columns: NT == 1: cols 0..3 hi / 4..7 lo of queries 0..3; NT == 2: tile 0 hi, tile 1 lo of queries 0..7
@@ -810,7 +813,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : 1) decod
 #pragma unroll
       for (int e = 0; e < 4; ++e) v[e] += __shfl_xor_sync(0xffffffffu, v[e], 2);  // lo columns j+2 -> j
     }
-    const float sc0 = 1.0f / v_scale<BITS>(2 * mt), sc1 = 1.0f / v_scale<BITS>(2 * mt + 1);
+    const float sc0 = 1.0f / v_scale<VBITS>(2 * mt), sc1 = 1.0f / v_scale<VBITS>(2 * mt + 1);
     v[0] *= sc0; v[1] *= sc0; v[2] *= sc1; v[3] *= sc1;
     if ((NT == 2) || (j < 2)) {
       const int i0 = 2 * j, i1 = 2 * j + 1;
@@ -915,10 +918,10 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : 1) decod
   }
 }
 
-template <int BITS, int NT, int NVG, int NW>
+template <int BITS, int VBITS, int NT, int NVG, int NW>
 cudaError_t launch_cfg(const DecodeParams& p, cudaStream_t stream) {
-  constexpr int smem = Stage<BITS, NVG, NW>::SMEM;
-  auto* kern = decode_mma_kernel<BITS, NT, NVG, NW>;
+  constexpr int smem = Stage<BITS, VBITS, NVG, NW>::SMEM;
+  auto* kern = decode_mma_kernel<BITS, VBITS, NT, NVG, NW>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   if (p.cluster < 1 || p.cluster > 16 || (p.cluster & (p.cluster - 1)) || p.n_split != p.cluster * p.n_parts)
@@ -946,24 +949,24 @@ cudaError_t launch_cfg(const DecodeParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <int BITS, int NT, int NVG>
+template <int BITS, int VBITS, int NT, int NVG>
 int occupancy_cfg() {
-  constexpr int smem = Stage<BITS, NVG, 4>::SMEM;
-  if (cudaFuncSetAttribute(decode_mma_kernel<BITS, NT, NVG, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-      cudaSuccess)
+  constexpr int smem = Stage<BITS, VBITS, NVG, 4>::SMEM;
+  if (cudaFuncSetAttribute(decode_mma_kernel<BITS, VBITS, NT, NVG, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           smem) != cudaSuccess)
     return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<BITS, NT, NVG, 4>, 4 * 32, smem) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<BITS, VBITS, NT, NVG, 4>, 4 * 32, smem) !=
       cudaSuccess)
     return 0;
   return n;
 }
 
 // Clusters of `cs` CTAs that can be resident at once (0 if such a cluster cannot launch).
-template <int BITS, int NT, int NVG, int NW>
+template <int BITS, int VBITS, int NT, int NVG, int NW>
 int max_clusters_cfg(int cs) {
-  constexpr int smem = Stage<BITS, NVG, NW>::SMEM;
-  auto* kern = decode_mma_kernel<BITS, NT, NVG, NW>;
+  constexpr int smem = Stage<BITS, VBITS, NVG, NW>::SMEM;
+  auto* kern = decode_mma_kernel<BITS, VBITS, NT, NVG, NW>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
   if (cs > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
@@ -982,54 +985,54 @@ int max_clusters_cfg(int cs) {
   return n;
 }
 
-template <int BITS, int NW>
+template <int BITS, int VBITS, int NW>
 int max_clusters_nw(int r, int n_vg, int cs) {
   if (r <= 4) {
-    if (n_vg == 1) return max_clusters_cfg<BITS, 1, 1, NW>(cs);
-    if (n_vg == 2) return max_clusters_cfg<BITS, 1, 2, NW>(cs);
-    return max_clusters_cfg<BITS, 1, 4, NW>(cs);
+    if (n_vg == 1) return max_clusters_cfg<BITS, VBITS, 1, 1, NW>(cs);
+    if (n_vg == 2) return max_clusters_cfg<BITS, VBITS, 1, 2, NW>(cs);
+    return max_clusters_cfg<BITS, VBITS, 1, 4, NW>(cs);
   }
-  if (n_vg == 1) return max_clusters_cfg<BITS, 2, 1, NW>(cs);
-  if (n_vg == 2) return max_clusters_cfg<BITS, 2, 2, NW>(cs);
-  return max_clusters_cfg<BITS, 2, 4, NW>(cs);
+  if (n_vg == 1) return max_clusters_cfg<BITS, VBITS, 2, 1, NW>(cs);
+  if (n_vg == 2) return max_clusters_cfg<BITS, VBITS, 2, 2, NW>(cs);
+  return max_clusters_cfg<BITS, VBITS, 2, 4, NW>(cs);
 }
 
-template <int BITS>
+template <int BITS, int VBITS>
 int max_clusters_bits(int r, int n_vg, int cs, int nw) {
-  return nw == 8 ? max_clusters_nw<BITS, 8>(r, n_vg, cs) : max_clusters_nw<BITS, 4>(r, n_vg, cs);
+  return nw == 8 ? max_clusters_nw<BITS, VBITS, 8>(r, n_vg, cs) : max_clusters_nw<BITS, VBITS, 4>(r, n_vg, cs);
 }
 
-template <int BITS, int NW>
+template <int BITS, int VBITS, int NW>
 cudaError_t launch_nw(const DecodeParams& p, cudaStream_t stream) {
   if (p.r <= 4) {
-    if (p.n_vg == 1) return launch_cfg<BITS, 1, 1, NW>(p, stream);
-    if (p.n_vg == 2) return launch_cfg<BITS, 1, 2, NW>(p, stream);
-    return launch_cfg<BITS, 1, 4, NW>(p, stream);
+    if (p.n_vg == 1) return launch_cfg<BITS, VBITS, 1, 1, NW>(p, stream);
+    if (p.n_vg == 2) return launch_cfg<BITS, VBITS, 1, 2, NW>(p, stream);
+    return launch_cfg<BITS, VBITS, 1, 4, NW>(p, stream);
   }
-  if (p.n_vg == 1) return launch_cfg<BITS, 2, 1, NW>(p, stream);
-  if (p.n_vg == 2) return launch_cfg<BITS, 2, 2, NW>(p, stream);
-  return launch_cfg<BITS, 2, 4, NW>(p, stream);
+  if (p.n_vg == 1) return launch_cfg<BITS, VBITS, 2, 1, NW>(p, stream);
+  if (p.n_vg == 2) return launch_cfg<BITS, VBITS, 2, 2, NW>(p, stream);
+  return launch_cfg<BITS, VBITS, 2, 4, NW>(p, stream);
 }
 
-template <int BITS>
+template <int BITS, int VBITS>
 cudaError_t launch_bits(const DecodeParams& p, cudaStream_t stream) {
   if (p.warps == 8) {
     if (p.n_parts != 1) return cudaErrorInvalidConfiguration;  // 8-warp CTAs merge in clusters only
-    return launch_nw<BITS, 8>(p, stream);
+    return launch_nw<BITS, VBITS, 8>(p, stream);
   }
-  return launch_nw<BITS, 4>(p, stream);
+  return launch_nw<BITS, VBITS, 4>(p, stream);
 }
 
-template <int BITS>
+template <int BITS, int VBITS>
 int occupancy_bits(int r, int n_vg) {
   if (r <= 4) {
-    if (n_vg == 1) return occupancy_cfg<BITS, 1, 1>();
-    if (n_vg == 2) return occupancy_cfg<BITS, 1, 2>();
-    return occupancy_cfg<BITS, 1, 4>();
+    if (n_vg == 1) return occupancy_cfg<BITS, VBITS, 1, 1>();
+    if (n_vg == 2) return occupancy_cfg<BITS, VBITS, 1, 2>();
+    return occupancy_cfg<BITS, VBITS, 1, 4>();
   }
-  if (n_vg == 1) return occupancy_cfg<BITS, 2, 1>();
-  if (n_vg == 2) return occupancy_cfg<BITS, 2, 2>();
-  return occupancy_cfg<BITS, 2, 4>();
+  if (n_vg == 1) return occupancy_cfg<BITS, VBITS, 2, 1>();
+  if (n_vg == 2) return occupancy_cfg<BITS, VBITS, 2, 2>();
+  return occupancy_cfg<BITS, VBITS, 2, 4>();
 }
 
 }  // namespace mma

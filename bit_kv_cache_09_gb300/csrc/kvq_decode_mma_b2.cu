@@ -3,10 +3,14 @@
 
 namespace kvq {
 
-cudaError_t launch_decode_mma_b2(const DecodeParams& p, cudaStream_t stream) { return mma::launch_bits<2>(p, stream); }
+cudaError_t launch_decode_mma_b2(const DecodeParams& p, int, cudaStream_t stream) {
+  return mma::launch_bits<2, 2>(p, stream);
+}
 
-int occupancy_decode_mma_b2(int r, int n_vg) { return mma::occupancy_bits<2>(r, n_vg); }
+int occupancy_decode_mma_b2(int r, int n_vg, int) { return mma::occupancy_bits<2, 2>(r, n_vg); }
 
-int max_clusters_decode_mma_b2(int r, int n_vg, int cs, int nw) { return mma::max_clusters_bits<2>(r, n_vg, cs, nw); }
+int max_clusters_decode_mma_b2(int r, int n_vg, int cs, int nw, int) {
+  return mma::max_clusters_bits<2, 2>(r, n_vg, cs, nw);
+}
 
 }  // namespace kvq

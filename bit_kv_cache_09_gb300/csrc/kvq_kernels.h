@@ -121,12 +121,13 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
-cudaError_t launch_append(const AppendParams& p, int bits, cudaStream_t stream);
-cudaError_t launch_dequant(const DequantParams& p, int bits, cudaStream_t stream);
-cudaError_t launch_decode_simt(const DecodeParams& p, int bits, cudaStream_t stream);
-cudaError_t launch_decode_mma(const DecodeParams& p, int bits, cudaStream_t stream);
-int occupancy_decode_mma(int bits, int r, int n_vg);  // resident CTAs per SM (0 on error)
-int max_clusters_decode_mma(int bits, int r, int n_vg, int cs, int nw);  // resident clusters of cs CTAs of nw warps
+// bits, vbits: key and value code widths (equal, or 8 and 4)
+cudaError_t launch_append(const AppendParams& p, int bits, int vbits, cudaStream_t stream);
+cudaError_t launch_dequant(const DequantParams& p, int bits, int vbits, cudaStream_t stream);
+cudaError_t launch_decode_simt(const DecodeParams& p, int bits, cudaStream_t stream);  // equal widths only
+cudaError_t launch_decode_mma(const DecodeParams& p, int bits, int vbits, cudaStream_t stream);
+int occupancy_decode_mma(int bits, int vbits, int r, int n_vg);  // resident CTAs per SM (0 on error)
+int max_clusters_decode_mma(int bits, int vbits, int r, int n_vg, int cs, int nw);  // resident clusters of cs CTAs
 int occupancy_decode_simt(int bits);
 
 }  // namespace kvq

@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(256) v_token_kernel(AppendParams p) {
 // Dequantize the first T tokens: one warp per (batch row, kv head, token).
 // x_hat = s * (u + q_min - zp), one binary32 product.
 // ---------------------------------------------------------------------------
-template <int BITS>
+template <int BITS, int VBITS>
 __global__ void __launch_bounds__(256) dequant_kernel(DequantParams p, int64_t n_rows) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t w = (int64_t)blockIdx.x * 8 + warp;
@@ -279,11 +279,11 @@ __global__ void __launch_bounds__(256) dequant_kernel(DequantParams p, int64_t n
     for (int e = 0; e < 4; ++e) {
       const int c = c0 + e;
       const int pos = 16 * (c & 7) + 2 * (c >> 4) + ((c >> 3) & 1);
-      const int bit = pos * BITS;
+      const int bit = pos * VBITS;
       const uint32_t unit = pair[2 * (bit >> 4) + (int)(t & 1)];
-      const uint32_t u = (unit >> (bit & 15)) & ((1u << BITS) - 1u);
+      const uint32_t u = (unit >> (bit & 15)) & ((1u << VBITS) - 1u);
       const __half2 m = meta[c / p.Gv];
-      vx[e] = __fmul_rn(__low2float(m), __fsub_rn((float)((int)u + (int)Q<BITS>::qmin), __high2float(m)));
+      vx[e] = __fmul_rn(__low2float(m), __fsub_rn((float)((int)u + (int)Q<VBITS>::qmin), __high2float(m)));
     }
   }
   *reinterpret_cast<float4*>(p.k_out + w * kHeadDim + c0) = make_float4(kx[0], kx[1], kx[2], kx[3]);
@@ -291,46 +291,45 @@ __global__ void __launch_bounds__(256) dequant_kernel(DequantParams p, int64_t n
 }
 
 template <int BITS>
-cudaError_t launch_append_bits(const AppendParams& p, cudaStream_t stream) {
-  if (p.n_groups > 0) {
-    dim3 grid((unsigned)p.n_groups, (unsigned)p.H, (unsigned)p.B);
-    cudaError_t e;
-    switch (p.G) {
-      case 32: e = launch_pdl(k_group_kernel<BITS, 32>, grid, dim3(256), 0, stream, p); break;
-      case 64: e = launch_pdl(k_group_kernel<BITS, 64>, grid, dim3(256), 0, stream, p); break;
-      default: e = launch_pdl(k_group_kernel<BITS, 128>, grid, dim3(256), 0, stream, p); break;
-    }
-    if (e != cudaSuccess) return e;
+cudaError_t launch_keys(const AppendParams& p, cudaStream_t stream) {
+  if (p.n_groups <= 0) return cudaSuccess;
+  dim3 grid((unsigned)p.n_groups, (unsigned)p.H, (unsigned)p.B);
+  switch (p.G) {
+    case 32: return launch_pdl(k_group_kernel<BITS, 32>, grid, dim3(256), 0, stream, p);
+    case 64: return launch_pdl(k_group_kernel<BITS, 64>, grid, dim3(256), 0, stream, p);
+    default: return launch_pdl(k_group_kernel<BITS, 128>, grid, dim3(256), 0, stream, p);
   }
-  const int64_t rows = p.n_new * p.H;  // per batch row
-  cudaError_t e = launch_pdl(v_token_kernel<BITS>, dim3((unsigned)((rows + 31) / 32), (unsigned)p.B), dim3(256), 0,
-                             stream, p);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
 }
 
-template <int BITS>
+template <int VBITS>
+cudaError_t launch_values(const AppendParams& p, cudaStream_t stream) {
+  const int64_t rows = p.n_new * p.H;  // per batch row
+  return launch_pdl(v_token_kernel<VBITS>, dim3((unsigned)((rows + 31) / 32), (unsigned)p.B), dim3(256), 0, stream, p);
+}
+
+template <int BITS, int VBITS>
 cudaError_t launch_dequant_bits(const DequantParams& p, cudaStream_t stream) {
   const int64_t rows = (int64_t)p.B * p.H * p.T;
-  dequant_kernel<BITS><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(p, rows);
+  dequant_kernel<BITS, VBITS><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(p, rows);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_append(const AppendParams& p, int bits, cudaStream_t stream) {
-  switch (bits) {
-    case 8: return launch_append_bits<8>(p, stream);
-    case 4: return launch_append_bits<4>(p, stream);
-    default: return launch_append_bits<2>(p, stream);
-  }
+cudaError_t launch_append(const AppendParams& p, int bits, int vbits, cudaStream_t stream) {
+  cudaError_t e = bits == 8 ? launch_keys<8>(p, stream) : (bits == 4 ? launch_keys<4>(p, stream) : launch_keys<2>(p, stream));
+  if (e != cudaSuccess) return e;
+  e = vbits == 8 ? launch_values<8>(p, stream) : (vbits == 4 ? launch_values<4>(p, stream) : launch_values<2>(p, stream));
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
 
-cudaError_t launch_dequant(const DequantParams& p, int bits, cudaStream_t stream) {
+cudaError_t launch_dequant(const DequantParams& p, int bits, int vbits, cudaStream_t stream) {
+  if (vbits != bits) return launch_dequant_bits<8, 4>(p, stream);  // the one mixed configuration
   switch (bits) {
-    case 8: return launch_dequant_bits<8>(p, stream);
-    case 4: return launch_dequant_bits<4>(p, stream);
-    default: return launch_dequant_bits<2>(p, stream);
+    case 8: return launch_dequant_bits<8, 8>(p, stream);
+    case 4: return launch_dequant_bits<4, 4>(p, stream);
+    default: return launch_dequant_bits<2, 2>(p, stream);
   }
 }
 

@@ -27,7 +27,10 @@
  *   binary16(s32) rounded toward +infinity; zp = q_min - rint(x_min / scale), clamped to
  *   +-65504 and stored as binary16 (nearest even); q = clamp(rint(x / scale) + zp).
  *   A group whose values are all equal is widened to include 0; an all-zero group
- *   gets scale 1. Codes are stored as u = q - q_min (unsigned, b bits).
+ *   gets scale 1. Codes are stored as u = q - q_min (unsigned, b bits). Keys use b =
+ *   bits, values b = v_bits (the same unless v_bits says otherwise: 8-bit keys with
+ *   4-bit values is the mixed recipe of "KV Cache Quantization — 8-bit and 4-bit",
+ *   § Why keys and values want different treatment).
  *
  * State after T tokens of one (layer, batch row, kv head)
  *   R_eff = residual_len, or k_group when residual_len == 0.
@@ -43,9 +46,9 @@
  *               row (little-endian bytes, low bits first).
  *     k_meta  : (S_pad / k_group) groups x d channels x {scale, zero_point} binary16.
  *     k_resid : R_eff rows of d binary16.
- *     v_codes : S_pad/2 pair rows of 2*d*b/8 bytes. Channel c of a token sits at
+ *     v_codes : S_pad/2 pair rows of 2*d*b_v/8 bytes (b_v = value code width). Channel c of a token sits at
  *               position pos(c) = (d/8)*(c%8) + 2*(c/16) + (c/8)%2 of that token's
- *               d*b/8-byte row; the rows of tokens 2p and 2p+1 are interleaved in
+ *               d*b_v/8-byte row; the rows of tokens 2p and 2p+1 are interleaved in
  *               16-bit units (32-bit word k of pair row p = unit k of token 2p in the
  *               low half, unit k of token 2p+1 in the high half).
  *     v_meta  : S_pad tokens x (d / v_group) groups x {scale, zero_point} binary16.
@@ -81,6 +84,7 @@ typedef enum {
 /* Cache shape and quantizer settings; the names follow the pages' problem
  * statement ("KV Cache Quantization — 8-bit and 4-bit", § The bytes-per-token
  * formula: L, n_kv, d_head, S). Supported: d_head == 128; bits in {2, 4, 8};
+ * v_bits == 0 (same as bits) or v_bits == bits, or bits == 8 with v_bits == 4;
  * k_group and v_group in {32, 64, 128}; residual_len == 0 or a multiple of k_group
  * up to 1024; 1 <= gqa_ratio <= 8; n_kv_heads <= 255; batch <= 4095;
  * 1 <= max_seq_len <= 2^24. */
@@ -91,10 +95,11 @@ typedef struct {
   int32_t gqa_ratio;    /* r: query heads per kv head; query head i reads kv head i / r */
   int32_t d_head;       /* d */
   int32_t max_seq_len;  /* capacity in tokens */
-  int32_t bits;         /* b: code width for keys and values */
+  int32_t bits;         /* b: code width of the keys (and of the values when v_bits == 0) */
   int32_t k_group;      /* G: tokens per key group (keys are quantized per channel) */
   int32_t v_group;      /* Gv: channels per value group (values are quantized per token) */
   int32_t residual_len; /* R: binary16 key residual capacity; 0 means k_group */
+  int32_t v_bits;       /* value code width; 0 means bits */
 } kvq_config;
 
 /* Device pointers to the five cache buffers of all layers (layout above). */

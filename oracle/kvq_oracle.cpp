@@ -293,18 +293,22 @@ void orc_unpack_v_token(const uint8_t* pairs, int d, int bits, int64_t t, uint8_
 //   keys   : per channel, over groups of G consecutive tokens; the newest
 //            T mod R_eff tokens stay binary16 in the residual window (slot t mod R_eff);
 //   values : per token, over groups of Gv consecutive channels.
+// Keys use `bits`-bit codes (b), values `v_bits`-bit codes (b_v; equal to b unless a
+// mixed-width cache is asked for, "KV Cache Quantization — 8-bit and 4-bit", § Why keys
+// and values want different treatment).
 // Inputs k_hist, v_hist: [T][d] binary16. Outputs in the packed layout above:
 //   k_codes [floor(T/R_eff)*R_eff][d*b/8], k_meta [groups][d][2], k_resid [R_eff][d],
-//   v_codes [ceil(T/2)][2*d*b/8], v_meta [T][d/Gv][2].
+//   v_codes [ceil(T/2)][2*d*b_v/8], v_meta [T][d/Gv][2].
 // Output buffers must be zero-initialised by the caller. Optional k_u [Tq][d] and
 // v_u [T][d] receive the unpacked codes. Returns Tq (quantized key tokens) or -1.
 // ---------------------------------------------------------------------------
 
-int64_t orc_cache_state(int d, int bits, int G, int Gv, int R, int64_t T, const uint16_t* k_hist,
+int64_t orc_cache_state(int d, int bits, int v_bits, int G, int Gv, int R, int64_t T, const uint16_t* k_hist,
                         const uint16_t* v_hist, uint8_t* k_codes, uint16_t* k_meta, uint16_t* k_resid,
                         uint8_t* v_codes, uint16_t* v_meta, uint8_t* k_u, uint8_t* v_u) {
   if (d <= 0 || d % 16 || G <= 0 || Gv <= 0 || d % Gv || R < 0 || (R > 0 && R % G) || T < 0) return -1;
   if (!(bits == 2 || bits == 4 || bits == 8)) return -1;
+  if (!(v_bits == 2 || v_bits == 4 || v_bits == 8)) return -1;
   const int64_t R_eff = R > 0 ? R : G;
   const int64_t Tq = (T / R_eff) * R_eff;
   const int64_t rowK = (int64_t)d * bits / 8;
@@ -336,12 +340,12 @@ int64_t orc_cache_state(int d, int bits, int G, int Gv, int R, int64_t T, const 
     for (int j = 0; j < ng; ++j) {
       const uint16_t* x = v_hist + t * d + (int64_t)j * Gv;
       uint16_t s_h, z_h;
-      orc_quant_params(x, Gv, 1, bits, &s_h, &z_h);
-      orc_quantize_values(x, Gv, 1, bits, s_h, z_h, u.data() + (size_t)j * Gv);
+      orc_quant_params(x, Gv, 1, v_bits, &s_h, &z_h);
+      orc_quantize_values(x, Gv, 1, v_bits, s_h, z_h, u.data() + (size_t)j * Gv);
       v_meta[(t * ng + j) * 2 + 0] = s_h;
       v_meta[(t * ng + j) * 2 + 1] = z_h;
     }
-    orc_pack_v_token(u.data(), d, bits, t, v_codes);
+    orc_pack_v_token(u.data(), d, v_bits, t, v_codes);
     if (v_u) std::memcpy(v_u + t * d, u.data(), (size_t)d);
   }
   return Tq;
@@ -350,7 +354,7 @@ int64_t orc_cache_state(int d, int bits, int G, int Gv, int R, int64_t T, const 
 // Dequantized keys and values of one (batch row, kv head) from a packed state:
 // k_out, v_out [T][d] binary32. Quantized keys and all values use
 // x_hat = scale * (q - zero_point); residual keys are the binary16 values.
-int orc_dequantize_state(int d, int bits, int G, int Gv, int R, int64_t T, const uint8_t* k_codes,
+int orc_dequantize_state(int d, int bits, int v_bits, int G, int Gv, int R, int64_t T, const uint8_t* k_codes,
                          const uint16_t* k_meta, const uint16_t* k_resid, const uint8_t* v_codes,
                          const uint16_t* v_meta, float* k_out, float* v_out) {
   if (d <= 0 || d % 16 || G <= 0 || Gv <= 0 || d % Gv || R < 0 || (R > 0 && R % G) || T < 0) return -1;
@@ -368,10 +372,11 @@ int orc_dequantize_state(int d, int bits, int G, int Gv, int R, int64_t T, const
       for (int c = 0; c < d; ++c) k_out[t * d + c] = orc_f32_from_f16(k_resid[(t % R_eff) * d + c]);
     }
     const int ng = d / Gv;
-    orc_unpack_v_token(v_codes, d, bits, t, u.data());
+    orc_unpack_v_token(v_codes, d, v_bits, t, u.data());
     for (int c = 0; c < d; ++c) {
       int j = c / Gv;
-      v_out[t * d + c] = orc_dequantize_value(u[(size_t)c], bits, v_meta[(t * ng + j) * 2], v_meta[(t * ng + j) * 2 + 1]);
+      v_out[t * d + c] =
+          orc_dequantize_value(u[(size_t)c], v_bits, v_meta[(t * ng + j) * 2], v_meta[(t * ng + j) * 2 + 1]);
     }
   }
   return 0;

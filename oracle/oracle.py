@@ -74,10 +74,10 @@ def lib():
             L.orc_pack_v_token.restype = None
             L.orc_unpack_v_token.argtypes = [_u8p, ctypes.c_int, ctypes.c_int, ctypes.c_int64, _u8p]
             L.orc_unpack_v_token.restype = None
-            L.orc_cache_state.argtypes = [ctypes.c_int] * 5 + [ctypes.c_int64, _u16p, _u16p, _u8p, _u16p, _u16p, _u8p,
+            L.orc_cache_state.argtypes = [ctypes.c_int] * 6 + [ctypes.c_int64, _u16p, _u16p, _u8p, _u16p, _u16p, _u8p,
                                                                _u16p, _u8p, _u8p]
             L.orc_cache_state.restype = ctypes.c_int64
-            L.orc_dequantize_state.argtypes = [ctypes.c_int] * 5 + [ctypes.c_int64, _u8p, _u16p, _u16p, _u8p, _u16p,
+            L.orc_dequantize_state.argtypes = [ctypes.c_int] * 6 + [ctypes.c_int64, _u8p, _u16p, _u16p, _u8p, _u16p,
                                                                     _f32p, _f32p]
             L.orc_dequantize_state.restype = ctypes.c_int
             L.orc_attention.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int64, _u16p, _f32p, _f32p,
@@ -198,8 +198,10 @@ class OracleState:
     v_u: np.ndarray  # [T][d] unpacked value codes
 
 
-def cache_state(k_hist, v_hist, *, d: int, bits: int, G: int, Gv: int, R: int) -> OracleState:
-    """Quantized cache of one (b, h) slice from its binary16 token history [T][d]."""
+def cache_state(k_hist, v_hist, *, d: int, bits: int, G: int, Gv: int, R: int, v_bits: int = 0) -> OracleState:
+    """Quantized cache of one (b, h) slice from its binary16 token history [T][d]; keys
+    with `bits`-bit codes, values with `v_bits`-bit codes (0: the same as the keys)."""
+    v_bits = v_bits or bits
     k = _as_u16(k_hist)
     v = _as_u16(v_hist)
     T = k.shape[0]
@@ -210,7 +212,7 @@ def cache_state(k_hist, v_hist, *, d: int, bits: int, G: int, Gv: int, R: int) -
     k_codes = np.zeros((Tq, rowK), np.uint8)
     k_meta = np.zeros((Tq // G, d, 2), np.uint16)
     k_resid = np.zeros((R_eff, d), np.uint16)
-    v_codes = np.zeros(((T + 1) // 2, 2 * rowK), np.uint8)
+    v_codes = np.zeros(((T + 1) // 2, 2 * (d * v_bits // 8)), np.uint8)
     v_meta = np.zeros((T, d // Gv, 2), np.uint16)
     k_u = np.zeros((Tq, d), np.uint8)
     v_u = np.zeros((T, d), np.uint8)
@@ -218,7 +220,7 @@ def cache_state(k_hist, v_hist, *, d: int, bits: int, G: int, Gv: int, R: int) -
     bufs = [np.zeros(1, a.dtype) if a.size == 0 else a for a in (k_codes, k_meta, k_resid, v_codes, v_meta, k_u, v_u)]
     kk = k if k.size else np.zeros(1, np.uint16)
     vv = v if v.size else np.zeros(1, np.uint16)
-    rc = lib().orc_cache_state(d, bits, G, Gv, R, T, _ptr(kk, _u16p), _ptr(vv, _u16p), _ptr(bufs[0], _u8p),
+    rc = lib().orc_cache_state(d, bits, v_bits, G, Gv, R, T, _ptr(kk, _u16p), _ptr(vv, _u16p), _ptr(bufs[0], _u8p),
                                _ptr(bufs[1], _u16p), _ptr(bufs[2], _u16p), _ptr(bufs[3], _u8p), _ptr(bufs[4], _u16p),
                                _ptr(bufs[5], _u8p), _ptr(bufs[6], _u8p))
     if rc < 0:
@@ -227,8 +229,9 @@ def cache_state(k_hist, v_hist, *, d: int, bits: int, G: int, Gv: int, R: int) -
     return OracleState(T, Tq, k_codes, k_meta, k_resid, v_codes, v_meta, k_u, v_u)
 
 
-def dequantize_state(st: OracleState, *, d: int, bits: int, G: int, Gv: int, R: int):
-    """(k_hat, v_hat) binary32 [T][d] from a packed slice state."""
+def dequantize_state(st: OracleState, *, d: int, bits: int, G: int, Gv: int, R: int, v_bits: int = 0):
+    """(k_hat, v_hat) binary32 [T][d] from a packed slice state (v_bits 0: same as bits)."""
+    v_bits = v_bits or bits
     T = st.T
     k_out = np.zeros((max(T, 1), d), np.float32)
     v_out = np.zeros((max(T, 1), d), np.float32)
@@ -236,7 +239,7 @@ def dequantize_state(st: OracleState, *, d: int, bits: int, G: int, Gv: int, R: 
     def nz(a):
         return np.ascontiguousarray(a) if a.size else np.zeros(1, a.dtype)
 
-    rc = lib().orc_dequantize_state(d, bits, G, Gv, R, T, _ptr(nz(st.k_codes), _u8p), _ptr(nz(st.k_meta), _u16p),
+    rc = lib().orc_dequantize_state(d, bits, v_bits, G, Gv, R, T, _ptr(nz(st.k_codes), _u8p), _ptr(nz(st.k_meta), _u16p),
                                     _ptr(nz(st.k_resid), _u16p), _ptr(nz(st.v_codes), _u8p),
                                     _ptr(nz(st.v_meta), _u16p), _ptr(k_out, _f32p), _ptr(v_out, _f32p))
     if rc != 0:

@@ -161,7 +161,12 @@ class Workload:
     gain: int
     seed: int
     shift: float = 5.0
+    v_bits: int = 0  # value code width; 0 => bits
     notes: str = field(default="", compare=False)
+
+    @property
+    def vbits(self) -> int:
+        return self.v_bits or self.bits
 
     @property
     def n_q(self) -> int:
@@ -197,6 +202,8 @@ WORKLOADS: dict[str, Workload] = {
                  notes="long-context int4 sweep, GQA 8, 32k x batch 4"),
         Workload("long-int4-64k", 32, 8, 8, 128, 2, 65536, 32, 4, 128, 128, 128, 4, 20, 20264,
                  notes="long-context int4 sweep, GQA 8, 65536 x batch 2"),
+        Workload("kivi-k8v4", 32, 8, 4, 128, 16, 8192, 32, 8, 128, 64, 128, 4, 20, 20265, v_bits=4,
+                 notes="mixed widths: int8 keys, int4 values; otherwise the KIVI-style int4 shape"),
     ]
 }
 

@@ -22,7 +22,9 @@ def cfg_dims(cache):
     R_eff = c.residual_len if c.residual_len > 0 else c.k_group
     S_pad = (c.max_seq_len + 127) // 128 * 128
     row = c.d_head * c.bits // 8
-    return dict(L=c.n_layers, B=c.batch, H=c.n_kv_heads, r=c.gqa_ratio, d=c.d_head, bits=c.bits, G=c.k_group,
+    vbits = c.v_bits or c.bits
+    return dict(L=c.n_layers, B=c.batch, H=c.n_kv_heads, r=c.gqa_ratio, d=c.d_head, bits=c.bits, vbits=vbits,
+                rowV=c.d_head * vbits // 8, G=c.k_group,
                 Gv=c.v_group, R=c.residual_len, R_eff=R_eff, S_pad=S_pad, row=row, n_vg=c.d_head // c.v_group)
 
 
@@ -43,14 +45,15 @@ def gpu_slice_state(cache, layer: int, b: int, h: int, T: int):
     km = km.reshape(Tq // g["G"], g["d"], 2)
     kr = part("k_resid", g["R_eff"] * g["d"] * 2, (T - Tq) * g["d"] * 2).view(np.uint16).reshape(T - Tq, g["d"])
     npairs = (T + 1) // 2
-    vc = part("v_codes", g["S_pad"] * g["row"], npairs * 2 * g["row"]).reshape(npairs, 2 * g["row"])
+    vc = part("v_codes", g["S_pad"] * g["rowV"], npairs * 2 * g["rowV"]).reshape(npairs, 2 * g["rowV"])
     vm = part("v_meta", g["S_pad"] * g["n_vg"] * 4, T * g["n_vg"] * 4).view(np.uint16).reshape(T, g["n_vg"], 2)
     return dict(k_codes=kc, k_meta=km, k_resid=kr, v_codes=vc, v_meta=vm, Tq=Tq)
 
 
 def oracle_slice_state(k_hist, v_hist, cache):
     g = cfg_dims(cache)
-    return oracle.cache_state(k_hist, v_hist, d=g["d"], bits=g["bits"], G=g["G"], Gv=g["Gv"], R=g["R"])
+    return oracle.cache_state(k_hist, v_hist, d=g["d"], bits=g["bits"], G=g["G"], Gv=g["Gv"], R=g["R"],
+                              v_bits=g["vbits"])
 
 
 def assert_slice_equal(gpu: dict, st: oracle.OracleState, where: str = ""):
@@ -73,13 +76,13 @@ def assert_slice_equal(gpu: dict, st: oracle.OracleState, where: str = ""):
 
 def oracle_attention(st: oracle.OracleState, q_rows, cache, softmax_scale):
     g = cfg_dims(cache)
-    kh, vh = oracle.dequantize_state(st, d=g["d"], bits=g["bits"], G=g["G"], Gv=g["Gv"], R=g["R"])
+    kh, vh = oracle.dequantize_state(st, d=g["d"], bits=g["bits"], G=g["G"], Gv=g["Gv"], R=g["R"], v_bits=g["vbits"])
     return oracle.attention(q_rows, kh, vh, softmax_scale)
 
 
 def small_workload(name="small", *, L=1, H=2, r=4, B=2, S=600, steps=8, bits=4, G=32, Gv=64, R=128, n_out=2,
-                   gain=20, seed=777):
-    return synth.Workload(name, L, H, r, 128, B, S, steps, bits, G, Gv, R, n_out, gain, seed)
+                   gain=20, seed=777, v_bits=0):
+    return synth.Workload(name, L, H, r, 128, B, S, steps, bits, G, Gv, R, n_out, gain, seed, v_bits=v_bits)
 
 
 def host_layer_inputs(w, layer, t0, nt):

@@ -45,7 +45,8 @@ def good_cfg(**kw):
 @pytest.mark.parametrize("kw,status", [
     (dict(bits=3), 2), (dict(bits=16), 2), (dict(d_head=64), 2), (dict(k_group=48), 2), (dict(v_group=16), 2),
     (dict(residual_len=100), 1), (dict(residual_len=2048), 2), (dict(gqa_ratio=9), 2), (dict(batch=0), 1),
-    (dict(max_seq_len=0), 1), (dict(n_kv_heads=256), 2),
+    (dict(max_seq_len=0), 1), (dict(n_kv_heads=256), 2), (dict(v_bits=3), 2), (dict(bits=4, v_bits=8), 2),
+    (dict(bits=4, v_bits=2), 2), (dict(bits=2, v_bits=4), 2),
 ])
 def test_bad_configs_are_rejected(lib, kw, status):
     sizes = (ctypes.c_size_t * 5)()
@@ -66,6 +67,18 @@ def test_buffer_sizes_follow_the_bytes_formula(lib):
         assert vm == oracle.kv_bytes(L, H * B, 128, S, 0, 4, Gv) / 2
         R_eff = R or G
         assert kr == L * B * H * R_eff * 128 * 2
+
+
+def test_mixed_width_buffer_sizes(lib):
+    """8-bit keys with 4-bit values: key codes at 8 bits, value codes at 4 bits per element."""
+    L, B, H, S = 3, 2, 4, 1024
+    same = kvq.kvq_buffer_sizes(good_cfg(n_layers=L, batch=B, n_kv_heads=H, max_seq_len=S, bits=8, k_group=128,
+                                         v_group=64, residual_len=128))
+    mixed = kvq.kvq_buffer_sizes(good_cfg(n_layers=L, batch=B, n_kv_heads=H, max_seq_len=S, bits=8, k_group=128,
+                                          v_group=64, residual_len=128, v_bits=4))
+    assert mixed[0] == same[0] and mixed[1] == same[1] and mixed[2] == same[2] and mixed[4] == same[4]
+    assert mixed[3] == oracle.kv_bytes(L, H * B, 128, S, 4) / 2
+    assert kvq.kvq_buffer_sizes(good_cfg(bits=8, v_bits=8)) == kvq.kvq_buffer_sizes(good_cfg(bits=8))
 
 
 def _bufs(ptr=4096):

@@ -277,3 +277,74 @@ def test_small_grid_long_sequence(bits, G, Gv, R, r):
             ref = oracle_attention(st, q_host[0, h * w.gqa:(h + 1) * w.gqa], cache, softmax_scale(w))
             assert float(np.abs(out[0, h * w.gqa:(h + 1) * w.gqa] - ref).max()) <= ATOL
     _check_all_slices(cache, w, 0, w.max_seq, k_host, v_host)
+
+
+MIXED = [
+    # G, Gv, R, r  (8-bit keys, 4-bit values)
+    (128, 64, 128, 4),
+    (32, 128, 0, 4),
+    (64, 32, 256, 3),
+    (128, 128, 128, 8),
+    (32, 64, 128, 1),
+]
+
+
+@pytest.mark.parametrize("G,Gv,R,r", MIXED)
+def test_mixed_widths_prefill_decode_flush_and_dequantize(G, Gv, R, r):
+    """8-bit keys with 4-bit values: a ragged prefill, decode steps across a residual
+    flush (attention call and fused step on two caches), and the dequantized history,
+    all against the oracle run with the same two widths."""
+    R_eff = R if R > 0 else G
+    off = min(37, R_eff - 5)
+    S = 3 * R_eff + off
+    steps = R_eff - off + 3
+    w = small_workload(bits=8, v_bits=4, G=G, Gv=Gv, R=R, r=r, B=2, H=2, S=S, steps=steps, seed=6100 + G + r)
+    split = QuantizedKVCache.for_workload(w)
+    fused = QuantizedKVCache.for_workload(w)
+    k_host, v_host = host_layer_inputs(w, 0, 0, w.max_seq)
+    for c in (split, fused):
+        c.append(0, 0, _dev(k_host[:, :S]), _dev(v_host[:, :S]))
+    _check_all_slices(split, w, 0, S, k_host, v_host)
+    for s in range(steps):
+        T = S + s
+        q_host = synth.gen_q(w.seed, 0, range(w.batch), T, w.n_q, w.d_head)
+        kd, vd, qd = _dev(k_host[:, T:T + 1]), _dev(v_host[:, T:T + 1]), _dev(q_host)
+        out_f = fused.decode_step(0, T, kd, vd, qd, softmax_scale(w))
+        split.append(0, T, kd, vd)
+        out_s = split.attention(0, T + 1, qd, softmax_scale(w), impl=kvq.DECODE_MMA)
+        assert torch.equal(out_f, out_s), (s, (out_f - out_s).abs().max().item())
+        if s in (0, steps - 4, steps - 3, steps - 1):
+            _check_all_slices(fused, w, 0, T + 1, k_host, v_host)
+            _check_attention(split, w, 0, T + 1, k_host, v_host, q_host, kvq.DECODE_MMA)
+    T = S + steps
+    kd, vd = split.dequantize(0, T)
+    for b in range(w.batch):
+        for h in range(w.n_kv):
+            st = oracle_slice_state(k_host[b, :T, h], v_host[b, :T, h], split)
+            kh, vh = oracle.dequantize_state(st, d=128, bits=8, G=G, Gv=Gv, R=R, v_bits=4)
+            assert np.array_equal(kd[b, h].cpu().numpy().view(np.uint32), kh.view(np.uint32))
+            assert np.array_equal(vd[b, h].cpu().numpy().view(np.uint32), vh.view(np.uint32))
+
+
+def test_mixed_widths_small_grid_long_sequence():
+    """8-bit keys with 4-bit values over ~4k tokens for two pairs (16-CTA clusters of
+    8-warp CTAs)."""
+    w = small_workload(bits=8, v_bits=4, G=128, Gv=64, R=128, r=4, B=1, H=2, S=3900, steps=2, seed=6500)
+    cache = QuantizedKVCache.for_workload(w)
+    k_host, v_host = host_layer_inputs(w, 0, 0, w.max_seq)
+    cache.append(0, 0, _dev(k_host[:, :w.seq]), _dev(v_host[:, :w.seq]))
+    q0 = synth.gen_q(w.seed, 0, range(w.batch), w.seq - 1, w.n_q, w.d_head)
+    _check_attention(cache, w, 0, w.seq, k_host, v_host, q0, kvq.DECODE_MMA)
+    _check_attention(cache, w, 0, w.seq, k_host, v_host, q0, kvq.DECODE_AUTO)
+
+
+def test_mixed_widths_have_no_simt_path():
+    """The scalar decode path handles one code width only; a mixed cache asks for the
+    tensor-core path and gets an UNSUPPORTED status from the scalar one."""
+    w = small_workload(bits=8, v_bits=4, G=32, Gv=64, R=128, B=1, H=1, S=40, steps=0, seed=1)
+    cache = QuantizedKVCache.for_workload(w)
+    k_host, v_host = host_layer_inputs(w, 0, 0, w.seq)
+    cache.append(0, 0, _dev(k_host), _dev(v_host))
+    q = _dev(synth.gen_q(w.seed, 0, range(1), w.seq - 1, w.n_q, w.d_head))
+    with pytest.raises(kvq.KVQError):
+        cache.attention(0, w.seq, q, softmax_scale(w), impl=kvq.DECODE_SIMT)

@@ -412,3 +412,23 @@ def test_cache_state_codes_agree_with_group_quantizer():
     sh, zh = oracle.quant_params(col, bits)
     assert (st.k_meta[g, c, 0], st.k_meta[g, c, 1]) == (sh, zh)
     assert np.array_equal(st.k_u[g * G:(g + 1) * G, c], oracle.quantize_values(col, bits, sh, zh))
+
+
+def test_mixed_width_state_is_the_two_single_width_states():
+    """A cache with 8-bit keys and 4-bit values holds exactly the keys of the all-8-bit
+    cache and the values of the all-4-bit cache (the two quantizers are independent)."""
+    rng = np.random.default_rng(11)
+    T, d = 300, 128
+    k = (rng.standard_normal((T, d)) * 2).astype(np.float16)
+    v = (rng.standard_normal((T, d)) * 0.5).astype(np.float16)
+    mixed = oracle.cache_state(k, v, d=d, bits=8, G=32, Gv=64, R=128, v_bits=4)
+    k8 = oracle.cache_state(k, v, d=d, bits=8, G=32, Gv=64, R=128)
+    v4 = oracle.cache_state(k, v, d=d, bits=4, G=32, Gv=64, R=128)
+    for name in ("k_codes", "k_meta", "k_resid", "k_u"):
+        assert np.array_equal(getattr(mixed, name), getattr(k8, name)), name
+    for name in ("v_codes", "v_meta", "v_u"):
+        assert np.array_equal(getattr(mixed, name), getattr(v4, name)), name
+    kh, vh = oracle.dequantize_state(mixed, d=d, bits=8, G=32, Gv=64, R=128, v_bits=4)
+    kh8, _ = oracle.dequantize_state(k8, d=d, bits=8, G=32, Gv=64, R=128)
+    _, vh4 = oracle.dequantize_state(v4, d=d, bits=4, G=32, Gv=64, R=128)
+    assert np.array_equal(kh, kh8) and np.array_equal(vh, vh4)
