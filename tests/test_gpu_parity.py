@@ -348,3 +348,37 @@ def test_mixed_widths_have_no_simt_path():
     q = _dev(synth.gen_q(w.seed, 0, range(1), w.seq - 1, w.n_q, w.d_head))
     with pytest.raises(kvq.KVQError):
         cache.attention(0, w.seq, q, softmax_scale(w), impl=kvq.DECODE_SIMT)
+
+
+@pytest.mark.parametrize("bits,v_bits,G,Gv,R,B,H,S", [
+    (4, 0, 128, 64, 128, 32, 4, 2049),
+    (2, 0, 32, 32, 128, 32, 4, 2049),
+    (8, 4, 128, 64, 128, 12, 4, 4000),
+    (8, 0, 128, 128, 0, 12, 4, 4000),
+])
+def test_large_grid(bits, v_bits, G, Gv, R, B, H, S):
+    """Grids of 48 or 128 (batch row, kv head) pairs (the large-grid split plans: several
+    splits per pair, merged in clusters or through the workspace): attention call and
+    fused decode step against the oracle for every pair."""
+    w = small_workload(bits=bits, v_bits=v_bits, G=G, Gv=Gv, R=R, r=4, B=B, H=H, S=S, steps=3,
+                       seed=7000 + bits + v_bits + B)
+    cache = QuantizedKVCache.for_workload(w)
+    k_host, v_host = host_layer_inputs(w, 0, 0, w.max_seq)
+    cache.append(0, 0, _dev(k_host[:, :S]), _dev(v_host[:, :S]))
+    assert kvq.kvq_decode_num_splits(cache.cfg, S) > 1
+    q0 = synth.gen_q(w.seed, 0, range(w.batch), S - 1, w.n_q, w.d_head)
+    _check_attention(cache, w, 0, S, k_host, v_host, q0, kvq.DECODE_MMA)
+    for s in range(w.steps):
+        T = S + s
+        q_host = synth.gen_q(w.seed, 0, range(w.batch), T, w.n_q, w.d_head)
+        out = cache.decode_step(0, T, _dev(k_host[:, T:T + 1]), _dev(v_host[:, T:T + 1]), _dev(q_host),
+                                softmax_scale(w)).cpu().numpy()
+        if s == w.steps - 1:
+            worst = 0.0
+            for b in range(w.batch):
+                for h in range(w.n_kv):
+                    st = oracle_slice_state(k_host[b, :T + 1, h], v_host[b, :T + 1, h], cache)
+                    ref = oracle_attention(st, q_host[b, h * w.gqa:(h + 1) * w.gqa], cache, softmax_scale(w))
+                    worst = max(worst, float(np.abs(out[b, h * w.gqa:(h + 1) * w.gqa] - ref).max()))
+            assert worst <= ATOL, worst
+    _check_all_slices(cache, w, 0, S + w.steps, k_host, v_host)
