@@ -298,13 +298,17 @@ __device__ __forceinline__ void lds_vmeta(const __half2* p, __half2* m) {
   }
 }
 
+// Resident CTAs per SM the register budget is sized for: 4 at 128 registers (r <= 4),
+// 3 at 168 (r <= 8: its hi and lo P.V products share one accumulator tile, which keeps
+// the kernel within 168 registers without spills).
 template <int NT>
 constexpr int min_blocks() {
-  return NT == 1 ? 4 : 2;
+  return NT == 1 ? 4 : 3;
 }
 
-// BITS, VBITS: key and value code widths; NT: PV n-tiles (1: r <= 4, hi/lo halves share one tile;
-// 2: r <= 8, hi tile + lo tile); NVG: value groups per token (d / Gv); NW: warps per
+// BITS, VBITS: key and value code widths; NT: PV weight tiles per k-step (1: r <= 4, hi/lo
+// halves share one tile; 2: r <= 8, a hi and a lo tile accumulated into the same output
+// tile); NVG: value groups per token (d / Gv); NW: warps per
 // CTA (4; 8 for small cluster-merged grids, where one CTA per SM is resident anyway and
 // twice the warps halve the iterations on the critical path).
 template <int BITS, int VBITS, int NT, int NVG, int NW>
@@ -356,6 +360,17 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : 1) decod
   __syncwarp();
   pdl_wait();  // everything above touched shared memory only
 
+  // Query rows of this kv head for warp w: rows w, w + NW, ... (lane l: channels
+  // [4l, 4l+4)). They are loaded before any stage copy is issued: behind the copies of
+  // all resident warps they would arrive only after the first stages, and the query
+  // fold (below) is on the path to the first iteration.
+  constexpr int kRowsPerWarp = (kMaxGqa + kWarps - 1) / kWarps;
+  uint2 qraw[kRowsPerWarp];
+#pragma unroll
+  for (int k = 0; k < kRowsPerWarp; ++k)
+    if (warp + k * kWarps < r)
+      qraw[k] = *reinterpret_cast<const uint2*>(p.q + (qrow0 + warp + k * kWarps) * kHeadDim + 4 * lane);
+
   // sources of the warp's first iteration; iteration i adds 32*i tokens
   const uint8_t* k_src = p.k_codes + slice * p.k_codes_slice + (int64_t)ts0 * ROW;
   const uint8_t* v_src = p.v_codes + slice * p.v_codes_slice + (int64_t)ts0 * ROWV;
@@ -401,13 +416,15 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : 1) decod
   }
   for (int i = 0; i < min(NS, n_mine); ++i) issue(i, i);
 
-  // Query rows of this kv head: warp w takes rows w, w + NW, ...; lane l holds channels
-  // [4l, 4l+4). Each row goes to q_s (binary32, for residual keys) and, normalised by
+  // Query rows (loaded above): each row goes to q_s (binary32, for residual keys) and, normalised by
   // 2^qe (qmax * 2^qe in [2^7, 2^8)) and divided by k_scale, to q2_s in key-pair order:
   // pair pi of chunk c = l/8 joins channels ca(pi) and cb(pi), which lie in this lane
   // (8-bit codes) or in the lane 1 (4-bit) or 2 (2-bit) above it.
-  for (int i = warp; i < r; i += kWarps) {
-    const uint2 raw = *reinterpret_cast<const uint2*>(p.q + (qrow0 + i) * kHeadDim + 4 * lane);
+#pragma unroll
+  for (int kq = 0; kq < kRowsPerWarp; ++kq) {
+    const int i = warp + kq * kWarps;
+    if (i >= r) break;
+    const uint2 raw = qraw[kq];
     float xq[4];
     {
       const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
@@ -454,23 +471,22 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : 1) decod
 
   // online softmax state of query qi (identical in the 4 lanes of row g)
   float m_run = -__int_as_float(0x7f800000), l_run = 0.0f;
-  float o[8][NT][4];
+  // PV accumulators: with r <= 4 one n-tile holds the hi (columns 0..3) and lo (4..7)
+  // products; with r > 4 the hi and lo products of queries 0..7 accumulate into the same
+  // tile through two MMAs (same MMA count as two tiles, half the registers)
+  float o[8][4];
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) o[mt][nt][e] = 0.0f;
+    for (int e = 0; e < 4; ++e) o[mt][e] = 0.0f;
   // zero-point sums per value group on the tensor cores: in an extra PV tile rows 0..7
   // are ones and rows 8..15 the tokens' zero points, so every lane accumulates
   // sum_t w_t (registers 0, 1) and sum_t zp_t w_t (registers 2, 3) of its two columns
-  float bacc[NVG][NT][4];
+  float bacc[NVG][4];
 #pragma unroll
   for (int k = 0; k < NVG; ++k)
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) bacc[k][nt][e] = 0.0f;
+    for (int e = 0; e < 4; ++e) bacc[k][e] = 0.0f;
   const int qe_mine = qe_s[qi];
 
   // QK A fragments of the current key group (or of the raw query for residual keys) in
@@ -670,17 +686,13 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : 1) decod
       const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * j);
       const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * j + 4);
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt)
+      for (int mt = 0; mt < 8; ++mt) {
+        o[mt][0] *= a0; o[mt][1] *= a1; o[mt][2] *= a0; o[mt][3] *= a1;
+      }
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          o[mt][nt][0] *= a0; o[mt][nt][1] *= a1; o[mt][nt][2] *= a0; o[mt][nt][3] *= a1;
-        }
-#pragma unroll
-      for (int k = 0; k < NVG; ++k)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          bacc[k][nt][0] *= a0; bacc[k][nt][1] *= a1; bacc[k][nt][2] *= a0; bacc[k][nt][3] *= a1;
-        }
+      for (int k = 0; k < NVG; ++k) {
+        bacc[k][0] *= a0; bacc[k][1] *= a1; bacc[k][2] *= a0; bacc[k][3] *= a1;
+      }
       m_run = m_new;
     }
     float pr[2][4];
@@ -728,7 +740,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : 1) decod
           za[e] = prmt2(m0, m1, 0x7632u);  // zero points of the token pair
         }
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma16816(bacc[vg][nt], kOne2, za[0], kOne2, za[1], bf[vg][nt][0], bf[vg][nt][1]);
+        for (int nt = 0; nt < NT; ++nt) mma16816(bacc[vg], kOne2, za[0], kOne2, za[1], bf[vg][nt][0], bf[vg][nt][1]);
       }
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
@@ -736,7 +748,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : 1) decod
         const uint32_t a0 = v_pair<VBITS>(vw[0], 2 * mt), a1 = v_pair<VBITS>(vw[0], 2 * mt + 1);
         const uint32_t a2 = v_pair<VBITS>(vw[1], 2 * mt), a3 = v_pair<VBITS>(vw[1], 2 * mt + 1);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma16816(o[mt][nt], a0, a1, a2, a3, bf[vg][nt][0], bf[vg][nt][1]);
+        for (int nt = 0; nt < NT; ++nt) mma16816(o[mt], a0, a1, a2, a3, bf[vg][nt][0], bf[vg][nt][1]);
       }
     }
   };
@@ -785,30 +797,26 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : 1) decod
     l_s[warp * kMaxGqa + g] = l_run;
   }
   // zero-point terms beta = q_min * sum_t w_t - sum_t zp_t w_t of queries 2j and 2j+1
-  // (columns 2j, 2j+1); NT == 1 adds the lo columns 4..7 (lanes j + 2), NT == 2 the lo tile
+  // (columns 2j, 2j+1); NT == 1 adds the lo columns 4..7 (lanes j + 2)
 #pragma unroll
   for (int k = 0; k < NVG; ++k) {
     float t[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      t[e] = bacc[k][0][e];
-      if (NT == 2) t[e] += bacc[k][NT - 1][e];
-      else t[e] += __shfl_xor_sync(0xffffffffu, t[e], 2);
+      t[e] = bacc[k][e];
+      if (NT == 1) t[e] += __shfl_xor_sync(0xffffffffu, t[e], 2);
     }
     if (g == 0 && (NT == 2 || j < 2)) {
       if (2 * j < r) beta_s[(warp * kMaxGqa + 2 * j) * NVG + k] = qmin_v * t[0] - t[2];
       if (2 * j + 1 < r) beta_s[(warp * kMaxGqa + 2 * j + 1) * NVG + k] = qmin_v * t[1] - t[3];
     }
   }
-  // PV columns: NT == 1: cols 0..3 hi / 4..7 lo of queries 0..3; NT == 2: tile 0 hi, tile 1 lo of queries 0..7
+  // PV columns: NT == 1: cols 0..3 hi / 4..7 lo of queries 0..3; NT == 2: queries 0..7 (hi + lo)
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) {
     float v[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      v[e] = o[mt][0][e];
-      if (NT == 2) v[e] += o[mt][NT - 1][e];
-    }
+    for (int e = 0; e < 4; ++e) v[e] = o[mt][e];
     if (NT == 1) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) v[e] += __shfl_xor_sync(0xffffffffu, v[e], 2);  // lo columns j+2 -> j
