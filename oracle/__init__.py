@@ -28,6 +28,11 @@ from .oracle import (  # noqa: F401
     unpack_v_token,
     cache_state,
     dequantize_state,
+    sym_params,
+    sym_quantize,
+    sym_dequantize_value,
+    cache_state_sym,
+    dequantize_state_sym,
     attention,
     OracleState,
 )

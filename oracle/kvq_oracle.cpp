@@ -35,6 +35,8 @@
 //                       empty (all zeros) the scale is 1.
 //   residual window  -> keys only; it holds the T mod R_eff newest tokens (R_eff = R,
 //                       or G when R = 0) and is quantized R_eff tokens at a time.
+//   symmetric scheme -> scale = max|x| / q_max rounded up to binary16, zero point 0,
+//                       one scale per token for keys and values, no residual window.
 //
 // Parity pins: see tests/test_oracle_pins.py. The packed byte layout and the
 // residual/flush bookkeeping are this project's own definitions (the pages fix
@@ -378,6 +380,93 @@ int orc_dequantize_state(int d, int bits, int v_bits, int G, int Gv, int R, int6
       v_out[t * d + c] =
           orc_dequantize_value(u[(size_t)c], v_bits, v_meta[(t * ng + j) * 2], v_meta[(t * ng + j) * 2 + 1]);
     }
+  }
+  return 0;
+}
+
+// ---------------------------------------------------------------------------
+// Symmetric quantizer, [A] § Symmetric vs asymmetric: the zero point is forced to 0
+// and the integer range is centred on real zero, x_hat = scale * q. Readings:
+//   scale  = max|x| / q_max (q_max = 2^(b-1) - 1), stored as binary16 rounded toward
+//            +infinity (so |x| / scale <= q_max), and the quantizer divides by it;
+//            an all-zero vector gets scale 1;
+//   q      = clamp(round(x / scale), q_min, q_max), kept as u = q - q_min.
+// ---------------------------------------------------------------------------
+
+int orc_sym_params(const uint16_t* x, int64_t n, int64_t stride, int bits, uint16_t* scale_h) {
+  if (n <= 0 || !(bits == 2 || bits == 4 || bits == 8)) return -1;
+  float amax = 0.0f;
+  for (int64_t i = 0; i < n; ++i) {
+    float v = std::fabs(orc_f32_from_f16(x[i * stride]));
+    if (v > amax) amax = v;
+  }
+  if (amax == 0.0f) {
+    *scale_h = 0x3C00;  // all zeros: scale 1
+  } else {
+    float s32 = amax / (float)qmax_of(bits);  // binary32, nearest-even
+    *scale_h = orc_f16_from_f32_ru(s32);
+  }
+  return 0;
+}
+
+int orc_sym_quantize(const uint16_t* x, int64_t n, int64_t stride, int bits, uint16_t scale_h, uint8_t* u_out) {
+  if (n < 0 || !(bits == 2 || bits == 4 || bits == 8)) return -1;
+  const float s = orc_f32_from_f16(scale_h);
+  const float qmin = (float)qmin_of(bits), qmax = (float)qmax_of(bits);
+  for (int64_t i = 0; i < n; ++i) {
+    float q = rne_integral(orc_f32_from_f16(x[i * stride]) / s);
+    if (q < qmin) q = qmin;
+    if (q > qmax) q = qmax;
+    u_out[i] = (uint8_t)(int)(q - qmin);
+  }
+  return 0;
+}
+
+// x_hat = scale * q, one binary32 product.
+float orc_sym_dequantize_value(int u, int bits, uint16_t scale_h) {
+  return orc_f32_from_f16(scale_h) * (float)(u + qmin_of(bits));
+}
+
+// Symmetric per-token int8 cache of one (batch row, kv head) after T tokens ("Sub-8-Bit
+// KV Cache Quantization Is Not a Free Lever for an RDNA4 Agent Swarm", § The RDNA4
+// kernel angle: one scale per token; [A] § Symmetric vs asymmetric): keys and values
+// are each quantized per token over all d channels with the symmetric quantizer; there
+// is no residual window. Layout: k_codes [T][d] (key rows as above), k_scale [T]
+// binary16, v_codes pair rows as above, v_meta [T][1][2] = (scale, 0). Optional k_u,
+// v_u [T][d] receive the unpacked codes. Returns 0, or -1 on a bad argument.
+int orc_cache_state_sym(int d, int64_t T, const uint16_t* k_hist, const uint16_t* v_hist, uint8_t* k_codes,
+                        uint16_t* k_scale, uint8_t* v_codes, uint16_t* v_meta, uint8_t* k_u, uint8_t* v_u) {
+  if (d <= 0 || d % 16 || T < 0) return -1;
+  const int bits = 8;
+  std::vector<uint8_t> u((size_t)d);
+  for (int64_t t = 0; t < T; ++t) {
+    uint16_t s_h;
+    orc_sym_params(k_hist + t * d, d, 1, bits, &s_h);
+    orc_sym_quantize(k_hist + t * d, d, 1, bits, s_h, u.data());
+    k_scale[t] = s_h;
+    orc_pack_k_row(u.data(), d, bits, k_codes + t * d);
+    if (k_u) std::memcpy(k_u + t * d, u.data(), (size_t)d);
+    orc_sym_params(v_hist + t * d, d, 1, bits, &s_h);
+    orc_sym_quantize(v_hist + t * d, d, 1, bits, s_h, u.data());
+    v_meta[t * 2 + 0] = s_h;
+    v_meta[t * 2 + 1] = 0;  // binary16 +0
+    orc_pack_v_token(u.data(), d, bits, t, v_codes);
+    if (v_u) std::memcpy(v_u + t * d, u.data(), (size_t)d);
+  }
+  return 0;
+}
+
+// Dequantized keys and values of a symmetric per-token state: k_out, v_out [T][d].
+int orc_dequantize_state_sym(int d, int64_t T, const uint8_t* k_codes, const uint16_t* k_scale,
+                             const uint8_t* v_codes, const uint16_t* v_meta, float* k_out, float* v_out) {
+  if (d <= 0 || d % 16 || T < 0) return -1;
+  const int bits = 8;
+  std::vector<uint8_t> u((size_t)d);
+  for (int64_t t = 0; t < T; ++t) {
+    orc_unpack_k_row(k_codes + t * d, d, bits, u.data());
+    for (int c = 0; c < d; ++c) k_out[t * d + c] = orc_sym_dequantize_value(u[(size_t)c], bits, k_scale[t]);
+    orc_unpack_v_token(v_codes, d, bits, t, u.data());
+    for (int c = 0; c < d; ++c) v_out[t * d + c] = orc_sym_dequantize_value(u[(size_t)c], bits, v_meta[t * 2]);
   }
   return 0;
 }

@@ -80,6 +80,18 @@ def lib():
             L.orc_dequantize_state.argtypes = [ctypes.c_int] * 6 + [ctypes.c_int64, _u8p, _u16p, _u16p, _u8p, _u16p,
                                                                     _f32p, _f32p]
             L.orc_dequantize_state.restype = ctypes.c_int
+            L.orc_sym_params.argtypes = [_u16p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, _u16p]
+            L.orc_sym_params.restype = ctypes.c_int
+            L.orc_sym_quantize.argtypes = [_u16p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_uint16, _u8p]
+            L.orc_sym_quantize.restype = ctypes.c_int
+            L.orc_sym_dequantize_value.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_uint16]
+            L.orc_sym_dequantize_value.restype = ctypes.c_float
+            L.orc_cache_state_sym.argtypes = [ctypes.c_int, ctypes.c_int64, _u16p, _u16p, _u8p, _u16p, _u8p, _u16p,
+                                              _u8p, _u8p]
+            L.orc_cache_state_sym.restype = ctypes.c_int
+            L.orc_dequantize_state_sym.argtypes = [ctypes.c_int, ctypes.c_int64, _u8p, _u16p, _u8p, _u16p, _f32p,
+                                                   _f32p]
+            L.orc_dequantize_state_sym.restype = ctypes.c_int
             L.orc_attention.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int64, _u16p, _f32p, _f32p,
                                         ctypes.c_float, _f32p]
             L.orc_attention.restype = ctypes.c_int
@@ -242,6 +254,71 @@ def dequantize_state(st: OracleState, *, d: int, bits: int, G: int, Gv: int, R: 
     rc = lib().orc_dequantize_state(d, bits, v_bits, G, Gv, R, T, _ptr(nz(st.k_codes), _u8p), _ptr(nz(st.k_meta), _u16p),
                                     _ptr(nz(st.k_resid), _u16p), _ptr(nz(st.v_codes), _u8p),
                                     _ptr(nz(st.v_meta), _u16p), _ptr(k_out, _f32p), _ptr(v_out, _f32p))
+    if rc != 0:
+        raise ValueError("bad cache shape")
+    return k_out[:T], v_out[:T]
+
+
+# ----------------------------------------------------------------------------- symmetric scheme
+def sym_params(x, bits: int = 8) -> int:
+    """Symmetric scale (binary16 bits) of a vector of binary16 values (zero point 0)."""
+    x = _as_u16(x).ravel()
+    s = ctypes.c_uint16()
+    if lib().orc_sym_params(_ptr(x, _u16p), x.size, 1, bits, ctypes.byref(s)) != 0:
+        raise ValueError("bad vector")
+    return int(s.value)
+
+
+def sym_quantize(x, bits: int, scale_h: int) -> np.ndarray:
+    """Codes u = q - q_min of q = clamp(round(x / scale), q_min, q_max)."""
+    x = _as_u16(x).ravel()
+    u = np.zeros(max(x.size, 1), np.uint8)
+    xx = x if x.size else np.zeros(1, np.uint16)
+    if lib().orc_sym_quantize(_ptr(xx, _u16p), x.size, 1, bits, scale_h, _ptr(u, _u8p)) != 0:
+        raise ValueError("bad arguments")
+    return u[:x.size]
+
+
+def sym_dequantize_value(u: int, bits: int, scale_h: int) -> float:
+    return float(lib().orc_sym_dequantize_value(int(u), bits, scale_h))
+
+
+def cache_state_sym(k_hist, v_hist, *, d: int) -> OracleState:
+    """Symmetric per-token int8 cache of one (b, h) slice: keys and values each with one
+    scale per token and zero point 0, no residual window. k_meta holds the per-token key
+    scales [T] (binary16 bits), v_meta [T][1][2] the value (scale, 0) pairs."""
+    k = _as_u16(k_hist)
+    v = _as_u16(v_hist)
+    T = k.shape[0]
+    assert k.shape == (T, d) and v.shape == (T, d)
+    k_codes = np.zeros((T, d), np.uint8)
+    k_meta = np.zeros((T,), np.uint16)
+    v_codes = np.zeros(((T + 1) // 2, 2 * d), np.uint8)
+    v_meta = np.zeros((T, 1, 2), np.uint16)
+    k_u = np.zeros((T, d), np.uint8)
+    v_u = np.zeros((T, d), np.uint8)
+    bufs = [np.zeros(1, a.dtype) if a.size == 0 else a for a in (k_codes, k_meta, v_codes, v_meta, k_u, v_u)]
+    kk = k if k.size else np.zeros(1, np.uint16)
+    vv = v if v.size else np.zeros(1, np.uint16)
+    rc = lib().orc_cache_state_sym(d, T, _ptr(kk, _u16p), _ptr(vv, _u16p), _ptr(bufs[0], _u8p), _ptr(bufs[1], _u16p),
+                                   _ptr(bufs[2], _u8p), _ptr(bufs[3], _u16p), _ptr(bufs[4], _u8p), _ptr(bufs[5], _u8p))
+    if rc != 0:
+        raise ValueError("bad cache shape")
+    return OracleState(T, T, k_codes, k_meta, np.zeros((0, d), np.uint16), v_codes, v_meta, k_u, v_u)
+
+
+def dequantize_state_sym(st: OracleState, *, d: int):
+    """(k_hat, v_hat) binary32 [T][d] of a symmetric per-token state."""
+    T = st.T
+    k_out = np.zeros((max(T, 1), d), np.float32)
+    v_out = np.zeros((max(T, 1), d), np.float32)
+
+    def nz(a):
+        return np.ascontiguousarray(a) if a.size else np.zeros(1, a.dtype)
+
+    rc = lib().orc_dequantize_state_sym(d, T, _ptr(nz(st.k_codes), _u8p), _ptr(nz(st.k_meta), _u16p),
+                                        _ptr(nz(st.v_codes), _u8p), _ptr(nz(st.v_meta), _u16p), _ptr(k_out, _f32p),
+                                        _ptr(v_out, _f32p))
     if rc != 0:
         raise ValueError("bad cache shape")
     return k_out[:T], v_out[:T]

@@ -432,3 +432,98 @@ def test_mixed_width_state_is_the_two_single_width_states():
     kh8, _ = oracle.dequantize_state(k8, d=d, bits=8, G=32, Gv=64, R=128)
     _, vh4 = oracle.dequantize_state(v4, d=d, bits=4, G=32, Gv=64, R=128)
     assert np.array_equal(kh, kh8) and np.array_equal(vh, vh4)
+
+
+# ----------------------------------------------------------------------------- symmetric scheme
+# "KV Cache Quantization — 8-bit and 4-bit", § Symmetric vs asymmetric: zero point 0, the
+# integer range centred on real zero, x_hat = scale * q; the -0.1 ... +3.0 example.
+
+def test_symmetric_worked_example_wastes_the_negative_codes():
+    """Data in [-0.1, 3.0]: the symmetric range must stretch to +-3.0. By hand:
+    3.0/127 = 1.51181... * 2^-6; rounded up to 10 fraction bits: (1 + 525/1024) * 2^-6
+    = 0.0236358642578125 (binary16 0x260D). -0.1 / scale = -4.23 -> q = -4; 3.0 / scale
+    = 126.93 -> q = 127. So only the codes -4..127 (132 of 256) are ever used, while the
+    asymmetric quantizer fitted to [-0.1, 3.0] spends all 256."""
+    grid = np.unique(np.linspace(-0.1, 3.0, 20001).astype(np.float16))
+    s = oracle.sym_params(grid, 8)
+    assert s == 0x260D
+    assert oracle.f32_from_f16(s) == 0.0236358642578125
+    q = oracle.sym_quantize(grid, 8, s).astype(int) - 128
+    assert q.min() == -4 and q.max() == 127
+    assert len(np.unique(q)) == 132
+    sa, za = oracle.quant_params(grid, 8)
+    ua = oracle.quantize_values(grid, 8, sa, za)
+    assert len(np.unique(ua)) == 256
+    # the symmetric step is about twice the asymmetric one: twice the worst-case error
+    assert 1.9 < oracle.f32_from_f16(s) / oracle.f32_from_f16(sa) < 2.0
+
+
+def test_symmetric_round_trip_on_grid():
+    """x = q * 2^-4 for every q in [-127, 127]: max|x| / 127 = 2^-4 exactly, so the
+    stored scale is 2^-4 and every value comes back exactly."""
+    q = np.arange(-127, 128)
+    x = (q * 0.0625).astype(np.float16)
+    s = oracle.sym_params(x, 8)
+    assert s == 0x2C00  # 2^-4
+    u = oracle.sym_quantize(x, 8, s)
+    assert np.array_equal(u.astype(int) - 128, q)
+    back = np.array([oracle.sym_dequantize_value(int(v), 8, s) for v in u])
+    assert np.array_equal(back, x.astype(np.float64))
+
+
+def test_symmetric_error_bound_and_odd_symmetry():
+    """|x - x_hat| <= scale / 2 (the quotient x / scale is one binary32 rounding away
+    from exact), no clipping (scale rounded up), and q(-x) = -q(x)."""
+    rng = np.random.default_rng(5)
+    for trial in range(200):
+        n = int(rng.integers(1, 300))
+        x = (rng.standard_normal(n) * 10.0 ** rng.uniform(-3, 3)).astype(np.float16)
+        if trial % 7 == 0:
+            x[rng.integers(n)] *= 40  # an outlier
+        s = oracle.sym_params(x, 8)
+        sf = oracle.f32_from_f16(s)
+        u = oracle.sym_quantize(x, 8, s)
+        q = u.astype(int) - 128
+        assert q.min() >= -127 and q.max() <= 127
+        xh = np.array([oracle.sym_dequantize_value(int(v), 8, s) for v in u])
+        assert np.all(np.abs(x.astype(np.float64) - xh) <= sf / 2 * (1 + 2.0 ** -20))
+        qn = oracle.sym_quantize(-x, 8, s).astype(int) - 128
+        assert np.array_equal(qn, -q)
+
+
+def test_symmetric_zero_vector():
+    x = np.zeros(128, np.float16)
+    s = oracle.sym_params(x, 8)
+    assert s == 0x3C00
+    u = oracle.sym_quantize(x, 8, s)
+    assert np.all(u == 128)
+    assert oracle.sym_dequantize_value(128, 8, s) == 0.0
+
+
+def test_symmetric_cache_is_per_token():
+    """Every token's keys and values carry their own scale: scaling one token's history
+    leaves the other tokens' codes untouched, and every dequantized row is within half
+    its own step of the input."""
+    rng = np.random.default_rng(9)
+    T, d = 37, 128
+    k = (rng.standard_normal((T, d)) * 2).astype(np.float16)
+    v = (rng.standard_normal((T, d)) * 0.5).astype(np.float16)
+    st = oracle.cache_state_sym(k, v, d=d)
+    assert st.Tq == T and st.k_meta.shape == (T,) and st.v_meta.shape == (T, 1, 2)
+    assert np.all(st.v_meta[:, 0, 1] == 0)
+    k2 = k.copy()
+    k2[5] *= np.float16(8)
+    st2 = oracle.cache_state_sym(k2, v, d=d)
+    others = np.arange(T) != 5
+    assert np.array_equal(st2.k_u[others], st.k_u[others])
+    assert np.array_equal(st2.k_u[5], st.k_u[5])  # a power-of-two rescale keeps the codes
+    assert st2.k_meta[5] != st.k_meta[5]
+    kh, vh = oracle.dequantize_state_sym(st, d=d)
+    ks = np.array([oracle.f32_from_f16(int(h)) for h in st.k_meta])
+    vs = np.array([oracle.f32_from_f16(int(h)) for h in st.v_meta[:, 0, 0]])
+    assert np.all(np.abs(k.astype(np.float64) - kh) <= ks[:, None] / 2 * (1 + 2.0 ** -20))
+    assert np.all(np.abs(v.astype(np.float64) - vh) <= vs[:, None] / 2 * (1 + 2.0 ** -20))
+    # the packed rows decode to the same codes
+    for t in (0, 1, 36):
+        assert np.array_equal(oracle.unpack_k_row(st.k_codes[t], d, 8), st.k_u[t])
+        assert np.array_equal(oracle.unpack_v_token(st.v_codes.ravel(), d, 8, t), st.v_u[t])
