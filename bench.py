@@ -36,6 +36,12 @@ DEFAULT_WORKLOAD = "llama8b-int8"
 
 
 # ----------------------------------------------------------------------------- byte accounting
+def key_meta_bytes(w, n_keys: int) -> int:
+    """Key metadata of n_keys quantized tokens of one slice: (scale, zero point) per channel
+    and group of k_group tokens, or one binary16 scale per token in the symmetric scheme."""
+    return n_keys * 2 if w.symmetric else (n_keys // w.k_group) * w.d_head * 4
+
+
 def attn_bytes_per_layer(w, T: int) -> int:
     """Algorithmic bytes one decode-attention launch (one layer) moves at T cached tokens:
     packed key codes + key metadata of the quantized tokens, binary16 residual keys,
@@ -43,7 +49,7 @@ def attn_bytes_per_layer(w, T: int) -> int:
     d, b, bv = w.d_head, w.bits, w.vbits
     R = w.r_eff
     Tq = (T // R) * R
-    per_slice = (Tq * (d * b // 8) + (Tq // w.k_group) * d * 4 + (T - Tq) * 2 * d + T * (d * bv // 8)
+    per_slice = (Tq * (d * b // 8) + key_meta_bytes(w, Tq) + (T - Tq) * 2 * d + T * (d * bv // 8)
                  + T * (d // w.v_group) * 4)
     return w.batch * w.n_kv * per_slice + w.batch * w.n_q * d * 2 + w.batch * w.n_q * d * 4
 
@@ -58,7 +64,7 @@ def append_bytes_per_layer(w, s_cur: int, n_new: int = 1) -> int:
     per = n_new * (2 * d * 2 + d * bv // 8 + (d // w.v_group) * 4)
     per += max(0, T - max(A1, s_cur)) * 2 * d  # residual writes
     if A1 > A0:
-        per += (s_cur - A0) * 2 * d + (A1 - A0) * (d * b // 8) + ((A1 - A0) // w.k_group) * d * 4
+        per += (s_cur - A0) * 2 * d + (A1 - A0) * (d * b // 8) + key_meta_bytes(w, A1 - A0)
     return w.batch * w.n_kv * per
 
 
@@ -67,7 +73,7 @@ def prefill_bytes_per_layer(w, S: int) -> int:
     values read; key codes + group metadata, residual keys, value codes + metadata written."""
     d, b, bv = w.d_head, w.bits, w.vbits
     Tq = (S // w.r_eff) * w.r_eff
-    per = S * 2 * d * 2 + Tq * (d * b // 8) + (Tq // w.k_group) * d * 4 + (S - Tq) * 2 * d
+    per = S * 2 * d * 2 + Tq * (d * b // 8) + key_meta_bytes(w, Tq) + (S - Tq) * 2 * d
     per += S * (d * bv // 8) + S * (d // w.v_group) * 4
     return w.batch * w.n_kv * per
 
@@ -196,7 +202,7 @@ def _slice_bytes(w, T: int) -> int:
     d, bits, vbits = w.d_head, w.bits, w.vbits
     R = w.r_eff
     Tq = (T // R) * R
-    return (Tq * (d * bits // 8) + (Tq // w.k_group) * d * 4 + (T - Tq) * 2 * d + T * (d * vbits // 8)
+    return (Tq * (d * bits // 8) + key_meta_bytes(w, Tq) + (T - Tq) * 2 * d + T * (d * vbits // 8)
             + T * (d // w.v_group) * 4 + w.gqa * d * 6)
 
 
@@ -210,8 +216,11 @@ def oracle_prepare(w, layer: int, T: int, n_slices: int):
         b, h = divmod(idx, w.n_kv)
         k = synth.k_slice(w, layer, b, h, range(T))
         v = synth.v_slice(w, layer, b, h, range(T))
-        st = oracle.cache_state(k, v, d=w.d_head, bits=w.bits, G=w.k_group, Gv=w.v_group, R=w.residual,
-                                v_bits=w.vbits)
+        if w.symmetric:
+            st = oracle.cache_state_sym(k, v, d=w.d_head)
+        else:
+            st = oracle.cache_state(k, v, d=w.d_head, bits=w.bits, G=w.k_group, Gv=w.v_group, R=w.residual,
+                                    v_bits=w.vbits)
         out.append((st, synth.q_rows(w, layer, b, h, T - 1)))
     return out
 
@@ -224,8 +233,11 @@ def oracle_decode(w, prepared, budget_s: float = float("inf")):
     total_t, total_b, n = 0.0, 0, 0
     for st, q in prepared:
         t0 = time.perf_counter()
-        kh, vh = oracle.dequantize_state(st, d=w.d_head, bits=w.bits, G=w.k_group, Gv=w.v_group, R=w.residual,
-                                         v_bits=w.vbits)
+        if w.symmetric:
+            kh, vh = oracle.dequantize_state_sym(st, d=w.d_head)
+        else:
+            kh, vh = oracle.dequantize_state(st, d=w.d_head, bits=w.bits, G=w.k_group, Gv=w.v_group, R=w.residual,
+                                             v_bits=w.vbits)
         oracle.attention(q, kh, vh, w.softmax_scale)
         total_t += time.perf_counter() - t0
         total_b += _slice_bytes(w, st.T)
@@ -498,11 +510,12 @@ def main():
     if rank == 0:
         line = {"metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
                 "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                "dtype": (f"int{w.bits} codes" if w.vbits == w.bits else f"int{w.bits} key / int{w.vbits} value codes")
+                "dtype": ("int8 symmetric per-token codes" if w.symmetric else
+                          f"int{w.bits} codes" if w.vbits == w.bits else f"int{w.bits} key / int{w.vbits} value codes")
                 + ", f32 math", "data": "synthetic",
                 "tokens_per_s": round(tok_s, 1), "pct_of_peak": round(100 * gbs / world / peak, 2),
                 "config": {"workload": w.name, "layers": L, "batch": w.batch, "n_kv_heads": w.n_kv, "gqa": w.gqa,
-                           "d_head": w.d_head, "prompt_tokens": S, "bits": w.bits, "v_bits": w.vbits, "k_group": w.k_group,
+                           "d_head": w.d_head, "prompt_tokens": S, "bits": w.bits, "v_bits": w.vbits, "symmetric": w.symmetric, "k_group": w.k_group,
                            "v_group": w.v_group, "residual": w.residual, "decode": args.decode,
                            "cuda_graph": use_graph, "parallelism": f"replicas x{world}",
                            "l2": "per-step working set (all layers' packed cache) exceeds the 129 MB L2; no flush"},

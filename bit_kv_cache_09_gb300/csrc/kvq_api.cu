@@ -53,12 +53,13 @@ int device_sm_count() {
 // Resident CTAs per SM of the decode kernel that `impl` selects (cached per device).
 // Index of the (key, value) code widths: 8/8, 4/4, 2/2, 8/4.
 int width_index(const Geometry& g) {
+  if (g.sym) return 4;  // symmetric per-token int8
   if (g.vbits != g.bits) return 3;
   return g.bits == 8 ? 0 : (g.bits == 4 ? 1 : 2);
 }
 
 int decode_occupancy(const Geometry& g, kvq_decode_impl impl) {
-  static std::atomic<int> cache[16][2][4][2][3];  // device, impl, code widths, r class, value groups
+  static std::atomic<int> cache[16][2][5][2][3];  // device, impl, code scheme/widths, r class, value groups
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) dev = 0;
   const int ii = impl == KVQ_DECODE_SIMT ? 0 : 1;
@@ -68,7 +69,7 @@ int decode_occupancy(const Geometry& g, kvq_decode_impl impl) {
   std::atomic<int>& slot = cache[dev][ii][bi][ri][vi];
   int n = slot.load(std::memory_order_relaxed);
   if (n <= 0) {
-    n = ii == 0 ? kvq::occupancy_decode_simt(g.bits) : kvq::occupancy_decode_mma(g.bits, g.vbits, g.r, g.n_vg);
+    n = ii == 0 ? kvq::occupancy_decode_simt(g.bits) : kvq::occupancy_decode_mma(g.bits, g.vbits, g.r, g.n_vg, g.sym);
     if (n > 0) slot.store(n, std::memory_order_relaxed);
   }
   return n > 0 ? n : 1;
@@ -78,7 +79,7 @@ int decode_occupancy(const Geometry& g, kvq_decode_impl impl) {
 // kernel that can be resident at once on this device (<= 0: such a cluster cannot
 // launch); cached per device and kernel shape.
 int resident_clusters(const Geometry& g, int cs, int nw) {
-  static std::atomic<int> cache[16][4][2][3][5][2];  // device, code widths, r class, value groups, log2 size, warps
+  static std::atomic<int> cache[16][5][2][3][5][2];  // device, code scheme/widths, r class, value groups, log2 size, warps
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) dev = 0;
   const int bi = width_index(g);
@@ -89,7 +90,7 @@ int resident_clusters(const Geometry& g, int cs, int nw) {
   std::atomic<int>& slot = cache[dev][bi][ri][vi][lg][nw == 8 ? 1 : 0];
   int n = slot.load(std::memory_order_relaxed);
   if (n == 0) {
-    n = kvq::max_clusters_decode_mma(g.bits, g.vbits, g.r, g.n_vg, cs, nw);
+    n = kvq::max_clusters_decode_mma(g.bits, g.vbits, g.r, g.n_vg, cs, nw, g.sym);
     if (n <= 0) n = -1;
     slot.store(n, std::memory_order_relaxed);
   }
@@ -250,6 +251,7 @@ kvq_status kvq_quantize_append(const kvq_config* cfg, const kvq_buffers* bufs, i
   p.v_codes_slice = g.v_codes_slice;
   p.fd_H = kvq::make_fast_div((uint32_t)g.H);
   p.rows_32 = n_new * g.H < (int64_t(1) << 31);
+  p.sym = g.sym;
   cudaError_t e = kvq::launch_append(p, g.bits, g.vbits, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
@@ -285,6 +287,7 @@ kvq_status kvq_dequantize(const kvq_config* cfg, const kvq_buffers* bufs, int32_
   p.rowV = g.rowV;
   p.k_codes_slice = g.k_codes_slice;
   p.v_codes_slice = g.v_codes_slice;
+  p.sym = g.sym;
   cudaError_t e = kvq::launch_dequant(p, g.bits, g.vbits, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
@@ -360,12 +363,15 @@ kvq_status decode_launch(const kvq_config* cfg, const kvq_buffers* bufs, int32_t
   const kvq_decode_impl use = impl == KVQ_DECODE_SIMT ? KVQ_DECODE_SIMT : KVQ_DECODE_MMA;
   if (use == KVQ_DECODE_SIMT && (k_new || v_new)) return KVQ_ERR_UNSUPPORTED;
   if (use == KVQ_DECODE_SIMT && g.vbits != g.bits) return KVQ_ERR_UNSUPPORTED;  // CUDA-core kernel: equal widths
+  if (use == KVQ_DECODE_SIMT && g.sym) return KVQ_ERR_UNSUPPORTED;              // and the asymmetric scheme
+  if (g.sym && (k_new || v_new)) return KVQ_ERR_UNSUPPORTED;                   // no fused append for it
   const Plan pl = plan_splits(g, s_cur, use);
   p.n_split = (int)pl.n_split;
   p.chunk = pl.chunk;
   p.cluster = pl.cluster;
   p.n_parts = pl.n_parts;
   p.warps = pl.warps;
+  p.sym = g.sym;
   cudaError_t e = (use == KVQ_DECODE_SIMT) ? kvq::launch_decode_simt(p, g.bits, static_cast<cudaStream_t>(stream))
                                             : kvq::launch_decode_mma(p, g.bits, g.vbits, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
@@ -393,7 +399,7 @@ kvq_status kvq_decode_step(const kvq_config* cfg, const kvq_buffers* bufs, int32
   if (!aligned16(k_f16) || !aligned16(v_f16)) return KVQ_ERR_INVALID_ARG;
   if (s_cur + 1 > g.S_max) return KVQ_ERR_CAPACITY;
   const int64_t T = s_cur + 1;
-  if (T % g.R_eff == 0) {  // the append fills a residual window: quantize it with the append kernels
+  if (g.sym || T % g.R_eff == 0) {  // symmetric scheme, or the append fills a residual window: two launches
     st = kvq_quantize_append(cfg, bufs, layer, s_cur, 1, k_f16, v_f16, stream);
     if (st != KVQ_OK) return st;
     return decode_launch(cfg, bufs, layer, T, q_f16, softmax_scale, out, ws, ws_bytes, stream, KVQ_DECODE_AUTO,

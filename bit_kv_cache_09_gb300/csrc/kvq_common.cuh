@@ -7,6 +7,8 @@
 //   k_resid slice: R_eff rows x d binary16
 //   v_codes slice: S_pad/2 pair rows of 2*rowV bytes (rowV = d*b/8)
 //   v_meta  slice: S_pad tokens x d/Gv x half2(scale, zero_point)
+// Symmetric per-token scheme: k_meta slice = S_pad binary16 key scales, no k_resid,
+// Gv = d (v_meta holds half2(scale, 0)), every key quantized on append (Tq = T).
 #pragma once
 
 #include <cstddef>
@@ -23,6 +25,7 @@ constexpr int kMaxResidual = 1024;
 
 struct Geometry {
   int L, B, H, r, d, S_max, bits, vbits, G, Gv, R, R_eff;  // bits: keys, vbits: values
+  int sym;             // symmetric per-token int8 scheme
   int64_t S_pad;
   int64_t rowK, rowV;  // bytes per token row of key / value codes
   int n_vg;            // value groups per token (d / Gv)
@@ -47,6 +50,9 @@ inline kvq_status make_geometry(const kvq_config* c, Geometry* g) {
   if (c->residual_len > kMaxResidual) return KVQ_ERR_UNSUPPORTED;
   if (c->gqa_ratio > kMaxGqa) return KVQ_ERR_UNSUPPORTED;
   if (c->n_kv_heads > 255 || c->batch > 4095 || c->max_seq_len > (1 << 24)) return KVQ_ERR_UNSUPPORTED;
+  if (c->symmetric != 0 && c->symmetric != 1) return KVQ_ERR_INVALID_ARG;
+  if (c->symmetric && (c->bits != 8 || vbits != 8 || c->v_group != c->d_head)) return KVQ_ERR_UNSUPPORTED;
+  if (c->symmetric && c->residual_len != 0) return KVQ_ERR_INVALID_ARG;  // no residual window
   Geometry x;
   x.L = c->n_layers;
   x.B = c->batch;
@@ -59,14 +65,15 @@ inline kvq_status make_geometry(const kvq_config* c, Geometry* g) {
   x.G = c->k_group;
   x.Gv = c->v_group;
   x.R = c->residual_len;
-  x.R_eff = c->residual_len > 0 ? c->residual_len : c->k_group;
+  x.sym = c->symmetric;
+  x.R_eff = x.sym ? 1 : (c->residual_len > 0 ? c->residual_len : c->k_group);  // symmetric: Tq = T
   x.S_pad = ((int64_t)c->max_seq_len + kSeqAlign - 1) / kSeqAlign * kSeqAlign;
   x.rowK = (int64_t)x.d * x.bits / 8;
   x.rowV = (int64_t)x.d * x.vbits / 8;
   x.n_vg = x.d / x.Gv;
   x.k_codes_slice = x.S_pad * x.rowK;
-  x.k_meta_slice = (x.S_pad / x.G) * x.d * 4;
-  x.k_resid_slice = (int64_t)x.R_eff * x.d * 2;
+  x.k_meta_slice = x.sym ? x.S_pad * 2 : (x.S_pad / x.G) * x.d * 4;
+  x.k_resid_slice = x.sym ? 0 : (int64_t)x.R_eff * x.d * 2;
   x.v_codes_slice = x.S_pad * x.rowV;
   x.v_meta_slice = x.S_pad * x.n_vg * 4;
   x.n_slices = (int64_t)x.L * x.B * x.H;

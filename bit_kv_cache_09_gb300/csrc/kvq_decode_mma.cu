@@ -13,8 +13,12 @@ int occupancy_decode_mma_b2(int r, int n_vg, int vbits);
 int max_clusters_decode_mma_b8(int r, int n_vg, int cs, int nw, int vbits);
 int max_clusters_decode_mma_b4(int r, int n_vg, int cs, int nw, int vbits);
 int max_clusters_decode_mma_b2(int r, int n_vg, int cs, int nw, int vbits);
+cudaError_t launch_decode_mma_sym(const DecodeParams& p, cudaStream_t stream);
+int occupancy_decode_mma_sym(int r);
+int max_clusters_decode_mma_sym(int r, int cs, int nw);
 
 cudaError_t launch_decode_mma(const DecodeParams& p, int bits, int vbits, cudaStream_t stream) {
+  if (p.sym) return launch_decode_mma_sym(p, stream);
   switch (bits) {
     case 8: return launch_decode_mma_b8(p, vbits, stream);
     case 4: return launch_decode_mma_b4(p, vbits, stream);
@@ -22,7 +26,8 @@ cudaError_t launch_decode_mma(const DecodeParams& p, int bits, int vbits, cudaSt
   }
 }
 
-int occupancy_decode_mma(int bits, int vbits, int r, int n_vg) {
+int occupancy_decode_mma(int bits, int vbits, int r, int n_vg, int sym) {
+  if (sym) return occupancy_decode_mma_sym(r);
   switch (bits) {
     case 8: return occupancy_decode_mma_b8(r, n_vg, vbits);
     case 4: return occupancy_decode_mma_b4(r, n_vg, vbits);
@@ -30,7 +35,8 @@ int occupancy_decode_mma(int bits, int vbits, int r, int n_vg) {
   }
 }
 
-int max_clusters_decode_mma(int bits, int vbits, int r, int n_vg, int cs, int nw) {
+int max_clusters_decode_mma(int bits, int vbits, int r, int n_vg, int cs, int nw, int sym) {
+  if (sym) return max_clusters_decode_mma_sym(r, cs, nw);
   switch (bits) {
     case 8: return max_clusters_decode_mma_b8(r, n_vg, cs, nw, vbits);
     case 4: return max_clusters_decode_mma_b4(r, n_vg, cs, nw, vbits);

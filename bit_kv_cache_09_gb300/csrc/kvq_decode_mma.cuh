@@ -190,16 +190,18 @@ __device__ __forceinline__ constexpr float v_scale(int i) {
 }
 
 // One stage = one iteration of 32 tokens (two 16-token halves):
-//   [key codes 32*rowK][value pair rows 32*rowV][value meta 32*4*NVG B][key-group meta 512 B]
+//   [key codes 32*rowK][value pair rows 32*rowV][value meta 32*4*NVG B][key meta]
+// where the key meta is one key group's (scale, zero point) per channel (512 B), or in
+// the symmetric per-token scheme (SYM) the 32 tokens' binary16 key scales (64 B).
 // NW warps per CTA each own a ring of NS stages. After the loop the rings are reused
 // for the merges: per-warp partials (o, m, l, beta), the CTA partial read by the
 // cluster merge (cm, cl, co), then the scratch of the workspace merge.
-template <int BITS, int VBITS, int NVG, int NW>
+template <int BITS, int VBITS, int NVG, int NW, bool SYM = false>
 struct Stage {
   static constexpr int KB = 32 * BITS * 128 / 8;   // key codes of 32 tokens
   static constexpr int VB = 32 * VBITS * 128 / 8;  // value codes of 32 tokens
   static constexpr int VM = 32 * 4 * NVG;         // value meta of 32 tokens
-  static constexpr int KM = 512;                  // one key group's meta
+  static constexpr int KM = SYM ? 64 : 512;       // one key group's meta, or 32 key scales
   static constexpr int BYTES = KB + VB + VM + KM;
   static constexpr int NS = BITS == 2 ? 3 : 2;
   static constexpr int WARP_BYTES = NS * BYTES;
@@ -306,15 +308,21 @@ constexpr int min_blocks() {
   return NT == 1 ? 4 : 3;
 }
 
+// SYM: the symmetric per-token int8 scheme ("KV Cache Quantization — 8-bit and 4-bit",
+// § Symmetric vs asymmetric; one scale per token, "Sub-8-Bit KV Cache Quantization Is
+// Not a Free Lever for an RDNA4 Agent Swarm", § The RDNA4 kernel angle): no query fold;
+// the raw query meets the exact key codes on the tensor cores and the score of token t
+// is s_t * (2^24 acc + q_min * sum_c q_c) in softmax units; values as in the
+// asymmetric scheme with one group and zero point 0.
 // BITS, VBITS: key and value code widths; NT: PV weight tiles per k-step (1: r <= 4, hi/lo
 // halves share one tile; 2: r <= 8, a hi and a lo tile accumulated into the same output
 // tile); NVG: value groups per token (d / Gv); NW: warps per
 // CTA (4; 8 for small cluster-merged grids, where one CTA per SM is resident anyway and
 // twice the warps halve the iterations on the critical path).
-template <int BITS, int VBITS, int NT, int NVG, int NW>
+template <int BITS, int VBITS, int NT, int NVG, int NW, bool SYM = false>
 __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : 1) decode_mma_kernel(DecodeParams p) {
   constexpr int kWarps = NW;
-  using St = Stage<BITS, VBITS, NVG, NW>;
+  using St = Stage<BITS, VBITS, NVG, NW, SYM>;
   constexpr int NS = St::NS;
   constexpr int kTok = 32;  // tokens per iteration
   constexpr float qmin = -(float)(1 << (BITS - 1));     // keys
@@ -331,6 +339,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : 1) decod
   // by 2^qe_s[i] (so that |entry| < 2^8), as binary16 pairs
   __shared__ __align__(16) uint32_t q2_s[kMaxGqa][4][16];
   __shared__ int qe_s[kMaxGqa];
+  __shared__ float qsum_s[kMaxGqa];  // SYM: sum_c q_c of every query row
   __shared__ __align__(16) uint32_t qa_s[kWarps][(NT == 1) ? 16 : 32][36];  // padded rows: no bank conflicts
 
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -376,6 +385,8 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : 1) decod
   const uint8_t* v_src = p.v_codes + slice * p.v_codes_slice + (int64_t)ts0 * ROWV;
   const uint8_t* vm_src = reinterpret_cast<const uint8_t*>(p.v_meta + (slice * p.S_pad + ts0) * NVG);
   const __half2* km_base = p.k_meta + slice * (p.S_pad >> p.log2G) * kHeadDim;
+  // SYM: per-token key scales of the warp's first iteration (k_meta holds S_pad per slice)
+  const uint8_t* ksc_src = reinterpret_cast<const uint8_t*>(reinterpret_cast<const __half*>(p.k_meta) + slice * p.S_pad + ts0);
 
   // Copies of the warp's iteration i into stage sidx: every lane moves 16-byte pieces
   // (piece lane + 32c of each block) with cp.async and arrives on the stage barrier
@@ -396,13 +407,17 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : 1) decod
 #pragma unroll
     for (int c = 0; c < CKV; ++c) cp_async16(dst + St::KB + 512 * c, v_src + offv + 512 * c);
     if (16 * lane < St::VM) cp_async16(dst + St::KB + St::VB, vm_src + (size_t)i * St::VM + 16 * lane);
-    if (newgrp) cp_async16(dst + St::KB + St::VB + St::VM, km_base + ((ts >> p.log2G) << 7) + 4 * lane);
+    if constexpr (SYM) {
+      if (lane < 4) cp_async16(dst + St::KB + St::VB + St::VM, ksc_src + (size_t)i * 64 + 16 * lane);
+    } else {
+      if (newgrp) cp_async16(dst + St::KB + St::VB + St::VM, km_base + ((ts >> p.log2G) << 7) + 4 * lane);
+    }
     cp_async_arrive(smem_u32(&bars[warp][sidx]));
   };
   // Fused decode step: the CTA whose range holds the new token T-1 appends it first
   // (value row quantized per group into its half of the pair row, key row into its
   // residual slot); the barrier orders those global writes before the copies.
-  if (p.v_new != nullptr && t_begin <= T - 1 && T - 1 < t_end) {
+  if (!SYM && p.v_new != nullptr && t_begin <= T - 1 && T - 1 < t_end) {
     if (warp == 0) {
       const int t_new = T - 1;
       const int64_t row = (int64_t)b * p.H + h;  // [B][1][H][d]
@@ -432,6 +447,12 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : 1) decod
       xq[0] = a.x; xq[1] = a.y; xq[2] = c2.x; xq[3] = c2.y;
     }
     reinterpret_cast<float4*>(&q_s[i][0])[lane] = make_float4(xq[0], xq[1], xq[2], xq[3]);
+    if constexpr (SYM) {
+      float qs = (xq[0] + xq[1]) + (xq[2] + xq[3]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) qs += __shfl_xor_sync(0xffffffffu, qs, o);
+      if (lane == 0) qsum_s[i] = qs;
+    }
     float a = fmaxf(fmaxf(fabsf(xq[0]), fabsf(xq[1])), fmaxf(fabsf(xq[2]), fabsf(xq[3])));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
@@ -488,6 +509,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : 1) decod
 #pragma unroll
     for (int e = 0; e < 4; ++e) bacc[k][e] = 0.0f;
   const int qe_mine = qe_s[qi];
+  const float qmin_qsum = SYM ? qmin * qsum_s[qi] : 0.0f;  // SYM: q_min * sum_c q_c of query qi
 
   // QK A fragments of the current key group (or of the raw query for residual keys) in
   // shared memory, one padded row per (query, lane chunk): word 4ks + e is fragment
@@ -510,7 +532,18 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : 1) decod
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[hf][nt][e] = 0.0f;
     if (ts < Tq) {
-      if (i == 0 || (ts & (p.G - 1)) == 0) {
+      if (SYM && i == 0) {
+        // symmetric per-token keys: the raw query (binary16, exact) in natural channel pairs
+        __syncwarp();
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const float4 qv = reinterpret_cast<const float4*>(qrow)[ks];
+          reinterpret_cast<uint4*>(qa_row)[ks] = make_uint4(h2_bits(__floats2half2_rn(qv.x, qv.y)), 0u,
+                                                            h2_bits(__floats2half2_rn(qv.z, qv.w)), 0u);
+        }
+        __syncwarp();
+      }
+      if (!SYM && (i == 0 || (ts & (p.G - 1)) == 0)) {
         resid_frags = false;
         // Folded query of this key group, x_c = q_c s_c, as binary16 hi/lo pairs computed
         // with packed half arithmetic: q2_s holds q_c 2^qe / k_scale, the scales are
@@ -662,6 +695,17 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : 1) decod
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int e = 0; e < 2; ++e) s[hf][2 * nt + e] = fmaf(acc[hf][nt][e] + acc[hf][nt][e + 2], sc, bi);
+    if constexpr (SYM) {  // score of token t = s_t * (2^24 acc + q_min sum_c q_c), log2 units
+      const __half2* ksc = reinterpret_cast<const __half2*>(st + St::KB + St::VB + St::VM);
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const float2 kk = __half22float2(ksc[8 * hf + 4 * nt + j]);  // tokens 16hf + 8nt + 2j, + 1
+          s[hf][2 * nt] = (kk.x * p.scale_log2) * fmaf(acc[hf][nt][0] + acc[hf][nt][2], kTwo24, qmin_qsum);
+          s[hf][2 * nt + 1] = (kk.y * p.scale_log2) * fmaf(acc[hf][nt][1] + acc[hf][nt][3], kTwo24, qmin_qsum);
+        }
+    }
     if (ts + kTok > t_end) {  // ragged last iteration
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf)
@@ -926,10 +970,10 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : 1) decod
   }
 }
 
-template <int BITS, int VBITS, int NT, int NVG, int NW>
+template <int BITS, int VBITS, int NT, int NVG, int NW, bool SYM = false>
 cudaError_t launch_cfg(const DecodeParams& p, cudaStream_t stream) {
-  constexpr int smem = Stage<BITS, VBITS, NVG, NW>::SMEM;
-  auto* kern = decode_mma_kernel<BITS, VBITS, NT, NVG, NW>;
+  constexpr int smem = Stage<BITS, VBITS, NVG, NW, SYM>::SMEM;
+  auto* kern = decode_mma_kernel<BITS, VBITS, NT, NVG, NW, SYM>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   if (p.cluster < 1 || p.cluster > 16 || (p.cluster & (p.cluster - 1)) || p.n_split != p.cluster * p.n_parts)
@@ -957,24 +1001,24 @@ cudaError_t launch_cfg(const DecodeParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <int BITS, int VBITS, int NT, int NVG>
+template <int BITS, int VBITS, int NT, int NVG, bool SYM = false>
 int occupancy_cfg() {
-  constexpr int smem = Stage<BITS, VBITS, NVG, 4>::SMEM;
-  if (cudaFuncSetAttribute(decode_mma_kernel<BITS, VBITS, NT, NVG, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  constexpr int smem = Stage<BITS, VBITS, NVG, 4, SYM>::SMEM;
+  if (cudaFuncSetAttribute(decode_mma_kernel<BITS, VBITS, NT, NVG, 4, SYM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            smem) != cudaSuccess)
     return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<BITS, VBITS, NT, NVG, 4>, 4 * 32, smem) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<BITS, VBITS, NT, NVG, 4, SYM>, 4 * 32, smem) !=
       cudaSuccess)
     return 0;
   return n;
 }
 
 // Clusters of `cs` CTAs that can be resident at once (0 if such a cluster cannot launch).
-template <int BITS, int VBITS, int NT, int NVG, int NW>
+template <int BITS, int VBITS, int NT, int NVG, int NW, bool SYM = false>
 int max_clusters_cfg(int cs) {
-  constexpr int smem = Stage<BITS, VBITS, NVG, NW>::SMEM;
-  auto* kern = decode_mma_kernel<BITS, VBITS, NT, NVG, NW>;
+  constexpr int smem = Stage<BITS, VBITS, NVG, NW, SYM>::SMEM;
+  auto* kern = decode_mma_kernel<BITS, VBITS, NT, NVG, NW, SYM>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
   if (cs > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};

@@ -51,6 +51,7 @@ struct AppendParams {
   int64_t k_codes_slice, v_codes_slice;
   FastDiv fd_H;     // division by H of value-row indices below 2^31
   int rows_32;      // n_new * H < 2^31: value-row indices fit the fast division
+  int sym;          // symmetric per-token int8 scheme (k_meta: one binary16 scale per token)
 };
 
 struct DequantParams {
@@ -65,6 +66,7 @@ struct DequantParams {
   int B, H, G, Gv, R_eff, n_vg;
   int64_t S_pad, rowK, rowV;
   int64_t k_codes_slice, v_codes_slice;
+  int sym;  // symmetric per-token int8 scheme (k_meta: one binary16 scale per token)
 };
 
 struct DecodeParams {
@@ -92,6 +94,7 @@ struct DecodeParams {
   int cluster;        // CTAs per cluster (splits merged through distributed shared memory)
   int warps;          // warps per CTA of the tensor-core kernel: 4, or 8 (cluster merges only)
   int n_parts;        // partials merged through the workspace: n_split / cluster
+  int sym;            // symmetric per-token int8 scheme (k_meta: one binary16 scale per token)
   int B, H, r, G, Gv, R_eff, n_vg;
   int log2G;          // G is a power of two
   int64_t S_pad, rowK, rowV;
@@ -126,8 +129,9 @@ cudaError_t launch_append(const AppendParams& p, int bits, int vbits, cudaStream
 cudaError_t launch_dequant(const DequantParams& p, int bits, int vbits, cudaStream_t stream);
 cudaError_t launch_decode_simt(const DecodeParams& p, int bits, cudaStream_t stream);  // equal widths only
 cudaError_t launch_decode_mma(const DecodeParams& p, int bits, int vbits, cudaStream_t stream);
-int occupancy_decode_mma(int bits, int vbits, int r, int n_vg);  // resident CTAs per SM (0 on error)
-int max_clusters_decode_mma(int bits, int vbits, int r, int n_vg, int cs, int nw);  // resident clusters of cs CTAs
+// sym: the symmetric per-token int8 scheme (bits == vbits == 8, n_vg == 1)
+int occupancy_decode_mma(int bits, int vbits, int r, int n_vg, int sym);  // resident CTAs per SM (0 on error)
+int max_clusters_decode_mma(int bits, int vbits, int r, int n_vg, int cs, int nw, int sym);  // resident clusters of cs CTAs
 int occupancy_decode_simt(int bits);
 
 }  // namespace kvq

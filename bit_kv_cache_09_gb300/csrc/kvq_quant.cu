@@ -131,9 +131,10 @@ __global__ void __launch_bounds__(256, 4) k_group_kernel(AppendParams p) {
 // 8r + l its channels [16l, 16l + 16). A value group of Gv channels spans Gv/16 lanes.
 // In the pair-row layout channel 16l + i sits at position 16(i % 8) + 2l + i / 8, so
 // 8-bit codes fill their 16-bit units within a lane, 4-bit units take two lanes and
-// 2-bit units four.
+// 2-bit units four. SYM: the symmetric per-token scheme (one group of d channels,
+// scale from max|x|, zero point 0).
 // ---------------------------------------------------------------------------
-template <int BITS>
+template <int BITS, bool SYM = false>
 __global__ void __launch_bounds__(256) v_token_kernel(AppendParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sl = lane & 7;
@@ -170,20 +171,31 @@ __global__ void __launch_bounds__(256) v_token_kernel(AppendParams p) {
       x[2 * k + 1] = f.y;
     }
   }
-  float mn = x[0], mx = x[0];
-#pragma unroll
-  for (int i = 1; i < 16; ++i) {
-    mn = fminf(mn, x[i]);
-    mx = fmaxf(mx, x[i]);
-  }
   const int lpg = p.Gv >> 4;  // lanes per value group: 2, 4 or 8
-  for (int off = 1; off < lpg; off <<= 1) {
-    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-  }
   __half s_h, z_h;
   float s, rs, zp;
-  group_params<BITS>(mn, mx, s_h, z_h, s, rs, zp);
+  if constexpr (SYM) {
+    float a = fabsf(x[0]);
+#pragma unroll
+    for (int i = 1; i < 16; ++i) a = fmaxf(a, fabsf(x[i]));
+#pragma unroll
+    for (int off = 1; off < 8; off <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+    sym_params8(a, s_h, s, rs);
+    z_h = __float2half_rn(0.0f);
+    zp = 0.0f;
+  } else {
+    float mn = x[0], mx = x[0];
+#pragma unroll
+    for (int i = 1; i < 16; ++i) {
+      mn = fminf(mn, x[i]);
+      mx = fmaxf(mx, x[i]);
+    }
+    for (int off = 1; off < lpg; off <<= 1) {
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    }
+    group_params<BITS>(mn, mx, s_h, z_h, s, rs, zp);
+  }
   if (valid && sl % lpg == 0) p.v_meta[(slice * p.S_pad + t) * p.n_vg + sl / lpg] = __halves2half2(s_h, z_h);
   const float zpu = __fsub_rn(zp, Q<BITS>::qmin);
   uint32_t u[16];
@@ -238,11 +250,64 @@ __global__ void __launch_bounds__(256) v_token_kernel(AppendParams p) {
     }
   }
   // Keys of tokens past the last full residual window go to the residual.
-  if (valid && t >= p.A1) {
+  if (!SYM && valid && t >= p.A1) {
     const uint4* ks = reinterpret_cast<const uint4*>(p.k_in + w * kHeadDim + 16 * sl);
     uint4* kd = reinterpret_cast<uint4*>(p.k_resid + (slice * p.R_eff + (t - p.A1)) * kHeadDim + 16 * sl);
     kd[0] = ks[0];
     kd[1] = ks[1];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Symmetric per-token keys ("KV Cache Quantization — 8-bit and 4-bit", § Symmetric vs
+// asymmetric; one scale per token, "Sub-8-Bit KV Cache Quantization Is Not a Free Lever
+// for an RDNA4 Agent Swarm", § The RDNA4 kernel angle): rows assigned as in
+// v_token_kernel (four per warp, lane 8r + l holds channels [16l, 16l + 16)); the 8-bit
+// codes go to the key row in channel order (16 bytes per lane), the binary16 scale to
+// k_meta[slice][t].
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_token_sym_kernel(AppendParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sl = lane & 7;
+  const int64_t nb = p.n_new * p.H;
+  const int64_t wb_raw = ((int64_t)blockIdx.x * 8 + warp) * 4 + (lane >> 3);
+  pdl_wait();
+  pdl_allow_dependents();
+  const bool valid = wb_raw < nb;
+  const int64_t wb = valid ? wb_raw : nb - 1;  // lanes past the end read a real row and store nothing
+  const int64_t tt = wb / p.H;
+  const int h = (int)(wb % p.H);
+  const int b = blockIdx.y;
+  const int64_t w = (int64_t)b * nb + wb;
+  const int64_t t = p.s_cur + tt;
+  const int64_t slice = (int64_t)b * p.H + h;
+  float x[16];
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(p.k_in + w * kHeadDim + 16 * sl);
+    const uint4 a = src[0], c = src[1];
+    const uint32_t wd[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wd[k]));
+      x[2 * k] = f.x;
+      x[2 * k + 1] = f.y;
+    }
+  }
+  float a = fabsf(x[0]);
+#pragma unroll
+  for (int i = 1; i < 16; ++i) a = fmaxf(a, fabsf(x[i]));
+#pragma unroll
+  for (int off = 1; off < 8; off <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+  __half s_h;
+  float s, rs;
+  sym_params8(a, s_h, s, rs);
+  uint32_t wv[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 16; ++i) wv[i >> 2] |= quant_code<8>(x[i], s, rs, 128.0f) << (8 * (i & 3));
+  if (valid) {
+    *reinterpret_cast<uint4*>(p.k_codes + slice * p.k_codes_slice + t * p.rowK + 16 * sl) =
+        make_uint4(wv[0], wv[1], wv[2], wv[3]);
+    if (sl == 0) reinterpret_cast<__half*>(p.k_meta)[slice * p.S_pad + t] = s_h;
   }
 }
 
@@ -259,7 +324,12 @@ __global__ void __launch_bounds__(256) dequant_kernel(DequantParams p, int64_t n
   const int64_t slice = w / p.T;  // b * H + h
   const int c0 = 4 * lane;
   float kx[4], vx[4];
-  if (t < p.Tq) {
+  if (p.sym) {  // symmetric per-token keys: x_hat = s_t * (u + q_min)
+    const uint8_t* row = p.k_codes + slice * p.k_codes_slice + t * p.rowK;
+    const float s = __half2float(reinterpret_cast<const __half*>(p.k_meta)[slice * p.S_pad + t]);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) kx[e] = __fmul_rn(s, (float)((int)row[c0 + e] - 128));
+  } else if (t < p.Tq) {
     const uint8_t* row = p.k_codes + slice * p.k_codes_slice + t * p.rowK;
     const __half2* meta = p.k_meta + (slice * (p.S_pad / p.G) + t / p.G) * kHeadDim;
 #pragma unroll
@@ -301,10 +371,11 @@ cudaError_t launch_keys(const AppendParams& p, cudaStream_t stream) {
   }
 }
 
-template <int VBITS>
+template <int VBITS, bool SYM = false>
 cudaError_t launch_values(const AppendParams& p, cudaStream_t stream) {
   const int64_t rows = p.n_new * p.H;  // per batch row
-  return launch_pdl(v_token_kernel<VBITS>, dim3((unsigned)((rows + 31) / 32), (unsigned)p.B), dim3(256), 0, stream, p);
+  return launch_pdl(v_token_kernel<VBITS, SYM>, dim3((unsigned)((rows + 31) / 32), (unsigned)p.B), dim3(256), 0, stream,
+                    p);
 }
 
 template <int BITS, int VBITS>
@@ -317,6 +388,15 @@ cudaError_t launch_dequant_bits(const DequantParams& p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_append(const AppendParams& p, int bits, int vbits, cudaStream_t stream) {
+  if (p.sym) {  // symmetric per-token int8: keys and values quantized per token
+    const int64_t rows = p.n_new * p.H;
+    cudaError_t e = launch_pdl(k_token_sym_kernel, dim3((unsigned)((rows + 31) / 32), (unsigned)p.B), dim3(256), 0,
+                               stream, p);
+    if (e != cudaSuccess) return e;
+    e = launch_values<8, true>(p, stream);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+  }
   cudaError_t e = bits == 8 ? launch_keys<8>(p, stream) : (bits == 4 ? launch_keys<4>(p, stream) : launch_keys<2>(p, stream));
   if (e != cudaSuccess) return e;
   e = vbits == 8 ? launch_values<8>(p, stream) : (vbits == 4 ? launch_values<4>(p, stream) : launch_values<2>(p, stream));

@@ -77,6 +77,18 @@ __device__ __forceinline__ void group_params(float xmin, float xmax, __half& s_h
   zp = __half2float(z_h);
 }
 
+// Symmetric scale ("KV Cache Quantization — 8-bit and 4-bit", § Symmetric vs asymmetric:
+// zero point 0, integer range centred on real zero) from the exact binary32 max|x| of
+// binary16 inputs: s_h = binary16 round up of max|x| / 127 (RN(1/127) = 0x3C010204; the
+// quotient is correctly rounded, see div_rn), scale 1 for an all-zero vector; s and
+// rs = RN(1/s) as binary32. The code is then quant_code<8>(x, s, rs, 128) (zero point 0).
+__device__ __forceinline__ void sym_params8(float amax, __half& s_h, float& s, float& rs) {
+  if (amax == 0.0f) s_h = __float2half_rn(1.0f);
+  else s_h = __float2half_ru(div_rn(amax, 127.0f, __int_as_float(0x3C010204)));
+  s = __half2float(s_h);
+  rs = __frcp_rn(s);
+}
+
 // Code u = clamp(rint(x/s) + zp, q_min, q_max) - q_min of x in a group with binary16
 // scale s (rs = RN(1/s)); zpu = zp - q_min (an integer-valued binary32, so the shift
 // by q_min is exact and the clamp bounds become [0, 2^b - 1]).

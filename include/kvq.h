@@ -32,6 +32,16 @@
  *   4-bit values is the mixed recipe of "KV Cache Quantization — 8-bit and 4-bit",
  *   § Why keys and values want different treatment).
  *
+ * Symmetric per-token int8 scheme (symmetric = 1)
+ *   The symmetric quantizer of "KV Cache Quantization — 8-bit and 4-bit", § Symmetric
+ *   vs asymmetric (zero point 0, integer range centred on real zero, x_hat = scale * q)
+ *   with one scale per token for keys and for values — the per-token int8 cache of
+ *   "Sub-8-Bit KV Cache Quantization Is Not a Free Lever for an RDNA4 Agent Swarm",
+ *   § The RDNA4 kernel angle: s32 = max|x| / 127 over the token's d channels; the stored
+ *   scale is binary16(s32) rounded toward +infinity (an all-zero token gets scale 1);
+ *   q = clamp(rint(x / scale), -128, 127), stored as u = q + 128. There is no residual
+ *   window: every token's keys are quantized when it is appended.
+ *
  * State after T tokens of one (layer, batch row, kv head)
  *   R_eff = residual_len, or k_group when residual_len == 0.
  *   Keys of tokens [0, Tq), Tq = floor(T / R_eff) * R_eff, are quantized; keys of
@@ -52,6 +62,9 @@
  *               16-bit units (32-bit word k of pair row p = unit k of token 2p in the
  *               low half, unit k of token 2p+1 in the high half).
  *     v_meta  : S_pad tokens x (d / v_group) groups x {scale, zero_point} binary16.
+ *   Symmetric scheme: k_codes and v_codes as above (b = 8); k_meta is S_pad binary16 key
+ *   scales (one per token); v_meta holds {scale, +0} per token (v_group == d); there is
+ *   no k_resid (its size is 0 and its pointer may be NULL).
  *   Every buffer must be 256-byte aligned (torch and cudaMalloc allocations are) and
  *   zero-filled before the first append.
  *
@@ -87,7 +100,9 @@ typedef enum {
  * v_bits == 0 (same as bits) or v_bits == bits, or bits == 8 with v_bits == 4;
  * k_group and v_group in {32, 64, 128}; residual_len == 0 or a multiple of k_group
  * up to 1024; 1 <= gqa_ratio <= 8; n_kv_heads <= 255; batch <= 4095;
- * 1 <= max_seq_len <= 2^24. */
+ * 1 <= max_seq_len <= 2^24. symmetric == 1 needs bits == 8, v_bits in {0, 8},
+ * v_group == d_head and residual_len == 0 (k_group is then unused but must still be
+ * one of the values above). */
 typedef struct {
   int32_t n_layers;     /* L */
   int32_t batch;        /* B: sequences; all share one length */
@@ -100,6 +115,7 @@ typedef struct {
   int32_t v_group;      /* Gv: channels per value group (values are quantized per token) */
   int32_t residual_len; /* R: binary16 key residual capacity; 0 means k_group */
   int32_t v_bits;       /* value code width; 0 means bits */
+  int32_t symmetric;    /* 0: asymmetric (above); 1: symmetric per-token int8 keys and values */
 } kvq_config;
 
 /* Device pointers to the five cache buffers of all layers (layout above). */
@@ -157,7 +173,8 @@ kvq_status kvq_decode_attention(const kvq_config* cfg, const kvq_buffers* bufs, 
  * two launches otherwise. k_f16, v_f16: [batch][1][n_kv_heads][d_head] binary16
  * (16-byte aligned). Same cache state and outputs as the two calls ("KV Cache
  * Quantization — 8-bit and 4-bit", § Decode is memory-bound, so smaller is also
- * faster: one pass over the cache per step). */
+ * faster: one pass over the cache per step). The symmetric scheme always takes the two
+ * launches. */
 kvq_status kvq_decode_step(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur,
                            const void* k_f16, const void* v_f16, const void* q_f16, float softmax_scale, float* out,
                            void* ws, size_t ws_bytes, void* stream);
@@ -165,7 +182,7 @@ kvq_status kvq_decode_step(const kvq_config* cfg, const kvq_buffers* bufs, int32
 /* Kernel choice for kvq_decode_attention_impl. AUTO is what kvq_decode_attention uses. */
 typedef enum {
   KVQ_DECODE_AUTO = 0,
-  KVQ_DECODE_SIMT = 1, /* binary32 CUDA-core dot products */
+  KVQ_DECODE_SIMT = 1, /* binary32 CUDA-core dot products (asymmetric, equal code widths only) */
   KVQ_DECODE_MMA = 2   /* tensor-core m16n8k16 products over exact integer codes */
 } kvq_decode_impl;
 

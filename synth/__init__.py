@@ -162,6 +162,7 @@ class Workload:
     seed: int
     shift: float = 5.0
     v_bits: int = 0  # value code width; 0 => bits
+    symmetric: int = 0  # 1: symmetric per-token int8 keys and values (zero point 0, no residual)
     notes: str = field(default="", compare=False)
 
     @property
@@ -174,6 +175,8 @@ class Workload:
 
     @property
     def r_eff(self) -> int:
+        if self.symmetric:
+            return 1
         return self.residual if self.residual > 0 else self.k_group
 
     @property
@@ -204,6 +207,10 @@ WORKLOADS: dict[str, Workload] = {
                  notes="long-context int4 sweep, GQA 8, 65536 x batch 2"),
         Workload("kivi-k8v4", 32, 8, 4, 128, 16, 8192, 32, 8, 128, 64, 128, 4, 20, 20265, v_bits=4,
                  notes="mixed widths: int8 keys, int4 values; otherwise the KIVI-style int4 shape"),
+        Workload("llama8b-sym8", 32, 8, 4, 128, 1, 4096, 64, 8, 128, 128, 0, 4, 20, 20266, symmetric=1,
+                 notes="symmetric per-token int8 keys and values; otherwise the Llama-style 8B shape"),
+        Workload("sym8-b16", 32, 8, 4, 128, 16, 8192, 32, 8, 128, 128, 0, 4, 20, 20267, symmetric=1,
+                 notes="symmetric per-token int8 keys and values, batch 16, 8192-token prompt"),
     ]
 }
 

@@ -19,13 +19,15 @@ ATOL = 2e-3  # decode attention: max-abs error against the oracle's attention ov
 
 def cfg_dims(cache):
     c = cache.cfg
-    R_eff = c.residual_len if c.residual_len > 0 else c.k_group
+    sym = int(c.symmetric)
+    R_eff = 1 if sym else (c.residual_len if c.residual_len > 0 else c.k_group)
     S_pad = (c.max_seq_len + 127) // 128 * 128
     row = c.d_head * c.bits // 8
     vbits = c.v_bits or c.bits
     return dict(L=c.n_layers, B=c.batch, H=c.n_kv_heads, r=c.gqa_ratio, d=c.d_head, bits=c.bits, vbits=vbits,
                 rowV=c.d_head * vbits // 8, G=c.k_group,
-                Gv=c.v_group, R=c.residual_len, R_eff=R_eff, S_pad=S_pad, row=row, n_vg=c.d_head // c.v_group)
+                Gv=c.v_group, R=c.residual_len, R_eff=R_eff, S_pad=S_pad, row=row, n_vg=c.d_head // c.v_group,
+                sym=sym)
 
 
 def gpu_slice_state(cache, layer: int, b: int, h: int, T: int):
@@ -41,9 +43,13 @@ def gpu_slice_state(cache, layer: int, b: int, h: int, T: int):
         return buf[sl * slice_bytes: sl * slice_bytes + nbytes].cpu().numpy()
 
     kc = part("k_codes", g["S_pad"] * g["row"], Tq * g["row"]).reshape(Tq, g["row"])
-    km = part("k_meta", (g["S_pad"] // g["G"]) * g["d"] * 4, (Tq // g["G"]) * g["d"] * 4).view(np.uint16)
-    km = km.reshape(Tq // g["G"], g["d"], 2)
-    kr = part("k_resid", g["R_eff"] * g["d"] * 2, (T - Tq) * g["d"] * 2).view(np.uint16).reshape(T - Tq, g["d"])
+    if g["sym"]:  # one binary16 key scale per token, no residual window
+        km = part("k_meta", g["S_pad"] * 2, Tq * 2).view(np.uint16).reshape(Tq)
+        kr = np.zeros((0, g["d"]), np.uint16)
+    else:
+        km = part("k_meta", (g["S_pad"] // g["G"]) * g["d"] * 4, (Tq // g["G"]) * g["d"] * 4).view(np.uint16)
+        km = km.reshape(Tq // g["G"], g["d"], 2)
+        kr = part("k_resid", g["R_eff"] * g["d"] * 2, (T - Tq) * g["d"] * 2).view(np.uint16).reshape(T - Tq, g["d"])
     npairs = (T + 1) // 2
     vc = part("v_codes", g["S_pad"] * g["rowV"], npairs * 2 * g["rowV"]).reshape(npairs, 2 * g["rowV"])
     vm = part("v_meta", g["S_pad"] * g["n_vg"] * 4, T * g["n_vg"] * 4).view(np.uint16).reshape(T, g["n_vg"], 2)
@@ -52,6 +58,8 @@ def gpu_slice_state(cache, layer: int, b: int, h: int, T: int):
 
 def oracle_slice_state(k_hist, v_hist, cache):
     g = cfg_dims(cache)
+    if g["sym"]:
+        return oracle.cache_state_sym(k_hist, v_hist, d=g["d"])
     return oracle.cache_state(k_hist, v_hist, d=g["d"], bits=g["bits"], G=g["G"], Gv=g["Gv"], R=g["R"],
                               v_bits=g["vbits"])
 
@@ -66,6 +74,8 @@ def assert_slice_equal(gpu: dict, st: oracle.OracleState, where: str = ""):
             bad = np.argwhere(a != e)
             raise AssertionError(f"{where} {name}: {len(bad)} mismatches, first at {bad[:3].tolist()}")
     n_res = T - st.Tq
+    if n_res == 0 and gpu["k_resid"].size == 0:
+        return
     R_eff = st.k_resid.shape[0]
     # residual slot (t mod R_eff) of tokens [Tq, T); with Tq a multiple of R_eff that is t - Tq
     exp_res = st.k_resid[:n_res] if n_res <= R_eff else None
@@ -76,13 +86,18 @@ def assert_slice_equal(gpu: dict, st: oracle.OracleState, where: str = ""):
 
 def oracle_attention(st: oracle.OracleState, q_rows, cache, softmax_scale):
     g = cfg_dims(cache)
-    kh, vh = oracle.dequantize_state(st, d=g["d"], bits=g["bits"], G=g["G"], Gv=g["Gv"], R=g["R"], v_bits=g["vbits"])
+    if g["sym"]:
+        kh, vh = oracle.dequantize_state_sym(st, d=g["d"])
+    else:
+        kh, vh = oracle.dequantize_state(st, d=g["d"], bits=g["bits"], G=g["G"], Gv=g["Gv"], R=g["R"],
+                                         v_bits=g["vbits"])
     return oracle.attention(q_rows, kh, vh, softmax_scale)
 
 
 def small_workload(name="small", *, L=1, H=2, r=4, B=2, S=600, steps=8, bits=4, G=32, Gv=64, R=128, n_out=2,
-                   gain=20, seed=777, v_bits=0):
-    return synth.Workload(name, L, H, r, 128, B, S, steps, bits, G, Gv, R, n_out, gain, seed, v_bits=v_bits)
+                   gain=20, seed=777, v_bits=0, symmetric=0):
+    return synth.Workload(name, L, H, r, 128, B, S, steps, bits, G, Gv, R, n_out, gain, seed, v_bits=v_bits,
+                          symmetric=symmetric)
 
 
 def host_layer_inputs(w, layer, t0, nt):

@@ -47,6 +47,10 @@ def good_cfg(**kw):
     (dict(residual_len=100), 1), (dict(residual_len=2048), 2), (dict(gqa_ratio=9), 2), (dict(batch=0), 1),
     (dict(max_seq_len=0), 1), (dict(n_kv_heads=256), 2), (dict(v_bits=3), 2), (dict(bits=4, v_bits=8), 2),
     (dict(bits=4, v_bits=2), 2), (dict(bits=2, v_bits=4), 2),
+    # symmetric per-token int8: 8-bit codes, one value group, no residual window
+    (dict(symmetric=2), 1), (dict(symmetric=1, bits=4, v_group=128, residual_len=0), 2),
+    (dict(symmetric=1, bits=8, v_bits=4, v_group=128, residual_len=0), 2),
+    (dict(symmetric=1, bits=8, v_group=64, residual_len=0), 2), (dict(symmetric=1, bits=8, v_group=128), 1),
 ])
 def test_bad_configs_are_rejected(lib, kw, status):
     sizes = (ctypes.c_size_t * 5)()
@@ -79,6 +83,19 @@ def test_mixed_width_buffer_sizes(lib):
     assert mixed[0] == same[0] and mixed[1] == same[1] and mixed[2] == same[2] and mixed[4] == same[4]
     assert mixed[3] == oracle.kv_bytes(L, H * B, 128, S, 4) / 2
     assert kvq.kvq_buffer_sizes(good_cfg(bits=8, v_bits=8)) == kvq.kvq_buffer_sizes(good_cfg(bits=8))
+
+
+def test_symmetric_buffer_sizes(lib):
+    """Symmetric per-token int8: key and value rows of d bytes, one binary16 key scale and
+    one (scale, 0) value pair per token, no residual buffer."""
+    L, B, H, S = 3, 2, 4, 1000
+    S_pad = 1024
+    sizes = kvq.kvq_buffer_sizes(good_cfg(n_layers=L, batch=B, n_kv_heads=H, max_seq_len=S, bits=8, v_group=128,
+                                          residual_len=0, symmetric=1))
+    n = L * B * H
+    assert sizes == [n * S_pad * 128, n * S_pad * 2, 0, n * S_pad * 128, n * S_pad * 4]
+    # the bytes the pages count for an int8 cache, plus 6 metadata bytes per token and head
+    assert sizes[0] + sizes[3] == oracle.kv_bytes(L, H * B, 128, S_pad, 8)
 
 
 def _bufs(ptr=4096):
