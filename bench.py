@@ -81,6 +81,8 @@ def prefill_bytes_per_layer(w, S: int) -> int:
 def step_launches(w, s_cur: int, fused: bool = True) -> int:
     """Kernels one decode step launches: per layer one fused append+attention launch, or
     (separate calls, or a step that fills a residual window) append (+ key groups) and attention."""
+    if w.symmetric:  # no residual window: the fused step is always one launch; separately key + value + attention
+        return w.n_layers if fused else 3 * w.n_layers
     R = w.r_eff
     flush = ((s_cur + 1) // R) > (s_cur // R)
     if fused and not flush:

@@ -338,6 +338,8 @@ kvq_status decode_launch(const kvq_config* cfg, const kvq_buffers* bufs, int32_t
   p.k_resid_w = lp.k_resid;
   p.v_codes_w = lp.v_codes;
   p.v_meta_w = lp.v_meta;
+  p.k_codes_w = lp.k_codes;
+  p.k_meta_w = lp.k_meta;
   p.out = out;
   p.err = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + wl.err_off);
   p.tickets = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + wl.tickets_off);
@@ -364,7 +366,6 @@ kvq_status decode_launch(const kvq_config* cfg, const kvq_buffers* bufs, int32_t
   if (use == KVQ_DECODE_SIMT && (k_new || v_new)) return KVQ_ERR_UNSUPPORTED;
   if (use == KVQ_DECODE_SIMT && g.vbits != g.bits) return KVQ_ERR_UNSUPPORTED;  // CUDA-core kernel: equal widths
   if (use == KVQ_DECODE_SIMT && g.sym) return KVQ_ERR_UNSUPPORTED;              // and the asymmetric scheme
-  if (g.sym && (k_new || v_new)) return KVQ_ERR_UNSUPPORTED;                   // no fused append for it
   const Plan pl = plan_splits(g, s_cur, use);
   p.n_split = (int)pl.n_split;
   p.chunk = pl.chunk;
@@ -399,7 +400,7 @@ kvq_status kvq_decode_step(const kvq_config* cfg, const kvq_buffers* bufs, int32
   if (!aligned16(k_f16) || !aligned16(v_f16)) return KVQ_ERR_INVALID_ARG;
   if (s_cur + 1 > g.S_max) return KVQ_ERR_CAPACITY;
   const int64_t T = s_cur + 1;
-  if (g.sym || T % g.R_eff == 0) {  // symmetric scheme, or the append fills a residual window: two launches
+  if (!g.sym && T % g.R_eff == 0) {  // the append fills a residual window: quantize it with the append kernels
     st = kvq_quantize_append(cfg, bufs, layer, s_cur, 1, k_f16, v_f16, stream);
     if (st != KVQ_OK) return st;
     return decode_launch(cfg, bufs, layer, T, q_f16, softmax_scale, out, ws, ws_bytes, stream, KVQ_DECODE_AUTO,

@@ -417,15 +417,20 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : 1) decod
   // Fused decode step: the CTA whose range holds the new token T-1 appends it first
   // (value row quantized per group into its half of the pair row, key row into its
   // residual slot); the barrier orders those global writes before the copies.
-  if (!SYM && p.v_new != nullptr && t_begin <= T - 1 && T - 1 < t_end) {
+  if (p.v_new != nullptr && t_begin <= T - 1 && T - 1 < t_end) {
     if (warp == 0) {
       const int t_new = T - 1;
       const int64_t row = (int64_t)b * p.H + h;  // [B][1][H][d]
       uint16_t* pair = reinterpret_cast<uint16_t*>(p.v_codes_w + slice * p.v_codes_slice + (int64_t)(t_new >> 1) * 2 * ROWV);
-      quant::quantize_value_row<VBITS>(p.v_new + row * kHeadDim, pair, t_new & 1,
-                                      p.v_meta_w + (slice * p.S_pad + t_new) * NVG, p.Gv, lane, smem);
-      const uint2 kv = *reinterpret_cast<const uint2*>(p.k_new + row * kHeadDim + 4 * lane);
-      *reinterpret_cast<uint2*>(p.k_resid_w + (slice * p.R_eff + t_new % p.R_eff) * kHeadDim + 4 * lane) = kv;
+      quant::quantize_value_row<VBITS, SYM>(p.v_new + row * kHeadDim, pair, t_new & 1,
+                                           p.v_meta_w + (slice * p.S_pad + t_new) * NVG, p.Gv, lane, smem);
+      if constexpr (SYM) {  // the key row is quantized per token right away (no residual window)
+        quant::quantize_key_row_sym(p.k_new + row * kHeadDim, p.k_codes_w + slice * p.k_codes_slice + (int64_t)t_new * ROW,
+                                    reinterpret_cast<__half*>(p.k_meta_w) + slice * p.S_pad + t_new, lane);
+      } else {
+        const uint2 kv = *reinterpret_cast<const uint2*>(p.k_new + row * kHeadDim + 4 * lane);
+        *reinterpret_cast<uint2*>(p.k_resid_w + (slice * p.R_eff + t_new % p.R_eff) * kHeadDim + 4 * lane) = kv;
+      }
     }
     __syncthreads();
   }

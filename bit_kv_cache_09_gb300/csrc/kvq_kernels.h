@@ -83,6 +83,8 @@ struct DecodeParams {
   __half* k_resid_w;
   uint8_t* v_codes_w;
   __half2* v_meta_w;
+  uint8_t* k_codes_w;  // symmetric scheme: the new key row is quantized in place
+  __half2* k_meta_w;
   float* out;       // [B][H*r][d]
   uint32_t* err;      // error word: bit 0 = a wait for staged data timed out
   uint32_t* tickets;  // [B*H]

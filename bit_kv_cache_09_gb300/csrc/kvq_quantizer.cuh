@@ -119,21 +119,30 @@ __device__ __forceinline__ int v_channel_of_pos(int p) {
 // [4l, 4l+4)) per group of Gv channels, writes its (scale, zero point) pairs to
 // meta[0 .. d/Gv) and its codes, in stored-position order, into half `half_sel` of
 // the 16-bit units of its pair row. codes_s: 128 bytes of warp-private shared memory.
-template <int BITS>
+// SYM: the symmetric per-token scheme (BITS 8, one group of d channels, zero point 0).
+template <int BITS, bool SYM = false>
 __device__ __forceinline__ void quantize_value_row(const __half* v_row, uint16_t* pair_row, int half_sel, __half2* meta,
                                                    int Gv, int lane, uint8_t* codes_s) {
   float x[4];
   load4(v_row + 4 * lane, x);
-  float mn = fminf(fminf(x[0], x[1]), fminf(x[2], x[3]));
-  float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
   const int lanes_per_group = Gv / 4;  // 8, 16 or 32
-  for (int off = 1; off < lanes_per_group; off <<= 1) {
-    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-  }
   __half s_h, z_h;
   float s, rs, zp;
-  group_params<BITS>(mn, mx, s_h, z_h, s, rs, zp);
+  if constexpr (SYM) {
+    float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+    for (int off = 1; off < 32; off <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+    sym_params8(a, s_h, s, rs);
+    z_h = __float2half_rn(0.0f);
+    zp = 0.0f;
+  } else {
+    float mn = fminf(fminf(x[0], x[1]), fminf(x[2], x[3]));
+    float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+    for (int off = 1; off < lanes_per_group; off <<= 1) {
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    }
+    group_params<BITS>(mn, mx, s_h, z_h, s, rs, zp);
+  }
   if (lane % lanes_per_group == 0) meta[lane / lanes_per_group] = __halves2half2(s_h, z_h);
   const float zpu = __fsub_rn(zp, Q<BITS>::qmin);
 #pragma unroll
@@ -148,6 +157,25 @@ __device__ __forceinline__ void quantize_value_row(const __half* v_row, uint16_t
     pair_row[2 * k + half_sel] = (uint16_t)unit;
   }
   __syncwarp();
+}
+
+// One warp quantizes one key row of the symmetric per-token scheme (binary16, 128
+// channels; lane l holds channels [4l, 4l+4)): its binary16 scale to *scale_out and its
+// 8-bit codes, in channel order, to key_row.
+__device__ __forceinline__ void quantize_key_row_sym(const __half* k_row, uint8_t* key_row, __half* scale_out,
+                                                     int lane) {
+  float x[4];
+  load4(k_row + 4 * lane, x);
+  float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+  for (int off = 1; off < 32; off <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+  __half s_h;
+  float s, rs;
+  sym_params8(a, s_h, s, rs);
+  uint32_t w = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) w |= quant_code<8>(x[e], s, rs, 128.0f) << (8 * e);
+  reinterpret_cast<uint32_t*>(key_row)[lane] = w;
+  if (lane == 0) *scale_out = s_h;
 }
 
 }  // namespace quant

@@ -173,8 +173,8 @@ kvq_status kvq_decode_attention(const kvq_config* cfg, const kvq_buffers* bufs, 
  * two launches otherwise. k_f16, v_f16: [batch][1][n_kv_heads][d_head] binary16
  * (16-byte aligned). Same cache state and outputs as the two calls ("KV Cache
  * Quantization — 8-bit and 4-bit", § Decode is memory-bound, so smaller is also
- * faster: one pass over the cache per step). The symmetric scheme always takes the two
- * launches. */
+ * faster: one pass over the cache per step). In the symmetric scheme (no residual
+ * window) it is always one launch. */
 kvq_status kvq_decode_step(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur,
                            const void* k_f16, const void* v_f16, const void* q_f16, float softmax_scale, float* out,
                            void* ws, size_t ws_bytes, void* stream);
