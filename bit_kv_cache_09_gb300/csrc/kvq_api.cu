@@ -79,7 +79,7 @@ int decode_occupancy(const Geometry& g, kvq_decode_impl impl) {
 // kernel that can be resident at once on this device (<= 0: such a cluster cannot
 // launch); cached per device and kernel shape.
 int resident_clusters(const Geometry& g, int cs, int nw) {
-  static std::atomic<int> cache[16][5][2][3][5][2];  // device, code scheme/widths, r class, value groups, log2 size, warps
+  static std::atomic<int> cache[16][5][2][3][5][3];  // device, code scheme/widths, r class, value groups, log2 size, warps
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) dev = 0;
   const int bi = width_index(g);
@@ -87,7 +87,7 @@ int resident_clusters(const Geometry& g, int cs, int nw) {
   const int vi = g.n_vg == 1 ? 0 : (g.n_vg == 2 ? 1 : 2);
   int lg = 0;
   while ((1 << lg) < cs) ++lg;
-  std::atomic<int>& slot = cache[dev][bi][ri][vi][lg][nw == 8 ? 1 : 0];
+  std::atomic<int>& slot = cache[dev][bi][ri][vi][lg][nw == 8 ? 2 : (nw == 5 ? 1 : 0)];
   int n = slot.load(std::memory_order_relaxed);
   if (n == 0) {
     n = kvq::max_clusters_decode_mma(g.bits, g.vbits, g.r, g.n_vg, cs, nw, g.sym);
@@ -113,7 +113,7 @@ int decode_cluster_size(const Geometry& g, int64_t units, int nw) {
 // Small grids (at most 1/32 of the slots per pair): latency-bound, so each pair gets a
 // cluster of up to 16 CTAs, small enough that every warp's stages are all in flight at
 // once, merged through distributed shared memory without touching the workspace; CTAs
-// of 8 warps are used when that shortens the longest warp's run of iterations.
+// of 5 or 8 warps are used when that shortens the longest warp's run of iterations.
 struct Plan {
   int64_t n_split, chunk;
   int cluster, n_parts;
@@ -129,9 +129,9 @@ Plan plan_splits(const Geometry& g, int64_t T, kvq_decode_impl impl) {
   Plan pl;
   if (impl != KVQ_DECODE_SIMT && units * 32 <= slots) {
     int64_t best_run = -1;
-    for (int nw = 4; nw <= 8; nw += 4) {
+    for (int nw : {4, 5, 8}) {
       const int cs = decode_cluster_size(g, units, nw);
-      if (nw == 8 && cs < 2) continue;
+      if (nw != 4 && cs < 2) continue;
       int64_t c = (T + cs - 1) / cs;
       c = (c + align - 1) / align * align;
       const int64_t run = (c / 32 + nw - 1) / nw;  // iterations of the busiest warp

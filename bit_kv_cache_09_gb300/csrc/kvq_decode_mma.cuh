@@ -317,10 +317,11 @@ constexpr int min_blocks() {
 // BITS, VBITS: key and value code widths; NT: PV weight tiles per k-step (1: r <= 4, hi/lo
 // halves share one tile; 2: r <= 8, a hi and a lo tile accumulated into the same output
 // tile); NVG: value groups per token (d / Gv); NW: warps per
-// CTA (4; 8 for small cluster-merged grids, where one CTA per SM is resident anyway and
-// twice the warps halve the iterations on the critical path).
+// CTA (4; 5 or 8 for small cluster-merged grids, where few CTAs per SM are resident
+// anyway and more warps shorten the busiest warp's run of iterations; the 5-warp CTA
+// keeps two CTAs per SM).
 template <int BITS, int VBITS, int NT, int NVG, int NW, bool SYM = false>
-__global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : 1) decode_mma_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5 ? 2 : 1)) decode_mma_kernel(DecodeParams p) {
   constexpr int kWarps = NW;
   using St = Stage<BITS, VBITS, NVG, NW, SYM>;
   constexpr int NS = St::NS;
@@ -1056,6 +1057,7 @@ int max_clusters_nw(int r, int n_vg, int cs) {
 
 template <int BITS, int VBITS>
 int max_clusters_bits(int r, int n_vg, int cs, int nw) {
+  if (nw == 5) return max_clusters_nw<BITS, VBITS, 5>(r, n_vg, cs);
   return nw == 8 ? max_clusters_nw<BITS, VBITS, 8>(r, n_vg, cs) : max_clusters_nw<BITS, VBITS, 4>(r, n_vg, cs);
 }
 
@@ -1073,9 +1075,9 @@ cudaError_t launch_nw(const DecodeParams& p, cudaStream_t stream) {
 
 template <int BITS, int VBITS>
 cudaError_t launch_bits(const DecodeParams& p, cudaStream_t stream) {
-  if (p.warps == 8) {
-    if (p.n_parts != 1) return cudaErrorInvalidConfiguration;  // 8-warp CTAs merge in clusters only
-    return launch_nw<BITS, VBITS, 8>(p, stream);
+  if (p.warps == 8 || p.warps == 5) {
+    if (p.n_parts != 1) return cudaErrorInvalidConfiguration;  // 5- and 8-warp CTAs merge in clusters only
+    return p.warps == 8 ? launch_nw<BITS, VBITS, 8>(p, stream) : launch_nw<BITS, VBITS, 5>(p, stream);
   }
   return launch_nw<BITS, VBITS, 4>(p, stream);
 }
