@@ -31,6 +31,7 @@ from .oracle import (  # noqa: F401
     sym_params,
     sym_quantize,
     sym_dequantize_value,
+    split_outliers,
     cache_state_sym,
     dequantize_state_sym,
     attention,

@@ -37,12 +37,17 @@
 //                       or G when R = 0) and is quantized R_eff tokens at a time.
 //   symmetric scheme -> scale = max|x| / q_max rounded up to binary16, zero point 0,
 //                       one scale per token for keys and values, no residual window.
+//   outlier isolation-> per key row (symmetric scheme): the k channels farthest from the
+//                       row's lower median in |x - median| (binary32), ties to the lower
+//                       channel, kept as (channel, binary16 value) and zeroed in the
+//                       dense row that is then quantized.
 //
 // Parity pins: see tests/test_oracle_pins.py. The packed byte layout and the
 // residual/flush bookkeeping are this project's own definitions (the pages fix
 // neither): parity unpinned for the layout, which is checked only for
 // self-consistency (pack/unpack round trip, chunking invariance).
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -427,6 +432,35 @@ float orc_sym_dequantize_value(int u, int bits, uint16_t scale_h) {
   return orc_f32_from_f16(scale_h) * (float)(u + qmin_of(bits));
 }
 
+// Dense-and-sparse split of one vector of n binary16 values ("Sub-8-Bit KV Cache
+// Quantization Is Not a Free Lever for an RDNA4 Agent Swarm", § What the low-bit numbers
+// actually cost: per-vector dense-and-sparse quantization pulls the outliers out and
+// stores them separately; § The RDNA4 kernel angle: a sparse side channel read alongside
+// the dense one). The pages fix neither the rule nor k; here: the k entries farthest from
+// the vector's lower median (the ((n-1)/2)-th smallest value, counting from 0) in
+// binary32 |x - median|, taken in order of decreasing distance, ties to the lower index.
+// They go to idx_out/val_out (channel, binary16 value) and become +0 in dense_out.
+int orc_split_outliers(const uint16_t* x, int n, int k, uint16_t* idx_out, uint16_t* val_out, uint16_t* dense_out) {
+  if (n <= 0 || k < 0 || k > n) return -1;
+  std::vector<float> v((size_t)n), sorted((size_t)n), dist((size_t)n);
+  for (int c = 0; c < n; ++c) v[(size_t)c] = sorted[(size_t)c] = orc_f32_from_f16(x[c]);
+  std::sort(sorted.begin(), sorted.end());
+  const float med = sorted[(size_t)((n - 1) / 2)];
+  for (int c = 0; c < n; ++c) dist[(size_t)c] = std::fabs(v[(size_t)c] - med);
+  std::vector<char> taken((size_t)n, 0);
+  for (int c = 0; c < n; ++c) dense_out[c] = x[c];
+  for (int r = 0; r < k; ++r) {
+    int best = -1;
+    for (int c = 0; c < n; ++c)
+      if (!taken[(size_t)c] && (best < 0 || dist[(size_t)c] > dist[(size_t)best])) best = c;
+    taken[(size_t)best] = 1;
+    idx_out[r] = (uint16_t)best;
+    val_out[r] = x[best];
+    dense_out[best] = 0;  // binary16 +0
+  }
+  return 0;
+}
+
 // Symmetric per-token int8 cache of one (batch row, kv head) after T tokens ("Sub-8-Bit
 // KV Cache Quantization Is Not a Free Lever for an RDNA4 Agent Swarm", § The RDNA4
 // kernel angle: one scale per token; [A] § Symmetric vs asymmetric): keys and values
@@ -434,15 +468,28 @@ float orc_sym_dequantize_value(int u, int bits, uint16_t scale_h) {
 // is no residual window. Layout: k_codes [T][d] (key rows as above), k_scale [T]
 // binary16, v_codes pair rows as above, v_meta [T][1][2] = (scale, 0). Optional k_u,
 // v_u [T][d] receive the unpacked codes. Returns 0, or -1 on a bad argument.
-int orc_cache_state_sym(int d, int64_t T, const uint16_t* k_hist, const uint16_t* v_hist, uint8_t* k_codes,
-                        uint16_t* k_scale, uint8_t* v_codes, uint16_t* v_meta, uint8_t* k_u, uint8_t* v_u) {
-  if (d <= 0 || d % 16 || T < 0) return -1;
+// With k_out > 0 outliers per key row (see orc_split_outliers), the dense row is what
+// is quantized and k_sparse [T][k_out][2] receives the (channel, binary16 value) pairs.
+int orc_cache_state_sym(int d, int64_t T, int k_out, const uint16_t* k_hist, const uint16_t* v_hist, uint8_t* k_codes,
+                        uint16_t* k_scale, uint16_t* k_sparse, uint8_t* v_codes, uint16_t* v_meta, uint8_t* k_u,
+                        uint8_t* v_u) {
+  if (d <= 0 || d % 16 || T < 0 || k_out < 0 || k_out > d) return -1;
   const int bits = 8;
   std::vector<uint8_t> u((size_t)d);
+  std::vector<uint16_t> dense((size_t)d), idx((size_t)k_out + 1), val((size_t)k_out + 1);
   for (int64_t t = 0; t < T; ++t) {
     uint16_t s_h;
-    orc_sym_params(k_hist + t * d, d, 1, bits, &s_h);
-    orc_sym_quantize(k_hist + t * d, d, 1, bits, s_h, u.data());
+    const uint16_t* krow = k_hist + t * d;
+    if (k_out > 0) {
+      orc_split_outliers(krow, d, k_out, idx.data(), val.data(), dense.data());
+      for (int r = 0; r < k_out; ++r) {
+        k_sparse[(t * k_out + r) * 2 + 0] = idx[(size_t)r];
+        k_sparse[(t * k_out + r) * 2 + 1] = val[(size_t)r];
+      }
+      krow = dense.data();
+    }
+    orc_sym_params(krow, d, 1, bits, &s_h);
+    orc_sym_quantize(krow, d, 1, bits, s_h, u.data());
     k_scale[t] = s_h;
     orc_pack_k_row(u.data(), d, bits, k_codes + t * d);
     if (k_u) std::memcpy(k_u + t * d, u.data(), (size_t)d);
@@ -456,15 +503,20 @@ int orc_cache_state_sym(int d, int64_t T, const uint16_t* k_hist, const uint16_t
   return 0;
 }
 
-// Dequantized keys and values of a symmetric per-token state: k_out, v_out [T][d].
-int orc_dequantize_state_sym(int d, int64_t T, const uint8_t* k_codes, const uint16_t* k_scale,
-                             const uint8_t* v_codes, const uint16_t* v_meta, float* k_out, float* v_out) {
-  if (d <= 0 || d % 16 || T < 0) return -1;
+// Dequantized keys and values of a symmetric per-token state: k_out, v_out [T][d]. With
+// k_out_n > 0 outliers per key row the stored binary16 values replace the dense x_hat
+// (which is 0 there) at their channels.
+int orc_dequantize_state_sym(int d, int64_t T, int k_out_n, const uint8_t* k_codes, const uint16_t* k_scale,
+                             const uint16_t* k_sparse, const uint8_t* v_codes, const uint16_t* v_meta, float* k_out,
+                             float* v_out) {
+  if (d <= 0 || d % 16 || T < 0 || k_out_n < 0) return -1;
   const int bits = 8;
   std::vector<uint8_t> u((size_t)d);
   for (int64_t t = 0; t < T; ++t) {
     orc_unpack_k_row(k_codes + t * d, d, bits, u.data());
     for (int c = 0; c < d; ++c) k_out[t * d + c] = orc_sym_dequantize_value(u[(size_t)c], bits, k_scale[t]);
+    for (int r = 0; r < k_out_n; ++r)
+      k_out[t * d + k_sparse[(t * k_out_n + r) * 2]] += orc_f32_from_f16(k_sparse[(t * k_out_n + r) * 2 + 1]);
     orc_unpack_v_token(v_codes, d, bits, t, u.data());
     for (int c = 0; c < d; ++c) v_out[t * d + c] = orc_sym_dequantize_value(u[(size_t)c], bits, v_meta[t * 2]);
   }

@@ -86,11 +86,13 @@ def lib():
             L.orc_sym_quantize.restype = ctypes.c_int
             L.orc_sym_dequantize_value.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_uint16]
             L.orc_sym_dequantize_value.restype = ctypes.c_float
-            L.orc_cache_state_sym.argtypes = [ctypes.c_int, ctypes.c_int64, _u16p, _u16p, _u8p, _u16p, _u8p, _u16p,
-                                              _u8p, _u8p]
+            L.orc_split_outliers.argtypes = [_u16p, ctypes.c_int, ctypes.c_int, _u16p, _u16p, _u16p]
+            L.orc_split_outliers.restype = ctypes.c_int
+            L.orc_cache_state_sym.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int, _u16p, _u16p, _u8p, _u16p,
+                                              _u16p, _u8p, _u16p, _u8p, _u8p]
             L.orc_cache_state_sym.restype = ctypes.c_int
-            L.orc_dequantize_state_sym.argtypes = [ctypes.c_int, ctypes.c_int64, _u8p, _u16p, _u8p, _u16p, _f32p,
-                                                   _f32p]
+            L.orc_dequantize_state_sym.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int, _u8p, _u16p, _u16p,
+                                                   _u8p, _u16p, _f32p, _f32p]
             L.orc_dequantize_state_sym.restype = ctypes.c_int
             L.orc_attention.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int64, _u16p, _f32p, _f32p,
                                         ctypes.c_float, _f32p]
@@ -208,6 +210,7 @@ class OracleState:
     v_meta: np.ndarray  # [T][d/Gv][2] uint16
     k_u: np.ndarray  # [Tq][d] unpacked key codes
     v_u: np.ndarray  # [T][d] unpacked value codes
+    k_sparse: np.ndarray = None  # symmetric scheme with outliers: [T][k][2] (channel, binary16 value)
 
 
 def cache_state(k_hist, v_hist, *, d: int, bits: int, G: int, Gv: int, R: int, v_bits: int = 0) -> OracleState:
@@ -283,10 +286,22 @@ def sym_dequantize_value(u: int, bits: int, scale_h: int) -> float:
     return float(lib().orc_sym_dequantize_value(int(u), bits, scale_h))
 
 
-def cache_state_sym(k_hist, v_hist, *, d: int) -> OracleState:
+def split_outliers(x, k: int):
+    """(channels [k], binary16 values [k], dense row) of the dense-and-sparse split."""
+    x = _as_u16(x).ravel()
+    idx = np.zeros(max(k, 1), np.uint16)
+    val = np.zeros(max(k, 1), np.uint16)
+    dense = np.zeros(x.size, np.uint16)
+    if lib().orc_split_outliers(_ptr(x, _u16p), x.size, k, _ptr(idx, _u16p), _ptr(val, _u16p), _ptr(dense, _u16p)) != 0:
+        raise ValueError("bad arguments")
+    return idx[:k], val[:k], dense
+
+
+def cache_state_sym(k_hist, v_hist, *, d: int, k_outliers: int = 0) -> OracleState:
     """Symmetric per-token int8 cache of one (b, h) slice: keys and values each with one
     scale per token and zero point 0, no residual window. k_meta holds the per-token key
-    scales [T] (binary16 bits), v_meta [T][1][2] the value (scale, 0) pairs."""
+    scales [T] (binary16 bits), v_meta [T][1][2] the value (scale, 0) pairs; with
+    k_outliers > 0, k_sparse [T][k][2] the isolated key entries (channel, binary16)."""
     k = _as_u16(k_hist)
     v = _as_u16(v_hist)
     T = k.shape[0]
@@ -297,14 +312,17 @@ def cache_state_sym(k_hist, v_hist, *, d: int) -> OracleState:
     v_meta = np.zeros((T, 1, 2), np.uint16)
     k_u = np.zeros((T, d), np.uint8)
     v_u = np.zeros((T, d), np.uint8)
-    bufs = [np.zeros(1, a.dtype) if a.size == 0 else a for a in (k_codes, k_meta, v_codes, v_meta, k_u, v_u)]
+    k_sparse = np.zeros((T, k_outliers, 2), np.uint16)
+    bufs = [np.zeros(1, a.dtype) if a.size == 0 else a
+            for a in (k_codes, k_meta, v_codes, v_meta, k_u, v_u, k_sparse)]
     kk = k if k.size else np.zeros(1, np.uint16)
     vv = v if v.size else np.zeros(1, np.uint16)
-    rc = lib().orc_cache_state_sym(d, T, _ptr(kk, _u16p), _ptr(vv, _u16p), _ptr(bufs[0], _u8p), _ptr(bufs[1], _u16p),
-                                   _ptr(bufs[2], _u8p), _ptr(bufs[3], _u16p), _ptr(bufs[4], _u8p), _ptr(bufs[5], _u8p))
+    rc = lib().orc_cache_state_sym(d, T, k_outliers, _ptr(kk, _u16p), _ptr(vv, _u16p), _ptr(bufs[0], _u8p),
+                                   _ptr(bufs[1], _u16p), _ptr(bufs[6], _u16p), _ptr(bufs[2], _u8p),
+                                   _ptr(bufs[3], _u16p), _ptr(bufs[4], _u8p), _ptr(bufs[5], _u8p))
     if rc != 0:
         raise ValueError("bad cache shape")
-    return OracleState(T, T, k_codes, k_meta, np.zeros((0, d), np.uint16), v_codes, v_meta, k_u, v_u)
+    return OracleState(T, T, k_codes, k_meta, np.zeros((0, d), np.uint16), v_codes, v_meta, k_u, v_u, k_sparse)
 
 
 def dequantize_state_sym(st: OracleState, *, d: int):
@@ -316,9 +334,10 @@ def dequantize_state_sym(st: OracleState, *, d: int):
     def nz(a):
         return np.ascontiguousarray(a) if a.size else np.zeros(1, a.dtype)
 
-    rc = lib().orc_dequantize_state_sym(d, T, _ptr(nz(st.k_codes), _u8p), _ptr(nz(st.k_meta), _u16p),
-                                        _ptr(nz(st.v_codes), _u8p), _ptr(nz(st.v_meta), _u16p), _ptr(k_out, _f32p),
-                                        _ptr(v_out, _f32p))
+    ks = st.k_sparse if st.k_sparse is not None else np.zeros((T, 0, 2), np.uint16)
+    rc = lib().orc_dequantize_state_sym(d, T, ks.shape[1], _ptr(nz(st.k_codes), _u8p), _ptr(nz(st.k_meta), _u16p),
+                                        _ptr(nz(ks), _u16p), _ptr(nz(st.v_codes), _u8p), _ptr(nz(st.v_meta), _u16p),
+                                        _ptr(k_out, _f32p), _ptr(v_out, _f32p))
     if rc != 0:
         raise ValueError("bad cache shape")
     return k_out[:T], v_out[:T]

@@ -527,3 +527,62 @@ def test_symmetric_cache_is_per_token():
     for t in (0, 1, 36):
         assert np.array_equal(oracle.unpack_k_row(st.k_codes[t], d, 8), st.k_u[t])
         assert np.array_equal(oracle.unpack_v_token(st.v_codes.ravel(), d, 8, t), st.v_u[t])
+
+
+# ----------------------------------------------------------------------------- outlier isolation
+# "Sub-8-Bit KV Cache Quantization Is Not a Free Lever for an RDNA4 Agent Swarm", § What
+# the low-bit numbers actually cost (per-vector dense-and-sparse quantization) and § The
+# RDNA4 kernel angle (a sparse side channel). Reading: the k entries farthest from the
+# vector's lower median, in order of distance, ties to the lower index.
+
+def test_outlier_split_worked_example():
+    """x = [1, 2, 3, 4, 50, 5, 6, -40]: sorted, the lower median (index 3) is 3; the
+    distances are [2, 1, 0, 1, 47, 2, 3, 43], so the picks are 4 (50), 7 (-40), 6 (6),
+    then the tie at distance 2 goes to channel 0 before channel 5."""
+    x = np.array([1, 2, 3, 4, 50, 5, 6, -40], np.float16)
+    idx, val, dense = oracle.split_outliers(x, 4)
+    assert idx.tolist() == [4, 7, 6, 0]
+    assert val.view(np.float16).tolist() == [50.0, -40.0, 6.0, 1.0]
+    assert dense.view(np.float16).tolist() == [0, 2, 3, 4, 0, 5, 0, 0]
+    idx0, _, dense0 = oracle.split_outliers(x, 0)
+    assert idx0.size == 0 and np.array_equal(dense0, x.view(np.uint16))
+
+
+def test_outliers_shrink_the_dense_scale():
+    """A key row with three planted outliers: they are the three picks, their values come
+    back exactly, and the dense scale drops to max|rest| / 127 (rounded up), so every
+    other channel is within half of that smaller step."""
+    rng = np.random.default_rng(21)
+    x = rng.standard_normal(128).astype(np.float16)
+    planted = [5, 77, 120]
+    x[planted] = np.array([40.0, -35.0, 52.0], np.float16)
+    T = 1
+    st0 = oracle.cache_state_sym(x[None, :], x[None, :], d=128)
+    st = oracle.cache_state_sym(x[None, :], x[None, :], d=128, k_outliers=3)
+    assert sorted(st.k_sparse[0, :, 0].tolist()) == planted
+    rest = np.delete(x.astype(np.float32), planted)
+    assert st.k_meta[0] == oracle.f16_from_f32_ru(float(np.abs(rest).max() / np.float32(127)))
+    assert oracle.f32_from_f16(int(st.k_meta[0])) < oracle.f32_from_f16(int(st0.k_meta[0])) / 10
+    kh, _ = oracle.dequantize_state_sym(st, d=128)
+    assert np.array_equal(kh[0, planted], x[planted].astype(np.float32))
+    s = oracle.f32_from_f16(int(st.k_meta[0]))
+    others = np.setdiff1d(np.arange(128), planted)
+    assert np.all(np.abs(kh[0, others] - x[others].astype(np.float64)) <= s / 2 * (1 + 2.0 ** -20))
+    assert T == 1
+
+
+def test_outliers_cut_the_error_on_outlier_channels():
+    """Keys with planted outlier channels (the benchmark generator's a*z + 5 on 4
+    channels): isolating 4 entries per row lowers the worst error of the other channels
+    by more than 10x and leaves the isolated ones exact."""
+    import synth
+    w = synth.WORKLOADS["sym8-b16"]
+    T = 64
+    k = synth.k_slice(w, 0, 0, 0, range(T))
+    v = synth.v_slice(w, 0, 0, 0, range(T))
+    e0 = np.abs(oracle.dequantize_state_sym(oracle.cache_state_sym(k, v, d=128), d=128)[0] - k.astype(np.float64))
+    st = oracle.cache_state_sym(k, v, d=128, k_outliers=4)
+    e4 = np.abs(oracle.dequantize_state_sym(st, d=128)[0] - k.astype(np.float64))
+    assert e4.max() * 10 < e0.max()
+    for t in range(T):
+        assert np.all(e4[t, st.k_sparse[t, :, 0]] == 0)
