@@ -39,7 +39,7 @@ DEFAULT_WORKLOAD = "llama8b-int8"
 def key_meta_bytes(w, n_keys: int) -> int:
     """Key metadata of n_keys quantized tokens of one slice: (scale, zero point) per channel
     and group of k_group tokens, or one binary16 scale per token in the symmetric scheme."""
-    return n_keys * 2 if w.symmetric else (n_keys // w.k_group) * w.d_head * 4
+    return n_keys * (2 + 4 * w.k_outliers) if w.symmetric else (n_keys // w.k_group) * w.d_head * 4
 
 
 def attn_bytes_per_layer(w, T: int) -> int:
@@ -219,7 +219,7 @@ def oracle_prepare(w, layer: int, T: int, n_slices: int):
         k = synth.k_slice(w, layer, b, h, range(T))
         v = synth.v_slice(w, layer, b, h, range(T))
         if w.symmetric:
-            st = oracle.cache_state_sym(k, v, d=w.d_head)
+            st = oracle.cache_state_sym(k, v, d=w.d_head, k_outliers=w.k_outliers)
         else:
             st = oracle.cache_state(k, v, d=w.d_head, bits=w.bits, G=w.k_group, Gv=w.v_group, R=w.residual,
                                     v_bits=w.vbits)
@@ -512,12 +512,13 @@ def main():
     if rank == 0:
         line = {"metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
                 "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                "dtype": ("int8 symmetric per-token codes" if w.symmetric else
+                "dtype": ((f"int8 symmetric per-token codes + {w.k_outliers} binary16 key entries per token"
+                           if w.k_outliers else "int8 symmetric per-token codes") if w.symmetric else
                           f"int{w.bits} codes" if w.vbits == w.bits else f"int{w.bits} key / int{w.vbits} value codes")
                 + ", f32 math", "data": "synthetic",
                 "tokens_per_s": round(tok_s, 1), "pct_of_peak": round(100 * gbs / world / peak, 2),
                 "config": {"workload": w.name, "layers": L, "batch": w.batch, "n_kv_heads": w.n_kv, "gqa": w.gqa,
-                           "d_head": w.d_head, "prompt_tokens": S, "bits": w.bits, "v_bits": w.vbits, "symmetric": w.symmetric, "k_group": w.k_group,
+                           "d_head": w.d_head, "prompt_tokens": S, "bits": w.bits, "v_bits": w.vbits, "symmetric": w.symmetric, "k_outliers": w.k_outliers, "k_group": w.k_group,
                            "v_group": w.v_group, "residual": w.residual, "decode": args.decode,
                            "cuda_graph": use_graph, "parallelism": f"replicas x{world}",
                            "l2": "per-step working set (all layers' packed cache) exceeds the 129 MB L2; no flush"},

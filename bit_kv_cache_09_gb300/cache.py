@@ -15,10 +15,11 @@ from . import kvq
 
 class QuantizedKVCache:
     def __init__(self, *, n_layers, batch, n_kv_heads, gqa_ratio, d_head, max_seq_len, bits, k_group, v_group,
-                 residual_len, v_bits=0, symmetric=0, device="cuda"):
+                 residual_len, v_bits=0, symmetric=0, k_outliers=0, device="cuda"):
         self.cfg = kvq.make_config(n_layers=n_layers, batch=batch, n_kv_heads=n_kv_heads, gqa_ratio=gqa_ratio,
                                    d_head=d_head, max_seq_len=max_seq_len, bits=bits, k_group=k_group,
-                                   v_group=v_group, residual_len=residual_len, v_bits=v_bits, symmetric=symmetric)
+                                   v_group=v_group, residual_len=residual_len, v_bits=v_bits, symmetric=symmetric,
+                                   k_outliers=k_outliers)
         self.device = torch.device(device)
         sizes = kvq.kvq_buffer_sizes(self.cfg)
         # byte buffers, zero-filled as the ABI requires; torch allocations are 256-byte aligned
@@ -32,7 +33,8 @@ class QuantizedKVCache:
     def for_workload(cls, w, *, n_layers=None, device="cuda"):
         return cls(n_layers=n_layers or w.n_layers, batch=w.batch, n_kv_heads=w.n_kv, gqa_ratio=w.gqa,
                    d_head=w.d_head, max_seq_len=w.max_seq, bits=w.bits, k_group=w.k_group, v_group=w.v_group,
-                   residual_len=w.residual, v_bits=w.v_bits, symmetric=w.symmetric, device=device)
+                   residual_len=w.residual, v_bits=w.v_bits, symmetric=w.symmetric, k_outliers=w.k_outliers,
+                   device=device)
 
     @staticmethod
     def _stream() -> int:

@@ -53,13 +53,13 @@ int device_sm_count() {
 // Resident CTAs per SM of the decode kernel that `impl` selects (cached per device).
 // Index of the (key, value) code widths: 8/8, 4/4, 2/2, 8/4.
 int width_index(const Geometry& g) {
-  if (g.sym) return 4;  // symmetric per-token int8
+  if (g.sym) return g.kout > 0 ? 5 : 4;  // symmetric per-token int8 (with isolated key entries)
   if (g.vbits != g.bits) return 3;
   return g.bits == 8 ? 0 : (g.bits == 4 ? 1 : 2);
 }
 
 int decode_occupancy(const Geometry& g, kvq_decode_impl impl) {
-  static std::atomic<int> cache[16][2][5][2][3];  // device, impl, code scheme/widths, r class, value groups
+  static std::atomic<int> cache[16][2][6][2][3];  // device, impl, code scheme/widths, r class, value groups
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) dev = 0;
   const int ii = impl == KVQ_DECODE_SIMT ? 0 : 1;
@@ -69,7 +69,8 @@ int decode_occupancy(const Geometry& g, kvq_decode_impl impl) {
   std::atomic<int>& slot = cache[dev][ii][bi][ri][vi];
   int n = slot.load(std::memory_order_relaxed);
   if (n <= 0) {
-    n = ii == 0 ? kvq::occupancy_decode_simt(g.bits) : kvq::occupancy_decode_mma(g.bits, g.vbits, g.r, g.n_vg, g.sym);
+    n = ii == 0 ? kvq::occupancy_decode_simt(g.bits)
+                : kvq::occupancy_decode_mma(g.bits, g.vbits, g.r, g.n_vg, g.sym ? (g.kout > 0 ? 2 : 1) : 0);
     if (n > 0) slot.store(n, std::memory_order_relaxed);
   }
   return n > 0 ? n : 1;
@@ -79,7 +80,7 @@ int decode_occupancy(const Geometry& g, kvq_decode_impl impl) {
 // kernel that can be resident at once on this device (<= 0: such a cluster cannot
 // launch); cached per device and kernel shape.
 int resident_clusters(const Geometry& g, int cs, int nw) {
-  static std::atomic<int> cache[16][5][2][3][5][3];  // device, code scheme/widths, r class, value groups, log2 size, warps
+  static std::atomic<int> cache[16][6][2][3][5][3];  // device, code scheme/widths, r class, value groups, log2 size, warps
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) dev = 0;
   const int bi = width_index(g);
@@ -90,7 +91,7 @@ int resident_clusters(const Geometry& g, int cs, int nw) {
   std::atomic<int>& slot = cache[dev][bi][ri][vi][lg][nw == 8 ? 2 : (nw == 5 ? 1 : 0)];
   int n = slot.load(std::memory_order_relaxed);
   if (n == 0) {
-    n = kvq::max_clusters_decode_mma(g.bits, g.vbits, g.r, g.n_vg, cs, nw, g.sym);
+    n = kvq::max_clusters_decode_mma(g.bits, g.vbits, g.r, g.n_vg, cs, nw, g.sym ? (g.kout > 0 ? 2 : 1) : 0);
     if (n <= 0) n = -1;
     slot.store(n, std::memory_order_relaxed);
   }
@@ -248,6 +249,8 @@ kvq_status kvq_quantize_append(const kvq_config* cfg, const kvq_buffers* bufs, i
   p.rowK = g.rowK;
   p.rowV = g.rowV;
   p.k_codes_slice = g.k_codes_slice;
+  p.k_meta_slice = g.k_meta_slice;
+  p.kout = g.kout;
   p.v_codes_slice = g.v_codes_slice;
   p.fd_H = kvq::make_fast_div((uint32_t)g.H);
   p.rows_32 = n_new * g.H < (int64_t(1) << 31);
@@ -286,6 +289,8 @@ kvq_status kvq_dequantize(const kvq_config* cfg, const kvq_buffers* bufs, int32_
   p.rowK = g.rowK;
   p.rowV = g.rowV;
   p.k_codes_slice = g.k_codes_slice;
+  p.k_meta_slice = g.k_meta_slice;
+  p.kout = g.kout;
   p.v_codes_slice = g.v_codes_slice;
   p.sym = g.sym;
   cudaError_t e = kvq::launch_dequant(p, g.bits, g.vbits, static_cast<cudaStream_t>(stream));
@@ -360,6 +365,8 @@ kvq_status decode_launch(const kvq_config* cfg, const kvq_buffers* bufs, int32_t
   p.rowK = g.rowK;
   p.rowV = g.rowV;
   p.k_codes_slice = g.k_codes_slice;
+  p.k_meta_slice = g.k_meta_slice;
+  p.kout = g.kout;
   p.v_codes_slice = g.v_codes_slice;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   const kvq_decode_impl use = impl == KVQ_DECODE_SIMT ? KVQ_DECODE_SIMT : KVQ_DECODE_MMA;

@@ -7,7 +7,8 @@
 //   k_resid slice: R_eff rows x d binary16
 //   v_codes slice: S_pad/2 pair rows of 2*rowV bytes (rowV = d*b/8)
 //   v_meta  slice: S_pad tokens x d/Gv x half2(scale, zero_point)
-// Symmetric per-token scheme: k_meta slice = S_pad binary16 key scales, no k_resid,
+// Symmetric per-token scheme: k_meta slice = S_pad binary16 key scales (then, with kout
+// isolated entries per token, S_pad x kout x {channel u16, value binary16}), no k_resid,
 // Gv = d (v_meta holds half2(scale, 0)), every key quantized on append (Tq = T).
 #pragma once
 
@@ -26,6 +27,7 @@ constexpr int kMaxResidual = 1024;
 struct Geometry {
   int L, B, H, r, d, S_max, bits, vbits, G, Gv, R, R_eff;  // bits: keys, vbits: values
   int sym;             // symmetric per-token int8 scheme
+  int kout;            // symmetric scheme: isolated key entries per token
   int64_t S_pad;
   int64_t rowK, rowV;  // bytes per token row of key / value codes
   int n_vg;            // value groups per token (d / Gv)
@@ -53,6 +55,8 @@ inline kvq_status make_geometry(const kvq_config* c, Geometry* g) {
   if (c->symmetric != 0 && c->symmetric != 1) return KVQ_ERR_INVALID_ARG;
   if (c->symmetric && (c->bits != 8 || vbits != 8 || c->v_group != c->d_head)) return KVQ_ERR_UNSUPPORTED;
   if (c->symmetric && c->residual_len != 0) return KVQ_ERR_INVALID_ARG;  // no residual window
+  if (c->k_outliers < 0 || c->k_outliers > 4) return KVQ_ERR_UNSUPPORTED;
+  if (c->k_outliers > 0 && !c->symmetric) return KVQ_ERR_UNSUPPORTED;  // isolation of per-token key rows only
   Geometry x;
   x.L = c->n_layers;
   x.B = c->batch;
@@ -66,13 +70,14 @@ inline kvq_status make_geometry(const kvq_config* c, Geometry* g) {
   x.Gv = c->v_group;
   x.R = c->residual_len;
   x.sym = c->symmetric;
+  x.kout = c->k_outliers;
   x.R_eff = x.sym ? 1 : (c->residual_len > 0 ? c->residual_len : c->k_group);  // symmetric: Tq = T
   x.S_pad = ((int64_t)c->max_seq_len + kSeqAlign - 1) / kSeqAlign * kSeqAlign;
   x.rowK = (int64_t)x.d * x.bits / 8;
   x.rowV = (int64_t)x.d * x.vbits / 8;
   x.n_vg = x.d / x.Gv;
   x.k_codes_slice = x.S_pad * x.rowK;
-  x.k_meta_slice = x.sym ? x.S_pad * 2 : (x.S_pad / x.G) * x.d * 4;
+  x.k_meta_slice = x.sym ? x.S_pad * 2 + x.S_pad * x.kout * 4 : (x.S_pad / x.G) * x.d * 4;
   x.k_resid_slice = x.sym ? 0 : (int64_t)x.R_eff * x.d * 2;
   x.v_codes_slice = x.S_pad * x.rowV;
   x.v_meta_slice = x.S_pad * x.n_vg * 4;

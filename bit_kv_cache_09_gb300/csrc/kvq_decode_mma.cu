@@ -14,8 +14,8 @@ int max_clusters_decode_mma_b8(int r, int n_vg, int cs, int nw, int vbits);
 int max_clusters_decode_mma_b4(int r, int n_vg, int cs, int nw, int vbits);
 int max_clusters_decode_mma_b2(int r, int n_vg, int cs, int nw, int vbits);
 cudaError_t launch_decode_mma_sym(const DecodeParams& p, cudaStream_t stream);
-int occupancy_decode_mma_sym(int r);
-int max_clusters_decode_mma_sym(int r, int cs, int nw);
+int occupancy_decode_mma_sym(int r, int outl);
+int max_clusters_decode_mma_sym(int r, int cs, int nw, int outl);
 
 cudaError_t launch_decode_mma(const DecodeParams& p, int bits, int vbits, cudaStream_t stream) {
   if (p.sym) return launch_decode_mma_sym(p, stream);
@@ -27,7 +27,7 @@ cudaError_t launch_decode_mma(const DecodeParams& p, int bits, int vbits, cudaSt
 }
 
 int occupancy_decode_mma(int bits, int vbits, int r, int n_vg, int sym) {
-  if (sym) return occupancy_decode_mma_sym(r);
+  if (sym) return occupancy_decode_mma_sym(r, sym > 1);
   switch (bits) {
     case 8: return occupancy_decode_mma_b8(r, n_vg, vbits);
     case 4: return occupancy_decode_mma_b4(r, n_vg, vbits);
@@ -36,7 +36,7 @@ int occupancy_decode_mma(int bits, int vbits, int r, int n_vg, int sym) {
 }
 
 int max_clusters_decode_mma(int bits, int vbits, int r, int n_vg, int cs, int nw, int sym) {
-  if (sym) return max_clusters_decode_mma_sym(r, cs, nw);
+  if (sym) return max_clusters_decode_mma_sym(r, cs, nw, sym > 1);
   switch (bits) {
     case 8: return max_clusters_decode_mma_b8(r, n_vg, cs, nw, vbits);
     case 4: return max_clusters_decode_mma_b4(r, n_vg, cs, nw, vbits);

@@ -196,12 +196,12 @@ __device__ __forceinline__ constexpr float v_scale(int i) {
 // NW warps per CTA each own a ring of NS stages. After the loop the rings are reused
 // for the merges: per-warp partials (o, m, l, beta), the CTA partial read by the
 // cluster merge (cm, cl, co), then the scratch of the workspace merge.
-template <int BITS, int VBITS, int NVG, int NW, bool SYM = false>
+template <int BITS, int VBITS, int NVG, int NW, bool SYM = false, bool OUTL = false>
 struct Stage {
   static constexpr int KB = 32 * BITS * 128 / 8;   // key codes of 32 tokens
   static constexpr int VB = 32 * VBITS * 128 / 8;  // value codes of 32 tokens
   static constexpr int VM = 32 * 4 * NVG;         // value meta of 32 tokens
-  static constexpr int KM = SYM ? 64 : 512;       // one key group's meta, or 32 key scales
+  static constexpr int KM = SYM ? (OUTL ? 64 + 512 : 64) : 512;  // one key group's meta, or 32 key scales (+ up to 4 entries each)
   static constexpr int BYTES = KB + VB + VM + KM;
   static constexpr int NS = BITS == 2 ? 3 : 2;
   static constexpr int WARP_BYTES = NS * BYTES;
@@ -320,10 +320,10 @@ constexpr int min_blocks() {
 // CTA (4; 5 or 8 for small cluster-merged grids, where few CTAs per SM are resident
 // anyway and more warps shorten the busiest warp's run of iterations; the 5-warp CTA
 // keeps two CTAs per SM).
-template <int BITS, int VBITS, int NT, int NVG, int NW, bool SYM = false>
+template <int BITS, int VBITS, int NT, int NVG, int NW, bool SYM = false, bool OUTL = false>
 __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5 ? 2 : 1)) decode_mma_kernel(DecodeParams p) {
   constexpr int kWarps = NW;
-  using St = Stage<BITS, VBITS, NVG, NW, SYM>;
+  using St = Stage<BITS, VBITS, NVG, NW, SYM, OUTL>;
   constexpr int NS = St::NS;
   constexpr int kTok = 32;  // tokens per iteration
   constexpr float qmin = -(float)(1 << (BITS - 1));     // keys
@@ -387,7 +387,10 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
   const uint8_t* vm_src = reinterpret_cast<const uint8_t*>(p.v_meta + (slice * p.S_pad + ts0) * NVG);
   const __half2* km_base = p.k_meta + slice * (p.S_pad >> p.log2G) * kHeadDim;
   // SYM: per-token key scales of the warp's first iteration (k_meta holds S_pad per slice)
-  const uint8_t* ksc_src = reinterpret_cast<const uint8_t*>(reinterpret_cast<const __half*>(p.k_meta) + slice * p.S_pad + ts0);
+  const uint8_t* ksc_src = reinterpret_cast<const uint8_t*>(p.k_meta) + slice * p.k_meta_slice + (int64_t)ts0 * 2;
+  // SYM with isolated key entries: p.kout entries (4 B each) per token after the S_pad scales
+  const uint8_t* kent_src = reinterpret_cast<const uint8_t*>(p.k_meta) + slice * p.k_meta_slice + p.S_pad * 2 +
+                            (int64_t)ts0 * p.kout * 4;
 
   // Copies of the warp's iteration i into stage sidx: every lane moves 16-byte pieces
   // (piece lane + 32c of each block) with cp.async and arrives on the stage barrier
@@ -408,7 +411,13 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
 #pragma unroll
     for (int c = 0; c < CKV; ++c) cp_async16(dst + St::KB + 512 * c, v_src + offv + 512 * c);
     if (16 * lane < St::VM) cp_async16(dst + St::KB + St::VB, vm_src + (size_t)i * St::VM + 16 * lane);
-    if constexpr (SYM) {
+    if constexpr (SYM && OUTL) {  // pieces 0..3: 32 key scales; then 32 tokens x kout entries (128 kout bytes)
+      for (int pc = lane; pc < 4 + 8 * p.kout; pc += 32) {
+        const uint32_t dpc = dst + St::KB + St::VB + St::VM + 16 * (pc - lane);  // dst includes 16 * lane
+        if (pc < 4) cp_async16(dpc, ksc_src + (size_t)i * 64 + 16 * pc);
+        else cp_async16(dpc, kent_src + (size_t)i * 128 * p.kout + 16 * (pc - 4));
+      }
+    } else if constexpr (SYM) {
       if (lane < 4) cp_async16(dst + St::KB + St::VB + St::VM, ksc_src + (size_t)i * 64 + 16 * lane);
     } else {
       if (newgrp) cp_async16(dst + St::KB + St::VB + St::VM, km_base + ((ts >> p.log2G) << 7) + 4 * lane);
@@ -426,8 +435,11 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
       quant::quantize_value_row<VBITS, SYM>(p.v_new + row * kHeadDim, pair, t_new & 1,
                                            p.v_meta_w + (slice * p.S_pad + t_new) * NVG, p.Gv, lane, smem);
       if constexpr (SYM) {  // the key row is quantized per token right away (no residual window)
+        uint8_t* kmb = reinterpret_cast<uint8_t*>(p.k_meta_w) + slice * p.k_meta_slice;
         quant::quantize_key_row_sym(p.k_new + row * kHeadDim, p.k_codes_w + slice * p.k_codes_slice + (int64_t)t_new * ROW,
-                                    reinterpret_cast<__half*>(p.k_meta_w) + slice * p.S_pad + t_new, lane);
+                                    reinterpret_cast<__half*>(kmb) + t_new,
+                                    reinterpret_cast<uint32_t*>(kmb + p.S_pad * 2) + (int64_t)t_new * p.kout, p.kout, lane,
+                                    reinterpret_cast<float*>(smem) + 64);
       } else {
         const uint2 kv = *reinterpret_cast<const uint2*>(p.k_new + row * kHeadDim + 4 * lane);
         *reinterpret_cast<uint2*>(p.k_resid_w + (slice * p.R_eff + t_new % p.R_eff) * kHeadDim + 4 * lane) = kv;
@@ -711,6 +723,22 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
           s[hf][2 * nt] = (kk.x * p.scale_log2) * fmaf(acc[hf][nt][0] + acc[hf][nt][2], kTwo24, qmin_qsum);
           s[hf][2 * nt + 1] = (kk.y * p.scale_log2) * fmaf(acc[hf][nt][1] + acc[hf][nt][3], kTwo24, qmin_qsum);
         }
+      if constexpr (OUTL) {  // the sparse side list: q_c * x_c of every isolated key entry
+        const uint32_t* ent = reinterpret_cast<const uint32_t*>(st + St::KB + St::VB + St::VM + 64);
+        const float* qr = &q_s[qi][0];
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int tl = 16 * hf + 8 * (k >> 1) + 2 * j + (k & 1);
+            float sp = 0.0f;
+            for (int r = 0; r < p.kout; ++r) {
+              const uint32_t en = ent[tl * p.kout + r];  // channel | binary16 value << 16
+              sp = fmaf(__half2float(__ushort_as_half((unsigned short)(en >> 16))), qr[en & (kHeadDim - 1)], sp);
+            }
+            s[hf][k] = fmaf(sp, p.scale_log2, s[hf][k]);
+          }
+      }
     }
     if (ts + kTok > t_end) {  // ragged last iteration
 #pragma unroll
@@ -976,10 +1004,10 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
   }
 }
 
-template <int BITS, int VBITS, int NT, int NVG, int NW, bool SYM = false>
+template <int BITS, int VBITS, int NT, int NVG, int NW, bool SYM = false, bool OUTL = false>
 cudaError_t launch_cfg(const DecodeParams& p, cudaStream_t stream) {
-  constexpr int smem = Stage<BITS, VBITS, NVG, NW, SYM>::SMEM;
-  auto* kern = decode_mma_kernel<BITS, VBITS, NT, NVG, NW, SYM>;
+  constexpr int smem = Stage<BITS, VBITS, NVG, NW, SYM, OUTL>::SMEM;
+  auto* kern = decode_mma_kernel<BITS, VBITS, NT, NVG, NW, SYM, OUTL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   if (p.cluster < 1 || p.cluster > 16 || (p.cluster & (p.cluster - 1)) || p.n_split != p.cluster * p.n_parts)
@@ -1007,24 +1035,25 @@ cudaError_t launch_cfg(const DecodeParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <int BITS, int VBITS, int NT, int NVG, bool SYM = false>
+template <int BITS, int VBITS, int NT, int NVG, bool SYM = false, bool OUTL = false>
 int occupancy_cfg() {
-  constexpr int smem = Stage<BITS, VBITS, NVG, 4, SYM>::SMEM;
-  if (cudaFuncSetAttribute(decode_mma_kernel<BITS, VBITS, NT, NVG, 4, SYM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           smem) != cudaSuccess)
+  constexpr int smem = Stage<BITS, VBITS, NVG, 4, SYM, OUTL>::SMEM;
+  if (cudaFuncSetAttribute(decode_mma_kernel<BITS, VBITS, NT, NVG, 4, SYM, OUTL>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<BITS, VBITS, NT, NVG, 4, SYM>, 4 * 32, smem) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<BITS, VBITS, NT, NVG, 4, SYM, OUTL>, 4 * 32,
+                                                    smem) !=
       cudaSuccess)
     return 0;
   return n;
 }
 
 // Clusters of `cs` CTAs that can be resident at once (0 if such a cluster cannot launch).
-template <int BITS, int VBITS, int NT, int NVG, int NW, bool SYM = false>
+template <int BITS, int VBITS, int NT, int NVG, int NW, bool SYM = false, bool OUTL = false>
 int max_clusters_cfg(int cs) {
-  constexpr int smem = Stage<BITS, VBITS, NVG, NW, SYM>::SMEM;
-  auto* kern = decode_mma_kernel<BITS, VBITS, NT, NVG, NW, SYM>;
+  constexpr int smem = Stage<BITS, VBITS, NVG, NW, SYM, OUTL>::SMEM;
+  auto* kern = decode_mma_kernel<BITS, VBITS, NT, NVG, NW, SYM, OUTL>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
   if (cs > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};

@@ -49,9 +49,11 @@ struct AppendParams {
   int B, H, G, Gv, R_eff, n_vg;
   int64_t S_pad, rowK, rowV;
   int64_t k_codes_slice, v_codes_slice;
+  int64_t k_meta_slice;  // bytes of k_meta per slice
   FastDiv fd_H;     // division by H of value-row indices below 2^31
   int rows_32;      // n_new * H < 2^31: value-row indices fit the fast division
   int sym;          // symmetric per-token int8 scheme (k_meta: one binary16 scale per token)
+  int kout;         // symmetric scheme: isolated key entries per token (after the S_pad scales)
 };
 
 struct DequantParams {
@@ -66,7 +68,9 @@ struct DequantParams {
   int B, H, G, Gv, R_eff, n_vg;
   int64_t S_pad, rowK, rowV;
   int64_t k_codes_slice, v_codes_slice;
+  int64_t k_meta_slice;  // bytes of k_meta per slice
   int sym;  // symmetric per-token int8 scheme (k_meta: one binary16 scale per token)
+  int kout;  // symmetric scheme: isolated key entries per token (after the S_pad scales)
 };
 
 struct DecodeParams {
@@ -97,10 +101,12 @@ struct DecodeParams {
   int warps;          // warps per CTA of the tensor-core kernel: 4, or 8 (cluster merges only)
   int n_parts;        // partials merged through the workspace: n_split / cluster
   int sym;            // symmetric per-token int8 scheme (k_meta: one binary16 scale per token)
+  int kout;           // symmetric scheme: isolated key entries per token (after the S_pad scales)
   int B, H, r, G, Gv, R_eff, n_vg;
   int log2G;          // G is a power of two
   int64_t S_pad, rowK, rowV;
   int64_t k_codes_slice, v_codes_slice;
+  int64_t k_meta_slice;  // bytes of k_meta per slice
   float scale_log2;   // softmax_scale * log2(e)
 };
 
@@ -131,7 +137,8 @@ cudaError_t launch_append(const AppendParams& p, int bits, int vbits, cudaStream
 cudaError_t launch_dequant(const DequantParams& p, int bits, int vbits, cudaStream_t stream);
 cudaError_t launch_decode_simt(const DecodeParams& p, int bits, cudaStream_t stream);  // equal widths only
 cudaError_t launch_decode_mma(const DecodeParams& p, int bits, int vbits, cudaStream_t stream);
-// sym: the symmetric per-token int8 scheme (bits == vbits == 8, n_vg == 1)
+// sym: 0 asymmetric; 1 the symmetric per-token int8 scheme (bits == vbits == 8, n_vg == 1);
+// 2 the symmetric scheme with isolated key entries
 int occupancy_decode_mma(int bits, int vbits, int r, int n_vg, int sym);  // resident CTAs per SM (0 on error)
 int max_clusters_decode_mma(int bits, int vbits, int r, int n_vg, int cs, int nw, int sym);  // resident clusters of cs CTAs
 int occupancy_decode_simt(int bits);

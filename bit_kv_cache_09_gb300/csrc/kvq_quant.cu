@@ -307,8 +307,32 @@ __global__ void __launch_bounds__(256) k_token_sym_kernel(AppendParams p) {
   if (valid) {
     *reinterpret_cast<uint4*>(p.k_codes + slice * p.k_codes_slice + t * p.rowK + 16 * sl) =
         make_uint4(wv[0], wv[1], wv[2], wv[3]);
-    if (sl == 0) reinterpret_cast<__half*>(p.k_meta)[slice * p.S_pad + t] = s_h;
+    if (sl == 0) reinterpret_cast<__half*>(reinterpret_cast<uint8_t*>(p.k_meta) + slice * p.k_meta_slice)[t] = s_h;
   }
+}
+
+// ---------------------------------------------------------------------------
+// Symmetric per-token keys with outlier isolation (kout > 0): one warp per row (the
+// median and the farthest entries need the whole row), see quant::quantize_key_row_sym.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_token_sym_outlier_kernel(AppendParams p) {
+  __shared__ float vals_s[8][kHeadDim];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t nb = p.n_new * p.H;
+  const int64_t wb = (int64_t)blockIdx.x * 8 + warp;
+  pdl_wait();
+  pdl_allow_dependents();
+  if (wb >= nb) return;  // whole warp
+  const int64_t tt = wb / p.H;
+  const int h = (int)(wb % p.H);
+  const int b = blockIdx.y;
+  const int64_t w = (int64_t)b * nb + wb;
+  const int64_t t = p.s_cur + tt;
+  const int64_t slice = (int64_t)b * p.H + h;
+  uint8_t* kmb = reinterpret_cast<uint8_t*>(p.k_meta) + slice * p.k_meta_slice;
+  quantize_key_row_sym(p.k_in + w * kHeadDim, p.k_codes + slice * p.k_codes_slice + t * p.rowK,
+                       reinterpret_cast<__half*>(kmb) + t, reinterpret_cast<uint32_t*>(kmb + p.S_pad * 2) + t * p.kout,
+                       p.kout, lane, vals_s[warp]);
 }
 
 // ---------------------------------------------------------------------------
@@ -326,9 +350,19 @@ __global__ void __launch_bounds__(256) dequant_kernel(DequantParams p, int64_t n
   float kx[4], vx[4];
   if (p.sym) {  // symmetric per-token keys: x_hat = s_t * (u + q_min)
     const uint8_t* row = p.k_codes + slice * p.k_codes_slice + t * p.rowK;
-    const float s = __half2float(reinterpret_cast<const __half*>(p.k_meta)[slice * p.S_pad + t]);
+    const uint8_t* kmb = reinterpret_cast<const uint8_t*>(p.k_meta) + slice * p.k_meta_slice;
+    const float s = __half2float(reinterpret_cast<const __half*>(kmb)[t]);
 #pragma unroll
     for (int e = 0; e < 4; ++e) kx[e] = __fmul_rn(s, (float)((int)row[c0 + e] - 128));
+    // isolated entries: the stored binary16 value (the dense x_hat there is 0)
+    const uint32_t* ent = reinterpret_cast<const uint32_t*>(kmb + p.S_pad * 2) + t * p.kout;
+    for (int r = 0; r < p.kout; ++r) {
+      const uint32_t en = ent[r];
+      const int c = (int)(en & 0xFFFFu);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (c == c0 + e) kx[e] = __fadd_rn(kx[e], __half2float(__ushort_as_half((unsigned short)(en >> 16))));
+    }
   } else if (t < p.Tq) {
     const uint8_t* row = p.k_codes + slice * p.k_codes_slice + t * p.rowK;
     const __half2* meta = p.k_meta + (slice * (p.S_pad / p.G) + t / p.G) * kHeadDim;
@@ -390,8 +424,10 @@ cudaError_t launch_dequant_bits(const DequantParams& p, cudaStream_t stream) {
 cudaError_t launch_append(const AppendParams& p, int bits, int vbits, cudaStream_t stream) {
   if (p.sym) {  // symmetric per-token int8: keys and values quantized per token
     const int64_t rows = p.n_new * p.H;
-    cudaError_t e = launch_pdl(k_token_sym_kernel, dim3((unsigned)((rows + 31) / 32), (unsigned)p.B), dim3(256), 0,
-                               stream, p);
+    cudaError_t e = p.kout > 0 ? launch_pdl(k_token_sym_outlier_kernel, dim3((unsigned)((rows + 7) / 8), (unsigned)p.B),
+                                            dim3(256), 0, stream, p)
+                               : launch_pdl(k_token_sym_kernel, dim3((unsigned)((rows + 31) / 32), (unsigned)p.B),
+                                            dim3(256), 0, stream, p);
     if (e != cudaSuccess) return e;
     e = launch_values<8, true>(p, stream);
     if (e != cudaSuccess) return e;

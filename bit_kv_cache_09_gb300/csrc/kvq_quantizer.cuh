@@ -161,11 +161,77 @@ __device__ __forceinline__ void quantize_value_row(const __half* v_row, uint16_t
 
 // One warp quantizes one key row of the symmetric per-token scheme (binary16, 128
 // channels; lane l holds channels [4l, 4l+4)): its binary16 scale to *scale_out and its
-// 8-bit codes, in channel order, to key_row.
+// 8-bit codes, in channel order, to key_row. With kout > 0 the row's kout entries
+// farthest from its lower median (binary32 |x - median|, in order of decreasing
+// distance, ties to the lower channel; "Sub-8-Bit KV Cache Quantization Is Not a Free
+// Lever for an RDNA4 Agent Swarm", § What the low-bit numbers actually cost: per-vector
+// dense-and-sparse quantization) go to entries[0 .. kout) as channel | binary16 << 16
+// and are replaced by 0 before the scale is taken. vals_s: 128 floats of warp-private
+// shared memory.
 __device__ __forceinline__ void quantize_key_row_sym(const __half* k_row, uint8_t* key_row, __half* scale_out,
-                                                     int lane) {
+                                                     uint32_t* entries, int kout, int lane, float* vals_s) {
   float x[4];
   load4(k_row + 4 * lane, x);
+  if (kout > 0) {
+    const uint2 raw = *reinterpret_cast<const uint2*>(k_row + 4 * lane);
+    const uint32_t xb[4] = {raw.x & 0xFFFFu, raw.x >> 16, raw.y & 0xFFFFu, raw.y >> 16};
+    // lower median = sorted[63]: the value with at most 63 of the 128 values below it and
+    // more than 63 at or below it
+#pragma unroll
+    for (int e = 0; e < 4; ++e) vals_s[4 * lane + e] = x[e];
+    __syncwarp();
+    int lt[4] = {0, 0, 0, 0}, le[4] = {0, 0, 0, 0};
+    for (int i = 0; i < 128; ++i) {
+      const float y = vals_s[i];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        lt[e] += y < x[e];
+        le[e] += y <= x[e];
+      }
+    }
+    bool mine = false;
+    float medv = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (lt[e] <= 63 && 63 < le[e]) {
+        mine = true;
+        medv = x[e];
+      }
+    const float med = __shfl_sync(0xffffffffu, medv, __ffs(__ballot_sync(0xffffffffu, mine)) - 1);
+    float dist[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) dist[e] = fabsf(__fsub_rn(x[e], med));
+    bool taken[4] = {false, false, false, false};
+    for (int r = 0; r < kout; ++r) {
+      float bd = -1.0f;
+      int bc = 1 << 30;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (!taken[e] && dist[e] > bd) {
+          bd = dist[e];
+          bc = 4 * lane + e;
+        }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {  // farthest, ties to the lower channel
+        const float od = __shfl_xor_sync(0xffffffffu, bd, off);
+        const int oc = __shfl_xor_sync(0xffffffffu, bc, off);
+        if (od > bd || (od == bd && oc < bc)) {
+          bd = od;
+          bc = oc;
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (bc == 4 * lane + e) {
+          taken[e] = true;
+          entries[r] = (uint32_t)bc | (xb[e] << 16);
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (taken[e]) x[e] = 0.0f;
+    __syncwarp();  // vals_s may be reused by the caller
+  }
   float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
   for (int off = 1; off < 32; off <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
   __half s_h;

@@ -35,7 +35,7 @@ class KVQError(RuntimeError):
 class kvq_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("n_layers", "batch", "n_kv_heads", "gqa_ratio", "d_head",
                                                "max_seq_len", "bits", "k_group", "v_group", "residual_len",
-                                               "v_bits", "symmetric")]
+                                               "v_bits", "symmetric", "k_outliers")]
 
 
 class kvq_buffers(ctypes.Structure):
@@ -92,9 +92,9 @@ def _check(fn: str, status: int) -> None:
 
 
 def make_config(*, n_layers, batch, n_kv_heads, gqa_ratio, d_head, max_seq_len, bits, k_group, v_group,
-                residual_len, v_bits=0, symmetric=0) -> kvq_config:
+                residual_len, v_bits=0, symmetric=0, k_outliers=0) -> kvq_config:
     return kvq_config(n_layers, batch, n_kv_heads, gqa_ratio, d_head, max_seq_len, bits, k_group, v_group,
-                      residual_len, v_bits, int(symmetric))
+                      residual_len, v_bits, int(symmetric), int(k_outliers))
 
 
 def make_buffers(ptrs) -> kvq_buffers:

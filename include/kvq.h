@@ -41,6 +41,12 @@
  *   scale is binary16(s32) rounded toward +infinity (an all-zero token gets scale 1);
  *   q = clamp(rint(x / scale), -128, 127), stored as u = q + 128. There is no residual
  *   window: every token's keys are quantized when it is appended.
+ *   Outlier isolation (k_outliers = k > 0; dense-and-sparse quantization, "Sub-8-Bit …",
+ *   § What the low-bit numbers actually cost and § The RDNA4 kernel angle): before a key
+ *   row is quantized, its k entries farthest from the row's lower median (the 64th
+ *   smallest of the d = 128 values) in binary32 |x - median|, in order of decreasing
+ *   distance with ties to the lower channel, are stored as (channel, binary16 value)
+ *   and replaced by 0; k_hat is the dense x_hat plus those values at their channels.
  *
  * State after T tokens of one (layer, batch row, kv head)
  *   R_eff = residual_len, or k_group when residual_len == 0.
@@ -63,8 +69,9 @@
  *               low half, unit k of token 2p+1 in the high half).
  *     v_meta  : S_pad tokens x (d / v_group) groups x {scale, zero_point} binary16.
  *   Symmetric scheme: k_codes and v_codes as above (b = 8); k_meta is S_pad binary16 key
- *   scales (one per token); v_meta holds {scale, +0} per token (v_group == d); there is
- *   no k_resid (its size is 0 and its pointer may be NULL).
+ *   scales (one per token), followed when k_outliers = k > 0 by S_pad x k entries
+ *   {channel (uint16), value (binary16)}; v_meta holds {scale, +0} per token
+ *   (v_group == d); there is no k_resid (its size is 0 and its pointer may be NULL).
  *   Every buffer must be 256-byte aligned (torch and cudaMalloc allocations are) and
  *   zero-filled before the first append.
  *
@@ -102,7 +109,7 @@ typedef enum {
  * up to 1024; 1 <= gqa_ratio <= 8; n_kv_heads <= 255; batch <= 4095;
  * 1 <= max_seq_len <= 2^24. symmetric == 1 needs bits == 8, v_bits in {0, 8},
  * v_group == d_head and residual_len == 0 (k_group is then unused but must still be
- * one of the values above). */
+ * one of the values above); k_outliers in 0..4, and > 0 only with symmetric == 1. */
 typedef struct {
   int32_t n_layers;     /* L */
   int32_t batch;        /* B: sequences; all share one length */
@@ -116,6 +123,7 @@ typedef struct {
   int32_t residual_len; /* R: binary16 key residual capacity; 0 means k_group */
   int32_t v_bits;       /* value code width; 0 means bits */
   int32_t symmetric;    /* 0: asymmetric (above); 1: symmetric per-token int8 keys and values */
+  int32_t k_outliers;   /* symmetric scheme: key entries per token kept in a sparse side list (0..4) */
 } kvq_config;
 
 /* Device pointers to the five cache buffers of all layers (layout above). */

@@ -163,6 +163,7 @@ class Workload:
     shift: float = 5.0
     v_bits: int = 0  # value code width; 0 => bits
     symmetric: int = 0  # 1: symmetric per-token int8 keys and values (zero point 0, no residual)
+    k_outliers: int = 0  # symmetric scheme: key entries per token isolated in a sparse side list
     notes: str = field(default="", compare=False)
 
     @property
@@ -211,6 +212,8 @@ WORKLOADS: dict[str, Workload] = {
                  notes="symmetric per-token int8 keys and values; otherwise the Llama-style 8B shape"),
         Workload("sym8-b16", 32, 8, 4, 128, 16, 8192, 32, 8, 128, 128, 0, 4, 20, 20267, symmetric=1,
                  notes="symmetric per-token int8 keys and values, batch 16, 8192-token prompt"),
+        Workload("sym8o4-b16", 32, 8, 4, 128, 16, 8192, 32, 8, 128, 128, 0, 4, 20, 20268, symmetric=1, k_outliers=4,
+                 notes="sym8-b16 with 4 key entries per token isolated in a sparse side list"),
     ]
 }
 

@@ -27,7 +27,7 @@ def cfg_dims(cache):
     return dict(L=c.n_layers, B=c.batch, H=c.n_kv_heads, r=c.gqa_ratio, d=c.d_head, bits=c.bits, vbits=vbits,
                 rowV=c.d_head * vbits // 8, G=c.k_group,
                 Gv=c.v_group, R=c.residual_len, R_eff=R_eff, S_pad=S_pad, row=row, n_vg=c.d_head // c.v_group,
-                sym=sym)
+                sym=sym, kout=int(c.k_outliers))
 
 
 def gpu_slice_state(cache, layer: int, b: int, h: int, T: int):
@@ -43,8 +43,14 @@ def gpu_slice_state(cache, layer: int, b: int, h: int, T: int):
         return buf[sl * slice_bytes: sl * slice_bytes + nbytes].cpu().numpy()
 
     kc = part("k_codes", g["S_pad"] * g["row"], Tq * g["row"]).reshape(Tq, g["row"])
-    if g["sym"]:  # one binary16 key scale per token, no residual window
-        km = part("k_meta", g["S_pad"] * 2, Tq * 2).view(np.uint16).reshape(Tq)
+    ksp = None
+    if g["sym"]:  # one binary16 key scale per token (then the isolated entries), no residual window
+        km_slice = g["S_pad"] * 2 + g["S_pad"] * g["kout"] * 4
+        km = part("k_meta", km_slice, Tq * 2).view(np.uint16).reshape(Tq)
+        if g["kout"]:
+            buf = cache.buffer("k_meta")
+            off = sl * km_slice + g["S_pad"] * 2
+            ksp = buf[off: off + Tq * g["kout"] * 4].cpu().numpy().view(np.uint16).reshape(Tq, g["kout"], 2)
         kr = np.zeros((0, g["d"]), np.uint16)
     else:
         km = part("k_meta", (g["S_pad"] // g["G"]) * g["d"] * 4, (Tq // g["G"]) * g["d"] * 4).view(np.uint16)
@@ -53,13 +59,13 @@ def gpu_slice_state(cache, layer: int, b: int, h: int, T: int):
     npairs = (T + 1) // 2
     vc = part("v_codes", g["S_pad"] * g["rowV"], npairs * 2 * g["rowV"]).reshape(npairs, 2 * g["rowV"])
     vm = part("v_meta", g["S_pad"] * g["n_vg"] * 4, T * g["n_vg"] * 4).view(np.uint16).reshape(T, g["n_vg"], 2)
-    return dict(k_codes=kc, k_meta=km, k_resid=kr, v_codes=vc, v_meta=vm, Tq=Tq)
+    return dict(k_codes=kc, k_meta=km, k_resid=kr, v_codes=vc, v_meta=vm, Tq=Tq, k_sparse=ksp)
 
 
 def oracle_slice_state(k_hist, v_hist, cache):
     g = cfg_dims(cache)
     if g["sym"]:
-        return oracle.cache_state_sym(k_hist, v_hist, d=g["d"])
+        return oracle.cache_state_sym(k_hist, v_hist, d=g["d"], k_outliers=g["kout"])
     return oracle.cache_state(k_hist, v_hist, d=g["d"], bits=g["bits"], G=g["G"], Gv=g["Gv"], R=g["R"],
                               v_bits=g["vbits"])
 
@@ -67,6 +73,10 @@ def oracle_slice_state(k_hist, v_hist, cache):
 def assert_slice_equal(gpu: dict, st: oracle.OracleState, where: str = ""):
     T = st.T
     assert gpu["Tq"] == st.Tq
+    if st.k_sparse is not None and st.k_sparse.size:
+        if not np.array_equal(gpu["k_sparse"], st.k_sparse):
+            bad = np.argwhere(gpu["k_sparse"] != st.k_sparse)
+            raise AssertionError(f"{where} k_sparse: {len(bad)} mismatches, first at {bad[:3].tolist()}")
     for name in ("k_codes", "k_meta", "v_codes", "v_meta"):
         a, e = gpu[name], getattr(st, name)
         assert a.shape == e.shape, (where, name, a.shape, e.shape)
@@ -95,9 +105,9 @@ def oracle_attention(st: oracle.OracleState, q_rows, cache, softmax_scale):
 
 
 def small_workload(name="small", *, L=1, H=2, r=4, B=2, S=600, steps=8, bits=4, G=32, Gv=64, R=128, n_out=2,
-                   gain=20, seed=777, v_bits=0, symmetric=0):
+                   gain=20, seed=777, v_bits=0, symmetric=0, k_outliers=0):
     return synth.Workload(name, L, H, r, 128, B, S, steps, bits, G, Gv, R, n_out, gain, seed, v_bits=v_bits,
-                          symmetric=symmetric)
+                          symmetric=symmetric, k_outliers=k_outliers)
 
 
 def host_layer_inputs(w, layer, t0, nt):

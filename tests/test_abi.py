@@ -51,6 +51,9 @@ def good_cfg(**kw):
     (dict(symmetric=2), 1), (dict(symmetric=1, bits=4, v_group=128, residual_len=0), 2),
     (dict(symmetric=1, bits=8, v_bits=4, v_group=128, residual_len=0), 2),
     (dict(symmetric=1, bits=8, v_group=64, residual_len=0), 2), (dict(symmetric=1, bits=8, v_group=128), 1),
+    # outlier isolation: symmetric scheme only, 0..4 entries per token
+    (dict(k_outliers=2), 2), (dict(symmetric=1, bits=8, v_group=128, residual_len=0, k_outliers=5), 2),
+    (dict(symmetric=1, bits=8, v_group=128, residual_len=0, k_outliers=-1), 2),
 ])
 def test_bad_configs_are_rejected(lib, kw, status):
     sizes = (ctypes.c_size_t * 5)()
@@ -96,6 +99,18 @@ def test_symmetric_buffer_sizes(lib):
     assert sizes == [n * S_pad * 128, n * S_pad * 2, 0, n * S_pad * 128, n * S_pad * 4]
     # the bytes the pages count for an int8 cache, plus 6 metadata bytes per token and head
     assert sizes[0] + sizes[3] == oracle.kv_bytes(L, H * B, 128, S_pad, 8)
+
+
+def test_outlier_buffer_sizes(lib):
+    """k_outliers = k adds k (channel, binary16) entries of 4 bytes per token after the
+    per-token key scales."""
+    L, B, H, S = 2, 3, 2, 1000
+    S_pad, n = 1024, 2 * 3 * 2
+    for k in range(5):
+        sizes = kvq.kvq_buffer_sizes(good_cfg(n_layers=L, batch=B, n_kv_heads=H, max_seq_len=S, bits=8, v_group=128,
+                                              residual_len=0, symmetric=1, k_outliers=k))
+        assert sizes[1] == n * S_pad * (2 + 4 * k)
+        assert sizes[0] == sizes[3] == n * S_pad * 128 and sizes[2] == 0
 
 
 def _bufs(ptr=4096):

@@ -11,7 +11,7 @@ import bench
 import oracle
 import synth
 
-NAMES = ["llama8b-int8", "kivi-int4", "kivi-int2", "kivi-k8v4", "long-int4-16k", "sym8-b16"]
+NAMES = ["llama8b-int8", "kivi-int4", "kivi-int2", "kivi-k8v4", "long-int4-16k", "sym8-b16", "sym8o4-b16"]
 
 
 @pytest.mark.parametrize("name", NAMES)
@@ -22,11 +22,11 @@ def test_attention_bytes_equal_the_oracle_state(name, T):
     k = synth.k_slice(w, 0, 0, 0, range(T))
     v = synth.v_slice(w, 0, 0, 0, range(T))
     if w.symmetric:
-        st = oracle.cache_state_sym(k, v, d=d)
+        st = oracle.cache_state_sym(k, v, d=d, k_outliers=w.k_outliers)
     else:
         st = oracle.cache_state(k, v, d=d, bits=w.bits, G=w.k_group, Gv=w.v_group, R=w.residual, v_bits=w.vbits)
     state = (st.k_codes.nbytes + st.k_meta.nbytes + (T - st.Tq) * d * 2 + st.v_codes.nbytes
-             + st.v_meta.nbytes)
+             + st.v_meta.nbytes + (st.k_sparse.nbytes if st.k_sparse is not None else 0))
     io = w.n_q * d * 2 + w.n_q * d * 4  # binary16 queries in, binary32 outputs out
     assert bench.attn_bytes_per_layer(w, T) == state + io
 
@@ -39,9 +39,9 @@ def test_prefill_bytes_equal_inputs_plus_state(name):
     k = synth.k_slice(w, 0, 0, 0, range(T))
     v = synth.v_slice(w, 0, 0, 0, range(T))
     if w.symmetric:
-        st = oracle.cache_state_sym(k, v, d=d)
+        st = oracle.cache_state_sym(k, v, d=d, k_outliers=w.k_outliers)
     else:
         st = oracle.cache_state(k, v, d=d, bits=w.bits, G=w.k_group, Gv=w.v_group, R=w.residual, v_bits=w.vbits)
     written = (st.k_codes.nbytes + st.k_meta.nbytes + (T - st.Tq) * d * 2 + st.v_codes.nbytes
-               + st.v_meta.nbytes)
+               + st.v_meta.nbytes + (st.k_sparse.nbytes if st.k_sparse is not None else 0))
     assert bench.prefill_bytes_per_layer(w, T) == 2 * T * d * 2 + written

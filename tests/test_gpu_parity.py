@@ -432,3 +432,46 @@ def test_symmetric_per_token_int8(r, B, H, S, steps):
         kh, vh = oracle.dequantize_state_sym(st, d=128)
         assert np.array_equal(kd[b, h].cpu().numpy().view(np.uint32), kh.view(np.uint32))
         assert np.array_equal(vd[b, h].cpu().numpy().view(np.uint32), vh.view(np.uint32))
+
+
+@pytest.mark.parametrize("k_out,r,B,H,S,steps", [
+    (4, 4, 2, 2, 300, 4),     # small grid
+    (1, 8, 2, 2, 257, 3),     # GQA 8, one entry per token
+    (3, 4, 12, 4, 2100, 2),   # large grid
+])
+def test_symmetric_with_outlier_isolation(k_out, r, B, H, S, steps):
+    """Symmetric per-token int8 with k isolated key entries per token (dense-and-sparse):
+    codes, scales and the sparse side list bit-exact after a chunked prefill and fused
+    decode steps, attention (the sparse read path included) within 2e-3, and the
+    dequantized keys bit-exact (the stored binary16 values at their channels)."""
+    w = small_workload(bits=8, G=128, Gv=128, R=0, r=r, B=B, H=H, S=S, steps=steps, seed=9000 + S + k_out,
+                       symmetric=1, k_outliers=k_out)
+    cache = QuantizedKVCache.for_workload(w)
+    k_host, v_host = host_layer_inputs(w, 0, 0, w.max_seq)
+    cut = S // 2
+    cache.append(0, 0, _dev(k_host[:, :cut]), _dev(v_host[:, :cut]))
+    cache.append(0, cut, _dev(k_host[:, cut:S]), _dev(v_host[:, cut:S]))
+    _check_all_slices(cache, w, 0, S, k_host, v_host)
+    q0 = synth.gen_q(w.seed, 0, range(w.batch), S - 1, w.n_q, w.d_head)
+    _check_attention(cache, w, 0, S, k_host, v_host, q0, kvq.DECODE_MMA)
+    for s in range(steps):
+        T = S + s
+        q_host = synth.gen_q(w.seed, 0, range(w.batch), T, w.n_q, w.d_head)
+        out = cache.decode_step(0, T, _dev(k_host[:, T:T + 1]), _dev(v_host[:, T:T + 1]), _dev(q_host),
+                                softmax_scale(w)).cpu().numpy()
+        if s == steps - 1:
+            worst = 0.0
+            for b in range(w.batch):
+                for h in range(w.n_kv):
+                    st = oracle_slice_state(k_host[b, :T + 1, h], v_host[b, :T + 1, h], cache)
+                    ref = oracle_attention(st, q_host[b, h * w.gqa:(h + 1) * w.gqa], cache, softmax_scale(w))
+                    worst = max(worst, float(np.abs(out[b, h * w.gqa:(h + 1) * w.gqa] - ref).max()))
+            assert worst <= ATOL, worst
+    T = S + steps
+    _check_all_slices(cache, w, 0, T, k_host, v_host)
+    kd, vd = cache.dequantize(0, T)
+    for b, h in {(0, 0), (w.batch - 1, w.n_kv - 1)}:
+        st = oracle_slice_state(k_host[b, :T, h], v_host[b, :T, h], cache)
+        kh, vh = oracle.dequantize_state_sym(st, d=128)
+        assert np.array_equal(kd[b, h].cpu().numpy().view(np.uint32), kh.view(np.uint32))
+        assert np.array_equal(vd[b, h].cpu().numpy().view(np.uint32), vh.view(np.uint32))
