@@ -38,7 +38,8 @@ DEFAULT_WORKLOAD = "llama8b-int8"
 # ----------------------------------------------------------------------------- byte accounting
 def key_meta_bytes(w, n_keys: int) -> int:
     """Key metadata of n_keys quantized tokens of one slice: (scale, zero point) per channel
-    and group of k_group tokens, or one binary16 scale per token in the symmetric scheme."""
+    and group of k_group tokens, or in the symmetric scheme one binary16 scale per token
+    plus 4 bytes (channel, binary16 value) per isolated key entry."""
     return n_keys * (2 + 4 * w.k_outliers) if w.symmetric else (n_keys // w.k_group) * w.d_head * 4
 
 

@@ -211,7 +211,12 @@ struct Stage {
   static constexpr int EP_CM = EP_BETA + NW * kMaxGqa * NVG * 4;
   static constexpr int EP_SCRATCH = (EP_CM + (2 * kMaxGqa + kMaxGqa * kHeadDim) * 4 + 15) / 16 * 16;
   static constexpr int kEpilogueBytes = EP_SCRATCH + 4 * kMergeScratchFloats;
-  static constexpr int SMEM = NW * WARP_BYTES > kEpilogueBytes ? NW * WARP_BYTES : kEpilogueBytes;
+  // isolated key entries: per warp a [32 tokens][kMaxGqa + 1] binary32 table of the sparse
+  // score terms, after the stage rings (used in the loop only, like the rings)
+  static constexpr int SP = NW * WARP_BYTES;
+  static constexpr int SP_ROW = kMaxGqa + 1;
+  static constexpr int LOOP_BYTES = SP + (OUTL ? NW * 32 * SP_ROW * 4 : 0);
+  static constexpr int SMEM = LOOP_BYTES > kEpilogueBytes ? LOOP_BYTES : kEpilogueBytes;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -338,10 +343,13 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
   __shared__ __align__(16) float q_s[kMaxGqa][kHeadDim];
   // query row i in key-pair order of lane chunk c, pre-divided by k_scale and scaled
   // by 2^qe_s[i] (so that |entry| < 2^8), as binary16 pairs
-  __shared__ __align__(16) uint32_t q2_s[kMaxGqa][4][16];
+  __shared__ __align__(16) uint32_t q2_s[SYM ? 1 : kMaxGqa][4][16];  // not used by per-token key scales
   __shared__ int qe_s[kMaxGqa];
   __shared__ float qsum_s[kMaxGqa];  // SYM: sum_c q_c of every query row
-  __shared__ __align__(16) uint32_t qa_s[kWarps][(NT == 1) ? 16 : 32][36];  // padded rows: no bank conflicts
+  // padded rows: no bank conflicts. SYM keeps only the hi words (the lo rows of its A
+  // fragments are zero): 16 words per row, 18 with the padding
+  constexpr int kQA = SYM ? 18 : 36;
+  __shared__ __align__(16) uint32_t qa_s[kWarps][(NT == 1) ? 16 : 32][kQA];
 
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -438,8 +446,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
         uint8_t* kmb = reinterpret_cast<uint8_t*>(p.k_meta_w) + slice * p.k_meta_slice;
         quant::quantize_key_row_sym(p.k_new + row * kHeadDim, p.k_codes_w + slice * p.k_codes_slice + (int64_t)t_new * ROW,
                                     reinterpret_cast<__half*>(kmb) + t_new,
-                                    reinterpret_cast<uint32_t*>(kmb + p.S_pad * 2) + (int64_t)t_new * p.kout, p.kout, lane,
-                                    reinterpret_cast<float*>(smem) + 64);
+                                    reinterpret_cast<uint32_t*>(kmb + p.S_pad * 2) + (int64_t)t_new * p.kout, p.kout, lane);
       } else {
         const uint2 kv = *reinterpret_cast<const uint2*>(p.k_new + row * kHeadDim + 4 * lane);
         *reinterpret_cast<uint2*>(p.k_resid_w + (slice * p.R_eff + t_new % p.R_eff) * kHeadDim + 4 * lane) = kv;
@@ -476,32 +483,34 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
     for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
     const int qe = a > 0.0f ? 7 - (((__float_as_int(a) >> 23) & 0xFF) - 127) : 0;
     if (lane == 0) qe_s[i] = qe;
-    const float f = pow2f(qe);  // exact scaling by a power of two
-    float v[4], w[4];
+    if constexpr (!SYM) {  // per-token key scales need no folded query
+      const float f = pow2f(qe);  // exact scaling by a power of two
+      float v[4], w[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) v[k] = xq[k] * f;
-    constexpr int D = BITS == 8 ? 0 : (BITS == 4 ? 1 : 2);  // lane distance of a pair's second channel
+      for (int k = 0; k < 4; ++k) v[k] = xq[k] * f;
+      constexpr int D = BITS == 8 ? 0 : (BITS == 4 ? 1 : 2);  // lane distance of a pair's second channel
 #pragma unroll
-    for (int k = 0; k < 4; ++k) w[k] = D ? __shfl_down_sync(0xffffffffu, v[k], D) : v[k];
-    const int lc = lane & 7, c = lane >> 3;  // lane within its chunk, chunk
-    if (BITS == 8) {  // pairs 2lc (channels 4lc, 4lc+1) and 2lc+1 (4lc+2, 4lc+3)
-      q2_s[i][c][2 * lc] = h2_bits(__floats2half2_rn(v[0], v[1]));
-      q2_s[i][c][2 * lc + 1] = h2_bits(__floats2half2_rn(v[2], v[3]));
-    } else if (BITS == 4) {  // even lc: pairs 4m + e join channels 8m + e and 8m + e + 4 (m = lc/2)
-      if ((lc & 1) == 0) {
+      for (int k = 0; k < 4; ++k) w[k] = D ? __shfl_down_sync(0xffffffffu, v[k], D) : v[k];
+      const int lc = lane & 7, c = lane >> 3;  // lane within its chunk, chunk
+      if (BITS == 8) {  // pairs 2lc (channels 4lc, 4lc+1) and 2lc+1 (4lc+2, 4lc+3)
+        q2_s[i][c][2 * lc] = h2_bits(__floats2half2_rn(v[0], v[1]));
+        q2_s[i][c][2 * lc + 1] = h2_bits(__floats2half2_rn(v[2], v[3]));
+      } else if (BITS == 4) {  // even lc: pairs 4m + e join channels 8m + e and 8m + e + 4 (m = lc/2)
+        if ((lc & 1) == 0) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float ks = k_scale<BITS>(e);
-          q2_s[i][c][2 * lc + e] = h2_bits(__floats2half2_rn(v[e] / ks, w[e] / ks));
+          for (int e = 0; e < 4; ++e) {
+            const float ks = k_scale<BITS>(e);
+            q2_s[i][c][2 * lc + e] = h2_bits(__floats2half2_rn(v[e] / ks, w[e] / ks));
+          }
         }
-      }
-    } else {  // lc % 4 < 2: pairs 8m + 4(lc & 1) + k join channels 16m + 4(lc & 1) + k and + 8
-      if ((lc & 3) < 2) {
-        const int pi0 = 8 * (lc >> 2) + 4 * (lc & 1);
+      } else {  // lc % 4 < 2: pairs 8m + 4(lc & 1) + k join channels 16m + 4(lc & 1) + k and + 8
+        if ((lc & 3) < 2) {
+          const int pi0 = 8 * (lc >> 2) + 4 * (lc & 1);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float ks = (lc & 1) ? k_scale<BITS>(4 + k) : k_scale<BITS>(k);
-          q2_s[i][c][pi0 + k] = h2_bits(__floats2half2_rn(v[k] / ks, w[k] / ks));
+          for (int k = 0; k < 4; ++k) {
+            const float ks = (lc & 1) ? k_scale<BITS>(4 + k) : k_scale<BITS>(k);
+            q2_s[i][c][pi0 + k] = h2_bits(__floats2half2_rn(v[k] / ks, w[k] / ks));
+          }
         }
       }
     }
@@ -556,8 +565,8 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const float4 qv = reinterpret_cast<const float4*>(qrow)[ks];
-          reinterpret_cast<uint4*>(qa_row)[ks] = make_uint4(h2_bits(__floats2half2_rn(qv.x, qv.y)), 0u,
-                                                            h2_bits(__floats2half2_rn(qv.z, qv.w)), 0u);
+          reinterpret_cast<uint2*>(qa_row)[ks] =
+              make_uint2(h2_bits(__floats2half2_rn(qv.x, qv.y)), h2_bits(__floats2half2_rn(qv.z, qv.w)));
         }
         __syncwarp();
       }
@@ -656,7 +665,13 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
         for (int nt = 0; nt < 2; ++nt) lds_chunk<BITS>(st + (16 * hf + 8 * nt + g) * ROW + j * (ROW / 4), kw[hf][nt]);
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
-        const uint4 a = reinterpret_cast<const uint4*>(qa_row)[ks];
+        uint4 a;
+        if constexpr (SYM) {
+          const uint2 a2 = reinterpret_cast<const uint2*>(qa_row)[ks];
+          a = make_uint4(a2.x, 0u, a2.y, 0u);
+        } else {
+          a = reinterpret_cast<const uint4*>(qa_row)[ks];
+        }
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
@@ -664,7 +679,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
             mma16816(acc[hf][nt], a.x, a.y, a.z, a.w, k_pair<BITS>(kw[hf][nt], 2 * ks),
                      k_pair<BITS>(kw[hf][nt], 2 * ks + 1));
       }
-    } else {
+    } else if constexpr (!SYM) {  // binary16 residual keys (the symmetric scheme has none)
       if (!resid_frags) {
         resid_frags = true;  // raw query fragments for binary16 residual keys: natural channel pairs
         __syncwarp();
@@ -723,21 +738,46 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
           s[hf][2 * nt] = (kk.x * p.scale_log2) * fmaf(acc[hf][nt][0] + acc[hf][nt][2], kTwo24, qmin_qsum);
           s[hf][2 * nt + 1] = (kk.y * p.scale_log2) * fmaf(acc[hf][nt][1] + acc[hf][nt][3], kTwo24, qmin_qsum);
         }
-      if constexpr (OUTL) {  // the sparse side list: q_c * x_c of every isolated key entry
+      if constexpr (OUTL) {  // the sparse side list: x_c * q_c of every isolated key entry
+        // lane l takes token l: its entries (channel | binary16 value << 16) against every
+        // query row into the warp's table sp_w[token][row] (rows of kMaxGqa + 1 words: no
+        // bank conflicts), then every score lane reads its (token, row) term back
         const uint32_t* ent = reinterpret_cast<const uint32_t*>(st + St::KB + St::VB + St::VM + 64);
-        const float* qr = &q_s[qi][0];
+        float* sp_w = reinterpret_cast<float*>(smem + St::SP) + warp * 32 * St::SP_ROW;
+        const int ko = p.kout;
+        uint32_t en[4];
+        if (ko == 4) {
+          const uint4 e4 = *reinterpret_cast<const uint4*>(ent + 4 * lane);
+          en[0] = e4.x; en[1] = e4.y; en[2] = e4.z; en[3] = e4.w;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) en[e] = e < ko ? ent[lane * ko + e] : 0u;  // missing: channel 0, value +0
+        }
+        float xv[4];
+        int ch[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          xv[e] = __half2float(__ushort_as_half((unsigned short)(en[e] >> 16)));
+          ch[e] = (int)(en[e] & (kHeadDim - 1));
+        }
+        constexpr int kRows = NT == 1 ? 4 : kMaxGqa;
+#pragma unroll
+        for (int row = 0; row < kRows; ++row)
+          if (row < r) {
+            float sp = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sp = fmaf(xv[e], q_s[row][ch[e]], sp);
+            sp_w[lane * St::SP_ROW + row] = sp;
+          }
+        __syncwarp();
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const int tl = 16 * hf + 8 * (k >> 1) + 2 * j + (k & 1);
-            float sp = 0.0f;
-            for (int r = 0; r < p.kout; ++r) {
-              const uint32_t en = ent[tl * p.kout + r];  // channel | binary16 value << 16
-              sp = fmaf(__half2float(__ushort_as_half((unsigned short)(en >> 16))), qr[en & (kHeadDim - 1)], sp);
-            }
-            s[hf][k] = fmaf(sp, p.scale_log2, s[hf][k]);
+            s[hf][k] = fmaf(sp_w[tl * St::SP_ROW + qi], p.scale_log2, s[hf][k]);
           }
+        __syncwarp();  // the table is rewritten in the next iteration
       }
     }
     if (ts + kTok > t_end) {  // ragged last iteration

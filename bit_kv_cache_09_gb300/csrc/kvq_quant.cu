@@ -316,7 +316,6 @@ __global__ void __launch_bounds__(256) k_token_sym_kernel(AppendParams p) {
 // median and the farthest entries need the whole row), see quant::quantize_key_row_sym.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) k_token_sym_outlier_kernel(AppendParams p) {
-  __shared__ float vals_s[8][kHeadDim];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t nb = p.n_new * p.H;
   const int64_t wb = (int64_t)blockIdx.x * 8 + warp;
@@ -332,7 +331,7 @@ __global__ void __launch_bounds__(256) k_token_sym_outlier_kernel(AppendParams p
   uint8_t* kmb = reinterpret_cast<uint8_t*>(p.k_meta) + slice * p.k_meta_slice;
   quantize_key_row_sym(p.k_in + w * kHeadDim, p.k_codes + slice * p.k_codes_slice + t * p.rowK,
                        reinterpret_cast<__half*>(kmb) + t, reinterpret_cast<uint32_t*>(kmb + p.S_pad * 2) + t * p.kout,
-                       p.kout, lane, vals_s[warp]);
+                       p.kout, lane);
 }
 
 // ---------------------------------------------------------------------------

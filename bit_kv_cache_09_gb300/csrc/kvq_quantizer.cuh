@@ -166,38 +166,37 @@ __device__ __forceinline__ void quantize_value_row(const __half* v_row, uint16_t
 // distance, ties to the lower channel; "Sub-8-Bit KV Cache Quantization Is Not a Free
 // Lever for an RDNA4 Agent Swarm", § What the low-bit numbers actually cost: per-vector
 // dense-and-sparse quantization) go to entries[0 .. kout) as channel | binary16 << 16
-// and are replaced by 0 before the scale is taken. vals_s: 128 floats of warp-private
-// shared memory.
+// and are replaced by 0 before the scale is taken.
 __device__ __forceinline__ void quantize_key_row_sym(const __half* k_row, uint8_t* key_row, __half* scale_out,
-                                                     uint32_t* entries, int kout, int lane, float* vals_s) {
+                                                     uint32_t* entries, int kout, int lane) {
   float x[4];
   load4(k_row + 4 * lane, x);
   if (kout > 0) {
     const uint2 raw = *reinterpret_cast<const uint2*>(k_row + 4 * lane);
     const uint32_t xb[4] = {raw.x & 0xFFFFu, raw.x >> 16, raw.y & 0xFFFFu, raw.y >> 16};
-    // lower median = sorted[63]: the value with at most 63 of the 128 values below it and
-    // more than 63 at or below it
+    // lower median = the 64th smallest value (rank 63): a most-significant-bit-first radix
+    // select over order-preserving 16-bit keys of the binary16 inputs (negative values
+    // bit-inverted, positive ones with the sign bit set), one ballot per key and bit.
+    // -0 and +0 get distinct keys, which leaves |x - median| unchanged.
+    uint32_t key[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) vals_s[4 * lane + e] = x[e];
-    __syncwarp();
-    int lt[4] = {0, 0, 0, 0}, le[4] = {0, 0, 0, 0};
-    for (int i = 0; i < 128; ++i) {
-      const float y = vals_s[i];
+    for (int e = 0; e < 4; ++e) key[e] = (xb[e] & 0x8000u) ? (~xb[e] & 0xFFFFu) : (xb[e] | 0x8000u);
+    uint32_t prefix = 0;
+    int rank = 63;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        lt[e] += y < x[e];
-        le[e] += y <= x[e];
+    for (int bit = 15; bit >= 0; --bit) {
+      const uint32_t above = (0xFFFFu << (bit + 1)) & 0xFFFFu;  // the bits already decided
+      int n0 = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        n0 += __popc(__ballot_sync(0xffffffffu, ((key[e] ^ prefix) & above) == 0u && ((key[e] >> bit) & 1u) == 0u));
+      if (rank >= n0) {
+        rank -= n0;
+        prefix |= 1u << bit;
       }
     }
-    bool mine = false;
-    float medv = 0.0f;
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (lt[e] <= 63 && 63 < le[e]) {
-        mine = true;
-        medv = x[e];
-      }
-    const float med = __shfl_sync(0xffffffffu, medv, __ffs(__ballot_sync(0xffffffffu, mine)) - 1);
+    const uint32_t med_bits = (prefix & 0x8000u) ? (prefix & 0x7FFFu) : (~prefix & 0xFFFFu);
+    const float med = __half2float(__ushort_as_half((unsigned short)med_bits));
     float dist[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) dist[e] = fabsf(__fsub_rn(x[e], med));
@@ -230,7 +229,6 @@ __device__ __forceinline__ void quantize_key_row_sym(const __half* k_row, uint8_
 #pragma unroll
     for (int e = 0; e < 4; ++e)
       if (taken[e]) x[e] = 0.0f;
-    __syncwarp();  // vals_s may be reused by the caller
   }
   float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
   for (int off = 1; off < 32; off <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
