@@ -438,6 +438,7 @@ def test_symmetric_per_token_int8(r, B, H, S, steps):
     (4, 4, 2, 2, 300, 4),     # small grid
     (1, 8, 2, 2, 257, 3),     # GQA 8, one entry per token
     (3, 4, 12, 4, 2100, 2),   # large grid
+    (2, 2, 1, 3, 100, 2),     # GQA 2, two entries per token
 ])
 def test_symmetric_with_outlier_isolation(k_out, r, B, H, S, steps):
     """Symmetric per-token int8 with k isolated key entries per token (dense-and-sparse):
@@ -475,3 +476,66 @@ def test_symmetric_with_outlier_isolation(k_out, r, B, H, S, steps):
         kh, vh = oracle.dequantize_state_sym(st, d=128)
         assert np.array_equal(kd[b, h].cpu().numpy().view(np.uint32), kh.view(np.uint32))
         assert np.array_equal(vd[b, h].cpu().numpy().view(np.uint32), vh.view(np.uint32))
+
+
+def _adversarial_key_rows(rng):
+    """Binary16 key rows that stress the outlier selection: the lower median of rows with
+    signed zeros, constants, duplicates, two values, extremes and subnormals, and ties in
+    |x - median| (broken towards the lower channel)."""
+    d = 128
+    rows = [np.zeros(d, np.float16)]                                    # all +0
+    r = np.where(rng.random(d) < 0.5, np.float16(0.0), np.float16(-0.0)).astype(np.float16)
+    r[17] = 5.0
+    rows.append(r)                                                      # +0 / -0 mix, one entry away
+    rows.append(np.full(d, 1.5, np.float16))                            # constant row
+    rows.append((-np.abs(rng.standard_normal(d))).astype(np.float16))   # all negative
+    rows.append(rng.integers(-1, 2, d).astype(np.float16))              # three values only
+    r = rng.standard_normal(d).astype(np.float16)
+    r[3], r[90] = 65504.0, -65504.0
+    r[5], r[6], r[7] = np.float16(2.0 ** -24), -np.float16(2.0 ** -24), np.float16(2.0 ** -20)
+    rows.append(r)                                                      # extremes and subnormals
+    r = np.full(d, 2.0, np.float16)
+    r[rng.permutation(d)[:64]] = -2.0
+    rows.append(r)                                                      # two values, 64 each
+    r = np.full(d, 0.25, np.float16)
+    r[[10, 20, 30, 40, 50, 60]] = [3.0, -2.5, 3.0, -2.5, 3.0, -2.5]
+    rows.append(r)                                                      # six entries at one distance
+    r = rng.standard_normal(d).astype(np.float16)
+    r[[100, 8, 64, 1]] = [-7.0, 7.0, -7.0, 7.0]
+    rows.append(r)                                                      # four outliers of one magnitude
+    return rows
+
+
+def test_outlier_selection_on_adversarial_rows():
+    """Outlier isolation on hand-built key rows (signed zeros, constant and two-valued
+    rows, extremes, subnormals, distance ties), through the append kernel and through the
+    fused decode step: codes, scales and the sparse side list bit-exact against the
+    oracle, attention within 2e-3."""
+    w = small_workload(bits=8, G=128, Gv=128, R=0, r=4, B=2, H=2, S=64, steps=2, seed=9100,
+                       symmetric=1, k_outliers=4)
+    cache = QuantizedKVCache.for_workload(w)
+    k_host, v_host = host_layer_inputs(w, 0, 0, w.max_seq)
+    k_host = np.array(k_host, dtype=np.float16)
+    rows = _adversarial_key_rows(np.random.default_rng(9100))
+    for i, row in enumerate(rows):
+        k_host[0, i, 0] = row
+        k_host[1, 20 + i, 1] = row[::-1]
+    S = w.seq
+    k_host[0, S, 0] = rows[1]  # the fused step quantizes these new rows
+    k_host[1, S, 1] = rows[7]
+    k_host[0, S + 1, 1] = rows[0]
+    k_host[1, S + 1, 0] = rows[5]
+    cache.append(0, 0, _dev(k_host[:, :S]), _dev(v_host[:, :S]))
+    _check_all_slices(cache, w, 0, S, k_host, v_host)
+    for s in range(w.steps):
+        T = S + s
+        q_host = synth.gen_q(w.seed, 0, range(w.batch), T, w.n_q, w.d_head)
+        out = cache.decode_step(0, T, _dev(k_host[:, T:T + 1]), _dev(v_host[:, T:T + 1]), _dev(q_host),
+                                softmax_scale(w)).cpu().numpy()
+        _check_all_slices(cache, w, 0, T + 1, k_host, v_host)
+        for b in range(w.batch):
+            for h in range(w.n_kv):
+                st = oracle_slice_state(k_host[b, :T + 1, h], v_host[b, :T + 1, h], cache)
+                ref = oracle_attention(st, q_host[b, h * w.gqa:(h + 1) * w.gqa], cache, softmax_scale(w))
+                err = float(np.abs(out[b, h * w.gqa:(h + 1) * w.gqa] - ref).max())
+                assert err <= ATOL, (b, h, T + 1, err)

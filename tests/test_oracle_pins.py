@@ -548,6 +548,32 @@ def test_outlier_split_worked_example():
     assert idx0.size == 0 and np.array_equal(dense0, x.view(np.uint16))
 
 
+def test_outlier_split_ties_and_two_values():
+    """Ties in |x - median| go to the lower channel, and the median is the lower one:
+    (a) 0.25 on 122 channels and +3 / -2.5 alternating on channels 10 .. 60: the median is
+    0.25 and all six are 2.75 away, so the picks are channels 10, 20, 30, 40 in order;
+    (b) 64 channels at -2 and 64 at +2: the lower median is -2, every +2 is 4 away, so
+    the picks are the four lowest +2 channels; (c) a constant row: every distance is 0,
+    so channels 0 .. 3, and the dense row keeps the constant elsewhere."""
+    x = np.full(128, 0.25, np.float16)
+    x[[10, 20, 30, 40, 50, 60]] = [3.0, -2.5, 3.0, -2.5, 3.0, -2.5]
+    idx, val, dense = oracle.split_outliers(x, 4)
+    assert idx.tolist() == [10, 20, 30, 40]
+    assert val.view(np.float16).tolist() == [3.0, -2.5, 3.0, -2.5]
+    assert dense.view(np.float16)[[10, 20, 30, 40, 50, 60]].tolist() == [0, 0, 0, 0, 3.0, -2.5]
+    x = np.full(128, 2.0, np.float16)
+    neg = np.random.default_rng(5).permutation(128)[:64]
+    x[neg] = -2.0
+    pos = sorted(set(range(128)) - set(neg.tolist()))
+    idx, val, _ = oracle.split_outliers(x, 4)
+    assert idx.tolist() == pos[:4]
+    assert val.view(np.float16).tolist() == [2.0] * 4
+    x = np.full(128, 1.5, np.float16)
+    idx, val, dense = oracle.split_outliers(x, 3)
+    assert idx.tolist() == [0, 1, 2]
+    assert dense.view(np.float16).tolist() == [0.0] * 3 + [1.5] * 125
+
+
 def test_outliers_shrink_the_dense_scale():
     """A key row with three planted outliers: they are the three picks, their values come
     back exactly, and the dense scale drops to max|rest| / 127 (rounded up), so every
