@@ -4,6 +4,12 @@
 tensors and forwards every call to the ``kvq_*`` entry points with the tensors'
 device addresses and the current CUDA stream. No arithmetic of the path happens
 here.
+
+Decode launches pass ``KVQ_DECODE_EARLY_PREFETCH`` (their first cache tiles stream in
+while the previous kernel of the stream finishes) unless this object's previous launch
+on the same stream wrote the same layer. Kernels that write the cache buffers outside
+this object (through ``buffer()``) must therefore not directly precede a decode launch
+on the same stream; pass ``early=False`` after them.
 """
 
 from __future__ import annotations
@@ -28,6 +34,7 @@ class QuantizedKVCache:
         self.ws = torch.zeros(max(kvq.kvq_decode_workspace_size(self.cfg, max_seq_len), 16), dtype=torch.uint8,
                               device=self.device)
         self.n_q = n_kv_heads * gqa_ratio
+        self._last = None  # (stream, layer, wrote) of this object's previous launch
 
     @classmethod
     def for_workload(cls, w, *, n_layers=None, device="cuda"):
@@ -43,37 +50,57 @@ class QuantizedKVCache:
     def buffer(self, name: str) -> torch.Tensor:
         return self.buffers[kvq.BUFFER_NAMES.index(name)]
 
+    def _early(self, stream: int, layer: int, early) -> int:
+        """Flag bits of a decode launch of `layer` on `stream` (see the module docstring)."""
+        if early is None:
+            early = not (self._last is not None and self._last[0] == stream and self._last[1] == layer
+                         and self._last[2])
+        return kvq.DECODE_EARLY_PREFETCH if early else 0
+
     def append(self, layer: int, s_cur: int, k: torch.Tensor, v: torch.Tensor) -> None:
         """k, v: [batch][n_new][n_kv_heads][d_head] float16 on the device."""
         assert k.dtype == torch.float16 and v.dtype == torch.float16 and k.is_contiguous() and v.is_contiguous()
         assert k.shape == v.shape and k.dim() == 4
-        kvq.kvq_quantize_append(self.cfg, self.bufs, layer, s_cur, k.shape[1], k.data_ptr(), v.data_ptr(),
-                                self._stream())
+        stream = self._stream()
+        kvq.kvq_quantize_append(self.cfg, self.bufs, layer, s_cur, k.shape[1], k.data_ptr(), v.data_ptr(), stream)
+        self._last = (stream, layer, True)
 
     def dequantize(self, layer: int, s_cur: int):
         c = self.cfg
         k_out = torch.empty((c.batch, c.n_kv_heads, s_cur, c.d_head), dtype=torch.float32, device=self.device)
         v_out = torch.empty_like(k_out)
-        kvq.kvq_dequantize(self.cfg, self.bufs, layer, s_cur, k_out.data_ptr(), v_out.data_ptr(), self._stream())
+        stream = self._stream()
+        kvq.kvq_dequantize(self.cfg, self.bufs, layer, s_cur, k_out.data_ptr(), v_out.data_ptr(), stream)
+        self._last = (stream, layer, False)
         return k_out, v_out
 
     def attention(self, layer: int, s_cur: int, q: torch.Tensor, softmax_scale: float, out: torch.Tensor = None,
-                  impl: int = kvq.DECODE_AUTO) -> torch.Tensor:
+                  impl: int = kvq.DECODE_AUTO, early=None) -> torch.Tensor:
         """q: [batch][n_q][d_head] float16; returns out [batch][n_q][d_head] float32."""
         assert q.dtype == torch.float16 and q.is_contiguous()
         if out is None:
             out = torch.empty(q.shape, dtype=torch.float32, device=self.device)
-        kvq.kvq_decode_attention_impl(self.cfg, self.bufs, layer, s_cur, q.data_ptr(), softmax_scale, out.data_ptr(),
-                                      self.ws.data_ptr(), self.ws.numel(), self._stream(), impl)
+        stream = self._stream()
+        if impl == kvq.DECODE_AUTO:
+            kvq.kvq_decode_attention_ex(self.cfg, self.bufs, layer, s_cur, q.data_ptr(), softmax_scale,
+                                        out.data_ptr(), self.ws.data_ptr(), self.ws.numel(), stream,
+                                        self._early(stream, layer, early))
+        else:
+            kvq.kvq_decode_attention_impl(self.cfg, self.bufs, layer, s_cur, q.data_ptr(), softmax_scale,
+                                          out.data_ptr(), self.ws.data_ptr(), self.ws.numel(), stream, impl)
+        self._last = (stream, layer, False)
         return out
 
     def decode_step(self, layer: int, s_cur: int, k: torch.Tensor, v: torch.Tensor, q: torch.Tensor,
-                    softmax_scale: float, out: torch.Tensor = None) -> torch.Tensor:
+                    softmax_scale: float, out: torch.Tensor = None, early=None) -> torch.Tensor:
         """Append one token ([batch][1][n_kv][d] float16) and attend over s_cur + 1 tokens."""
         assert k.dtype == torch.float16 and v.dtype == torch.float16 and q.dtype == torch.float16
         assert k.is_contiguous() and v.is_contiguous() and q.is_contiguous() and k.shape[1] == 1
         if out is None:
             out = torch.empty(q.shape, dtype=torch.float32, device=self.device)
-        kvq.kvq_decode_step(self.cfg, self.bufs, layer, s_cur, k.data_ptr(), v.data_ptr(), q.data_ptr(), softmax_scale,
-                            out.data_ptr(), self.ws.data_ptr(), self.ws.numel(), self._stream())
+        stream = self._stream()
+        kvq.kvq_decode_step_ex(self.cfg, self.bufs, layer, s_cur, k.data_ptr(), v.data_ptr(), q.data_ptr(),
+                               softmax_scale, out.data_ptr(), self.ws.data_ptr(), self.ws.numel(), stream,
+                               self._early(stream, layer, early))
+        self._last = (stream, layer, True)
         return out

@@ -314,10 +314,12 @@ int32_t kvq_decode_num_splits(const kvq_config* cfg, int64_t s_cur) {
 namespace {
 
 // Checks and launches decode attention over s_cur tokens; when k_new/v_new are given
-// (tensor-core kernel only) the kernel first appends token s_cur - 1 itself.
+// (tensor-core kernel only) the kernel first appends token s_cur - 1 itself. early: the
+// tensor-core kernel copies its first cache tiles before waiting on the previous kernel
+// of the stream (KVQ_DECODE_EARLY_PREFETCH).
 kvq_status decode_launch(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur,
                          const void* q_f16, float softmax_scale, float* out, void* ws, size_t ws_bytes, void* stream,
-                         kvq_decode_impl impl, const void* k_new, const void* v_new) {
+                         kvq_decode_impl impl, const void* k_new, const void* v_new, bool early) {
   Geometry g;
   kvq_status st = kvq::make_geometry(cfg, &g);
   if (st != KVQ_OK) return st;
@@ -380,6 +382,7 @@ kvq_status decode_launch(const kvq_config* cfg, const kvq_buffers* bufs, int32_t
   p.n_parts = pl.n_parts;
   p.warps = pl.warps;
   p.sym = g.sym;
+  p.early = (early && use == KVQ_DECODE_MMA) ? 1 : 0;
   cudaError_t e = (use == KVQ_DECODE_SIMT) ? kvq::launch_decode_simt(p, g.bits, static_cast<cudaStream_t>(stream))
                                             : kvq::launch_decode_mma(p, g.bits, g.vbits, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
@@ -393,12 +396,22 @@ kvq_status kvq_decode_attention_impl(const kvq_config* cfg, const kvq_buffers* b
                                      const void* q_f16, float softmax_scale, float* out, void* ws,
                                      size_t ws_bytes, void* stream, kvq_decode_impl impl) {
   return decode_launch(cfg, bufs, layer, s_cur, q_f16, softmax_scale, out, ws, ws_bytes, stream, impl, nullptr,
-                       nullptr);
+                       nullptr, false);
 }
 
-kvq_status kvq_decode_step(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur,
-                           const void* k_f16, const void* v_f16, const void* q_f16, float softmax_scale, float* out,
-                           void* ws, size_t ws_bytes, void* stream) {
+kvq_status kvq_decode_attention_ex(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur,
+                                   const void* q_f16, float softmax_scale, float* out, void* ws, size_t ws_bytes,
+                                   void* stream, uint32_t flags) {
+  if (flags & ~(uint32_t)KVQ_DECODE_EARLY_PREFETCH) return KVQ_ERR_INVALID_ARG;
+  return decode_launch(cfg, bufs, layer, s_cur, q_f16, softmax_scale, out, ws, ws_bytes, stream, KVQ_DECODE_AUTO,
+                       nullptr, nullptr, (flags & KVQ_DECODE_EARLY_PREFETCH) != 0);
+}
+
+kvq_status kvq_decode_step_ex(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur,
+                              const void* k_f16, const void* v_f16, const void* q_f16, float softmax_scale, float* out,
+                              void* ws, size_t ws_bytes, void* stream, uint32_t flags) {
+  if (flags & ~(uint32_t)KVQ_DECODE_EARLY_PREFETCH) return KVQ_ERR_INVALID_ARG;
+  const bool early = (flags & KVQ_DECODE_EARLY_PREFETCH) != 0;
   Geometry g;
   kvq_status st = kvq::make_geometry(cfg, &g);
   if (st != KVQ_OK) return st;
@@ -410,11 +423,18 @@ kvq_status kvq_decode_step(const kvq_config* cfg, const kvq_buffers* bufs, int32
   if (!g.sym && T % g.R_eff == 0) {  // the append fills a residual window: quantize it with the append kernels
     st = kvq_quantize_append(cfg, bufs, layer, s_cur, 1, k_f16, v_f16, stream);
     if (st != KVQ_OK) return st;
+    // the kernel just launched writes this layer: the attention launch waits for it
     return decode_launch(cfg, bufs, layer, T, q_f16, softmax_scale, out, ws, ws_bytes, stream, KVQ_DECODE_AUTO,
-                         nullptr, nullptr);
+                         nullptr, nullptr, false);
   }
   return decode_launch(cfg, bufs, layer, T, q_f16, softmax_scale, out, ws, ws_bytes, stream, KVQ_DECODE_AUTO, k_f16,
-                       v_f16);
+                       v_f16, early);
+}
+
+kvq_status kvq_decode_step(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur,
+                           const void* k_f16, const void* v_f16, const void* q_f16, float softmax_scale, float* out,
+                           void* ws, size_t ws_bytes, void* stream) {
+  return kvq_decode_step_ex(cfg, bufs, layer, s_cur, k_f16, v_f16, q_f16, softmax_scale, out, ws, ws_bytes, stream, 0u);
 }
 
 kvq_status kvq_decode_attention(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur,

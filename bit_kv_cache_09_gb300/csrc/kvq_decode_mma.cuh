@@ -376,18 +376,6 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncwarp();
-  pdl_wait();  // everything above touched shared memory only
-
-  // Query rows of this kv head for warp w: rows w, w + NW, ... (lane l: channels
-  // [4l, 4l+4)). They are loaded before any stage copy is issued: behind the copies of
-  // all resident warps they would arrive only after the first stages, and the query
-  // fold (below) is on the path to the first iteration.
-  constexpr int kRowsPerWarp = (kMaxGqa + kWarps - 1) / kWarps;
-  uint2 qraw[kRowsPerWarp];
-#pragma unroll
-  for (int k = 0; k < kRowsPerWarp; ++k)
-    if (warp + k * kWarps < r)
-      qraw[k] = *reinterpret_cast<const uint2*>(p.q + (qrow0 + warp + k * kWarps) * kHeadDim + 4 * lane);
 
   // sources of the warp's first iteration; iteration i adds 32*i tokens
   const uint8_t* k_src = p.k_codes + slice * p.k_codes_slice + (int64_t)ts0 * ROW;
@@ -432,6 +420,28 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
     }
     cp_async_arrive(smem_u32(&bars[warp][sidx]));
   };
+  // With p.early the warp's first stages are in flight before the wait on the previous
+  // kernel, except the stage that holds the new token T-1 of a fused step (its rows are
+  // written below, after the wait).
+  const bool owner = p.v_new != nullptr && t_begin <= T - 1 && T - 1 < t_end;
+  const int i_new = (owner && ts0 <= T - 1) ? (T - 1 - ts0) / kTok : -1;
+  if (p.early) {
+    for (int i = 0; i < min(NS, n_mine); ++i)
+      if (i != i_new) issue(i, i);
+  }
+  pdl_wait();  // above: shared memory and, with p.early, cache tiles the previous kernel does not write
+
+  // Query rows of this kv head for warp w: rows w, w + NW, ... (lane l: channels
+  // [4l, 4l+4)). Without p.early they are loaded before any stage copy is issued: behind
+  // the copies of all resident warps they would arrive only after the first stages, and
+  // the query fold (below) is on the path to the first iteration.
+  constexpr int kRowsPerWarp = (kMaxGqa + kWarps - 1) / kWarps;
+  uint2 qraw[kRowsPerWarp];
+#pragma unroll
+  for (int k = 0; k < kRowsPerWarp; ++k)
+    if (warp + k * kWarps < r)
+      qraw[k] = *reinterpret_cast<const uint2*>(p.q + (qrow0 + warp + k * kWarps) * kHeadDim + 4 * lane);
+
   // Fused decode step: the CTA whose range holds the new token T-1 appends it first
   // (value row quantized per group into its half of the pair row, key row into its
   // residual slot); the barrier orders those global writes before the copies.
@@ -454,7 +464,8 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
     }
     __syncthreads();
   }
-  for (int i = 0; i < min(NS, n_mine); ++i) issue(i, i);
+  for (int i = 0; i < min(NS, n_mine); ++i)
+    if (!p.early || i == i_new) issue(i, i);
 
   // Query rows (loaded above): each row goes to q_s (binary32, for residual keys) and, normalised by
   // 2^qe (qmax * 2^qe in [2^7, 2^8)) and divided by k_scale, to q2_s in key-pair order:

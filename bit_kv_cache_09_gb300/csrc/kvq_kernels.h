@@ -102,6 +102,9 @@ struct DecodeParams {
   int n_parts;        // partials merged through the workspace: n_split / cluster
   int sym;            // symmetric per-token int8 scheme (k_meta: one binary16 scale per token)
   int kout;           // symmetric scheme: isolated key entries per token (after the S_pad scales)
+  int early;          // tensor-core kernel: the first stages are copied before the wait on the
+                      // previous kernel of the stream (the caller guarantees it writes no cache
+                      // memory of this layer); queries and new rows are read after the wait
   int B, H, r, G, Gv, R_eff, n_vg;
   int log2G;          // G is a power of two
   int64_t S_pad, rowK, rowV;

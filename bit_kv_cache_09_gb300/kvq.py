@@ -21,9 +21,11 @@ STATUS_NAMES = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_UNSUPPORTED",
                 4: "KVQ_ERR_WORKSPACE", 5: "KVQ_ERR_CUDA"}
 BUFFER_NAMES = ("k_codes", "k_meta", "k_resid", "v_codes", "v_meta")
 DECODE_AUTO, DECODE_SIMT, DECODE_MMA = 0, 1, 2
+DECODE_EARLY_PREFETCH = 1  # flag bit of kvq_decode_attention_ex / kvq_decode_step_ex
 EXPORTED = ("kvq_buffer_sizes", "kvq_quantize_append", "kvq_dequantize", "kvq_decode_workspace_size",
             "kvq_decode_attention", "kvq_decode_attention_impl", "kvq_decode_num_splits", "kvq_status_string",
-            "kvq_version", "kvq_decode_attention_noalloc", "kvq_decode_step")
+            "kvq_version", "kvq_decode_attention_noalloc", "kvq_decode_step", "kvq_decode_attention_ex",
+            "kvq_decode_step_ex")
 
 
 class KVQError(RuntimeError):
@@ -76,6 +78,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.kvq_decode_step.argtypes = [cfgp, bufp, ctypes.c_int32, ctypes.c_int64, vp, vp, vp, ctypes.c_float, vp, vp,
                                       ctypes.c_size_t, vp]
         L.kvq_decode_step.restype = ctypes.c_int
+        L.kvq_decode_attention_ex.argtypes = L.kvq_decode_attention.argtypes + [ctypes.c_uint32]
+        L.kvq_decode_attention_ex.restype = ctypes.c_int
+        L.kvq_decode_step_ex.argtypes = L.kvq_decode_step.argtypes + [ctypes.c_uint32]
+        L.kvq_decode_step_ex.restype = ctypes.c_int
         L.kvq_decode_num_splits.argtypes = [cfgp, ctypes.c_int64]
         L.kvq_decode_num_splits.restype = ctypes.c_int32
         L.kvq_status_string.argtypes = [ctypes.c_int]
@@ -154,6 +160,22 @@ def kvq_decode_step(cfg: kvq_config, bufs: kvq_buffers, layer: int, s_cur: int, 
                     softmax_scale: float, out: int, ws: int, ws_bytes: int, stream: int = 0) -> None:
     _check("kvq_decode_step", load().kvq_decode_step(ctypes.byref(cfg), ctypes.byref(bufs), layer, s_cur, k_f16, v_f16,
                                                      q_f16, softmax_scale, out, ws, ws_bytes, stream))
+
+
+def kvq_decode_attention_ex(cfg: kvq_config, bufs: kvq_buffers, layer: int, s_cur: int, q_f16: int,
+                            softmax_scale: float, out: int, ws: int, ws_bytes: int, stream: int = 0,
+                            flags: int = 0) -> None:
+    _check("kvq_decode_attention_ex",
+           load().kvq_decode_attention_ex(ctypes.byref(cfg), ctypes.byref(bufs), layer, s_cur, q_f16, softmax_scale,
+                                          out, ws, ws_bytes, stream, flags))
+
+
+def kvq_decode_step_ex(cfg: kvq_config, bufs: kvq_buffers, layer: int, s_cur: int, k_f16: int, v_f16: int,
+                       q_f16: int, softmax_scale: float, out: int, ws: int, ws_bytes: int, stream: int = 0,
+                       flags: int = 0) -> None:
+    _check("kvq_decode_step_ex", load().kvq_decode_step_ex(ctypes.byref(cfg), ctypes.byref(bufs), layer, s_cur, k_f16,
+                                                           v_f16, q_f16, softmax_scale, out, ws, ws_bytes, stream,
+                                                           flags))
 
 
 def kvq_decode_attention_noalloc(cfg: kvq_config, bufs: kvq_buffers, layer: int, s_cur: int, q_f16: int,

@@ -187,6 +187,32 @@ kvq_status kvq_decode_step(const kvq_config* cfg, const kvq_buffers* bufs, int32
                            const void* k_f16, const void* v_f16, const void* q_f16, float softmax_scale, float* out,
                            void* ws, size_t ws_bytes, void* stream);
 
+/* Flag bits of kvq_decode_attention_ex and kvq_decode_step_ex (other bits:
+ * KVQ_ERR_INVALID_ARG).
+ * KVQ_DECODE_EARLY_PREFETCH: the tensor-core kernel starts copying this layer's cache
+ * tiles before the kernel launched just before it on `stream` has finished (with
+ * programmatic dependent launch the two overlap: this launch's first tiles stream in
+ * while the previous one merges its partials). The caller guarantees that this previous
+ * kernel writes no cache memory of `layer`; kernels before it have finished by then,
+ * because every launch of this library waits for its predecessor before it lets the
+ * next one start. Decode steps that visit the layers of a model in turn (n_layers > 1)
+ * meet the condition; a step that directly follows kvq_quantize_append or
+ * kvq_decode_step of the same layer does not. Queries and new key/value rows are always
+ * read after the wait. No counterpart in the pages: a scheduling choice of this library. */
+#define KVQ_DECODE_EARLY_PREFETCH 1u
+
+/* kvq_decode_attention with flag bits (0: identical to kvq_decode_attention). */
+kvq_status kvq_decode_attention_ex(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur,
+                                   const void* q_f16, float softmax_scale, float* out, void* ws, size_t ws_bytes,
+                                   void* stream, uint32_t flags);
+
+/* kvq_decode_step with flag bits (0: identical to kvq_decode_step). When the step takes
+ * two launches (the new token fills a residual window) the flag applies to neither: the
+ * attention launch reads what the append launch before it wrote. */
+kvq_status kvq_decode_step_ex(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur,
+                              const void* k_f16, const void* v_f16, const void* q_f16, float softmax_scale,
+                              float* out, void* ws, size_t ws_bytes, void* stream, uint32_t flags);
+
 /* Kernel choice for kvq_decode_attention_impl. AUTO is what kvq_decode_attention uses. */
 typedef enum {
   KVQ_DECODE_AUTO = 0,

@@ -152,6 +152,43 @@ def test_decode_argument_checks(lib):
     assert lib.kvq_dequantize(B(cfg), B(bufs), 0, 1001, 4096, 4096, None) == 3
 
 
+def test_decode_flag_checks(lib):
+    """Unknown flag bits of the _ex entry points are rejected on the host; the early-prefetch
+    bit passes the flag check and meets the same argument checks as the plain calls."""
+    cfg = good_cfg()
+    B = ctypes.byref
+    bufs = _bufs()
+    need = kvq.kvq_decode_workspace_size(cfg, 500)
+    att = lambda s, flags: lib.kvq_decode_attention_ex(B(cfg), B(bufs), 0, s, 4096, ctypes.c_float(0.088), 4096,  # noqa: E731
+                                                       4096, need, None, flags)
+    step = lambda s, flags: lib.kvq_decode_step_ex(B(cfg), B(bufs), 0, s, 4096, 4096, 4096, ctypes.c_float(0.088),  # noqa: E731
+                                                   4096, 4096, need, None, flags)
+    assert kvq.DECODE_EARLY_PREFETCH == 1
+    assert att(500, 2) == 1 and att(500, 0x80000000) == 1
+    assert step(499, 2) == 1 and step(499, 3) == 1
+    assert att(0, kvq.DECODE_EARLY_PREFETCH) == 1      # no tokens
+    assert att(1001, kvq.DECODE_EARLY_PREFETCH) == 3   # capacity
+    assert step(1000, kvq.DECODE_EARLY_PREFETCH) == 3  # capacity
+    assert step(-1, kvq.DECODE_EARLY_PREFETCH) == 1
+
+
+def test_early_prefetch_flag_follows_the_previous_launch():
+    """The cache object sets the early-prefetch bit unless its previous launch on the same
+    stream wrote the same layer (host logic only)."""
+    from bit_kv_cache_09_gb300.cache import QuantizedKVCache
+    c = QuantizedKVCache.__new__(QuantizedKVCache)
+    c._last = None
+    E = kvq.DECODE_EARLY_PREFETCH
+    assert c._early(7, 0, None) == E               # nothing launched yet
+    c._last = (7, 0, True)                          # wrote layer 0 on stream 7
+    assert c._early(7, 0, None) == 0
+    assert c._early(7, 1, None) == E                # another layer
+    assert c._early(8, 0, None) == E                # another stream
+    assert c._early(7, 1, False) == 0 and c._early(7, 0, True) == E   # explicit choice wins
+    c._last = (7, 0, False)                         # read layer 0 only
+    assert c._early(7, 0, None) == E
+
+
 def test_status_strings(lib):
     for s in range(6):
         assert kvq.kvq_status_string(s)

@@ -539,3 +539,48 @@ def test_outlier_selection_on_adversarial_rows():
                 ref = oracle_attention(st, q_host[b, h * w.gqa:(h + 1) * w.gqa], cache, softmax_scale(w))
                 err = float(np.abs(out[b, h * w.gqa:(h + 1) * w.gqa] - ref).max())
                 assert err <= ATOL, (b, h, T + 1, err)
+
+
+@pytest.mark.parametrize("kind", ["asym4", "int8", "sym8o4"])
+def test_layer_interleaved_decode_with_early_prefetch(kind):
+    """Decode steps that visit three layers in turn, as a model does: every launch after the
+    first starts streaming its cache tiles before the previous layer's kernel has finished
+    (KVQ_DECODE_EARLY_PREFETCH, set by the cache object). The asymmetric case fills a
+    residual window during the steps (the two-launch path, which runs without the flag).
+    Every layer's cache state bit-exact and its attention within 2e-3 at every step, then
+    an attention-only pass over the layers."""
+    cfg = {
+        "asym4": dict(bits=4, G=32, Gv=64, R=64, r=4, B=2, H=2, S=250, steps=8),
+        "int8": dict(bits=8, G=128, Gv=128, R=0, r=4, B=1, H=4, S=500, steps=4),
+        "sym8o4": dict(bits=8, G=128, Gv=128, R=0, r=4, B=2, H=2, S=300, steps=4, symmetric=1, k_outliers=4),
+    }[kind]
+    w = small_workload(L=3, seed=9200 + len(kind), **cfg)
+    cache = QuantizedKVCache.for_workload(w)
+    host = [host_layer_inputs(w, layer, 0, w.max_seq) for layer in range(w.n_layers)]
+    S = w.seq
+    for layer in range(w.n_layers):
+        cache.append(layer, 0, _dev(host[layer][0][:, :S]), _dev(host[layer][1][:, :S]))
+    stream = torch.cuda.current_stream().cuda_stream
+    flushed = False
+    for s in range(w.steps):
+        T = S + s
+        for layer in range(w.n_layers):
+            assert cache._early(stream, layer, None) == kvq.DECODE_EARLY_PREFETCH
+            k_host, v_host = host[layer]
+            flushed |= not w.symmetric and (T + 1) % max(w.residual, w.k_group) == 0
+            q_host = synth.gen_q(w.seed, layer, range(w.batch), T, w.n_q, w.d_head)
+            out = cache.decode_step(layer, T, _dev(k_host[:, T:T + 1]), _dev(v_host[:, T:T + 1]), _dev(q_host),
+                                    softmax_scale(w)).cpu().numpy()
+            for b in range(w.batch):
+                for h in range(w.n_kv):
+                    st = oracle_slice_state(k_host[b, :T + 1, h], v_host[b, :T + 1, h], cache)
+                    ref = oracle_attention(st, q_host[b, h * w.gqa:(h + 1) * w.gqa], cache, softmax_scale(w))
+                    err = float(np.abs(out[b, h * w.gqa:(h + 1) * w.gqa] - ref).max())
+                    assert err <= ATOL, (kind, layer, b, h, T + 1, err)
+    assert flushed == (kind == "asym4")
+    T = S + w.steps
+    for layer in range(w.n_layers):
+        _check_all_slices(cache, w, layer, T, *host[layer])
+    for layer in range(w.n_layers):
+        q_host = synth.gen_q(w.seed, layer, range(w.batch), T - 1, w.n_q, w.d_head)
+        _check_attention(cache, w, layer, T, *host[layer], q_host, kvq.DECODE_AUTO)
