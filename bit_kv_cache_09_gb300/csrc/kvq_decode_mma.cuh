@@ -430,6 +430,10 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
       if (i != i_new) issue(i, i);
   }
   pdl_wait();  // above: shared memory and, with p.early, cache tiles the previous kernel does not write
+  // The next kernel of the stream may launch its CTAs once every CTA of this grid is past
+  // its wait (so the kernel before this one has finished): they take SM slots as this
+  // grid's CTAs exit, rather than after the slowest CTA's loop.
+  pdl_allow_dependents();
 
   // Query rows of this kv head for warp w: rows w, w + NW, ... (lane l: channels
   // [4l, 4l+4)). Without p.early they are loaded before any stage copy is issued: behind
@@ -903,7 +907,6 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
     }
   }
 
-  pdl_allow_dependents();  // the next kernel of the stream may start its prologue
   if (failed_at >= 0) {
     // a stage never completed: flag it and drain (bounded) what is still in flight
     if (lane == 0) atomicOr(p.err, 1u);
