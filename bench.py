@@ -261,6 +261,13 @@ def cpu_desc():
     return "unknown"
 
 
+def workload_config(w, L: int, S: int) -> dict:
+    """The workload keys of `config`, shared by both arms' lines."""
+    return {"workload": w.name, "layers": L, "batch": w.batch, "n_kv_heads": w.n_kv, "gqa": w.gqa,
+            "d_head": w.d_head, "prompt_tokens": S, "bits": w.bits, "v_bits": w.vbits, "symmetric": w.symmetric,
+            "k_outliers": w.k_outliers, "k_group": w.k_group, "v_group": w.v_group, "residual": w.residual}
+
+
 def run_reference(args, w):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -281,7 +288,8 @@ def run_reference(args, w):
     line = {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "layers_timed": 1, "T": T, "sample": f"{slices} (batch row, kv head) slices of layer 0 per step"},
+            "config": {**workload_config(w, w.n_layers, w.seq), "layers_timed": 1, "T": T,
+                       "sample": f"{slices} (batch row, kv head) slices of layer 0 per step"},
             "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": f"oracle decode attention (dequantize packed slice + float64 softmax attention) over {slices} (b,h) slices of layer 0 at T={T}; CPU {cpu_desc()}"},
             "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -518,9 +526,7 @@ def main():
                           f"int{w.bits} codes" if w.vbits == w.bits else f"int{w.bits} key / int{w.vbits} value codes")
                 + ", f32 math", "data": "synthetic",
                 "tokens_per_s": round(tok_s, 1), "pct_of_peak": round(100 * gbs / world / peak, 2),
-                "config": {"workload": w.name, "layers": L, "batch": w.batch, "n_kv_heads": w.n_kv, "gqa": w.gqa,
-                           "d_head": w.d_head, "prompt_tokens": S, "bits": w.bits, "v_bits": w.vbits, "symmetric": w.symmetric, "k_outliers": w.k_outliers, "k_group": w.k_group,
-                           "v_group": w.v_group, "residual": w.residual, "decode": args.decode,
+                "config": {**workload_config(w, L, S), "decode": args.decode,
                            "cuda_graph": use_graph, "parallelism": f"replicas x{world}",
                            "l2": "per-step working set (all layers' packed cache) exceeds the 129 MB L2; no flush"},
                 "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
