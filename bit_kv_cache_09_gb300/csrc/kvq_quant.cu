@@ -329,7 +329,7 @@ __global__ void __launch_bounds__(256) k_token_sym_outlier_kernel(AppendParams p
   const int64_t t = p.s_cur + tt;
   const int64_t slice = (int64_t)b * p.H + h;
   uint8_t* kmb = reinterpret_cast<uint8_t*>(p.k_meta) + slice * p.k_meta_slice;
-  quantize_key_row_sym(p.k_in + w * kHeadDim, p.k_codes + slice * p.k_codes_slice + t * p.rowK,
+  quantize_key_row_sym<true>(p.k_in + w * kHeadDim, p.k_codes + slice * p.k_codes_slice + t * p.rowK,
                        reinterpret_cast<__half*>(kmb) + t, reinterpret_cast<uint32_t*>(kmb + p.S_pad * 2) + t * p.kout,
                        p.kout, lane);
 }

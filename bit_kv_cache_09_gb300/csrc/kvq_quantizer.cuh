@@ -159,6 +159,42 @@ __device__ __forceinline__ void quantize_value_row(const __half* v_row, uint16_t
   __syncwarp();
 }
 
+// The 64th smallest (index 63 in ascending order) of the warp's 128 keys, lane l holding
+// elements 4l .. 4l + 3: a bitonic sorting network over the 128 positions (Batcher),
+// compare-exchanges at distance 1 and 2 inside a lane, at distance 4j across lanes l and
+// l ^ j with a shuffle; position 63 is element 3 of lane 15 after the last stage.
+__device__ __forceinline__ uint32_t sorted_key_63(const uint32_t (&key_in)[4], int lane) {
+  uint32_t a[4] = {key_in[0], key_in[1], key_in[2], key_in[3]};
+#pragma unroll
+  for (int k = 2; k <= 128; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (j >= 4) {
+        const int lj = j >> 2;                         // partner lane distance
+        const bool up = k == 128 || ((lane & (k >> 2)) == 0);  // this block sorts ascending
+        const bool low = (lane & lj) == 0;             // this lane holds the lower positions
+        const bool keep_min = (up == low);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t o = __shfl_xor_sync(0xffffffffu, a[e], lj);
+          a[e] = keep_min ? min(a[e], o) : max(a[e], o);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (e & j) continue;                         // e is the lower position of the pair (e, e + j)
+          const int i = 4 * lane + e;
+          const bool up = (i & k) == 0;
+          const uint32_t lo = min(a[e], a[e + j]), hi = max(a[e], a[e + j]);
+          a[e] = up ? lo : hi;
+          a[e + j] = up ? hi : lo;
+        }
+      }
+    }
+  }
+  return __shfl_sync(0xffffffffu, a[3], 15);
+}
+
 // One warp quantizes one key row of the symmetric per-token scheme (binary16, 128
 // channels; lane l holds channels [4l, 4l+4)): its binary16 scale to *scale_out and its
 // 8-bit codes, in channel order, to key_row. With kout > 0 the row's kout entries
@@ -166,7 +202,11 @@ __device__ __forceinline__ void quantize_value_row(const __half* v_row, uint16_t
 // distance, ties to the lower channel; "Sub-8-Bit KV Cache Quantization Is Not a Free
 // Lever for an RDNA4 Agent Swarm", § What the low-bit numbers actually cost: per-vector
 // dense-and-sparse quantization) go to entries[0 .. kout) as channel | binary16 << 16
-// and are replaced by 0 before the scale is taken.
+// and are replaced by 0 before the scale is taken. SORT picks how the lower median is
+// found: a bitonic sort of the row's 128 order keys (fewer instructions; the append
+// kernel) or a radix select with warp ballots (the fused decode step); both give the
+// exact 64th smallest value.
+template <bool SORT = false>
 __device__ __forceinline__ void quantize_key_row_sym(const __half* k_row, uint8_t* key_row, __half* scale_out,
                                                      uint32_t* entries, int kout, int lane) {
   float x[4];
@@ -182,17 +222,21 @@ __device__ __forceinline__ void quantize_key_row_sym(const __half* k_row, uint8_
 #pragma unroll
     for (int e = 0; e < 4; ++e) key[e] = (xb[e] & 0x8000u) ? (~xb[e] & 0xFFFFu) : (xb[e] | 0x8000u);
     uint32_t prefix = 0;
-    int rank = 63;
+    if constexpr (SORT) {
+      prefix = sorted_key_63(key, lane);
+    } else {
+      int rank = 63;
 #pragma unroll
-    for (int bit = 15; bit >= 0; --bit) {
-      const uint32_t above = (0xFFFFu << (bit + 1)) & 0xFFFFu;  // the bits already decided
-      int n0 = 0;
+      for (int bit = 15; bit >= 0; --bit) {
+        const uint32_t above = (0xFFFFu << (bit + 1)) & 0xFFFFu;  // the bits already decided
+        int n0 = 0;
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        n0 += __popc(__ballot_sync(0xffffffffu, ((key[e] ^ prefix) & above) == 0u && ((key[e] >> bit) & 1u) == 0u));
-      if (rank >= n0) {
-        rank -= n0;
-        prefix |= 1u << bit;
+        for (int e = 0; e < 4; ++e)
+          n0 += __popc(__ballot_sync(0xffffffffu, ((key[e] ^ prefix) & above) == 0u && ((key[e] >> bit) & 1u) == 0u));
+        if (rank >= n0) {
+          rank -= n0;
+          prefix |= 1u << bit;
+        }
       }
     }
     const uint32_t med_bits = (prefix & 0x8000u) ? (prefix & 0x7FFFu) : (~prefix & 0xFFFFu);
