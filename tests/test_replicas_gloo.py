@@ -75,3 +75,33 @@ def test_single_rank_is_identity():
 
     assert bench.max_over_ranks(3.5) == 3.5
     assert bench.whole_job_rate(10, 1, 2.0) == 5.0
+
+
+def test_reference_arm_line_on_rank_0(capsys, monkeypatch):
+    """Rank 0 of the reference arm times the oracle and prints one JSON line with the
+    contract's keys, the same workload config keys as the GPU arm, and its e2e block."""
+    sys.path.insert(0, ROOT)
+    import json
+
+    import bench
+    import synth
+
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setenv("KVQ_REF_SLICES", "1")
+
+    class A:
+        steps, warmup, gpus = 1, 1, 1
+
+    w = synth.WORKLOADS["tiny-int8"]
+    assert bench.run_reference(A(), w) == 0
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["value"] > 0 and d["higher_is_better"] is True
+    assert {k: d["config"][k] for k in bench.workload_config(w, w.n_layers, w.seq)} == \
+        bench.workload_config(w, w.n_layers, w.seq)
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    assert d["e2e"]["value"] == d["value"] and d["e2e"]["h2d_bytes_per_step"] == 0
