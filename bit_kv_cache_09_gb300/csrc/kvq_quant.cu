@@ -7,8 +7,9 @@
 // two distributions, not one). Every floating-point step is one explicitly rounded
 // binary32 intrinsic (this file is also compiled with -fmad=false), so codes, scales
 // and zero points are reproducible bit for bit:
-//   s_h = binary16_round_up((x_max - x_min) / (q_max - q_min))
-//   zp  = clamp(q_min - rint(x_min / s_h), +-65504) -> binary16 (nearest even)
+//   s_h = binary16_round_up(max((x_max - x_min) / (q_max - q_min),
+//                               max|x| / (2048 - 2^bits)))
+//   zp  = q_min - rint(x_min / s_h) -> binary16 (an integer of magnitude <= 2048: exact)
 //   u   = clamp(rint(x / s_h) + zp, q_min, q_max) - q_min
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>

@@ -5,8 +5,9 @@
 // 4-bit", § Integer quantization in one screen. Every floating-point step is one
 // explicitly rounded binary32 intrinsic, so no compiler contraction can change a
 // result and codes, scales and zero points are reproducible bit for bit:
-//   s_h = binary16_round_up((x_max - x_min) / (q_max - q_min))
-//   zp  = clamp(q_min - rint(x_min / s_h), +-65504) -> binary16 (nearest even)
+//   s_h = binary16_round_up(max((x_max - x_min) / (q_max - q_min),
+//                               max|x| / (2048 - 2^bits)))
+//   zp  = q_min - rint(x_min / s_h) -> binary16 (an integer of magnitude <= 2048: exact)
 //   u   = clamp(rint(x / s_h) + zp, q_min, q_max) - q_min
 #pragma once
 
@@ -67,12 +68,17 @@ __device__ __forceinline__ void group_params(float xmin, float xmax, __half& s_h
     s_h = __float2half_rn(1.0f);  // all zeros: scale 1
   } else {
     const float range = __fsub_rn(xmax, xmin);
-    s_h = __float2half_ru(div_rn(range, __fsub_rn(Q<BITS>::qmax, Q<BITS>::qmin), inv_levels<BITS>()));
+    float s32 = div_rn(range, __fsub_rn(Q<BITS>::qmax, Q<BITS>::qmin), inv_levels<BITS>());
+    // binary16 holds every integer only up to 2048: a narrow group far from zero gets the
+    // wider scale max|x| / (2048 - 2^BITS), so that |x / scale| <= 2048 - 2^BITS and the
+    // zero point (|zp| <= 2048 - 2^(BITS-1)) is stored exactly
+    const float s_far = __fdiv_rn(fmaxf(fabsf(xmin), fabsf(xmax)), (float)(2048 - (1 << BITS)));
+    s32 = fmaxf(s32, s_far);
+    s_h = __float2half_ru(s32);
   }
   s = __half2float(s_h);
   rs = __frcp_rn(s);
-  float z = __fsub_rn(Q<BITS>::qmin, rintf(div_rn(xmin, s, rs)));
-  z = fminf(fmaxf(z, -65504.0f), 65504.0f);
+  const float z = __fsub_rn(Q<BITS>::qmin, rintf(div_rn(xmin, s, rs)));  // an integer, |z| <= 2048
   z_h = __float2half_rn(z);
   zp = __half2float(z_h);
 }

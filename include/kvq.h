@@ -23,12 +23,15 @@
  *
  * Arithmetic (bit-exact contract of the quantizer)
  *   All of it in IEEE binary32, round to nearest even, no contraction:
- *   range = x_max - x_min; s32 = range / (q_max - q_min); the stored scale is
- *   binary16(s32) rounded toward +infinity; zp = q_min - rint(x_min / scale), clamped to
- *   +-65504 and stored as binary16 (nearest even); q = clamp(rint(x / scale) + zp).
- *   A group whose values are all equal is widened to include 0; an all-zero group
- *   gets scale 1. Codes are stored as u = q - q_min (unsigned, b bits). Keys use b =
- *   bits, values b = v_bits (the same unless v_bits says otherwise: 8-bit keys with
+ *   range = x_max - x_min; s32 = max(range / (q_max - q_min), max|x| / (2048 - 2^b));
+ *   the stored scale is binary16(s32) rounded toward +infinity; zp = q_min -
+ *   rint(x_min / scale), an integer of magnitude <= 2048 and so exact in binary16;
+ *   q = clamp(rint(x / scale) + zp). The second term of s32 only matters for a narrow
+ *   group far from zero, whose zero point would otherwise exceed the integers binary16
+ *   holds exactly; with it |x - x_hat| <= scale/2 holds for every group. A group whose
+ *   values are all equal is widened to include 0; an all-zero group gets scale 1.
+ *   Codes are stored as u = q - q_min (unsigned, b bits). Keys use b = bits, values
+ *   b = v_bits (the same unless v_bits says otherwise: 8-bit keys with
  *   4-bit values is the mixed recipe of "KV Cache Quantization — 8-bit and 4-bit",
  *   § Why keys and values want different treatment).
  *

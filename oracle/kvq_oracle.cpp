@@ -27,8 +27,10 @@
 //   round()          -> round half to even, in binary32.
 //   stored scale     -> binary16, rounded toward +infinity from the binary32 quotient,
 //                       and the quantizer divides by that stored value.
-//   zero point       -> binary16 (round to nearest even, clamped to +-65504), and the
-//                       quantizer adds that stored value.
+//   zero point       -> binary16 (an integer, exact there), and the quantizer adds
+//                       that stored value; a narrow group far from zero, whose zero
+//                       point would exceed the binary16 integers (2048), gets the
+//                       wider scale max|x| / (2048 - 2^bits) instead.
 //   q = clamp(round(x/scale) + zero_point, q_min, q_max), codes kept as u = q - q_min.
 //   int2 range       -> [-2, 1].
 //   degenerate group -> if x_max == x_min widen the range to include 0; if it is still
@@ -44,8 +46,9 @@
 //
 // Parity pins: see tests/test_oracle_pins.py. The packed byte layout and the
 // residual/flush bookkeeping are this project's own definitions (the pages fix
-// neither): parity unpinned for the layout, which is checked only for
-// self-consistency (pack/unpack round trip, chunking invariance).
+// neither). The layout functions are pinned against bytes derived by hand from the
+// layout's written rules (tests/golden/layout_bytes.json); the flush bookkeeping by
+// chunking invariance and the residual-window tests.
 
 #include <algorithm>
 #include <cmath>
@@ -175,13 +178,19 @@ int orc_quant_params(const uint16_t* x, int64_t n, int64_t stride, int bits, uin
   } else {
     float range = xmax - xmin;                  // binary32, nearest-even
     float s32 = range / (float)(qmax - qmin);   // binary32, nearest-even
+    // The zero point is stored in binary16, which holds every integer only up to 2048.
+    // A narrow group far from zero would need a larger one, so its scale is widened to
+    // max|x| / (2048 - 2^bits): then |x / scale| <= 2048 - 2^bits for every x of the
+    // group, |zero_point| <= 2048 - 2^(bits-1) is stored exactly, and the half-step
+    // bound |x - x_hat| <= scale/2 holds with the stored (wider) scale.
+    float amax = std::fabs(xmin) > std::fabs(xmax) ? std::fabs(xmin) : std::fabs(xmax);
+    float s_far = amax / (float)(2048 - (1 << bits));  // binary32, nearest-even
+    if (s_far > s32) s32 = s_far;
     s_h = orc_f16_from_f32_ru(s32);             // stored scale, rounded up
   }
   float s = orc_f32_from_f16(s_h);
   float t = xmin / s;
-  float zp = (float)qmin - rne_integral(t);
-  if (zp > 65504.0f) zp = 65504.0f;
-  if (zp < -65504.0f) zp = -65504.0f;
+  float zp = (float)qmin - rne_integral(t);     // an integer of magnitude <= 2048
   *scale_h = s_h;
   *zp_h = orc_f16_from_f32_rne(zp);
   return 0;
@@ -227,7 +236,7 @@ double orc_kv_bytes(int64_t L, int64_t n_kv, int64_t d_head, int64_t S, double b
 }
 
 // ---------------------------------------------------------------------------
-// Packed layout (this project's definition; parity unpinned).
+// Packed layout (this project's definition; pinned by hand-derived bytes).
 //   Key row (one token, d channels): channel c occupies bits [c*b, c*b + b) of the
 //   row, little-endian bytes, low bits first.
 //   Value rows: channel c is stored at position

@@ -162,49 +162,73 @@ def test_error_bound_half_step(bits):
         xhat = np.array([oracle.dequantize_value(int(v), bits, sh, zh) for v in u], np.float64)
         err = np.abs(xd - xhat)
         zp = float(np.uint16(zh).view(np.float16))
-        if abs(zp) <= 2048:
-            if xd.max() > xd.min():  # (a constant group is widened to include 0)
-                assert u[int(np.argmin(xd))] == 0  # the smallest value lands on q_min
-            assert err.max() <= s / 2 * (1 + 2.0**-20) + 1e-30, (bits, err.max(), s)
-        else:
-            # binary16 holds integers exactly only up to 2048: the stored zero point may be
-            # one step off, which moves one end of the group into the clamp (see below)
-            # stored zero point off by up to half its binary16 spacing: self-consistency only
-            assert np.array_equal(xhat, (np.float32(s) * (u.astype(np.float32) + qmin - np.float32(zp))).astype(np.float64))
+        assert abs(zp) <= 2048 and zp == int(zp)  # an exact binary16 integer
+        if xd.max() > xd.min():  # (a constant group is widened to include 0)
+            assert u[int(np.argmin(xd))] == 0  # the smallest value lands on q_min
+        assert err.max() <= s / 2 * (1 + 2.0**-20) + 1e-30, (bits, err.max(), s)
 
 
-def test_zero_point_beyond_binary16_integers():
-    """A narrow group far from zero needs |zero_point| > 2048, which binary16 stores
-    only to the nearest even integer; quantization then stays self-consistent with
-    the stored value (x_hat = scale * (q - zp_h)) and within one step and a half."""
-    x = _f16(7.0 + 2.0**-8 * np.array([-1, 0, 1, 1, 0, -1, 0, 1]))  # three neighbouring binary16 values
-    sh, zh = oracle.quant_params(x, 2)
-    s = float(np.uint16(sh).view(np.float16))
-    zp = float(np.uint16(zh).view(np.float16))
-    assert abs(zp) > 2048 and zp % 2 == 0
-    u = oracle.quantize_values(x, 2, sh, zh)
-    for xi, ui in zip(x.astype(np.float64), u):
-        xhat = oracle.dequantize_value(int(ui), 2, sh, zh)
-        assert xhat == np.float32(s) * np.float32(int(ui) - 2 - zp)
-        assert abs(xhat - xi) <= 1.5 * s
+def test_narrow_groups_far_from_zero_keep_the_half_step_bound(golden_dir):
+    """Hand-derived groups whose zero point would exceed the binary16 integers under the
+    range rule alone: the widened scale max|x| / (2048 - 2^bits) (tests/golden/
+    quant_far_from_zero.json) keeps the zero point exact and |x - x_hat| <= scale/2."""
+    g = json.load(open(os.path.join(golden_dir, "quant_far_from_zero.json")))
+    for case in g["cases"]:
+        bits = case["bits"]
+        x = _f16(case["x"])
+        sh, zh = oracle.quant_params(x, bits)
+        assert sh == int(case["scale_f16"], 16) and zh == int(case["zp_f16"], 16), (bits, hex(sh), hex(zh))
+        u = oracle.quantize_values(x, bits, sh, zh)
+        assert u.tolist() == case["u"]
+        s = float(np.uint16(sh).view(np.float16))
+        for xi, ui in zip(x.astype(np.float64), u):
+            assert abs(oracle.dequantize_value(int(ui), bits, sh, zh) - xi) <= s / 2
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_near_constant_groups_anywhere_keep_the_half_step_bound(bits):
+    """Groups of two or three neighbouring binary16 values at every magnitude from 2^-10
+    to 60000, both signs: the stored zero point is an exact integer and every value is
+    within half a (stored) step of its reconstruction."""
+    for e in range(-10, 16):
+        for sign in (1.0, -1.0):
+            c = np.float16(sign * 1.37 * 2.0**e)
+            up = np.nextafter(c, np.float16(np.inf))
+            dn = np.nextafter(c, np.float16(-np.inf))
+            for grp in ([c, up], [dn, c, up], [c, c, up, c]):
+                x = _f16(grp)
+                if not np.isfinite(x.astype(np.float64)).all():
+                    continue
+                sh, zh = oracle.quant_params(x, bits)
+                s = float(np.uint16(sh).view(np.float16))
+                zp = float(np.uint16(zh).view(np.float16))
+                assert abs(zp) <= 2048 and zp == int(zp)
+                u = oracle.quantize_values(x, bits, sh, zh)
+                for xi, ui in zip(x.astype(np.float64), u):
+                    assert abs(oracle.dequantize_value(int(ui), bits, sh, zh) - xi) <= s / 2 * (1 + 2.0**-20)
 
 
 @pytest.mark.parametrize("bits", [2, 4, 8])
 def test_scale_is_range_over_levels_rounded_up(bits):
-    """scale = (x_max - x_min)/(q_max - q_min), stored in binary16 rounded up."""
+    """scale = (x_max - x_min)/(q_max - q_min), stored in binary16 rounded up; a narrow
+    group far from zero takes max|x| / (2048 - 2^bits) when that is larger."""
     rng = np.random.default_rng(200 + bits)
     N = oracle.qmax(bits) - oracle.qmin(bits)
+    widened = 0
     for x in _groups(rng, 200, 64):
         xd = x.astype(np.float64)
         if xd.max() == xd.min():
             continue  # constant groups follow the widening rule (test_degenerate_groups)
-        exact = (xd.max() - xd.min()) / N
+        far = np.abs(xd).max() / (2048 - 2**bits)
+        exact = max((xd.max() - xd.min()) / N, far)
+        widened += far > (xd.max() - xd.min()) / N
         sh, _ = oracle.quant_params(x, bits)
         s = np.uint16(sh).view(np.float16)
         below = np.float64(np.nextafter(s, np.float16(-np.inf)))
         # rounded up from a binary32 quotient: within one binary16 step above, never a step below
         assert float(s) >= exact * (1 - 2.0**-22)
         assert below < exact * (1 + 2.0**-22)
+    assert widened > 0  # the narrow groups around 7.0 take the wider scale
 
 
 def test_degenerate_groups():
@@ -376,6 +400,54 @@ def test_residual_window_keeps_newest_tokens_in_f16():
     # R = 0: the residual holds T mod G tokens
     st0 = oracle.cache_state(k16, v16, d=d, bits=bits, G=G, Gv=Gv, R=0)
     assert st0.Tq == (T // G) * G
+
+
+# ----------------------------------------------------------------------------- packed layout against its written rules
+def _golden_layout(golden_dir):
+    return json.load(open(os.path.join(golden_dir, "layout_bytes.json")))
+
+
+def test_key_rows_match_hand_derived_bytes(golden_dir):
+    """Key rows packed by the oracle against bytes derived by hand from the layout text
+    (tests/golden/layout_bytes.json): bit order inside a byte, byte order, code width."""
+    d = 128
+    for case in _golden_layout(golden_dir)["k_rows"]:
+        bits = case["bits"]
+        nbytes = d * bits // 8
+        if "pattern" in case:
+            c = np.arange(d)
+            u = {"c": c, "c % 16": c % 16, "(c + c // 4) % 4": (c + c // 4) % 4}[case["pattern"]].astype(np.uint8)
+            if case.get("bytes_hex") == "range":
+                want = np.arange(nbytes, dtype=np.uint8)
+            else:
+                per = [int(x, 16) for x in case["period"]]
+                want = np.array([per[k % len(per)] for k in range(nbytes)], np.uint8)
+        else:
+            u = np.zeros(d, np.uint8)
+            for ch, code in case["codes"].items():
+                u[int(ch)] = code
+            want = np.zeros(nbytes, np.uint8)
+            for k, v in case["nonzero"].items():
+                want[int(k)] = int(v, 16)
+        got = oracle.pack_k_row(u, d, bits)
+        assert np.array_equal(got, want), (case["name"], np.flatnonzero(got != want)[:8])
+
+
+def test_value_pair_rows_match_hand_derived_bytes(golden_dir):
+    """One-hot value tokens packed into a pair row against hand-derived bytes: the
+    channel permutation pos(c), the bit position inside the row, and which 16-bit half
+    of each word the even and the odd token take."""
+    d = 128
+    for case in _golden_layout(golden_dir)["v_pairs"]:
+        bits = case["bits"]
+        u = np.zeros(d, np.uint8)
+        u[case["channel"]] = case["code"]
+        pairs = np.zeros(2 * d * bits // 8, np.uint8)
+        oracle.pack_v_token(u, d, bits, 0 + case["odd"], pairs)
+        want = np.zeros_like(pairs)
+        for k, v in case["nonzero"].items():
+            want[int(k)] = int(v, 16)
+        assert np.array_equal(pairs, want), (case, np.flatnonzero(pairs)[:4], pairs[np.flatnonzero(pairs)[:4]])
 
 
 # ----------------------------------------------------------------------------- layout self-consistency (parity unpinned)
