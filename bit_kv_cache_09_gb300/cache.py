@@ -57,6 +57,14 @@ class QuantizedKVCache:
                          and self._last[2])
         return kvq.DECODE_EARLY_PREFETCH if early else 0
 
+    def check_errors(self) -> None:
+        """Raise KVQDeviceError if a decode launch since the last check recorded a
+        device-side error (a bounded wait that ran out); clears the word. Synchronizes
+        the current stream."""
+        word = kvq.kvq_decode_error(self.ws.data_ptr(), self.ws.numel(), self._stream())
+        if word:
+            raise kvq.KVQDeviceError(word)
+
     def append(self, layer: int, s_cur: int, k: torch.Tensor, v: torch.Tensor) -> None:
         """k, v: [batch][n_new][n_kv_heads][d_head] float16 on the device."""
         assert k.dtype == torch.float16 and v.dtype == torch.float16 and k.is_contiguous() and v.is_contiguous()
@@ -75,8 +83,9 @@ class QuantizedKVCache:
         return k_out, v_out
 
     def attention(self, layer: int, s_cur: int, q: torch.Tensor, softmax_scale: float, out: torch.Tensor = None,
-                  impl: int = kvq.DECODE_AUTO, early=None) -> torch.Tensor:
-        """q: [batch][n_q][d_head] float16; returns out [batch][n_q][d_head] float32."""
+                  impl: int = kvq.DECODE_AUTO, early=None, flags: int = 0) -> torch.Tensor:
+        """q: [batch][n_q][d_head] float16; returns out [batch][n_q][d_head] float32.
+        flags: extra kvq_decode_attention_ex flag bits (KVQ_DECODE_ZERO_WAIT_LIMIT)."""
         assert q.dtype == torch.float16 and q.is_contiguous()
         if out is None:
             out = torch.empty(q.shape, dtype=torch.float32, device=self.device)
@@ -84,7 +93,7 @@ class QuantizedKVCache:
         if impl == kvq.DECODE_AUTO:
             kvq.kvq_decode_attention_ex(self.cfg, self.bufs, layer, s_cur, q.data_ptr(), softmax_scale,
                                         out.data_ptr(), self.ws.data_ptr(), self.ws.numel(), stream,
-                                        self._early(stream, layer, early))
+                                        self._early(stream, layer, early) | flags)
         else:
             kvq.kvq_decode_attention_impl(self.cfg, self.bufs, layer, s_cur, q.data_ptr(), softmax_scale,
                                           out.data_ptr(), self.ws.data_ptr(), self.ws.numel(), stream, impl)

@@ -311,15 +311,17 @@ int32_t kvq_decode_num_splits(const kvq_config* cfg, int64_t s_cur) {
 
 }  // extern "C"
 
-namespace {
+namespace kvq {
 
-// Checks and launches decode attention over s_cur tokens; when k_new/v_new are given
-// (tensor-core kernel only) the kernel first appends token s_cur - 1 itself. early: the
-// tensor-core kernel copies its first cache tiles before waiting on the previous kernel
-// of the stream (KVQ_DECODE_EARLY_PREFETCH).
-kvq_status decode_launch(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur,
-                         const void* q_f16, float softmax_scale, float* out, void* ws, size_t ws_bytes, void* stream,
-                         kvq_decode_impl impl, const void* k_new, const void* v_new, bool early) {
+// Checks a decode-attention call over s_cur tokens and fills its launch description;
+// launches nothing. When k_new/v_new are given (tensor-core kernel only) the kernel
+// first appends token s_cur - 1 itself. early: the tensor-core kernel copies its first
+// cache tiles before waiting on the previous kernel of the stream
+// (KVQ_DECODE_EARLY_PREFETCH). wait_ns: time limit of the kernel's bounded waits.
+kvq_status decode_prepare(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur,
+                          const void* q_f16, float softmax_scale, float* out, void* ws, size_t ws_bytes,
+                          kvq_decode_impl impl, const void* k_new, const void* v_new, bool early, uint64_t wait_ns,
+                          DecodeCall* call) {
   Geometry g;
   kvq_status st = kvq::make_geometry(cfg, &g);
   if (st != KVQ_OK) return st;
@@ -332,8 +334,13 @@ kvq_status decode_launch(const kvq_config* cfg, const kvq_buffers* bufs, int32_t
   if (s_cur > g.S_max) return KVQ_ERR_CAPACITY;
   const kvq::WorkspaceLayout wl = kvq::workspace_layout(g, s_cur);
   if (!aligned16(ws) || ws_bytes < wl.total) return KVQ_ERR_WORKSPACE;
+  const kvq_decode_impl use = impl == KVQ_DECODE_SIMT ? KVQ_DECODE_SIMT : KVQ_DECODE_MMA;
+  if (use == KVQ_DECODE_SIMT && (k_new || v_new)) return KVQ_ERR_UNSUPPORTED;
+  if (use == KVQ_DECODE_SIMT && g.vbits != g.bits) return KVQ_ERR_UNSUPPORTED;  // CUDA-core kernel: equal widths
+  if (use == KVQ_DECODE_SIMT && g.sym) return KVQ_ERR_UNSUPPORTED;              // and the asymmetric scheme
   const LayerPtrs lp = layer_ptrs(g, bufs, layer);
-  kvq::DecodeParams p;
+  kvq::DecodeParams& p = call->p;
+  p = kvq::DecodeParams{};
   p.k_codes = lp.k_codes;
   p.k_meta = lp.k_meta;
   p.k_resid = lp.k_resid;
@@ -349,6 +356,7 @@ kvq_status decode_launch(const kvq_config* cfg, const kvq_buffers* bufs, int32_t
   p.k_meta_w = lp.k_meta;
   p.out = out;
   p.err = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + wl.err_off);
+  p.wait_ns = wait_ns;
   p.tickets = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + wl.tickets_off);
   p.ws_ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) + wl.ml_off);
   p.ws_o = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + wl.o_off);
@@ -371,10 +379,6 @@ kvq_status decode_launch(const kvq_config* cfg, const kvq_buffers* bufs, int32_t
   p.kout = g.kout;
   p.v_codes_slice = g.v_codes_slice;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
-  const kvq_decode_impl use = impl == KVQ_DECODE_SIMT ? KVQ_DECODE_SIMT : KVQ_DECODE_MMA;
-  if (use == KVQ_DECODE_SIMT && (k_new || v_new)) return KVQ_ERR_UNSUPPORTED;
-  if (use == KVQ_DECODE_SIMT && g.vbits != g.bits) return KVQ_ERR_UNSUPPORTED;  // CUDA-core kernel: equal widths
-  if (use == KVQ_DECODE_SIMT && g.sym) return KVQ_ERR_UNSUPPORTED;              // and the asymmetric scheme
   const Plan pl = plan_splits(g, s_cur, use);
   p.n_split = (int)pl.n_split;
   p.chunk = pl.chunk;
@@ -383,10 +387,46 @@ kvq_status decode_launch(const kvq_config* cfg, const kvq_buffers* bufs, int32_t
   p.warps = pl.warps;
   p.sym = g.sym;
   p.early = (early && use == KVQ_DECODE_MMA) ? 1 : 0;
-  cudaError_t e = (use == KVQ_DECODE_SIMT) ? kvq::launch_decode_simt(p, g.bits, static_cast<cudaStream_t>(stream))
-                                            : kvq::launch_decode_mma(p, g.bits, g.vbits, static_cast<cudaStream_t>(stream));
+  call->simt = use == KVQ_DECODE_SIMT;
+  call->bits = g.bits;
+  call->vbits = g.vbits;
+  call->counters_bytes = wl.ml_off;
+  return KVQ_OK;
+}
+
+kvq_status decode_enqueue(const DecodeCall& call, cudaStream_t stream) {
+  const cudaError_t e = call.simt ? kvq::launch_decode_simt(call.p, call.bits, stream)
+                                  : kvq::launch_decode_mma(call.p, call.bits, call.vbits, stream);
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
+
+// Reads the error word at `err` (device) once all work enqueued before on `stream` has
+// finished, stores it in *out and clears it.
+kvq_status read_error_word(uint32_t* err, cudaStream_t stream, uint32_t* out) {
+  if (cudaMemcpyAsync(out, err, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (cudaMemsetAsync(err, 0, sizeof(uint32_t), stream) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return KVQ_ERR_CUDA;
+  return KVQ_OK;
+}
+
+}  // namespace kvq
+
+namespace {
+
+kvq_status decode_launch(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur,
+                         const void* q_f16, float softmax_scale, float* out, void* ws, size_t ws_bytes, void* stream,
+                         kvq_decode_impl impl, const void* k_new, const void* v_new, bool early,
+                         uint64_t wait_ns = kvq::kDefaultWaitNs) {
+  kvq::DecodeCall call;
+  const kvq_status st = kvq::decode_prepare(cfg, bufs, layer, s_cur, q_f16, softmax_scale, out, ws, ws_bytes, impl,
+                                            k_new, v_new, early, wait_ns, &call);
+  if (st != KVQ_OK) return st;
+  return kvq::decode_enqueue(call, static_cast<cudaStream_t>(stream));
+}
+
+uint64_t wait_limit(uint32_t flags) { return (flags & KVQ_DECODE_ZERO_WAIT_LIMIT) ? 0ull : kvq::kDefaultWaitNs; }
+
+constexpr uint32_t kDecodeFlags = KVQ_DECODE_EARLY_PREFETCH | KVQ_DECODE_ZERO_WAIT_LIMIT;
 
 }  // namespace
 
@@ -402,15 +442,15 @@ kvq_status kvq_decode_attention_impl(const kvq_config* cfg, const kvq_buffers* b
 kvq_status kvq_decode_attention_ex(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur,
                                    const void* q_f16, float softmax_scale, float* out, void* ws, size_t ws_bytes,
                                    void* stream, uint32_t flags) {
-  if (flags & ~(uint32_t)KVQ_DECODE_EARLY_PREFETCH) return KVQ_ERR_INVALID_ARG;
+  if (flags & ~kDecodeFlags) return KVQ_ERR_INVALID_ARG;
   return decode_launch(cfg, bufs, layer, s_cur, q_f16, softmax_scale, out, ws, ws_bytes, stream, KVQ_DECODE_AUTO,
-                       nullptr, nullptr, (flags & KVQ_DECODE_EARLY_PREFETCH) != 0);
+                       nullptr, nullptr, (flags & KVQ_DECODE_EARLY_PREFETCH) != 0, wait_limit(flags));
 }
 
 kvq_status kvq_decode_step_ex(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur,
                               const void* k_f16, const void* v_f16, const void* q_f16, float softmax_scale, float* out,
                               void* ws, size_t ws_bytes, void* stream, uint32_t flags) {
-  if (flags & ~(uint32_t)KVQ_DECODE_EARLY_PREFETCH) return KVQ_ERR_INVALID_ARG;
+  if (flags & ~kDecodeFlags) return KVQ_ERR_INVALID_ARG;
   const bool early = (flags & KVQ_DECODE_EARLY_PREFETCH) != 0;
   Geometry g;
   kvq_status st = kvq::make_geometry(cfg, &g);
@@ -425,10 +465,10 @@ kvq_status kvq_decode_step_ex(const kvq_config* cfg, const kvq_buffers* bufs, in
     if (st != KVQ_OK) return st;
     // the kernel just launched writes this layer: the attention launch waits for it
     return decode_launch(cfg, bufs, layer, T, q_f16, softmax_scale, out, ws, ws_bytes, stream, KVQ_DECODE_AUTO,
-                         nullptr, nullptr, false);
+                         nullptr, nullptr, false, wait_limit(flags));
   }
   return decode_launch(cfg, bufs, layer, T, q_f16, softmax_scale, out, ws, ws_bytes, stream, KVQ_DECODE_AUTO, k_f16,
-                       v_f16, early);
+                       v_f16, early, wait_limit(flags));
 }
 
 kvq_status kvq_decode_step(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur,
@@ -445,3 +485,9 @@ kvq_status kvq_decode_attention(const kvq_config* cfg, const kvq_buffers* bufs, 
 }
 
 }  // extern "C"
+
+extern "C" kvq_status kvq_decode_error(void* ws, size_t ws_bytes, void* stream, uint32_t* err_out) {
+  if (!err_out) return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(ws) || ws_bytes < 256) return KVQ_ERR_WORKSPACE;
+  return kvq::read_error_word(static_cast<uint32_t*>(ws), static_cast<cudaStream_t>(stream), err_out);
+}

@@ -243,16 +243,20 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
-// Wait for a stage's copies; gives up after ~2 s (returns false) instead of spinning forever.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Wait for a stage's copies; gives up after limit_ns of %globaltimer (returns false)
+// instead of spinning forever. A limit of 0 gives up at once, without looking.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (limit_ns == 0) return false;
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   while (true) {
     for (int k = 0; k < 64; ++k)
       if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > 2000000000ull) return false;
+    if (global_ns() - t0 > limit_ns) return false;
   }
 }
+
+constexpr uint64_t kDrainWaitNs = 2000000000ull;  // draining the copies in flight after a failed wait
 
 // 16-byte asynchronous global -> shared copy (L2 only), per thread.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
@@ -890,7 +894,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
   int sidx = 0;
   uint32_t phase = 0;
   for (int i = 0; i < n_mine; ++i) {
-    if (!mbar_wait(smem_u32(&bars[warp][sidx]), phase)) {
+    if (!mbar_wait(smem_u32(&bars[warp][sidx]), phase, p.wait_ns)) {
       failed_at = i;
       break;
     }
@@ -908,10 +912,11 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
   }
 
   if (failed_at >= 0) {
-    // a stage never completed: flag it and drain (bounded) what is still in flight
-    if (lane == 0) atomicOr(p.err, 1u);
+    // a stage did not complete in time: flag it (the host reads the word with
+    // kvq_decode_error) and drain (bounded) what is still in flight
+    if (lane == 0) atomicOr(p.err, KVQ_DECODE_ERR_WAIT_TIMEOUT);
     for (int i = failed_at; i < min(n_mine, failed_at + NS); ++i)
-      mbar_wait(smem_u32(&bars[warp][i % NS]), (uint32_t)((i / NS) & 1));
+      mbar_wait(smem_u32(&bars[warp][i % NS]), (uint32_t)((i / NS) & 1), kDrainWaitNs);
     asm volatile("cp.async.wait_all;" ::: "memory");  // no copy may land after the CTA exits
   }
   __syncwarp();

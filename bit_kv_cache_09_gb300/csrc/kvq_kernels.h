@@ -6,6 +6,8 @@
 
 #include <cstdint>
 
+#include "../../include/kvq.h"
+
 namespace kvq {
 
 // All pointers are already offset to the layer's first slice (layer, batch 0, head 0).
@@ -90,7 +92,8 @@ struct DecodeParams {
   uint8_t* k_codes_w;  // symmetric scheme: the new key row is quantized in place
   __half2* k_meta_w;
   float* out;       // [B][H*r][d]
-  uint32_t* err;      // error word: bit 0 = a wait for staged data timed out
+  uint32_t* err;      // error word (KVQ_DECODE_ERR_* bits), read by kvq_decode_error
+  uint64_t wait_ns;   // time limit of every bounded wait of the tensor-core kernel (0: give up at once)
   uint32_t* tickets;  // [B*H]
   float2* ws_ml;      // [B][H*r][cap] (running max in log2 units, denominator)
   float* ws_o;        // [B][H*r][cap][d]
@@ -135,6 +138,18 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
+// Time limit of the tensor-core kernel's bounded waits unless a call asks for 0.
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+
+// One checked decode-attention launch (kvq_api.cu): decode_prepare validates every
+// argument and fills it without touching the device; decode_enqueue launches it.
+struct DecodeCall {
+  DecodeParams p;
+  bool simt;
+  int bits, vbits;
+  size_t counters_bytes;  // leading workspace bytes (error word, tickets) that must start at zero
+};
+
 // bits, vbits: key and value code widths (equal, or 8 and 4)
 cudaError_t launch_append(const AppendParams& p, int bits, int vbits, cudaStream_t stream);
 cudaError_t launch_dequant(const DequantParams& p, int bits, int vbits, cudaStream_t stream);
@@ -145,5 +160,12 @@ cudaError_t launch_decode_mma(const DecodeParams& p, int bits, int vbits, cudaSt
 int occupancy_decode_mma(int bits, int vbits, int r, int n_vg, int sym);  // resident CTAs per SM (0 on error)
 int max_clusters_decode_mma(int bits, int vbits, int r, int n_vg, int cs, int nw, int sym);  // resident clusters of cs CTAs
 int occupancy_decode_simt(int bits);
+
+kvq_status decode_prepare(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur,
+                          const void* q_f16, float softmax_scale, float* out, void* ws, size_t ws_bytes,
+                          kvq_decode_impl impl, const void* k_new, const void* v_new, bool early, uint64_t wait_ns,
+                          DecodeCall* call);
+kvq_status decode_enqueue(const DecodeCall& call, cudaStream_t stream);
+kvq_status read_error_word(uint32_t* err, cudaStream_t stream, uint32_t* out);
 
 }  // namespace kvq

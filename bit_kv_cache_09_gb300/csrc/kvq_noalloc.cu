@@ -15,6 +15,7 @@
 #include <mutex>
 
 #include "kvq_common.cuh"
+#include "kvq_kernels.h"
 
 namespace {
 
@@ -52,13 +53,26 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
   const kvq_status st = kvq::make_geometry(cfg, &g);
   if (st != KVQ_OK) return st;
   if (s_cur < 1) return KVQ_ERR_INVALID_ARG;
-  const kvq::WorkspaceLayout wl = kvq::workspace_layout(g, s_cur);
-  if (wl.total > kStaticScratchBytes) return KVQ_ERR_WORKSPACE;  // beyond the static scratch
+  if (kvq::workspace_layout(g, s_cur).total > kStaticScratchBytes) return KVQ_ERR_WORKSPACE;  // beyond the static scratch
   void* scratch = nullptr;
   if (scratch_address(&scratch) != cudaSuccess) return KVQ_ERR_CUDA;
+  // Every argument is checked before the shared array is touched: a rejected call
+  // writes nothing into it (another stream's decode may be using it).
+  kvq::DecodeCall call;
+  const kvq_status chk = kvq::decode_prepare(cfg, bufs, layer, s_cur, q_f16, softmax_scale, out, scratch,
+                                             kStaticScratchBytes, KVQ_DECODE_AUTO, nullptr, nullptr, false,
+                                             kvq::kDefaultWaitNs, &call);
+  if (chk != KVQ_OK) return chk;
   // The error word and the split counters must start at zero; the array keeps the
   // previous call's contents, so clear them on the caller's stream.
-  if (cudaMemsetAsync(scratch, 0, wl.ml_off, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
-  return kvq_decode_attention(cfg, bufs, layer, s_cur, q_f16, softmax_scale, out, scratch, kStaticScratchBytes,
-                              stream);
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(scratch, 0, call.counters_bytes, s) != cudaSuccess) return KVQ_ERR_CUDA;
+  return kvq::decode_enqueue(call, s);
+}
+
+extern "C" kvq_status kvq_decode_noalloc_error(void* stream, uint32_t* err_out) {
+  if (!err_out) return KVQ_ERR_INVALID_ARG;
+  void* scratch = nullptr;
+  if (scratch_address(&scratch) != cudaSuccess) return KVQ_ERR_CUDA;
+  return kvq::read_error_word(static_cast<uint32_t*>(scratch), static_cast<cudaStream_t>(stream), err_out);
 }

@@ -21,17 +21,28 @@ STATUS_NAMES = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_UNSUPPORTED",
                 4: "KVQ_ERR_WORKSPACE", 5: "KVQ_ERR_CUDA"}
 BUFFER_NAMES = ("k_codes", "k_meta", "k_resid", "v_codes", "v_meta")
 DECODE_AUTO, DECODE_SIMT, DECODE_MMA = 0, 1, 2
-DECODE_EARLY_PREFETCH = 1  # flag bit of kvq_decode_attention_ex / kvq_decode_step_ex
+DECODE_EARLY_PREFETCH = 1  # flag bits of kvq_decode_attention_ex / kvq_decode_step_ex
+DECODE_ZERO_WAIT_LIMIT = 2
+DECODE_ERR_WAIT_TIMEOUT = 1  # bit of the decode error word
 EXPORTED = ("kvq_buffer_sizes", "kvq_quantize_append", "kvq_dequantize", "kvq_decode_workspace_size",
             "kvq_decode_attention", "kvq_decode_attention_impl", "kvq_decode_num_splits", "kvq_status_string",
             "kvq_version", "kvq_decode_attention_noalloc", "kvq_decode_step", "kvq_decode_attention_ex",
-            "kvq_decode_step_ex")
+            "kvq_decode_step_ex", "kvq_decode_error", "kvq_decode_noalloc_error")
 
 
 class KVQError(RuntimeError):
     def __init__(self, fn: str, status: int, message: str):
         super().__init__(f"{fn}: {STATUS_NAMES.get(status, status)} ({message})")
         self.status = status
+
+
+class KVQDeviceError(RuntimeError):
+    """A decode launch reported a device-side error in its workspace error word."""
+
+    def __init__(self, word: int):
+        names = [n for bit, n in ((DECODE_ERR_WAIT_TIMEOUT, "a wait for staged cache tiles timed out"),) if word & bit]
+        super().__init__(f"decode error word 0x{word:x}: {'; '.join(names) or 'unknown bits'}")
+        self.word = word
 
 
 class kvq_config(ctypes.Structure):
@@ -82,6 +93,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.kvq_decode_attention_ex.restype = ctypes.c_int
         L.kvq_decode_step_ex.argtypes = L.kvq_decode_step.argtypes + [ctypes.c_uint32]
         L.kvq_decode_step_ex.restype = ctypes.c_int
+        L.kvq_decode_error.argtypes = [vp, ctypes.c_size_t, vp, ctypes.POINTER(ctypes.c_uint32)]
+        L.kvq_decode_error.restype = ctypes.c_int
+        L.kvq_decode_noalloc_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+        L.kvq_decode_noalloc_error.restype = ctypes.c_int
         L.kvq_decode_num_splits.argtypes = [cfgp, ctypes.c_int64]
         L.kvq_decode_num_splits.restype = ctypes.c_int32
         L.kvq_status_string.argtypes = [ctypes.c_int]
@@ -185,3 +200,17 @@ def kvq_decode_attention_noalloc(cfg: kvq_config, bufs: kvq_buffers, layer: int,
     _check("kvq_decode_attention_noalloc",
            load().kvq_decode_attention_noalloc(ctypes.byref(cfg), ctypes.byref(bufs), layer, s_cur, q_f16,
                                                softmax_scale, out, stream))
+
+
+def kvq_decode_error(ws: int, ws_bytes: int, stream: int = 0) -> int:
+    """The decode error word of workspace `ws` (synchronizes `stream`, then clears it)."""
+    word = ctypes.c_uint32(0)
+    _check("kvq_decode_error", load().kvq_decode_error(ws, ws_bytes, stream, ctypes.byref(word)))
+    return int(word.value)
+
+
+def kvq_decode_noalloc_error(stream: int = 0) -> int:
+    """The error word of the last kvq_decode_attention_noalloc call on the current device."""
+    word = ctypes.c_uint32(0)
+    _check("kvq_decode_noalloc_error", load().kvq_decode_noalloc_error(stream, ctypes.byref(word)))
+    return int(word.value)

@@ -162,9 +162,9 @@ kvq_status kvq_dequantize(const kvq_config* cfg, const kvq_buffers* bufs, int32_
                           float* k_out, float* v_out, void* stream);
 
 /* Bytes of device workspace kvq_decode_attention needs for s_cur cached tokens
- * (0 for a bad config). The workspace holds split-K partials and per-(batch, kv head)
- * counters; zero-fill it once before its first use: every call leaves the counters
- * at zero again. */
+ * (0 for a bad config). The workspace holds an error word (first 4 bytes, see
+ * kvq_decode_error), per-(batch, kv head) counters and split-K partials; zero-fill it
+ * once before its first use: every call leaves the counters at zero again. */
 size_t kvq_decode_workspace_size(const kvq_config* cfg, int64_t s_cur);
 
 /* Decode attention of one layer over its s_cur >= 1 cached tokens (the token just
@@ -203,6 +203,16 @@ kvq_status kvq_decode_step(const kvq_config* cfg, const kvq_buffers* bufs, int32
  * kvq_decode_step of the same layer does not. Queries and new key/value rows are always
  * read after the wait. No counterpart in the pages: a scheduling choice of this library. */
 #define KVQ_DECODE_EARLY_PREFETCH 1u
+/* KVQ_DECODE_ZERO_WAIT_LIMIT: the tensor-core kernel's bounded waits for its staged cache
+ * tiles get a time limit of 0 (normally about 2 s of the GPU's global timer): every
+ * CTA gives up at its first wait, drains the copies it has in flight, records
+ * KVQ_DECODE_ERR_WAIT_TIMEOUT in the workspace error word and finishes, so the
+ * outputs of that call are undefined. For testing the failure path: nothing faults or
+ * hangs, and the context stays usable. */
+#define KVQ_DECODE_ZERO_WAIT_LIMIT 2u
+
+/* Bits of the decode error word (kvq_decode_error). */
+#define KVQ_DECODE_ERR_WAIT_TIMEOUT 1u /* a wait for staged cache tiles ran out of time */
 
 /* kvq_decode_attention with flag bits (0: identical to kvq_decode_attention). */
 kvq_status kvq_decode_attention_ex(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur,
@@ -215,6 +225,16 @@ kvq_status kvq_decode_attention_ex(const kvq_config* cfg, const kvq_buffers* buf
 kvq_status kvq_decode_step_ex(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur,
                               const void* k_f16, const void* v_f16, const void* q_f16, float softmax_scale,
                               float* out, void* ws, size_t ws_bytes, void* stream, uint32_t flags);
+
+/* Device-side status of decode launches. The tensor-core kernel bounds every wait for
+ * its staged cache tiles; a wait that runs out sets KVQ_DECODE_ERR_WAIT_TIMEOUT in the
+ * error word (the first 4 bytes of the workspace `ws`), and the outputs of that launch
+ * are then not to be trusted, although the call returned KVQ_OK. This call waits until
+ * every launch enqueued before it on `stream` has finished (it synchronizes the
+ * stream), stores the word in *err_out (0: no error since the last read) and clears
+ * it. ws_bytes: the workspace size (at least 256). Returns KVQ_ERR_WORKSPACE for a
+ * missing or misaligned workspace, KVQ_ERR_CUDA if the copy fails. */
+kvq_status kvq_decode_error(void* ws, size_t ws_bytes, void* stream, uint32_t* err_out);
 
 /* Kernel choice for kvq_decode_attention_impl. AUTO is what kvq_decode_attention uses. */
 typedef enum {
@@ -239,11 +259,18 @@ kvq_status kvq_decode_attention_impl(const kvq_config* cfg, const kvq_buffers* b
  * allocating library call). Its first call on a device looks up the array's device
  * address (cudaGetSymbolAddress) with that device current; make that first call before
  * any stream capture. Every call on a device shares the one array: it clears the
- * array's counters on `stream` and then runs the same kernels as kvq_decode_attention,
+ * array's counters and error word on `stream` (after all its argument checks, so a
+ * rejected call writes nothing) and then runs the same kernels as kvq_decode_attention,
  * so calls whose executions overlap on the GPU (other streams, other threads) race and
- * must be ordered by the caller. */
+ * must be ordered by the caller. The looked-up address is kept per device for the life
+ * of the process; it does not survive cudaDeviceReset. */
 kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const kvq_buffers* bufs, int32_t layer, int64_t s_cur,
                                         const void* q_f16, float softmax_scale, float* out, void* stream);
+
+/* kvq_decode_error for the static array of kvq_decode_attention_noalloc on the current
+ * device: the error word of the last noalloc call (each call clears it first). Like
+ * that call it allocates nothing; it synchronizes `stream`. */
+kvq_status kvq_decode_noalloc_error(void* stream, uint32_t* err_out);
 
 /* Number of split-K partitions kvq_decode_attention uses for s_cur tokens (>= 1),
  * or 0 for a bad config. */

@@ -120,3 +120,29 @@ def host_layer_inputs(w, layer, t0, nt):
 
 def softmax_scale(w):
     return 1.0 / math.sqrt(w.d_head)
+
+
+def oracle_slice_job(job):
+    """Oracle side of one (layer, batch row, kv head) slice of a full-size workload, for a
+    process pool: the packed state after each T in `job["Ts"]` (the state after the last T
+    is returned in full) and the oracle attention of the query rows given for each T.
+    Runs in a worker process (spawned, no CUDA); inputs come from the host generator."""
+    w, layer, b, h = job["w"], job["layer"], job["b"], job["h"]
+    T_max = max(job["Ts"])
+    k = synth.k_slice(w, layer, b, h, range(T_max))
+    v = synth.v_slice(w, layer, b, h, range(T_max))
+    out = {"key": (layer, b, h), "att": {}}
+    for T in job["Ts"]:
+        if w.symmetric:
+            st = oracle.cache_state_sym(k[:T], v[:T], d=w.d_head, k_outliers=w.k_outliers)
+            kh, vh = oracle.dequantize_state_sym(st, d=w.d_head)
+        else:
+            st = oracle.cache_state(k[:T], v[:T], d=w.d_head, bits=w.bits, G=w.k_group, Gv=w.v_group, R=w.residual,
+                                    v_bits=w.vbits)
+            kh, vh = oracle.dequantize_state(st, d=w.d_head, bits=w.bits, G=w.k_group, Gv=w.v_group, R=w.residual,
+                                             v_bits=w.vbits)
+        if T in job["q"]:
+            out["att"][T] = oracle.attention(job["q"][T], kh, vh, w.softmax_scale)
+        if T == T_max:
+            out["state"] = st
+    return out

@@ -163,13 +163,26 @@ def test_decode_flag_checks(lib):
                                                        4096, need, None, flags)
     step = lambda s, flags: lib.kvq_decode_step_ex(B(cfg), B(bufs), 0, s, 4096, 4096, 4096, ctypes.c_float(0.088),  # noqa: E731
                                                    4096, 4096, need, None, flags)
-    assert kvq.DECODE_EARLY_PREFETCH == 1
-    assert att(500, 2) == 1 and att(500, 0x80000000) == 1
-    assert step(499, 2) == 1 and step(499, 3) == 1
-    assert att(0, kvq.DECODE_EARLY_PREFETCH) == 1      # no tokens
-    assert att(1001, kvq.DECODE_EARLY_PREFETCH) == 3   # capacity
-    assert step(1000, kvq.DECODE_EARLY_PREFETCH) == 3  # capacity
-    assert step(-1, kvq.DECODE_EARLY_PREFETCH) == 1
+    assert kvq.DECODE_EARLY_PREFETCH == 1 and kvq.DECODE_ZERO_WAIT_LIMIT == 2
+    assert att(500, 4) == 1 and att(500, 0x80000000) == 1
+    assert step(499, 4) == 1 and step(499, 7) == 1
+    for flag in (kvq.DECODE_EARLY_PREFETCH, kvq.DECODE_ZERO_WAIT_LIMIT):
+        assert att(0, flag) == 1      # no tokens
+        assert att(1001, flag) == 3   # capacity
+        assert step(1000, flag) == 3  # capacity
+        assert step(-1, flag) == 1
+
+
+def test_error_word_reader_checks(lib):
+    """kvq_decode_error / kvq_decode_noalloc_error reject a missing output, workspace or a
+    workspace too small for the error word on the host, before touching the device."""
+    err = ctypes.c_uint32(7)
+    assert lib.kvq_decode_error(4096, 4096, None, None) == 1
+    assert lib.kvq_decode_error(None, 4096, None, ctypes.byref(err)) == 4
+    assert lib.kvq_decode_error(4100, 4096, None, ctypes.byref(err)) == 4
+    assert lib.kvq_decode_error(4096, 255, None, ctypes.byref(err)) == 4
+    assert lib.kvq_decode_noalloc_error(None, None) == 1
+    assert err.value == 7
 
 
 def test_early_prefetch_flag_follows_the_previous_launch():

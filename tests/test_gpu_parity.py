@@ -584,3 +584,131 @@ def test_layer_interleaved_decode_with_early_prefetch(kind):
     for layer in range(w.n_layers):
         q_host = synth.gen_q(w.seed, layer, range(w.batch), T - 1, w.n_q, w.d_head)
         _check_attention(cache, w, layer, T, *host[layer], q_host, kvq.DECODE_AUTO)
+
+
+def _subnormals(n, sign_mix=True):
+    """n binary16 subnormals k * 2^-24 with k in [1, 1023], mixed signs."""
+    k = (np.arange(n) * 97 % 1023 + 1).astype(np.float64)
+    s = np.where(np.arange(n) % 3 == 0, -1.0, 1.0) if sign_mix else 1.0
+    return (s * k * 2.0**-24).astype(np.float16)
+
+
+def _narrow(n, centre, step):
+    """n values from {centre - step, centre, centre + step} (neighbouring binary16 values)."""
+    return (centre + ((np.arange(n) % 3) - 1) * step).astype(np.float16)
+
+
+def _edge_history(w):
+    """Keys and values [B][T][H][d] of the seeded generator with planted edge groups:
+    keys - a constant channel over a group (two signs), an all-zero group, narrow groups
+    far from zero (around 7 and -1000: the widened scale), binary16 subnormals, and
+    +-65504 in one channel (slice (0, 0) in the prompt; slice (1, 1) in the residual
+    window that a decode step flushes); values - all-zero, constant, narrow-far-from-zero
+    and subnormal groups in prompt rows and in rows appended by the fused step, and
+    +-65504 groups in rows whose softmax weight is exactly 0 (their slice's attention is
+    held by the +65504 key)."""
+    k, v = host_layer_inputs(w, 0, 0, w.max_seq)
+    k, v = np.array(k, np.float16), np.array(v, np.float16)
+    S, Gv = w.seq, w.v_group
+    g1 = slice(Gv, 2 * Gv) if w.d_head // Gv > 1 else slice(0, Gv)
+    # keys of the prompt's quantized groups (G = 32)
+    k[:, 0:32, :, 3] = 1.5
+    k[:, 0:32, :, 4] = -0.75
+    k[:, 32:64] = 0.0
+    k[:, 64:96, :, 5] = _narrow(32, 7.0, 2.0**-8)[None, :, None]
+    k[:, 64:96, :, 6] = _narrow(32, -1000.0, 0.5)[None, :, None]
+    k[:, 96:128, :, 9] = _subnormals(32)[None, :, None]
+    k[0, 96, 0, 7], k[0, 97, 0, 7] = 65504.0, -65504.0
+    # keys of the residual window quantized by a decode step (tokens 128 .. 191)
+    k[:, 128:160, :, 11] = 3.25
+    k[:, 160:192, :, 12] = _narrow(32, 7.0, 2.0**-8)[None, :, None]
+    k[:, 160:192, :, 14] = _subnormals(32)[None, :, None]
+    k[1, 170, 1, 13], k[1, 180, 1, 13] = 65504.0, -65504.0
+    # values: prompt rows 10..13 and fused-step rows S+1..S+4 in every slice
+    for t in (10, S + 1):
+        v[:, t, :, 0:Gv] = 0.0
+    for t in (11, S + 2):
+        v[:, t, :, g1] = -2.25
+    for t in (12, S + 3):
+        v[:, t, :, 0:Gv] = _narrow(Gv, 7.0, 2.0**-8)[None, None]
+    for t in (13, S + 4):
+        v[:, t, :, 0:Gv] = _subnormals(Gv)[None, None]
+    ext = np.resize(np.array([65504.0, -65504.0, 0.0, 1.0], np.float16), Gv)
+    v[0, 50, 0, 0:Gv] = ext
+    v[0, S + 5, 0, 0:Gv] = ext
+    v[1, 171, 1, 0:Gv] = ext
+    return k, v
+
+
+def _edge_queries(w, T):
+    """Queries of the step at token T; query rows of slice (0, 0) read channel 7 and those of
+    slice (1, 1) channel 13 with weight 1, so the planted +65504 keys hold their softmax."""
+    q = np.array(synth.gen_q(w.seed, 0, range(w.batch), T, w.n_q, w.d_head), np.float16)
+    q[0, 0:w.gqa, 7] = 1.0
+    q[1, w.gqa:2 * w.gqa, 13] = 1.0
+    return q
+
+
+@pytest.mark.parametrize("bits,Gv", [(8, 64), (4, 32), (2, 32)])
+def test_asymmetric_edge_groups(bits, Gv):
+    """Planted degenerate and extreme groups (see _edge_history) through the key-group and
+    value-token append kernels (prompt), the fused decode step (new value rows, new key
+    rows into the residual) and the key-group kernel of the step that fills the residual
+    window: every byte of codes, metadata and residual bit-exact against the oracle,
+    dequantized values bit-exact, attention within 2e-3 before and after the flush."""
+    R = 64
+    S = 2 * R + 20
+    steps = R - 20 + 3  # the step at token 2R + R - 1 fills the window: tokens 128 .. 191 are quantized
+    w = small_workload(bits=bits, G=32, Gv=Gv, R=R, r=4, B=2, H=2, S=S, steps=steps, seed=9300 + bits)
+    cache = QuantizedKVCache.for_workload(w)
+    k_host, v_host = _edge_history(w)
+    cache.append(0, 0, _dev(k_host[:, :S]), _dev(v_host[:, :S]))
+    _check_all_slices(cache, w, 0, S, k_host, v_host)
+    flush_step = 3 * R - 1 - S
+    for s in range(steps):
+        T = S + s
+        q_host = _edge_queries(w, T)
+        out = cache.decode_step(0, T, _dev(k_host[:, T:T + 1]), _dev(v_host[:, T:T + 1]), _dev(q_host),
+                                softmax_scale(w)).cpu().numpy()
+        if s not in (0, 5, 22, 23, flush_step, steps - 1):
+            continue
+        _check_all_slices(cache, w, 0, T + 1, k_host, v_host)
+        for b in range(w.batch):
+            for h in range(w.n_kv):
+                st = oracle_slice_state(k_host[b, :T + 1, h], v_host[b, :T + 1, h], cache)
+                ref = oracle_attention(st, q_host[b, h * w.gqa:(h + 1) * w.gqa], cache, softmax_scale(w))
+                err = float(np.abs(out[b, h * w.gqa:(h + 1) * w.gqa] - ref).max())
+                assert err <= ATOL, (bits, b, h, T + 1, err)
+    T = S + steps
+    assert (T // R) * R == 3 * R  # the window of tokens 128 .. 191 was quantized
+    kd, vd = cache.dequantize(0, T)
+    for b in range(w.batch):
+        for h in range(w.n_kv):
+            st = oracle_slice_state(k_host[b, :T, h], v_host[b, :T, h], cache)
+            kh, vh = oracle.dequantize_state(st, d=128, bits=bits, G=w.k_group, Gv=w.v_group, R=w.residual)
+            assert np.array_equal(kd[b, h].cpu().numpy().view(np.uint32), kh.view(np.uint32)), (b, h)
+            assert np.array_equal(vd[b, h].cpu().numpy().view(np.uint32), vh.view(np.uint32)), (b, h)
+            if (b, h) == (0, 0):  # the +-65504 key group: widened to the full range, all other codes 0-ish
+                assert np.abs(kh[96:98, 7]).min() > 20000
+
+
+@pytest.mark.parametrize("B,H,S", [(2, 2, 700), (6, 8, 3000)])
+def test_zero_wait_limit_reports_a_timeout(B, H, S):
+    """KVQ_DECODE_ZERO_WAIT_LIMIT gives every bounded wait of the tensor-core kernel a limit
+    of 0: each CTA gives up at its first wait, drains its copies and finishes (small grid:
+    cluster merge; large grid: workspace merge). The launch returns KVQ_OK, the error word
+    records the timeout and check_errors() raises; the next plain launch is correct and
+    leaves the word clear (nothing faulted, the context stays usable)."""
+    w = small_workload(bits=4, G=128, Gv=64, R=128, r=4, B=B, H=H, S=S, steps=1, seed=9400 + B)
+    cache = QuantizedKVCache.for_workload(w)
+    k_host, v_host = host_layer_inputs(w, 0, 0, w.max_seq)
+    cache.append(0, 0, _dev(k_host[:, :S]), _dev(v_host[:, :S]))
+    cache.check_errors()  # nothing recorded yet
+    q_host = synth.gen_q(w.seed, 0, range(w.batch), S - 1, w.n_q, w.d_head)
+    cache.attention(0, S, _dev(q_host), softmax_scale(w), flags=kvq.DECODE_ZERO_WAIT_LIMIT)
+    with pytest.raises(kvq.KVQDeviceError) as e:
+        cache.check_errors()
+    assert e.value.word & kvq.DECODE_ERR_WAIT_TIMEOUT
+    cache.check_errors()  # the read cleared it
+    _check_attention(cache, w, 0, S, k_host, v_host, q_host, kvq.DECODE_AUTO)
+    cache.check_errors()
