@@ -111,14 +111,6 @@ __device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) 
 
 constexpr uint32_t kOne2 = 0x3C003C00u;  // half2(1, 1)
 
-// hi = binary16(x), lo = binary16(x - hi) for a pair, packed as half2 bit patterns.
-__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-  const __half2 h = __floats2half2_rn(x0, x1);
-  const float2 hf = __half22float2(h);
-  hi = h2_bits(h);
-  lo = h2_bits(__floats2half2_rn(x0 - hf.x, x1 - hf.y));
-}
-
 // Words of one lane's chunk of a key row / value pair row (rowK/4 bytes).
 template <int BITS>
 struct Chunk {
@@ -354,6 +346,9 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
   // fragments are zero): 16 words per row, 18 with the padding
   constexpr int kQA = SYM ? 18 : 36;
   __shared__ __align__(16) uint32_t qa_s[kWarps][(NT == 1) ? 16 : 32][kQA];
+  // fused step: codes of the new value row on their way into the pair row. Not the stage
+  // rings: with early prefetch their first stages are already being filled.
+  __shared__ __align__(16) uint8_t append_s[kHeadDim];
 
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -459,7 +454,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
       const int64_t row = (int64_t)b * p.H + h;  // [B][1][H][d]
       uint16_t* pair = reinterpret_cast<uint16_t*>(p.v_codes_w + slice * p.v_codes_slice + (int64_t)(t_new >> 1) * 2 * ROWV);
       quant::quantize_value_row<VBITS, SYM>(p.v_new + row * kHeadDim, pair, t_new & 1,
-                                           p.v_meta_w + (slice * p.S_pad + t_new) * NVG, p.Gv, lane, smem);
+                                           p.v_meta_w + (slice * p.S_pad + t_new) * NVG, p.Gv, lane, append_s);
       if constexpr (SYM) {  // the key row is quantized per token right away (no residual window)
         uint8_t* kmb = reinterpret_cast<uint8_t*>(p.k_meta_w) + slice * p.k_meta_slice;
         quant::quantize_key_row_sym(p.k_new + row * kHeadDim, p.k_codes_w + slice * p.k_codes_slice + (int64_t)t_new * ROW,
@@ -806,17 +801,18 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
         for (int k = 0; k < 4; ++k)
           if (ts + 16 * hf + (k >> 1) * 8 + 2 * j + (k & 1) >= t_end) s[hf][k] = -__int_as_float(0x7f800000);
     }
-    float mx = fmaxf(fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[0][2], s[0][3])),
-                     fmaxf(fmaxf(s[1][0], s[1][1]), fmaxf(s[1][2], s[1][3])));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    const float m_new = fmaxf(m_run, mx);
     // Lazy rescale: the running max is only moved when a score exceeds it by more than
     // kTau (log2 units), so p = 2^(s - m_run) <= 2^kTau. kTau keeps every binary16
     // weight p*s finite for any binary16 value group: the largest value scale is
-    // 131008 / (2^b - 1) rounded up (514, 8734, 43669 for b = 8, 4, 2).
+    // 131008 / (2^b - 1) rounded up (514, 8734, 43669 for b = 8, 4, 2). The lane's own
+    // scores decide whether any row needs it; only then is the row max gathered.
     constexpr float kTau = VBITS == 8 ? 6.0f : (VBITS == 4 ? 2.0f : 0.5f);
-    if (__any_sync(0xffffffffu, m_new > m_run + kTau)) {
+    float mx = fmaxf(fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[0][2], s[0][3])),
+                     fmaxf(fmaxf(s[1][0], s[1][1]), fmaxf(s[1][2], s[1][3])));
+    if (__any_sync(0xffffffffu, mx > m_run + kTau)) {
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float m_new = fmaxf(m_run, mx);
       const float alpha = ex2(m_run - m_new);  // 0 on the first iteration (m_run = -inf)
       l_run *= alpha;
       // PV column n holds the query of row n: alphas of columns 2j, 2j+1 live in rows 2j, 2j+1
@@ -832,15 +828,25 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
       }
       m_run = m_new;
     }
-    float pr[2][4];
+    // p = 2^(s - m_run) rounded once to binary16 (token pairs (2j, 2j+1) and (8+2j, 9+2j)
+    // of each half). The denominator sums the same rounded values, so the softmax weights
+    // are p16 / sum(p16): the rounding perturbs each weight by at most 2^-11 relative and
+    // moves an output by at most that times its spread of values. The value weights
+    // w = p16 * s are then exact as hi = fl(p16 s), lo = fl(p16 s - hi).
+    uint32_t ph[2][2];
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        pr[hf][k] = ex2(s[hf][k] - m_run);
-        l_run += pr[hf][k];
+      for (int e = 0; e < 2; ++e) {
+        const __half2 h = __floats2half2_rn(ex2(s[hf][2 * e] - m_run), ex2(s[hf][2 * e + 1] - m_run));
+        const float2 f = __half22float2(h);
+        l_run += f.x + f.y;
+        ph[hf][e] = h2_bits(h);
       }
-    // values: weights p * s per value group, split into binary16 halves
+    // NT == 1: lanes g < 4 supply the hi halves of their query's weights, lanes g >= 4 the lo
+    // halves: out = fl(p s + c) with c = 0 (hi) or c = -fl(p s) (lo)
+    const uint32_t lo_mask = lo_lane ? 0xFFFFFFFFu : 0u;
+    // values: weights p * s per value group, as binary16 hi/lo halves
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
       uint32_t vw[2][CWV];
@@ -851,10 +857,6 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
       __half2 mlo[2 * NVG], mhi[2 * NVG];  // tokens (2j, 2j+1) and (8+2j, 9+2j)
       lds_vmeta<NVG>(vms + (2 * j) * NVG, mlo);
       lds_vmeta<NVG>(vms + (8 + 2 * j) * NVG, mhi);
-      // p of the token pairs (2j, 2j+1) and (8+2j, 9+2j) as binary16 hi/lo halves
-      uint32_t ph[2], pl[2];
-      split2(pr[hf][0], pr[hf][1], ph[0], pl[0]);
-      split2(pr[hf][2], pr[hf][3], ph[1], pl[1]);
       uint32_t bf[NVG][NT][2];
 #pragma unroll
       for (int vg = 0; vg < NVG; ++vg) {
@@ -862,17 +864,13 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const uint32_t m0 = h2_bits(e ? mhi[vg] : mlo[vg]), m1 = h2_bits(e ? mhi[NVG + vg] : mlo[NVG + vg]);
-          // weights w = p * s with packed half arithmetic: hi = fl(p_hi s),
-          // lo = fl(p_lo s + fl(p_hi s - hi))
-          const uint32_t s2 = prmt2(m0, m1, 0x5410u);
-          uint32_t whi, wlo;
-          hmul2_split(ph[e], s2, whi, wlo);
-          wlo = hfma2(pl[e], s2, wlo);
+          const uint32_t s2 = prmt2(m0, m1, 0x5410u);  // value scales of the token pair
+          const uint32_t whi = hmul2(ph[hf][e], s2);
           if (NT == 1) {
-            bf[vg][0][e] = lo_lane ? wlo : whi;
+            bf[vg][0][e] = hfma2(ph[hf][e], s2, (whi ^ 0x80008000u) & lo_mask);
           } else {
             bf[vg][0][e] = whi;
-            bf[vg][NT - 1][e] = wlo;
+            bf[vg][NT - 1][e] = hfma2(ph[hf][e], s2, hneg2(whi));
           }
           za[e] = prmt2(m0, m1, 0x7632u);  // zero points of the token pair
         }

@@ -541,18 +541,21 @@ def test_outlier_selection_on_adversarial_rows():
                 assert err <= ATOL, (b, h, T + 1, err)
 
 
-@pytest.mark.parametrize("kind", ["asym4", "int8", "sym8o4"])
+@pytest.mark.parametrize("kind", ["asym4", "int8", "sym8o4", "asym2-large", "sym8-large"])
 def test_layer_interleaved_decode_with_early_prefetch(kind):
     """Decode steps that visit three layers in turn, as a model does: every launch after the
     first starts streaming its cache tiles before the previous layer's kernel has finished
     (KVQ_DECODE_EARLY_PREFETCH, set by the cache object). The asymmetric case fills a
     residual window during the steps (the two-launch path, which runs without the flag).
-    Every layer's cache state bit-exact and its attention within 2e-3 at every step, then
-    an attention-only pass over the layers."""
+    The large-grid cases give the CTA that appends the new token several warps with
+    early stages in flight while it appends. Every layer's cache state bit-exact and its
+    attention within 2e-3 at every step, then an attention-only pass over the layers."""
     cfg = {
         "asym4": dict(bits=4, G=32, Gv=64, R=64, r=4, B=2, H=2, S=250, steps=8),
         "int8": dict(bits=8, G=128, Gv=128, R=0, r=4, B=1, H=4, S=500, steps=4),
         "sym8o4": dict(bits=8, G=128, Gv=128, R=0, r=4, B=2, H=2, S=300, steps=4, symmetric=1, k_outliers=4),
+        "asym2-large": dict(bits=2, G=32, Gv=32, R=128, r=4, B=6, H=8, S=1500, steps=3),
+        "sym8-large": dict(bits=8, G=128, Gv=128, R=0, r=4, B=6, H=8, S=1500, steps=3, symmetric=1),
     }[kind]
     w = small_workload(L=3, seed=9200 + len(kind), **cfg)
     cache = QuantizedKVCache.for_workload(w)
