@@ -58,6 +58,24 @@ __device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a1, uin
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// The same product with a zero accumulator input (first k-step of a tile).
+__device__ __forceinline__ void mma16816_z(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                           uint32_t b1) {
+  const float z = 0.0f;
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};\n"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(z));
+}
+
+// Transpose of an 8x8 matrix of 16-bit elements held one row pair per lane (lane l:
+// row l/4, columns 2(l%4), 2(l%4)+1), which is the accumulator layout of an 8-row slice
+// of an m16n8 tile packed to binary16; the result is the k16 x n8 operand layout.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t d;
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(x));
+  return d;
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t sel) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(0u), "r"(sel));
@@ -345,7 +363,12 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
   // padded rows: no bank conflicts. SYM keeps only the hi words (the lo rows of its A
   // fragments are zero): 16 words per row, 18 with the padding
   constexpr int kQA = SYM ? 18 : 36;
-  __shared__ __align__(16) uint32_t qa_s[kWarps][(NT == 1) ? 16 : 32][kQA];
+  __shared__ __align__(16) uint32_t qa_s[(NT == 1) ? 1 : kWarps][(NT == 1) ? 1 : 32][kQA];
+  // r <= 4 (NT == 1): key codes are the A operand (token rows) and the query the B operand,
+  // column n = 2q + h holding query q's hi (h = 0) or lo (h = 1) halves; one padded row of
+  // B fragments per (column, lane chunk): word 2ks + e is fragment register e of k-step ks
+  constexpr int kQB = 20;
+  __shared__ __align__(16) uint32_t qb_s[(NT == 1) ? kWarps : 1][8][4][kQB];
   // fused step: codes of the new value row on their way into the pair row. Not the stage
   // rings: with early prefetch their first stages are already being filled.
   __shared__ __align__(16) uint8_t append_s[kHeadDim];
@@ -355,7 +378,6 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
   const int g = lane >> 2, j = lane & 3;
   const int r = p.r;
   const int qi = (NT == 1) ? ((g & 3) % r) : (g % r);  // query head of QK row g / PV column g
-  const bool lo_lane = (NT == 1) && (g >= 4);            // supplies the lo half of p in the PV tile
   const int64_t slice = (int64_t)b * p.H + h;
   const int64_t qrow0 = (int64_t)b * p.H * r + (int64_t)h * r;
 
@@ -549,20 +571,205 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
   for (int k = 0; k < NVG; ++k)
 #pragma unroll
     for (int e = 0; e < 4; ++e) bacc[k][e] = 0.0f;
-  const int qe_mine = qe_s[qi];
-  const float qmin_qsum = SYM ? qmin * qsum_s[qi] : 0.0f;  // SYM: q_min * sum_c q_c of query qi
+  // query of this lane's scores: with r <= 4 the lanes of column pair (2j, 2j+1) score query
+  // j; with r > 4 row g scores query g
+  const int qj = (NT == 1) ? (j % r) : qi;
+  const int qe_mine = qe_s[qj];
+  const float qmin_qsum = SYM ? qmin * qsum_s[qj] : 0.0f;  // SYM: q_min * sum_c q_c of the lane's query
 
-  // QK A fragments of the current key group (or of the raw query for residual keys) in
-  // shared memory, one padded row per (query, lane chunk): word 4ks + e is fragment
-  // register e of k-step ks. With r <= 4 the lanes g and g + 4 share a row and each
-  // computes half of it (k-steps 4h .. 4h + 3, h = g / 4).
-  uint32_t* qa_row = &qa_s[warp][(NT == 1) ? ((g & 3) * 4 + j) : lane][0];
+  // r > 4: QK A fragments of the current key group (or of the raw query for residual keys)
+  // in shared memory, one padded row per (query, lane chunk): word 4ks + e is fragment
+  // register e of k-step ks. r <= 4: B fragments of column g (query g / 2, hi or lo
+  // halves), row (g, j) of qb_s. Either way a lane folds query qi (= (g & 3) % r for r <= 4)
+  // over half hh of its chunk (r <= 4: lanes g and g + 4 split the chunk).
+  uint32_t* qa_row = &qa_s[(NT == 1) ? 0 : warp][(NT == 1) ? 0 : lane][0];
+  uint32_t* qb_row = &qb_s[(NT == 1) ? warp : 0][(NT == 1) ? g : 0][(NT == 1) ? j : 0][0];
   const int hh = (NT == 1) ? (g >> 2) : 0;  // first half this lane folds
   float qscale = 0.0f, qbias = 0.0f;
   bool resid_frags = false;
-  const float* qrow = &q_s[qi][32 * j];
+  // raw query row of the fragments for residual (and symmetric) keys: r <= 4 column g's query
+  const float* qrow = &q_s[(NT == 1) ? ((g >> 1) % r) : qi][32 * j];
 
-  // Scores of iteration i (stage st) as MMA accumulators, with the (scale, bias) that
+  // Folded query of a key group, x_c = q_c s_c, as binary16 hi/lo pairs computed with
+  // packed half arithmetic: q2_s holds q_c 2^qe / k_scale, the scales are scaled by 2^Es
+  // so that the largest is in [2^7, 2^8) (no overflow, products below 2^16); hi = fl(q s),
+  // lo = fl(q s - hi). Pairs 8h .. 8h + 7 of a lane chunk cover its local channels
+  // [16h, 16h + 16) for every code width. Sets qscale and qbias of the group.
+  auto fold_group = [&](const uint8_t* st) {
+    constexpr int NH = (NT == 1) ? 1 : 2;  // halves folded by this lane
+    const uint4* mp = reinterpret_cast<const uint4*>(st + St::KB + St::VB + St::VM) + 8 * j;
+    uint32_t mw[NH][16];  // (scale, zero point) of the lane's channels of each half it folds
+#pragma unroll
+    for (int u = 0; u < NH; ++u)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint4 v = mp[4 * (hh + u) + k];
+        mw[u][4 * k] = v.x; mw[u][4 * k + 1] = v.y; mw[u][4 * k + 2] = v.z; mw[u][4 * k + 3] = v.w;
+      }
+    uint32_t s2[NH][8];
+    uint32_t mx = 0u;
+#pragma unroll
+    for (int u = 0; u < NH; ++u) {
+#pragma unroll
+      for (int pl = 0; pl < 8; ++pl)
+        s2[u][pl] = prmt2(mw[u][k_pair_ca<BITS>(pl)], mw[u][k_pair_cb<BITS>(pl)], 0x5410u);
+      const uint32_t m01 = hmax2(s2[u][0], s2[u][1]), m23 = hmax2(s2[u][2], s2[u][3]);
+      const uint32_t m45 = hmax2(s2[u][4], s2[u][5]), m67 = hmax2(s2[u][6], s2[u][7]);
+      const uint32_t m = hmax2(hmax2(m01, m23), hmax2(m45, m67));
+      mx = (u == 0) ? m : hmax2(mx, m);
+    }
+    if (NT == 1) mx = hmax2(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    mx = hmax2(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = hmax2(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    // scales are positive: the larger bit pattern is the larger value
+    const uint32_t smax = max(mx & 0xFFFFu, mx >> 16);
+    const int Es = min(15, 7 - (max((int)(smax >> 10), 1) - 15));  // in [-8, 15]
+    const uint32_t pe = (uint32_t)(Es + 15) << 10;
+    const uint32_t p2 = pe | (pe << 16);  // half2(2^Es, 2^Es)
+    // bias = sum_c x_c (q_min - zp_c) on the tensor cores, from the fragments just
+    // computed: an extra key tile whose column 0 is k_scale 2^-8 (ones, lane g = 0)
+    // and column 1 zp_c k_scale 2^-8 (lane g = 1). With r <= 4, rows g < 4 run on
+    // the first half of the channels and rows g >= 4 on the second in the same MMA,
+    // so lane g = 5 supplies the second half's zero points in column 5 and a query's
+    // bias adds rows q and q + 4.
+    float bt[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    const uint32_t ones_col = (g == 0) ? kOne2 : 0u;
+    const uint32_t zsel = (g == 1 || (NT == 1 && g == 5)) ? kOne2 : 0u;
+#pragma unroll
+    for (int u = 0; u < NH; ++u) {
+      const int h = hh + u;
+      const uint4* qp = reinterpret_cast<const uint4*>(&q2_s[qi][j][8 * h]);
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {  // k-steps 4h + 2k, 4h + 2k + 1
+        const uint4 qv = qp[k];
+        const uint32_t qq[4] = {qv.x, qv.y, qv.z, qv.w};
+        uint32_t f[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) hmul2_split(qq[e], hmul2(s2[u][4 * k + e], p2), f[2 * e], f[2 * e + 1]);
+        if constexpr (NT == 1) {  // hi halves of pairs 8h + 4k + e to column 2(g & 3), lo to the next
+          uint32_t* cb = &qb_s[warp][2 * (g & 3)][j][8 * h + 4 * k];
+          *reinterpret_cast<uint4*>(cb) = make_uint4(f[0], f[2], f[4], f[6]);
+          *reinterpret_cast<uint4*>(cb + 4 * kQB) = make_uint4(f[1], f[3], f[5], f[7]);
+        } else {
+          reinterpret_cast<uint4*>(qa_row)[4 * h + 2 * k] = make_uint4(f[0], f[1], f[2], f[3]);
+          reinterpret_cast<uint4*>(qa_row)[4 * h + 2 * k + 1] = make_uint4(f[4], f[5], f[6], f[7]);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          uint32_t bz[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int pl = 4 * k + 2 * kk + e;
+            const uint32_t z2 = prmt2(mw[u][k_pair_ca<BITS>(pl)], mw[u][k_pair_cb<BITS>(pl)], 0x7632u);
+            bz[e] = hmul2(hfma2(z2, zsel, ones_col), kc_bits<BITS>(pl));
+          }
+          mma16816(bt, f[4 * kk], f[4 * kk + 1], f[4 * kk + 2], f[4 * kk + 3], bz[0], bz[1]);
+        }
+      }
+    }
+    __syncwarp();
+    // lanes j = 0 hold columns 0 and 1 of rows g (hi) and g + 8 (lo), lanes j = 2 column 5
+    const float t0 = bt[0] + bt[2], tz = bt[1] + bt[3];
+    float bsum;
+    if (NT == 1) {  // rows q and q + 4 hold query q's two halves of the channels
+      const int q = qj;
+      const float ones = __shfl_sync(0xffffffffu, t0, 4 * q) + __shfl_sync(0xffffffffu, t0, 4 * q + 16);
+      const float zz = __shfl_sync(0xffffffffu, tz, 4 * q) + __shfl_sync(0xffffffffu, tz, 4 * q + 18);
+      bsum = qmin * ones - zz;
+    } else {
+      bsum = __shfl_sync(0xffffffffu, qmin * t0 - tz, lane & ~3);
+    }
+    const int E = qe_mine + Es;
+    qscale = pow2f(24 - E) * p.scale_log2;
+    qbias = bsum * pow2f(8 - E) * p.scale_log2;
+  };
+
+  // r <= 4: B fragments of the raw query (binary16, exact) in natural channel pairs, for
+  // residual binary16 keys and the symmetric scheme; lo columns are zero.
+  auto raw_query_frags_t = [&]() {
+    __syncwarp();
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const float4 qv = reinterpret_cast<const float4*>(qrow)[ks];
+      const uint32_t w0 = (g & 1) ? 0u : h2_bits(__floats2half2_rn(qv.x, qv.y));
+      const uint32_t w1 = (g & 1) ? 0u : h2_bits(__floats2half2_rn(qv.z, qv.w));
+      reinterpret_cast<uint2*>(qb_row)[ks] = make_uint2(w0, w1);
+    }
+    __syncwarp();
+  };
+
+  // r <= 4: scores of iteration i (stage st) as MMA accumulators acc[m-tile][e]: rows are
+  // tokens 16 hf + g (e = 0, 1) and 16 hf + 8 + g (e = 2, 3), columns 2j (hi) and 2j + 1
+  // (lo) of query j; s = (acc[e] + acc[e + 1]) * sc + bi.
+  auto qk_t = [&](int i, const uint8_t* st, float (&acc)[2][4], float& sc, float& bi) {
+    const int ts = ts0 + i * kTok;
+    if (ts < Tq) {
+      if (SYM && i == 0) raw_query_frags_t();
+      if (!SYM && (i == 0 || (ts & (p.G - 1)) == 0)) {
+        resid_frags = false;
+        fold_group(st);
+      }
+      uint32_t kw[2][2][CW];
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) lds_chunk<BITS>(st + (16 * hf + 8 * nt + g) * ROW + j * (ROW / 4), kw[hf][nt]);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {  // k-steps 2k, 2k + 1
+        const uint4 bq = reinterpret_cast<const uint4*>(qb_row)[k];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int ks = 2 * k + u;
+          const uint32_t b0 = u ? bq.z : bq.x, b1 = u ? bq.w : bq.y;
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const uint32_t a0 = k_pair<BITS>(kw[hf][0], 2 * ks), a1 = k_pair<BITS>(kw[hf][1], 2 * ks);
+            const uint32_t a2 = k_pair<BITS>(kw[hf][0], 2 * ks + 1), a3 = k_pair<BITS>(kw[hf][1], 2 * ks + 1);
+            if (ks == 0) mma16816_z(acc[hf], a0, a1, a2, a3, b0, b1);
+            else mma16816(acc[hf], a0, a1, a2, a3, b0, b1);
+          }
+        }
+      }
+    } else if constexpr (!SYM) {  // binary16 residual keys (the symmetric scheme has none)
+      if (!resid_frags) {
+        resid_frags = true;
+        raw_query_frags_t();
+        qscale = p.scale_log2;
+        qbias = 0.0f;
+      }
+      const __half* kr = p.k_resid + slice * (int64_t)p.R_eff * kHeadDim;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        // residual slots of tokens [Tq, T) are t - Tq (Tq is a multiple of the window);
+        // rows g and g + 8 of the m-tile, the lane's 32 channels, natural pairs
+        uint32_t kw[2][16];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const uint4* rp = reinterpret_cast<const uint4*>(kr + (ts - Tq + 16 * hf + 8 * nt + g) * kHeadDim + 32 * j);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint4 v = rp[k];  // plain load: the fused step may have written this row
+            kw[nt][4 * k] = v.x; kw[nt][4 * k + 1] = v.y; kw[nt][4 * k + 2] = v.z; kw[nt][4 * k + 3] = v.w;
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint4 bq = reinterpret_cast<const uint4*>(qb_row)[k];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int ks = 2 * k + u;
+            const uint32_t b0 = u ? bq.z : bq.x, b1 = u ? bq.w : bq.y;
+            if (ks == 0) mma16816_z(acc[hf], kw[0][0], kw[1][0], kw[0][1], kw[1][1], b0, b1);
+            else mma16816(acc[hf], kw[0][2 * ks], kw[1][2 * ks], kw[0][2 * ks + 1], kw[1][2 * ks + 1], b0, b1);
+          }
+        }
+      }
+    }
+    sc = qscale;
+    bi = qbias;
+  };
+
+  // r > 4: scores of iteration i (stage st) as MMA accumulators, with the (scale, bias) that
   // turn them into log2-unit scores: s = acc * sc + bi.
   auto qk = [&](int i, const uint8_t* st, float (&acc)[2][2][4], float& sc, float& bi) {
     const int ts = ts0 + i * kTok;
@@ -586,91 +793,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
       }
       if (!SYM && (i == 0 || (ts & (p.G - 1)) == 0)) {
         resid_frags = false;
-        // Folded query of this key group, x_c = q_c s_c, as binary16 hi/lo pairs computed
-        // with packed half arithmetic: q2_s holds q_c 2^qe / k_scale, the scales are
-        // scaled by 2^Es so that the largest is in [2^7, 2^8) (no overflow, products
-        // below 2^16); hi = fl(q s), lo = fl(q s - hi). Pairs 8h .. 8h + 7 of a lane
-        // chunk cover its local channels [16h, 16h + 16) for every code width.
-        constexpr int NH = (NT == 1) ? 1 : 2;  // halves folded by this lane
-        const uint4* mp = reinterpret_cast<const uint4*>(st + St::KB + St::VB + St::VM) + 8 * j;
-        uint32_t mw[NH][16];  // (scale, zero point) of the lane's channels of each half it folds
-#pragma unroll
-        for (int u = 0; u < NH; ++u)
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint4 v = mp[4 * (hh + u) + k];
-            mw[u][4 * k] = v.x; mw[u][4 * k + 1] = v.y; mw[u][4 * k + 2] = v.z; mw[u][4 * k + 3] = v.w;
-          }
-        uint32_t s2[NH][8];
-        uint32_t mx = 0u;
-#pragma unroll
-        for (int u = 0; u < NH; ++u) {
-#pragma unroll
-          for (int pl = 0; pl < 8; ++pl)
-            s2[u][pl] = prmt2(mw[u][k_pair_ca<BITS>(pl)], mw[u][k_pair_cb<BITS>(pl)], 0x5410u);
-          const uint32_t m01 = hmax2(s2[u][0], s2[u][1]), m23 = hmax2(s2[u][2], s2[u][3]);
-          const uint32_t m45 = hmax2(s2[u][4], s2[u][5]), m67 = hmax2(s2[u][6], s2[u][7]);
-          const uint32_t m = hmax2(hmax2(m01, m23), hmax2(m45, m67));
-          mx = (u == 0) ? m : hmax2(mx, m);
-        }
-        if (NT == 1) mx = hmax2(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        mx = hmax2(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = hmax2(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        // scales are positive: the larger bit pattern is the larger value
-        const uint32_t smax = max(mx & 0xFFFFu, mx >> 16);
-        const int Es = min(15, 7 - (max((int)(smax >> 10), 1) - 15));  // in [-8, 15]
-        const uint32_t pe = (uint32_t)(Es + 15) << 10;
-        const uint32_t p2 = pe | (pe << 16);  // half2(2^Es, 2^Es)
-        // bias = sum_c x_c (q_min - zp_c) on the tensor cores, from the fragments just
-        // computed: an extra key tile whose column 0 is k_scale 2^-8 (ones, lane g = 0)
-        // and column 1 zp_c k_scale 2^-8 (lane g = 1). With r <= 4, rows g < 4 run on
-        // the first half of the channels and rows g >= 4 on the second in the same MMA,
-        // so lane g = 5 supplies the second half's zero points in column 5 and a query's
-        // bias adds rows q and q + 4.
-        float bt[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        const uint32_t ones_col = (g == 0) ? kOne2 : 0u;
-        const uint32_t zsel = (g == 1 || (NT == 1 && g == 5)) ? kOne2 : 0u;
-#pragma unroll
-        for (int u = 0; u < NH; ++u) {
-          const int h = hh + u;
-          const uint4* qp = reinterpret_cast<const uint4*>(&q2_s[qi][j][8 * h]);
-#pragma unroll
-          for (int k = 0; k < 2; ++k) {  // k-steps 4h + 2k, 4h + 2k + 1
-            const uint4 qv = qp[k];
-            const uint32_t qq[4] = {qv.x, qv.y, qv.z, qv.w};
-            uint32_t f[8];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) hmul2_split(qq[e], hmul2(s2[u][4 * k + e], p2), f[2 * e], f[2 * e + 1]);
-            reinterpret_cast<uint4*>(qa_row)[4 * h + 2 * k] = make_uint4(f[0], f[1], f[2], f[3]);
-            reinterpret_cast<uint4*>(qa_row)[4 * h + 2 * k + 1] = make_uint4(f[4], f[5], f[6], f[7]);
-#pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
-              uint32_t bz[2];
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const int pl = 4 * k + 2 * kk + e;
-                const uint32_t z2 = prmt2(mw[u][k_pair_ca<BITS>(pl)], mw[u][k_pair_cb<BITS>(pl)], 0x7632u);
-                bz[e] = hmul2(hfma2(z2, zsel, ones_col), kc_bits<BITS>(pl));
-              }
-              mma16816(bt, f[4 * kk], f[4 * kk + 1], f[4 * kk + 2], f[4 * kk + 3], bz[0], bz[1]);
-            }
-          }
-        }
-        __syncwarp();
-        // lanes j = 0 hold columns 0 and 1 of rows g (hi) and g + 8 (lo), lanes j = 2 column 5
-        const float t0 = bt[0] + bt[2], tz = bt[1] + bt[3];
-        float bsum;
-        if (NT == 1) {
-          const int q = g & 3;
-          const float ones = __shfl_sync(0xffffffffu, t0, 4 * q) + __shfl_sync(0xffffffffu, t0, 4 * q + 16);
-          const float zz = __shfl_sync(0xffffffffu, tz, 4 * q) + __shfl_sync(0xffffffffu, tz, 4 * q + 18);
-          bsum = qmin * ones - zz;
-        } else {
-          bsum = __shfl_sync(0xffffffffu, qmin * t0 - tz, lane & ~3);
-        }
-        const int E = qe_mine + Es;
-        qscale = pow2f(24 - E) * p.scale_log2;
-        qbias = bsum * pow2f(8 - E) * p.scale_log2;
+        fold_group(st);
       }
       uint32_t kw[2][2][CW];
 #pragma unroll
@@ -731,7 +854,155 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
     bi = qbias;
   };
 
-  // Online softmax and P.V of iteration i (stage st) from its score accumulators.
+  // P.V of one stage from the binary16 softmax weights ph[hf][e] of the lane's B column (token
+  // pairs (2j, 2j+1), e = 0, and (8+2j, 9+2j), e = 1, of each 16-token half hf): weights
+  // w = p * s per value group as binary16 hi/lo halves (lo_mask selects lanes that supply
+  // the lo halves), value codes as the A operand, zero-point sums as one more tile.
+  auto pv = [&](const uint8_t* st, const uint32_t (&ph)[2][2], uint32_t lo_mask) {
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      uint32_t vw[2][CWV];
+#pragma unroll
+      for (int pi = 0; pi < 2; ++pi)
+        lds_chunk<VBITS>(st + St::KB + (8 * hf + 4 * pi + j) * (2 * ROWV) + g * (ROWV / 4), vw[pi]);
+      const __half2* vms = reinterpret_cast<const __half2*>(st + St::KB + St::VB) + 16 * hf * NVG;
+      __half2 mlo[2 * NVG], mhi[2 * NVG];  // tokens (2j, 2j+1) and (8+2j, 9+2j)
+      lds_vmeta<NVG>(vms + (2 * j) * NVG, mlo);
+      lds_vmeta<NVG>(vms + (8 + 2 * j) * NVG, mhi);
+      uint32_t bf[NVG][NT][2];
+#pragma unroll
+      for (int vg = 0; vg < NVG; ++vg) {
+        uint32_t za[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const uint32_t m0 = h2_bits(e ? mhi[vg] : mlo[vg]), m1 = h2_bits(e ? mhi[NVG + vg] : mlo[NVG + vg]);
+          const uint32_t s2 = prmt2(m0, m1, 0x5410u);  // value scales of the token pair
+          const uint32_t whi = hmul2(ph[hf][e], s2);
+          if (NT == 1) {
+            bf[vg][0][e] = hfma2(ph[hf][e], s2, (whi ^ 0x80008000u) & lo_mask);
+          } else {
+            bf[vg][0][e] = whi;
+            bf[vg][NT - 1][e] = hfma2(ph[hf][e], s2, hneg2(whi));
+          }
+          za[e] = prmt2(m0, m1, 0x7632u);  // zero points of the token pair
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma16816(bacc[vg], kOne2, za[0], kOne2, za[1], bf[vg][nt][0], bf[vg][nt][1]);
+      }
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        const int vg = (mt * NVG) / 8;  // compile-time after unrolling
+        const uint32_t a0 = v_pair<VBITS>(vw[0], 2 * mt), a1 = v_pair<VBITS>(vw[0], 2 * mt + 1);
+        const uint32_t a2 = v_pair<VBITS>(vw[1], 2 * mt), a3 = v_pair<VBITS>(vw[1], 2 * mt + 1);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma16816(o[mt], a0, a1, a2, a3, bf[vg][nt][0], bf[vg][nt][1]);
+      }
+    }
+  };
+
+  // r <= 4: online softmax of query qj over the lane's tokens 16hf + g and 16hf + 8 + g, then
+  // the weights, packed to binary16 and transposed into the B-operand layout of P.V.
+  auto softmax_pv_t = [&](int i, const uint8_t* st, const float (&acc)[2][4], float sc, float bi) {
+    const int ts = ts0 + i * kTok;
+    float s[2][2];  // [hf][e]: token ts + 16hf + 8e + g, log2 units
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) s[hf][e] = fmaf(acc[hf][2 * e] + acc[hf][2 * e + 1], sc, bi);
+    if constexpr (SYM) {  // score of token t = s_t * (2^24 acc + q_min sum_c q_c), log2 units
+      const __half* ksc = reinterpret_cast<const __half*>(st + St::KB + St::VB + St::VM);
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float kk = __half2float(ksc[16 * hf + 8 * e + g]);
+          s[hf][e] = (kk * p.scale_log2) * fmaf(acc[hf][2 * e] + acc[hf][2 * e + 1], kTwo24, qmin_qsum);
+        }
+      if constexpr (OUTL) {  // the sparse side list: x_c * q_c of every isolated key entry
+        // lane l takes token l: its entries (channel | binary16 value << 16) against every
+        // query row into the warp's table sp_w[token][row] (rows of kMaxGqa + 1 words: no
+        // bank conflicts), then every score lane reads its (token, row) term back
+        const uint32_t* ent = reinterpret_cast<const uint32_t*>(st + St::KB + St::VB + St::VM + 64);
+        float* sp_w = reinterpret_cast<float*>(smem + St::SP) + warp * 32 * St::SP_ROW;
+        const int ko = p.kout;
+        uint32_t en[4];
+        if (ko == 4) {
+          const uint4 e4 = *reinterpret_cast<const uint4*>(ent + 4 * lane);
+          en[0] = e4.x; en[1] = e4.y; en[2] = e4.z; en[3] = e4.w;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) en[e] = e < ko ? ent[lane * ko + e] : 0u;  // missing: channel 0, value +0
+        }
+        float xv[4];
+        int ch[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          xv[e] = __half2float(__ushort_as_half((unsigned short)(en[e] >> 16)));
+          ch[e] = (int)(en[e] & (kHeadDim - 1));
+        }
+        constexpr int kRows = NT == 1 ? 4 : kMaxGqa;
+#pragma unroll
+        for (int row = 0; row < kRows; ++row)
+          if (row < r) {
+            float sp = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sp = fmaf(xv[e], q_s[row][ch[e]], sp);
+            sp_w[lane * St::SP_ROW + row] = sp;
+          }
+        __syncwarp();
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            s[hf][e] = fmaf(sp_w[(16 * hf + 8 * e + g) * St::SP_ROW + qj], p.scale_log2, s[hf][e]);
+        __syncwarp();  // the table is rewritten in the next iteration
+      }
+    }
+    if (ts + kTok > t_end) {  // ragged last iteration
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+          if (ts + 16 * hf + 8 * e + g >= t_end) s[hf][e] = -__int_as_float(0x7f800000);
+    }
+    // lazy rescale as in softmax_pv; the column max gathers the 8 lanes g of query qj
+    constexpr float kTau = VBITS == 8 ? 6.0f : (VBITS == 4 ? 2.0f : 0.5f);
+    float mx = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+    if (__any_sync(0xffffffffu, mx > m_run + kTau)) {
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const float m_new = fmaxf(m_run, mx);
+      const float alpha = ex2(m_run - m_new);  // 0 on the first iteration (m_run = -inf)
+      l_run *= alpha;
+      // P.V columns 2j, 2j + 1 (and the zero-point tile's) belong to this lane's query
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[mt][e] *= alpha;
+#pragma unroll
+      for (int k = 0; k < NVG; ++k)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) bacc[k][e] *= alpha;
+      m_run = m_new;
+    }
+    // p rounded once to binary16 (the denominator sums the same values); lane (g, j) holds
+    // row g, columns 2j and 2j + 1 of an 8x8 matrix [token][column] whose column n carries
+    // query n / 2 — both columns p(token, qj) — and its transpose is the P.V B fragment
+    // of column g: tokens (2j, 2j + 1) of query g / 2
+    uint32_t ph[2][2];
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const __half2 h = __float2half2_rn(ex2(s[hf][e] - m_run));
+        l_run += __low2float(h);
+        ph[hf][e] = movmatrix_t(h2_bits(h));
+      }
+    pv(st, ph, (g & 1) ? 0xFFFFFFFFu : 0u);  // odd columns carry the lo halves
+  };
+
+  // r > 4: online softmax and P.V of iteration i (stage st) from its score accumulators.
   auto softmax_pv = [&](int i, const uint8_t* st, const float (&acc)[2][2][4], float sc, float bi) {
     const int ts = ts0 + i * kTok;
     // scores (log2 units) of tokens ts + 16hf + {2j, 2j+1, 8+2j, 9+2j} for query qi
@@ -843,49 +1114,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
         l_run += f.x + f.y;
         ph[hf][e] = h2_bits(h);
       }
-    // NT == 1: lanes g < 4 supply the hi halves of their query's weights, lanes g >= 4 the lo
-    // halves: out = fl(p s + c) with c = 0 (hi) or c = -fl(p s) (lo)
-    const uint32_t lo_mask = lo_lane ? 0xFFFFFFFFu : 0u;
-    // values: weights p * s per value group, as binary16 hi/lo halves
-#pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-      uint32_t vw[2][CWV];
-#pragma unroll
-      for (int pi = 0; pi < 2; ++pi)
-        lds_chunk<VBITS>(st + St::KB + (8 * hf + 4 * pi + j) * (2 * ROWV) + g * (ROWV / 4), vw[pi]);
-      const __half2* vms = reinterpret_cast<const __half2*>(st + St::KB + St::VB) + 16 * hf * NVG;
-      __half2 mlo[2 * NVG], mhi[2 * NVG];  // tokens (2j, 2j+1) and (8+2j, 9+2j)
-      lds_vmeta<NVG>(vms + (2 * j) * NVG, mlo);
-      lds_vmeta<NVG>(vms + (8 + 2 * j) * NVG, mhi);
-      uint32_t bf[NVG][NT][2];
-#pragma unroll
-      for (int vg = 0; vg < NVG; ++vg) {
-        uint32_t za[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const uint32_t m0 = h2_bits(e ? mhi[vg] : mlo[vg]), m1 = h2_bits(e ? mhi[NVG + vg] : mlo[NVG + vg]);
-          const uint32_t s2 = prmt2(m0, m1, 0x5410u);  // value scales of the token pair
-          const uint32_t whi = hmul2(ph[hf][e], s2);
-          if (NT == 1) {
-            bf[vg][0][e] = hfma2(ph[hf][e], s2, (whi ^ 0x80008000u) & lo_mask);
-          } else {
-            bf[vg][0][e] = whi;
-            bf[vg][NT - 1][e] = hfma2(ph[hf][e], s2, hneg2(whi));
-          }
-          za[e] = prmt2(m0, m1, 0x7632u);  // zero points of the token pair
-        }
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma16816(bacc[vg], kOne2, za[0], kOne2, za[1], bf[vg][nt][0], bf[vg][nt][1]);
-      }
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        const int vg = (mt * NVG) / 8;  // compile-time after unrolling
-        const uint32_t a0 = v_pair<VBITS>(vw[0], 2 * mt), a1 = v_pair<VBITS>(vw[0], 2 * mt + 1);
-        const uint32_t a2 = v_pair<VBITS>(vw[1], 2 * mt), a3 = v_pair<VBITS>(vw[1], 2 * mt + 1);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma16816(o[mt], a0, a1, a2, a3, bf[vg][nt][0], bf[vg][nt][1]);
-      }
-    }
+    pv(st, ph, 0u);
   };
 
   int failed_at = -1;
@@ -897,10 +1126,16 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
       break;
     }
     const uint8_t* st = wbase + sidx * St::BYTES;
-    float acc[2][2][4];
     float sc, bi;
-    qk(i, st, acc, sc, bi);
-    softmax_pv(i, st, acc, sc, bi);
+    if constexpr (NT == 1) {
+      float acc[2][4];
+      qk_t(i, st, acc, sc, bi);
+      softmax_pv_t(i, st, acc, sc, bi);
+    } else {
+      float acc[2][2][4];
+      qk(i, st, acc, sc, bi);
+      softmax_pv(i, st, acc, sc, bi);
+    }
     __syncwarp();  // every lane is done with stage sidx
     if (i + NS < n_mine) issue(i + NS, sidx);
     if (++sidx == NS) {
@@ -925,44 +1160,57 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
   float* m_s = o_s + kWarps * kMaxGqa * kHeadDim;
   float* l_s = m_s + kWarps * kMaxGqa;
   float* beta_s = l_s + kWarps * kMaxGqa;  // [kWarps][kMaxGqa][NVG]
-  l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-  l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
-  if (j == 0 && g < r) {  // row g holds query g for g < r
-    m_s[warp * kMaxGqa + g] = m_run;
-    l_s[warp * kMaxGqa + g] = l_run;
-  }
-  // zero-point terms beta = q_min * sum_t w_t - sum_t zp_t w_t of queries 2j and 2j+1
-  // (columns 2j, 2j+1); NT == 1 adds the lo columns 4..7 (lanes j + 2)
+  if constexpr (NT == 1) {
+    // lanes (g, j) hold query j: its denominator over the 8 lanes g, its zero-point sums in
+    // columns 2j (hi) and 2j + 1 (lo) of rows 0 (sum w) and 8 (sum zp w), its outputs in
+    // columns 2j, 2j + 1 of channel rows g and g + 8 of every m-tile
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 4);
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 8);
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 16);
+    if (g == 0 && j < r) {
+      m_s[warp * kMaxGqa + j] = m_run;
+      l_s[warp * kMaxGqa + j] = l_run;
 #pragma unroll
-  for (int k = 0; k < NVG; ++k) {
-    float t[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      t[e] = bacc[k][e];
-      if (NT == 1) t[e] += __shfl_xor_sync(0xffffffffu, t[e], 2);
+      for (int k = 0; k < NVG; ++k)
+        beta_s[(warp * kMaxGqa + j) * NVG + k] = qmin_v * (bacc[k][0] + bacc[k][1]) - (bacc[k][2] + bacc[k][3]);
     }
-    if (g == 0 && (NT == 2 || j < 2)) {
-      if (2 * j < r) beta_s[(warp * kMaxGqa + 2 * j) * NVG + k] = qmin_v * t[0] - t[2];
-      if (2 * j + 1 < r) beta_s[(warp * kMaxGqa + 2 * j + 1) * NVG + k] = qmin_v * t[1] - t[3];
+    if (j < r) {
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        const float sc0 = 1.0f / v_scale<VBITS>(2 * mt), sc1 = 1.0f / v_scale<VBITS>(2 * mt + 1);
+        const int c0 = 16 * mt + g;
+        o_s[(warp * kMaxGqa + j) * kHeadDim + c0] = (o[mt][0] + o[mt][1]) * sc0;
+        o_s[(warp * kMaxGqa + j) * kHeadDim + c0 + 8] = (o[mt][2] + o[mt][3]) * sc1;
+      }
     }
-  }
-  // PV columns: NT == 1: cols 0..3 hi / 4..7 lo of queries 0..3; NT == 2: queries 0..7 (hi + lo)
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt) {
-    float v[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) v[e] = o[mt][e];
-    if (NT == 1) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) v[e] += __shfl_xor_sync(0xffffffffu, v[e], 2);  // lo columns j+2 -> j
+  } else {  // r > 4: row g holds query g; PV columns 2j, 2j + 1 queries 2j, 2j + 1 (hi + lo)
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+    if (j == 0 && g < r) {
+      m_s[warp * kMaxGqa + g] = m_run;
+      l_s[warp * kMaxGqa + g] = l_run;
     }
-    const float sc0 = 1.0f / v_scale<VBITS>(2 * mt), sc1 = 1.0f / v_scale<VBITS>(2 * mt + 1);
-    v[0] *= sc0; v[1] *= sc0; v[2] *= sc1; v[3] *= sc1;
-    if ((NT == 2) || (j < 2)) {
+    // zero-point terms beta = q_min * sum_t w_t - sum_t zp_t w_t of queries 2j and 2j + 1
+#pragma unroll
+    for (int k = 0; k < NVG; ++k) {
+      if (g == 0) {
+        if (2 * j < r) beta_s[(warp * kMaxGqa + 2 * j) * NVG + k] = qmin_v * bacc[k][0] - bacc[k][2];
+        if (2 * j + 1 < r) beta_s[(warp * kMaxGqa + 2 * j + 1) * NVG + k] = qmin_v * bacc[k][1] - bacc[k][3];
+      }
+    }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      const float sc0 = 1.0f / v_scale<VBITS>(2 * mt), sc1 = 1.0f / v_scale<VBITS>(2 * mt + 1);
       const int i0 = 2 * j, i1 = 2 * j + 1;
       const int c0 = 16 * mt + g, c1 = c0 + 8;
-      if (i0 < r) { o_s[(warp * kMaxGqa + i0) * kHeadDim + c0] = v[0]; o_s[(warp * kMaxGqa + i0) * kHeadDim + c1] = v[2]; }
-      if (i1 < r) { o_s[(warp * kMaxGqa + i1) * kHeadDim + c0] = v[1]; o_s[(warp * kMaxGqa + i1) * kHeadDim + c1] = v[3]; }
+      if (i0 < r) {
+        o_s[(warp * kMaxGqa + i0) * kHeadDim + c0] = o[mt][0] * sc0;
+        o_s[(warp * kMaxGqa + i0) * kHeadDim + c1] = o[mt][2] * sc1;
+      }
+      if (i1 < r) {
+        o_s[(warp * kMaxGqa + i1) * kHeadDim + c0] = o[mt][1] * sc0;
+        o_s[(warp * kMaxGqa + i1) * kHeadDim + c1] = o[mt][3] * sc1;
+      }
     }
   }
   __syncthreads();
