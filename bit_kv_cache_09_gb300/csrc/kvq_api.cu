@@ -3,6 +3,7 @@
 // before any launch, and a failed check launches nothing.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 
@@ -119,6 +120,11 @@ struct Plan {
   int64_t n_split, chunk;
   int cluster, n_parts;
   int warps = 4;
+  // mixed plan: the first pairs_hi pairs take n_split splits of `chunk` tokens, the others
+  // n_split - 1 splits of chunk_lo tokens; every pair merges through the workspace
+  int mixed = 0;
+  int pairs_hi = 0;
+  int64_t chunk_lo = 0;
 };
 
 Plan plan_splits(const Geometry& g, int64_t T, kvq_decode_impl impl) {
@@ -178,6 +184,44 @@ Plan plan_splits(const Geometry& g, int64_t T, kvq_decode_impl impl) {
       resident_clusters(g, (int)pl.n_split, 4) > 0) {
     pl.cluster = (int)pl.n_split;
     pl.n_parts = 1;
+  }
+  // Balanced alternative (tensor-core kernel): fill the resident slots exactly, k splits for
+  // most pairs and k + 1 for the rest. The loop is bound by instruction issue per SM, so a
+  // launch lasts as long as its busiest SM's share of work, and with equal splits that do
+  // not fill the slots some SMs hold one CTA more than others. Busiest SM, in warp
+  // iterations, with CTAs spread over the SMs in launch order: the uniform plan's
+  // ceil(CTAs / SMs) CTAs; the mixed plan's ceil(long CTAs / SMs) long and the rest short
+  // ones. Ties keep the uniform plan, and so does a uniform plan that merges its splits in
+  // clusters: measured on GB300, the balance then does not pay for the workspace merge
+  // (kivi-int4 +0.5 %, kivi-k8v4 -3 %), while it does against one split per pair
+  // (kivi-int2 +9 %).
+  if (impl != KVQ_DECODE_SIMT && pl.cluster == 1) {
+    const int64_t occ = slots / sms;
+    const int64_t k = slots / units;  // splits of most pairs
+    const int64_t pairs_hi = slots - units * k;
+    auto warp_iters = [&](int64_t chunk) { return (chunk / 32 + 3) / 4; };
+    auto chunk_of = [&](int64_t splits) { return ((T + splits - 1) / splits + align - 1) / align * align; };
+    if (k >= 1 && pairs_hi > 0 && k + 1 <= max_k) {
+      const int64_t c_hi = chunk_of(k + 1), c_lo = chunk_of(k);
+      if ((T + c_hi - 1) / c_hi == k + 1 && (T + c_lo - 1) / c_lo == k) {
+        const int64_t n_long = (units - pairs_hi) * k;
+        const int64_t per_sm_long = std::min<int64_t>(occ, (n_long + sms - 1) / sms);
+        const int64_t mixed_cost = per_sm_long * (fixed_it + warp_iters(c_lo)) +
+                                   (occ - per_sm_long) * (fixed_it + warp_iters(c_hi));
+        const int64_t n_uni = units * pl.n_split;
+        const int64_t uni_cost = n_uni <= slots ? ((n_uni + sms - 1) / sms) * (fixed_it + warp_iters(pl.chunk))
+                                                : ((n_uni + slots - 1) / slots) * occ * (fixed_it + warp_iters(pl.chunk));
+        if (mixed_cost < uni_cost) {
+          pl.mixed = 1;
+          pl.n_split = k + 1;
+          pl.chunk = c_hi;
+          pl.chunk_lo = c_lo;
+          pl.pairs_hi = (int)pairs_hi;
+          pl.cluster = 1;
+          pl.n_parts = (int)(k + 1);
+        }
+      }
+    }
   }
   return pl;
 }
@@ -385,6 +429,11 @@ kvq_status decode_prepare(const kvq_config* cfg, const kvq_buffers* bufs, int32_
   p.cluster = pl.cluster;
   p.n_parts = pl.n_parts;
   p.warps = pl.warps;
+  p.mixed = pl.mixed;
+  p.n_hi = (int)pl.n_split;
+  p.pairs_hi = pl.pairs_hi;
+  p.chunk_hi = pl.chunk;
+  p.chunk_lo = pl.chunk_lo;
   p.sym = g.sym;
   p.early = (early && use == KVQ_DECODE_MMA) ? 1 : 0;
   call->simt = use == KVQ_DECODE_SIMT;

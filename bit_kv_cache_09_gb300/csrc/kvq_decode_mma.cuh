@@ -373,7 +373,34 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
   // rings: with early prefetch their first stages are already being filled.
   __shared__ __align__(16) uint8_t append_s[kHeadDim];
 
-  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  // this CTA's (batch row, kv head) pair, split, split length and the number of parts its
+  // pair merges through the workspace
+  int split, h, b, n_parts;
+  int64_t chunk;
+  if (p.mixed) {
+    const int c = blockIdx.x, ctas_hi = p.pairs_hi * p.n_hi;
+    int pair;
+    if (c < ctas_hi) {
+      pair = c / p.n_hi;
+      split = c - pair * p.n_hi;
+      n_parts = p.n_hi;
+      chunk = p.chunk_hi;
+    } else {
+      const int n_lo = p.n_hi - 1, c2 = c - ctas_hi;
+      pair = p.pairs_hi + c2 / n_lo;
+      split = c2 - (c2 / n_lo) * n_lo;
+      n_parts = n_lo;
+      chunk = p.chunk_lo;
+    }
+    b = pair / p.H;
+    h = pair - b * p.H;
+  } else {
+    split = blockIdx.x;
+    h = blockIdx.y;
+    b = blockIdx.z;
+    n_parts = p.n_parts;
+    chunk = p.chunk;
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, j = lane & 3;
   const int r = p.r;
@@ -382,8 +409,8 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
   const int64_t qrow0 = (int64_t)b * p.H * r + (int64_t)h * r;
 
   const int T = (int)p.T, Tq = (int)p.Tq;
-  const int t_begin = split * (int)p.chunk;  // chunk is a multiple of 32
-  const int t_end = min(t_begin + (int)p.chunk, T);
+  const int t_begin = split * (int)chunk;  // chunk is a multiple of 32
+  const int t_end = min(t_begin + (int)chunk, T);
   const int n_it = max(0, (t_end - t_begin + kTok - 1) / kTok);  // 0 for a trailing empty split
   // balanced contiguous runs of iterations per warp (warp w: [w*n_it/NW, (w+1)*n_it/NW))
   const int it0 = (warp * n_it) / kWarps;
@@ -1236,7 +1263,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
       acc += wt * fmaf(o_s[(w * kMaxGqa + i) * kHeadDim + c], kTwo24, beta_s[(w * kMaxGqa + i) * NVG + vgc]);
     }
     if (p.cluster == 1) {  // no cluster: this CTA's partial is the split's partial
-      if (p.n_parts == 1) {
+      if (n_parts == 1) {
         p.out[(qrow0 + i) * kHeadDim + c] = acc / L;
       } else {
         p.ws_o[((qrow0 + i) * p.cap + split) * kHeadDim + c] = acc;
@@ -1253,7 +1280,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
   if (p.cluster == 1) {
     // the workspace merge runs with 4-warp CTAs only (the host never plans NW = 8 with parts)
     if constexpr (NW == 4) {
-      if (p.n_parts > 1) merge_if_last(p, slice, qrow0, reinterpret_cast<float*>(smem + St::EP_SCRATCH));
+      if (n_parts > 1) merge_if_last(p, n_parts, slice, qrow0, reinterpret_cast<float*>(smem + St::EP_SCRATCH));
     }
     return;
   }
@@ -1293,19 +1320,19 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
           acc += wt * oq[q];
         }
       }
-      if (p.n_parts == 1) {
+      if (n_parts == 1) {
         p.out[(qrow0 + i) * kHeadDim + cc] = acc / L;
       } else {
         p.ws_o[((qrow0 + i) * p.cap + part) * kHeadDim + cc] = acc;
         if (rank == 0 && o_idx % S == 0) p.ws_ml[(qrow0 + i) * p.cap + part] = make_float2(M, L);
       }
     }
-    if (p.n_parts > 1) __threadfence();  // slices visible device-wide before the ticket
+    if (n_parts > 1) __threadfence();  // slices visible device-wide before the ticket
   }
   cluster.sync();  // the other CTAs keep their shared memory until every rank has read it
   if constexpr (NW == 4) {
-    if (p.n_parts > 1 && cluster.block_rank() == 0)
-      merge_if_last(p, slice, qrow0, reinterpret_cast<float*>(smem + St::EP_SCRATCH));
+    if (n_parts > 1 && cluster.block_rank() == 0)
+      merge_if_last(p, n_parts, slice, qrow0, reinterpret_cast<float*>(smem + St::EP_SCRATCH));
   }
 }
 
@@ -1317,12 +1344,14 @@ cudaError_t launch_cfg(const DecodeParams& p, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   if (p.cluster < 1 || p.cluster > 16 || (p.cluster & (p.cluster - 1)) || p.n_split != p.cluster * p.n_parts)
     return cudaErrorInvalidConfiguration;
+  if (p.mixed && (p.cluster != 1 || p.n_hi < 2 || p.pairs_hi < 1 || p.pairs_hi >= p.B * p.H)) return cudaErrorInvalidConfiguration;
   if (p.cluster > 8) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)p.n_split, (unsigned)p.H, (unsigned)p.B);
+  cfg.gridDim = p.mixed ? dim3((unsigned)(p.pairs_hi * p.n_hi + (p.B * p.H - p.pairs_hi) * (p.n_hi - 1)), 1u, 1u)
+                        : dim3((unsigned)p.n_split, (unsigned)p.H, (unsigned)p.B);
   cfg.blockDim = dim3(NW * 32, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;

@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(128) decode_simt_kernel(DecodeParams p) {
   }
   for (int i = 0; i < p.r; ++i) p.ws_o[((qrow0 + i) * p.cap + split) * kHeadDim + c_own] = o[i];
   if (tid < p.r) p.ws_ml[(qrow0 + tid) * p.cap + split] = make_float2(m_s[tid], l_s[tid]);
-  merge_if_last(p, slice, qrow0, &qk_s[0][0][0]);  // the folded-query buffer is free now
+  merge_if_last(p, p.n_parts, slice, qrow0, &qk_s[0][0][0]);  // the folded-query buffer is free now
 }
 
 }  // namespace

@@ -100,6 +100,12 @@ struct DecodeParams {
   int64_t T, Tq;
   int64_t chunk;      // tokens per split (multiple of 128)
   int n_split, cap;
+  // mixed plan (tensor-core kernel, no clusters): a one-dimensional grid where the first
+  // pairs_hi (batch row, kv head) pairs take n_hi splits of chunk_hi tokens and the other
+  // pairs n_hi - 1 splits of chunk_lo tokens (pairs in slice order); 0: grid (n_split, H, B)
+  int mixed;
+  int n_hi, pairs_hi;
+  int64_t chunk_hi, chunk_lo;
   int cluster;        // CTAs per cluster (splits merged through distributed shared memory)
   int warps;          // warps per CTA of the tensor-core kernel: 4, or 8 (cluster merges only)
   int n_parts;        // partials merged through the workspace: n_split / cluster

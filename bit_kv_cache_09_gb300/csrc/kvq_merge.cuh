@@ -20,10 +20,12 @@ constexpr int kMaxSplits = 256;
 
 constexpr int kMergeScratchFloats = kMaxGqa * kMaxSplits + kMaxGqa;
 
-// Called by all 128 threads of the CTA after it wrote its partials. Returns after
+// Called by all 128 threads of the CTA after it wrote its partials (n_parts: partials of
+// this CTA's pair). Returns after
 // writing the outputs if this CTA was the last of its (batch row, kv head).
 // `scratch`: shared memory of at least kMergeScratchFloats floats, free for reuse.
-__device__ __forceinline__ void merge_if_last(const DecodeParams& p, int64_t slice, int64_t qrow0, float* scratch) {
+__device__ __forceinline__ void merge_if_last(const DecodeParams& p, int n_parts, int64_t slice, int64_t qrow0,
+                                              float* scratch) {
   __shared__ int last_s;
   float (*w_s)[kMaxSplits] = reinterpret_cast<float (*)[kMaxSplits]>(scratch);
   float* inv_l_s = scratch + kMaxGqa * kMaxSplits;
@@ -31,7 +33,7 @@ __device__ __forceinline__ void merge_if_last(const DecodeParams& p, int64_t sli
   __syncthreads();
   if (threadIdx.x == 0) {
     const uint32_t ticket = atomicAdd(&p.tickets[slice], 1u);
-    last_s = (ticket == (uint32_t)(p.n_parts - 1));
+    last_s = (ticket == (uint32_t)(n_parts - 1));
   }
   __syncthreads();
   if (!last_s) return;
@@ -45,7 +47,7 @@ __device__ __forceinline__ void merge_if_last(const DecodeParams& p, int64_t sli
 #pragma unroll
     for (int k = 0; k < kMaxSplits / 32; ++k) {
       const int s = lane + 32 * k;
-      v[k] = (s < p.n_parts) ? __ldcg(&ml[s]) : make_float2(-__int_as_float(0x7f800000), 0.0f);
+      v[k] = (s < n_parts) ? __ldcg(&ml[s]) : make_float2(-__int_as_float(0x7f800000), 0.0f);
       M = fmaxf(M, v[k].x);
     }
 #pragma unroll
@@ -54,7 +56,7 @@ __device__ __forceinline__ void merge_if_last(const DecodeParams& p, int64_t sli
 #pragma unroll
     for (int k = 0; k < kMaxSplits / 32; ++k) {
       const int s = lane + 32 * k;
-      if (s < p.n_parts) {
+      if (s < n_parts) {
         const float wt = exp2f(v[k].x - M);
         w_s[i][s] = wt;
         L += wt * v[k].y;
@@ -70,20 +72,20 @@ __device__ __forceinline__ void merge_if_last(const DecodeParams& p, int64_t sli
   float acc[kMaxGqa];
 #pragma unroll
   for (int i = 0; i < kMaxGqa; ++i) acc[i] = 0.0f;
-  for (int s0 = 0; s0 < p.n_parts; s0 += 4) {
+  for (int s0 = 0; s0 < n_parts; s0 += 4) {
     float ov[kMaxGqa][4];
 #pragma unroll
     for (int i = 0; i < kMaxGqa; ++i)
 #pragma unroll
       for (int u = 0; u < 4; ++u)
-        ov[i][u] = (i < p.r && s0 + u < p.n_parts)
+        ov[i][u] = (i < p.r && s0 + u < n_parts)
                        ? __ldcg(p.ws_o + ((qrow0 + i) * p.cap + s0 + u) * kHeadDim + c)
                        : 0.0f;
 #pragma unroll
     for (int i = 0; i < kMaxGqa; ++i)
 #pragma unroll
       for (int u = 0; u < 4; ++u)
-        if (i < p.r && s0 + u < p.n_parts) acc[i] = fmaf(w_s[i][s0 + u], ov[i][u], acc[i]);
+        if (i < p.r && s0 + u < n_parts) acc[i] = fmaf(w_s[i][s0 + u], ov[i][u], acc[i]);
   }
 #pragma unroll
   for (int i = 0; i < kMaxGqa; ++i)

@@ -272,8 +272,9 @@ kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const kvq_buffers
  * that call it allocates nothing; it synchronizes `stream`. */
 kvq_status kvq_decode_noalloc_error(void* stream, uint32_t* err_out);
 
-/* Number of split-K partitions kvq_decode_attention uses for s_cur tokens (>= 1),
- * or 0 for a bad config. */
+/* Number of split-K partitions kvq_decode_attention gives a (batch row, kv head) pair
+ * for s_cur tokens (>= 1; when pairs get different counts, the largest), or 0 for a bad
+ * config. */
 int32_t kvq_decode_num_splits(const kvq_config* cfg, int64_t s_cur);
 
 /* Human-readable name of a status code (static string). */
