@@ -38,9 +38,10 @@ DEFAULT_WORKLOAD = "kivi-int2"  # the largest single-GPU workload: int2, batch 6
 # ----------------------------------------------------------------------------- byte accounting
 def key_meta_bytes(w, n_keys: int) -> int:
     """Key metadata of n_keys quantized tokens of one slice: (scale, zero point) per channel
-    and group of k_group tokens, or in the symmetric scheme one binary16 scale per token
+    and group of k_group tokens, or in the symmetric scheme one binary16 scale per token;
     plus 4 bytes (channel, binary16 value) per isolated key entry."""
-    return n_keys * (2 + 4 * w.k_outliers) if w.symmetric else (n_keys // w.k_group) * w.d_head * 4
+    iso = n_keys * 4 * w.k_outliers  # isolated entries of the quantized key rows
+    return n_keys * 2 + iso if w.symmetric else (n_keys // w.k_group) * w.d_head * 4 + iso
 
 
 def attn_bytes_per_layer(w, T: int) -> int:
@@ -226,7 +227,7 @@ def oracle_prepare(w, layer: int, T: int, n_slices: int, budget_s: float = float
             st = oracle.cache_state_sym(k, v, d=w.d_head, k_outliers=w.k_outliers)
         else:
             st = oracle.cache_state(k, v, d=w.d_head, bits=w.bits, G=w.k_group, Gv=w.v_group, R=w.residual,
-                                    v_bits=w.vbits)
+                                    v_bits=w.vbits, k_outliers=w.k_outliers)
         t_pre += time.perf_counter() - t0
         b_pre += prefill_bytes_per_layer(w, T) // (w.batch * w.n_kv)
         out.append((st, synth.q_rows(w, layer, b, h, T - 1)))

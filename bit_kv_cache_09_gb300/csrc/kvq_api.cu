@@ -55,12 +55,16 @@ int device_sm_count() {
 // Index of the (key, value) code widths: 8/8, 4/4, 2/2, 8/4.
 int width_index(const Geometry& g) {
   if (g.sym) return g.kout > 0 ? 5 : 4;  // symmetric per-token int8 (with isolated key entries)
-  if (g.vbits != g.bits) return 3;
-  return g.bits == 8 ? 0 : (g.bits == 4 ? 1 : 2);
+  const int w = g.vbits != g.bits ? 3 : (g.bits == 8 ? 0 : (g.bits == 4 ? 1 : 2));
+  return g.kout > 0 ? 6 + w : w;  // per-channel keys, with isolated key entries: 6..9
 }
 
+// Kernel family of the occupancy queries: 0 asymmetric, 1 symmetric, 2 symmetric with
+// isolated key entries, 3 asymmetric with isolated key entries.
+int scheme(const Geometry& g) { return g.sym ? (g.kout > 0 ? 2 : 1) : (g.kout > 0 ? 3 : 0); }
+
 int decode_occupancy(const Geometry& g, kvq_decode_impl impl) {
-  static std::atomic<int> cache[16][2][6][2][3];  // device, impl, code scheme/widths, r class, value groups
+  static std::atomic<int> cache[16][2][10][2][3];  // device, impl, code scheme/widths, r class, value groups
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) dev = 0;
   const int ii = impl == KVQ_DECODE_SIMT ? 0 : 1;
@@ -71,7 +75,7 @@ int decode_occupancy(const Geometry& g, kvq_decode_impl impl) {
   int n = slot.load(std::memory_order_relaxed);
   if (n <= 0) {
     n = ii == 0 ? kvq::occupancy_decode_simt(g.bits)
-                : kvq::occupancy_decode_mma(g.bits, g.vbits, g.r, g.n_vg, g.sym ? (g.kout > 0 ? 2 : 1) : 0);
+                : kvq::occupancy_decode_mma(g.bits, g.vbits, g.r, g.n_vg, scheme(g));
     if (n > 0) slot.store(n, std::memory_order_relaxed);
   }
   return n > 0 ? n : 1;
@@ -81,7 +85,7 @@ int decode_occupancy(const Geometry& g, kvq_decode_impl impl) {
 // kernel that can be resident at once on this device (<= 0: such a cluster cannot
 // launch); cached per device and kernel shape.
 int resident_clusters(const Geometry& g, int cs, int nw) {
-  static std::atomic<int> cache[16][6][2][3][5][3];  // device, code scheme/widths, r class, value groups, log2 size, warps
+  static std::atomic<int> cache[16][10][2][3][5][3];  // device, code scheme/widths, r class, value groups, log2 size, warps
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) dev = 0;
   const int bi = width_index(g);
@@ -92,7 +96,7 @@ int resident_clusters(const Geometry& g, int cs, int nw) {
   std::atomic<int>& slot = cache[dev][bi][ri][vi][lg][nw == 8 ? 2 : (nw == 5 ? 1 : 0)];
   int n = slot.load(std::memory_order_relaxed);
   if (n == 0) {
-    n = kvq::max_clusters_decode_mma(g.bits, g.vbits, g.r, g.n_vg, cs, nw, g.sym ? (g.kout > 0 ? 2 : 1) : 0);
+    n = kvq::max_clusters_decode_mma(g.bits, g.vbits, g.r, g.n_vg, cs, nw, scheme(g));
     if (n <= 0) n = -1;
     slot.store(n, std::memory_order_relaxed);
   }
@@ -381,7 +385,7 @@ kvq_status decode_prepare(const kvq_config* cfg, const kvq_buffers* bufs, int32_
   const kvq_decode_impl use = impl == KVQ_DECODE_SIMT ? KVQ_DECODE_SIMT : KVQ_DECODE_MMA;
   if (use == KVQ_DECODE_SIMT && (k_new || v_new)) return KVQ_ERR_UNSUPPORTED;
   if (use == KVQ_DECODE_SIMT && g.vbits != g.bits) return KVQ_ERR_UNSUPPORTED;  // CUDA-core kernel: equal widths
-  if (use == KVQ_DECODE_SIMT && g.sym) return KVQ_ERR_UNSUPPORTED;              // and the asymmetric scheme
+  if (use == KVQ_DECODE_SIMT && (g.sym || g.kout > 0)) return KVQ_ERR_UNSUPPORTED;  // and plain asymmetric keys
   const LayerPtrs lp = layer_ptrs(g, bufs, layer);
   kvq::DecodeParams& p = call->p;
   p = kvq::DecodeParams{};

@@ -3,7 +3,8 @@
 // Geometry of the packed cache (see include/kvq.h for the byte layout):
 //   slice (layer l, batch row b, kv head h) = (l * B + b) * H + h
 //   k_codes slice: S_pad rows of rowK = d*b/8 bytes
-//   k_meta  slice: S_pad/G groups x d x half2(scale, zero_point)
+//   k_meta  slice: S_pad/G groups x d x half2(scale, zero_point), then (kout > 0)
+//                  S_pad x kout isolated entries {channel u16, value binary16}
 //   k_resid slice: R_eff rows x d binary16
 //   v_codes slice: S_pad/2 pair rows of 2*rowV bytes (rowV = d*b/8)
 //   v_meta  slice: S_pad tokens x d/Gv x half2(scale, zero_point)
@@ -27,7 +28,7 @@ constexpr int kMaxResidual = 1024;
 struct Geometry {
   int L, B, H, r, d, S_max, bits, vbits, G, Gv, R, R_eff;  // bits: keys, vbits: values
   int sym;             // symmetric per-token int8 scheme
-  int kout;            // symmetric scheme: isolated key entries per token
+  int kout;            // isolated key entries per token (both schemes)
   int64_t S_pad;
   int64_t rowK, rowV;  // bytes per token row of key / value codes
   int n_vg;            // value groups per token (d / Gv)
@@ -56,7 +57,8 @@ inline kvq_status make_geometry(const kvq_config* c, Geometry* g) {
   if (c->symmetric && (c->bits != 8 || vbits != 8 || c->v_group != c->d_head)) return KVQ_ERR_UNSUPPORTED;
   if (c->symmetric && c->residual_len != 0) return KVQ_ERR_INVALID_ARG;  // no residual window
   if (c->k_outliers < 0 || c->k_outliers > 4) return KVQ_ERR_UNSUPPORTED;
-  if (c->k_outliers > 0 && !c->symmetric) return KVQ_ERR_UNSUPPORTED;  // isolation of per-token key rows only
+  // isolated key entries with per-channel keys: decode kernels for r <= 4 only
+  if (c->k_outliers > 0 && !c->symmetric && c->gqa_ratio > 4) return KVQ_ERR_UNSUPPORTED;
   Geometry x;
   x.L = c->n_layers;
   x.B = c->batch;
@@ -77,7 +79,8 @@ inline kvq_status make_geometry(const kvq_config* c, Geometry* g) {
   x.rowV = (int64_t)x.d * x.vbits / 8;
   x.n_vg = x.d / x.Gv;
   x.k_codes_slice = x.S_pad * x.rowK;
-  x.k_meta_slice = x.sym ? x.S_pad * 2 + x.S_pad * x.kout * 4 : (x.S_pad / x.G) * x.d * 4;
+  // group (scale, zero point) pairs or per-token scales, then kout entries per token
+  x.k_meta_slice = (x.sym ? x.S_pad * 2 : (x.S_pad / x.G) * x.d * 4) + x.S_pad * x.kout * 4;
   x.k_resid_slice = x.sym ? 0 : (int64_t)x.R_eff * x.d * 2;
   x.v_codes_slice = x.S_pad * x.rowV;
   x.v_meta_slice = x.S_pad * x.n_vg * 4;

@@ -211,7 +211,10 @@ struct Stage {
   static constexpr int KB = 32 * BITS * 128 / 8;   // key codes of 32 tokens
   static constexpr int VB = 32 * VBITS * 128 / 8;  // value codes of 32 tokens
   static constexpr int VM = 32 * 4 * NVG;         // value meta of 32 tokens
-  static constexpr int KM = SYM ? (OUTL ? 64 + 512 : 64) : 512;  // one key group's meta, or 32 key scales (+ up to 4 entries each)
+  // one key group's meta, or 32 key scales; with isolated key entries (OUTL) followed by the
+  // 32 tokens' entry lists (up to 4 entries of 4 bytes each) at offset KE
+  static constexpr int KE = SYM ? 64 : 512;
+  static constexpr int KM = KE + (OUTL ? 512 : 0);
   static constexpr int BYTES = KB + VB + VM + KM;
   static constexpr int NS = BITS == 2 ? 3 : 2;
   static constexpr int WARP_BYTES = NS * BYTES;
@@ -230,6 +233,7 @@ struct Stage {
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
 
 // A stage barrier completes a phase when all 32 lanes of the warp have seen their
 // copies of the stage land (cp.async.mbarrier.arrive.noinc, one arrival per lane).
@@ -339,7 +343,8 @@ constexpr int min_blocks() {
 // CTA (4; 5 or 8 for small cluster-merged grids, where few CTAs per SM are resident
 // anyway and more warps shorten the busiest warp's run of iterations; the 5-warp CTA
 // keeps two CTAs per SM).
-template <int BITS, int VBITS, int NT, int NVG, int NW, bool SYM = false, bool OUTL = false>
+// MIXED: the grid is a mixed plan's one-dimensional list of CTAs (4-warp CTAs only).
+template <int BITS, int VBITS, int NT, int NVG, int NW, bool SYM = false, bool OUTL = false, bool MIXED = false>
 __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5 ? 2 : 1)) decode_mma_kernel(DecodeParams p) {
   constexpr int kWarps = NW;
   using St = Stage<BITS, VBITS, NVG, NW, SYM, OUTL>;
@@ -374,33 +379,31 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
   __shared__ __align__(16) uint8_t append_s[kHeadDim];
 
   // this CTA's (batch row, kv head) pair, split, split length and the number of parts its
-  // pair merges through the workspace
-  int split, h, b, n_parts;
-  int64_t chunk;
-  if (p.mixed) {
-    const int c = blockIdx.x, ctas_hi = p.pairs_hi * p.n_hi;
+  // pair merges through the workspace: from the grid (n_split, H, B), or from a mixed plan's
+  // list (the first pairs_hi pairs in n_hi splits of chunk_hi tokens, the rest in n_hi - 1
+  // splits of chunk_lo tokens)
+  int split_m = 0, h_m = 0, b_m = 0, parts_m = 0, chunk_m = 0;
+  if constexpr (MIXED) {
+    const int c = (int)blockIdx.x, ctas_hi = p.pairs_hi * p.n_hi;
     int pair;
     if (c < ctas_hi) {
       pair = c / p.n_hi;
-      split = c - pair * p.n_hi;
-      n_parts = p.n_hi;
-      chunk = p.chunk_hi;
+      split_m = c - pair * p.n_hi;
+      parts_m = p.n_hi;
+      chunk_m = (int)p.chunk_hi;
     } else {
       const int n_lo = p.n_hi - 1, c2 = c - ctas_hi;
       pair = p.pairs_hi + c2 / n_lo;
-      split = c2 - (c2 / n_lo) * n_lo;
-      n_parts = n_lo;
-      chunk = p.chunk_lo;
+      split_m = c2 - (c2 / n_lo) * n_lo;
+      parts_m = n_lo;
+      chunk_m = (int)p.chunk_lo;
     }
-    b = pair / p.H;
-    h = pair - b * p.H;
-  } else {
-    split = blockIdx.x;
-    h = blockIdx.y;
-    b = blockIdx.z;
-    n_parts = p.n_parts;
-    chunk = p.chunk;
+    b_m = pair / p.H;
+    h_m = pair - b_m * p.H;
   }
+  const int split = MIXED ? split_m : (int)blockIdx.x;
+  const int h = MIXED ? h_m : (int)blockIdx.y, b = MIXED ? b_m : (int)blockIdx.z;
+  const int n_parts = MIXED ? parts_m : p.n_parts;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, j = lane & 3;
   const int r = p.r;
@@ -409,8 +412,8 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
   const int64_t qrow0 = (int64_t)b * p.H * r + (int64_t)h * r;
 
   const int T = (int)p.T, Tq = (int)p.Tq;
-  const int t_begin = split * (int)chunk;  // chunk is a multiple of 32
-  const int t_end = min(t_begin + (int)chunk, T);
+  const int t_begin = split * (MIXED ? chunk_m : (int)p.chunk);  // chunk is a multiple of 32
+  const int t_end = min(t_begin + (MIXED ? chunk_m : (int)p.chunk), T);
   const int n_it = max(0, (t_end - t_begin + kTok - 1) / kTok);  // 0 for a trailing empty split
   // balanced contiguous runs of iterations per warp (warp w: [w*n_it/NW, (w+1)*n_it/NW))
   const int it0 = (warp * n_it) / kWarps;
@@ -429,12 +432,14 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
   const uint8_t* k_src = p.k_codes + slice * p.k_codes_slice + (int64_t)ts0 * ROW;
   const uint8_t* v_src = p.v_codes + slice * p.v_codes_slice + (int64_t)ts0 * ROWV;
   const uint8_t* vm_src = reinterpret_cast<const uint8_t*>(p.v_meta + (slice * p.S_pad + ts0) * NVG);
-  const __half2* km_base = p.k_meta + slice * (p.S_pad >> p.log2G) * kHeadDim;
+  const __half2* km_base =
+      reinterpret_cast<const __half2*>(reinterpret_cast<const uint8_t*>(p.k_meta) + slice * p.k_meta_slice);
   // SYM: per-token key scales of the warp's first iteration (k_meta holds S_pad per slice)
   const uint8_t* ksc_src = reinterpret_cast<const uint8_t*>(p.k_meta) + slice * p.k_meta_slice + (int64_t)ts0 * 2;
-  // SYM with isolated key entries: p.kout entries (4 B each) per token after the S_pad scales
-  const uint8_t* kent_src = reinterpret_cast<const uint8_t*>(p.k_meta) + slice * p.k_meta_slice + p.S_pad * 2 +
-                            (int64_t)ts0 * p.kout * 4;
+  // isolated key entries: p.kout entries (4 B each) per token after the S_pad key scales
+  // (symmetric scheme) or after the key groups' (scale, zero point) pairs
+  const uint8_t* kent_src = reinterpret_cast<const uint8_t*>(p.k_meta) + slice * p.k_meta_slice +
+                            (SYM ? p.S_pad * 2 : (p.S_pad >> p.log2G) * kHeadDim * 4) + (int64_t)ts0 * p.kout * 4;
 
   // Copies of the warp's iteration i into stage sidx: every lane moves 16-byte pieces
   // (piece lane + 32c of each block) with cp.async and arrives on the stage barrier
@@ -465,6 +470,10 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
       if (lane < 4) cp_async16(dst + St::KB + St::VB + St::VM, ksc_src + (size_t)i * 64 + 16 * lane);
     } else {
       if (newgrp) cp_async16(dst + St::KB + St::VB + St::VM, km_base + ((ts >> p.log2G) << 7) + 4 * lane);
+      if constexpr (OUTL) {  // the 32 quantized tokens' entry lists (128 kout bytes; residual keys have none)
+        if (quant && lane < 8 * p.kout)
+          cp_async16(dst + St::KB + St::VB + St::VM + St::KE, kent_src + (size_t)i * 128 * p.kout + 16 * lane);
+      }
     }
     cp_async_arrive(smem_u32(&bars[warp][sidx]));
   };
@@ -945,11 +954,13 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
           const float kk = __half2float(ksc[16 * hf + 8 * e + g]);
           s[hf][e] = (kk * p.scale_log2) * fmaf(acc[hf][2 * e] + acc[hf][2 * e + 1], kTwo24, qmin_qsum);
         }
-      if constexpr (OUTL) {  // the sparse side list: x_c * q_c of every isolated key entry
+    }
+    if constexpr (OUTL) {  // the sparse side list: x_c * q_c of every isolated key entry
+      if (SYM || ts < Tq) {  // residual (binary16) keys have no isolated entries
         // lane l takes token l: its entries (channel | binary16 value << 16) against every
         // query row into the warp's table sp_w[token][row] (rows of kMaxGqa + 1 words: no
         // bank conflicts), then every score lane reads its (token, row) term back
-        const uint32_t* ent = reinterpret_cast<const uint32_t*>(st + St::KB + St::VB + St::VM + 64);
+        const uint32_t* ent = reinterpret_cast<const uint32_t*>(st + St::KB + St::VB + St::VM + St::KE);
         float* sp_w = reinterpret_cast<float*>(smem + St::SP) + warp * 32 * St::SP_ROW;
         const int ko = p.kout;
         uint32_t en[4];
@@ -1054,7 +1065,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
         // lane l takes token l: its entries (channel | binary16 value << 16) against every
         // query row into the warp's table sp_w[token][row] (rows of kMaxGqa + 1 words: no
         // bank conflicts), then every score lane reads its (token, row) term back
-        const uint32_t* ent = reinterpret_cast<const uint32_t*>(st + St::KB + St::VB + St::VM + 64);
+        const uint32_t* ent = reinterpret_cast<const uint32_t*>(st + St::KB + St::VB + St::VM + St::KE);
         float* sp_w = reinterpret_cast<float*>(smem + St::SP) + warp * 32 * St::SP_ROW;
         const int ko = p.kout;
         uint32_t en[4];
@@ -1336,21 +1347,21 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
   }
 }
 
-template <int BITS, int VBITS, int NT, int NVG, int NW, bool SYM = false, bool OUTL = false>
-cudaError_t launch_cfg(const DecodeParams& p, cudaStream_t stream) {
+template <int BITS, int VBITS, int NT, int NVG, int NW, bool SYM, bool OUTL, bool MIXED>
+cudaError_t launch_cfg_impl(const DecodeParams& p, cudaStream_t stream) {
   constexpr int smem = Stage<BITS, VBITS, NVG, NW, SYM, OUTL>::SMEM;
-  auto* kern = decode_mma_kernel<BITS, VBITS, NT, NVG, NW, SYM, OUTL>;
+  auto* kern = decode_mma_kernel<BITS, VBITS, NT, NVG, NW, SYM, OUTL, MIXED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   if (p.cluster < 1 || p.cluster > 16 || (p.cluster & (p.cluster - 1)) || p.n_split != p.cluster * p.n_parts)
     return cudaErrorInvalidConfiguration;
-  if (p.mixed && (p.cluster != 1 || p.n_hi < 2 || p.pairs_hi < 1 || p.pairs_hi >= p.B * p.H)) return cudaErrorInvalidConfiguration;
+  if (MIXED && (p.cluster != 1 || p.n_hi < 2 || p.pairs_hi < 1 || p.pairs_hi >= p.B * p.H)) return cudaErrorInvalidConfiguration;
   if (p.cluster > 8) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = p.mixed ? dim3((unsigned)(p.pairs_hi * p.n_hi + (p.B * p.H - p.pairs_hi) * (p.n_hi - 1)), 1u, 1u)
+  cfg.gridDim = MIXED ? dim3((unsigned)(p.pairs_hi * p.n_hi + (p.B * p.H - p.pairs_hi) * (p.n_hi - 1)), 1u, 1u)
                         : dim3((unsigned)p.n_split, (unsigned)p.H, (unsigned)p.B);
   cfg.blockDim = dim3(NW * 32, 1, 1);
   cfg.dynamicSmemBytes = smem;
@@ -1367,6 +1378,15 @@ cudaError_t launch_cfg(const DecodeParams& p, cudaStream_t stream) {
   e = cudaLaunchKernelEx(&cfg, kern, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+template <int BITS, int VBITS, int NT, int NVG, int NW, bool SYM = false, bool OUTL = false>
+cudaError_t launch_cfg(const DecodeParams& p, cudaStream_t stream) {
+  if constexpr (NW == 4) {
+    if (p.mixed) return launch_cfg_impl<BITS, VBITS, NT, NVG, NW, SYM, OUTL, true>(p, stream);
+  }
+  if (p.mixed) return cudaErrorInvalidConfiguration;  // mixed plans use 4-warp CTAs
+  return launch_cfg_impl<BITS, VBITS, NT, NVG, NW, SYM, OUTL, false>(p, stream);
 }
 
 template <int BITS, int VBITS, int NT, int NVG, bool SYM = false, bool OUTL = false>

@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(128) decode_simt_kernel(DecodeParams p) {
   for (int i = 0; i < kRM; ++i) o[i] = 0.0f;
 
   const uint8_t* kc = p.k_codes + slice * p.k_codes_slice;
-  const __half2* km = p.k_meta + slice * (p.S_pad / p.G) * kHeadDim;
+  const __half2* km = reinterpret_cast<const __half2*>(reinterpret_cast<const uint8_t*>(p.k_meta) + slice * p.k_meta_slice);
   const __half* kr = p.k_resid + slice * (int64_t)p.R_eff * kHeadDim;
   const uint8_t* vc = p.v_codes + slice * p.v_codes_slice;
   const __half2* vm = p.v_meta + slice * p.S_pad * p.n_vg;

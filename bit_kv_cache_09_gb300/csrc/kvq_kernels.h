@@ -162,7 +162,7 @@ cudaError_t launch_dequant(const DequantParams& p, int bits, int vbits, cudaStre
 cudaError_t launch_decode_simt(const DecodeParams& p, int bits, cudaStream_t stream);  // equal widths only
 cudaError_t launch_decode_mma(const DecodeParams& p, int bits, int vbits, cudaStream_t stream);
 // sym: 0 asymmetric; 1 the symmetric per-token int8 scheme (bits == vbits == 8, n_vg == 1);
-// 2 the symmetric scheme with isolated key entries
+// 2 the symmetric scheme with isolated key entries; 3 asymmetric with isolated key entries (r <= 4)
 int occupancy_decode_mma(int bits, int vbits, int r, int n_vg, int sym);  // resident CTAs per SM (0 on error)
 int max_clusters_decode_mma(int bits, int vbits, int r, int n_vg, int cs, int nw, int sym);  // resident clusters of cs CTAs
 int occupancy_decode_simt(int bits);

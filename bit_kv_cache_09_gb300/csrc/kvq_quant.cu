@@ -72,6 +72,25 @@ __global__ void __launch_bounds__(256, 4) k_group_kernel(AppendParams p) {
     const int64_t t = t0 + warp + 8 * k;
     const __half* row = (t < p.s_cur) ? resid + t * kHeadDim : in + t * in_stride;
     x[k] = *reinterpret_cast<const uint2*>(row + 4 * lane);
+  }
+  if (p.kout > 0) {
+    // dense-and-sparse keys: every row of the group gives up its kout farthest entries
+    // (their binary16 values to the row's entry list after the group metadata) before the
+    // per-channel ranges are taken; they become +0 in the dense row
+    uint32_t* ent = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(p.k_meta) + slice * p.k_meta_slice +
+                                                (p.S_pad / G) * kHeadDim * 4);
+#pragma unroll
+    for (int k = 0; k < PER_WARP; ++k) {
+      const int64_t t = t0 + warp + 8 * k;
+      const uint32_t xb[4] = {x[k].x & 0xFFFFu, x[k].x >> 16, x[k].y & 0xFFFFu, x[k].y >> 16};
+      bool taken[4];
+      split_row_outliers<true>(xb, taken, ent + t * p.kout, p.kout, lane);
+      x[k].x &= (taken[0] ? 0xFFFF0000u : 0xFFFFFFFFu) & (taken[1] ? 0x0000FFFFu : 0xFFFFFFFFu);
+      x[k].y &= (taken[2] ? 0xFFFF0000u : 0xFFFFFFFFu) & (taken[3] ? 0x0000FFFFu : 0xFFFFFFFFu);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < PER_WARP; ++k) {
     const __half2 a = *reinterpret_cast<const __half2*>(&x[k].x), c = *reinterpret_cast<const __half2*>(&x[k].y);
     if (k == 0) {
       mn2[0] = a; mx2[0] = a; mn2[1] = c; mx2[1] = c;
@@ -103,7 +122,8 @@ __global__ void __launch_bounds__(256, 4) k_group_kernel(AppendParams p) {
     s_sc[c] = s;
     s_rs[c] = rs;
     s_zp[c] = __fsub_rn(zp, Q<BITS>::qmin);
-    p.k_meta[(slice * (p.S_pad / G) + g) * kHeadDim + c] = __halves2half2(s_h, z_h);
+    reinterpret_cast<__half2*>(reinterpret_cast<uint8_t*>(p.k_meta) + slice * p.k_meta_slice)[g * kHeadDim + c] =
+        __halves2half2(s_h, z_h);
   }
   __syncthreads();
   float s[4], rs[4], zp[4];
@@ -365,13 +385,26 @@ __global__ void __launch_bounds__(256) dequant_kernel(DequantParams p, int64_t n
     }
   } else if (t < p.Tq) {
     const uint8_t* row = p.k_codes + slice * p.k_codes_slice + t * p.rowK;
-    const __half2* meta = p.k_meta + (slice * (p.S_pad / p.G) + t / p.G) * kHeadDim;
+    const __half2* meta = reinterpret_cast<const __half2*>(reinterpret_cast<const uint8_t*>(p.k_meta) +
+                                                           slice * p.k_meta_slice) + (t / p.G) * kHeadDim;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int c = c0 + e;
       const uint32_t u = (row[(c * BITS) >> 3] >> ((c * BITS) & 7)) & ((1u << BITS) - 1u);
       const __half2 m = meta[c];
       kx[e] = __fmul_rn(__low2float(m), __fsub_rn((float)((int)u + (int)Q<BITS>::qmin), __high2float(m)));
+    }
+    // isolated entries after the group metadata: the stored binary16 value is added to the
+    // dense x_hat there (the dense row held +0 at that channel)
+    const uint32_t* ent = reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(p.k_meta) +
+                                                            slice * p.k_meta_slice + (p.S_pad / p.G) * kHeadDim * 4) +
+                          t * p.kout;
+    for (int r = 0; r < p.kout; ++r) {
+      const uint32_t en = ent[r];
+      const int c = (int)(en & 0xFFFFu);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (c == c0 + e) kx[e] = __fadd_rn(kx[e], __half2float(__ushort_as_half((unsigned short)(en >> 16))));
     }
   } else {
     load4(p.k_resid + (slice * p.R_eff + t % p.R_eff) * kHeadDim + c0, kx);

@@ -201,17 +201,83 @@ __device__ __forceinline__ uint32_t sorted_key_63(const uint32_t (&key_in)[4], i
   return __shfl_sync(0xffffffffu, a[3], 15);
 }
 
+// Dense-and-sparse split of one key row ("Sub-8-Bit KV Cache Quantization Is Not a Free
+// Lever for an RDNA4 Agent Swarm", § What the low-bit numbers actually cost: per-vector
+// dense-and-sparse quantization). The warp holds the row's 128 binary16 values, lane l the
+// bit patterns xb[0..3] of channels [4l, 4l+4); the row's kout entries farthest from its
+// lower median (the 64th smallest value) in binary32 |x - median|, in order of decreasing
+// distance, ties to the lower channel, go to entries[0 .. kout) as channel | binary16 << 16
+// (written by the lane that holds them) and are marked in `taken` (the caller replaces them
+// by +0). SORT picks how the lower median is found: a bitonic sort of the row's 128 order
+// keys (fewer instructions; the append kernels) or a radix select with warp ballots (the
+// fused decode step); both give the exact 64th smallest value.
+template <bool SORT>
+__device__ __forceinline__ void split_row_outliers(const uint32_t (&xb)[4], bool (&taken)[4], uint32_t* entries,
+                                                   int kout, int lane) {
+  // order-preserving 16-bit keys of the binary16 inputs (negative values bit-inverted,
+  // positive ones with the sign bit set); -0 and +0 get distinct keys, which leaves
+  // |x - median| unchanged
+  uint32_t key[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) key[e] = (xb[e] & 0x8000u) ? (~xb[e] & 0xFFFFu) : (xb[e] | 0x8000u);
+  uint32_t prefix = 0;
+  if constexpr (SORT) {
+    prefix = sorted_key_63(key, lane);
+  } else {  // most-significant-bit-first radix select of rank 63, one ballot per key and bit
+    int rank = 63;
+#pragma unroll
+    for (int bit = 15; bit >= 0; --bit) {
+      const uint32_t above = (0xFFFFu << (bit + 1)) & 0xFFFFu;  // the bits already decided
+      int n0 = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        n0 += __popc(__ballot_sync(0xffffffffu, ((key[e] ^ prefix) & above) == 0u && ((key[e] >> bit) & 1u) == 0u));
+      if (rank >= n0) {
+        rank -= n0;
+        prefix |= 1u << bit;
+      }
+    }
+  }
+  const uint32_t med_bits = (prefix & 0x8000u) ? (prefix & 0x7FFFu) : (~prefix & 0xFFFFu);
+  const float med = __half2float(__ushort_as_half((unsigned short)med_bits));
+  float dist[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    taken[e] = false;
+    dist[e] = fabsf(__fsub_rn(__half2float(__ushort_as_half((unsigned short)xb[e])), med));
+  }
+  for (int r = 0; r < kout; ++r) {
+    float bd = -1.0f;
+    int bc = 1 << 30;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (!taken[e] && dist[e] > bd) {
+        bd = dist[e];
+        bc = 4 * lane + e;
+      }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {  // farthest, ties to the lower channel
+      const float od = __shfl_xor_sync(0xffffffffu, bd, off);
+      const int oc = __shfl_xor_sync(0xffffffffu, bc, off);
+      if (od > bd || (od == bd && oc < bc)) {
+        bd = od;
+        bc = oc;
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (bc == 4 * lane + e) {
+        taken[e] = true;
+        entries[r] = (uint32_t)bc | (xb[e] << 16);
+      }
+  }
+}
+
 // One warp quantizes one key row of the symmetric per-token scheme (binary16, 128
 // channels; lane l holds channels [4l, 4l+4)): its binary16 scale to *scale_out and its
-// 8-bit codes, in channel order, to key_row. With kout > 0 the row's kout entries
-// farthest from its lower median (binary32 |x - median|, in order of decreasing
-// distance, ties to the lower channel; "Sub-8-Bit KV Cache Quantization Is Not a Free
-// Lever for an RDNA4 Agent Swarm", § What the low-bit numbers actually cost: per-vector
-// dense-and-sparse quantization) go to entries[0 .. kout) as channel | binary16 << 16
-// and are replaced by 0 before the scale is taken. SORT picks how the lower median is
-// found: a bitonic sort of the row's 128 order keys (fewer instructions; the append
-// kernel) or a radix select with warp ballots (the fused decode step); both give the
-// exact 64th smallest value.
+// 8-bit codes, in channel order, to key_row. With kout > 0 the row's kout farthest
+// entries are split off first (split_row_outliers) and replaced by 0 before the scale
+// is taken.
 template <bool SORT = false>
 __device__ __forceinline__ void quantize_key_row_sym(const __half* k_row, uint8_t* key_row, __half* scale_out,
                                                      uint32_t* entries, int kout, int lane) {
@@ -220,62 +286,8 @@ __device__ __forceinline__ void quantize_key_row_sym(const __half* k_row, uint8_
   if (kout > 0) {
     const uint2 raw = *reinterpret_cast<const uint2*>(k_row + 4 * lane);
     const uint32_t xb[4] = {raw.x & 0xFFFFu, raw.x >> 16, raw.y & 0xFFFFu, raw.y >> 16};
-    // lower median = the 64th smallest value (rank 63): a most-significant-bit-first radix
-    // select over order-preserving 16-bit keys of the binary16 inputs (negative values
-    // bit-inverted, positive ones with the sign bit set), one ballot per key and bit.
-    // -0 and +0 get distinct keys, which leaves |x - median| unchanged.
-    uint32_t key[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) key[e] = (xb[e] & 0x8000u) ? (~xb[e] & 0xFFFFu) : (xb[e] | 0x8000u);
-    uint32_t prefix = 0;
-    if constexpr (SORT) {
-      prefix = sorted_key_63(key, lane);
-    } else {
-      int rank = 63;
-#pragma unroll
-      for (int bit = 15; bit >= 0; --bit) {
-        const uint32_t above = (0xFFFFu << (bit + 1)) & 0xFFFFu;  // the bits already decided
-        int n0 = 0;
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          n0 += __popc(__ballot_sync(0xffffffffu, ((key[e] ^ prefix) & above) == 0u && ((key[e] >> bit) & 1u) == 0u));
-        if (rank >= n0) {
-          rank -= n0;
-          prefix |= 1u << bit;
-        }
-      }
-    }
-    const uint32_t med_bits = (prefix & 0x8000u) ? (prefix & 0x7FFFu) : (~prefix & 0xFFFFu);
-    const float med = __half2float(__ushort_as_half((unsigned short)med_bits));
-    float dist[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) dist[e] = fabsf(__fsub_rn(x[e], med));
-    bool taken[4] = {false, false, false, false};
-    for (int r = 0; r < kout; ++r) {
-      float bd = -1.0f;
-      int bc = 1 << 30;
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (!taken[e] && dist[e] > bd) {
-          bd = dist[e];
-          bc = 4 * lane + e;
-        }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {  // farthest, ties to the lower channel
-        const float od = __shfl_xor_sync(0xffffffffu, bd, off);
-        const int oc = __shfl_xor_sync(0xffffffffu, bc, off);
-        if (od > bd || (od == bd && oc < bc)) {
-          bd = od;
-          bc = oc;
-        }
-      }
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (bc == 4 * lane + e) {
-          taken[e] = true;
-          entries[r] = (uint32_t)bc | (xb[e] << 16);
-        }
-    }
+    bool taken[4];
+    split_row_outliers<SORT>(xb, taken, entries, kout, lane);
 #pragma unroll
     for (int e = 0; e < 4; ++e)
       if (taken[e]) x[e] = 0.0f;

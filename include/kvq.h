@@ -50,6 +50,10 @@
  *   smallest of the d = 128 values) in binary32 |x - median|, in order of decreasing
  *   distance with ties to the lower channel, are stored as (channel, binary16 value)
  *   and replaced by 0; k_hat is the dense x_hat plus those values at their channels.
+ *   The asymmetric scheme takes the same per-row split (gqa_ratio <= 4): a key row is
+ *   split when its token leaves the binary16 residual window, and the per-channel
+ *   groups are then formed over the dense rows (the isolated entries read as 0 there).
+ *   Residual rows are exact binary16 copies and carry no entries.
  *
  * State after T tokens of one (layer, batch row, kv head)
  *   R_eff = residual_len, or k_group when residual_len == 0.
@@ -63,7 +67,9 @@
  *   slices are ordered [layer][batch][kv head]. Per slice:
  *     k_codes : S_pad rows of d*b/8 bytes. Channel c occupies bits [c*b, c*b+b) of its
  *               row (little-endian bytes, low bits first).
- *     k_meta  : (S_pad / k_group) groups x d channels x {scale, zero_point} binary16.
+ *     k_meta  : (S_pad / k_group) groups x d channels x {scale, zero_point} binary16,
+ *               followed when k_outliers = k > 0 by S_pad x k entries {channel (uint16),
+ *               value (binary16)} (entries of tokens >= Tq are undefined).
  *     k_resid : R_eff rows of d binary16.
  *     v_codes : S_pad/2 pair rows of 2*d*b_v/8 bytes (b_v = value code width). Channel c of a token sits at
  *               position pos(c) = (d/8)*(c%8) + 2*(c/16) + (c/8)%2 of that token's
@@ -112,7 +118,8 @@ typedef enum {
  * up to 1024; 1 <= gqa_ratio <= 8; n_kv_heads <= 255; batch <= 4095;
  * 1 <= max_seq_len <= 2^24. symmetric == 1 needs bits == 8, v_bits in {0, 8},
  * v_group == d_head and residual_len == 0 (k_group is then unused but must still be
- * one of the values above); k_outliers in 0..4, and > 0 only with symmetric == 1. */
+ * one of the values above); k_outliers in 0..4, and > 0 with symmetric == 0 only when
+ * gqa_ratio <= 4. */
 typedef struct {
   int32_t n_layers;     /* L */
   int32_t batch;        /* B: sequences; all share one length */
@@ -126,7 +133,7 @@ typedef struct {
   int32_t residual_len; /* R: binary16 key residual capacity; 0 means k_group */
   int32_t v_bits;       /* value code width; 0 means bits */
   int32_t symmetric;    /* 0: asymmetric (above); 1: symmetric per-token int8 keys and values */
-  int32_t k_outliers;   /* symmetric scheme: key entries per token kept in a sparse side list (0..4) */
+  int32_t k_outliers;   /* key entries per token kept in a sparse side list (0..4) */
 } kvq_config;
 
 /* Device pointers to the five cache buffers of all layers (layout above). */

@@ -39,10 +39,11 @@
 //                       or G when R = 0) and is quantized R_eff tokens at a time.
 //   symmetric scheme -> scale = max|x| / q_max rounded up to binary16, zero point 0,
 //                       one scale per token for keys and values, no residual window.
-//   outlier isolation-> per key row (symmetric scheme): the k channels farthest from the
+//   outlier isolation-> per key row (either scheme): the k channels farthest from the
 //                       row's lower median in |x - median| (binary32), ties to the lower
 //                       channel, kept as (channel, binary16 value) and zeroed in the
-//                       dense row that is then quantized.
+//                       dense row that is then quantized (per token in the symmetric
+//                       scheme; with per-channel keys, when the row's group is formed).
 //
 // Parity pins: see tests/test_oracle_pins.py. The packed byte layout and the
 // residual/flush bookkeeping are this project's own definitions (the pages fix
@@ -314,15 +315,20 @@ void orc_unpack_v_token(const uint8_t* pairs, int d, int bits, int64_t t, uint8_
 // and values want different treatment).
 // Inputs k_hist, v_hist: [T][d] binary16. Outputs in the packed layout above:
 //   k_codes [floor(T/R_eff)*R_eff][d*b/8], k_meta [groups][d][2], k_resid [R_eff][d],
-//   v_codes [ceil(T/2)][2*d*b_v/8], v_meta [T][d/Gv][2].
+//   v_codes [ceil(T/2)][2*d*b_v/8], v_meta [T][d/Gv][2]; with k_out > 0 isolated key entries
+//   per quantized row, k_sparse [Tq][k_out][2] (see below).
 // Output buffers must be zero-initialised by the caller. Optional k_u [Tq][d] and
 // v_u [T][d] receive the unpacked codes. Returns Tq (quantized key tokens) or -1.
 // ---------------------------------------------------------------------------
 
-int64_t orc_cache_state(int d, int bits, int v_bits, int G, int Gv, int R, int64_t T, const uint16_t* k_hist,
-                        const uint16_t* v_hist, uint8_t* k_codes, uint16_t* k_meta, uint16_t* k_resid,
-                        uint8_t* v_codes, uint16_t* v_meta, uint8_t* k_u, uint8_t* v_u) {
+int orc_split_outliers(const uint16_t* x, int n, int k, uint16_t* idx_out, uint16_t* val_out, uint16_t* dense_out);
+
+int64_t orc_cache_state(int d, int bits, int v_bits, int G, int Gv, int R, int64_t T, int k_out,
+                        const uint16_t* k_hist, const uint16_t* v_hist, uint8_t* k_codes, uint16_t* k_meta,
+                        uint16_t* k_sparse, uint16_t* k_resid, uint8_t* v_codes, uint16_t* v_meta, uint8_t* k_u,
+                        uint8_t* v_u) {
   if (d <= 0 || d % 16 || G <= 0 || Gv <= 0 || d % Gv || R < 0 || (R > 0 && R % G) || T < 0) return -1;
+  if (k_out < 0 || k_out > d) return -1;
   if (!(bits == 2 || bits == 4 || bits == 8)) return -1;
   if (!(v_bits == 2 || v_bits == 4 || v_bits == 8)) return -1;
   const int64_t R_eff = R > 0 ? R : G;
@@ -330,10 +336,27 @@ int64_t orc_cache_state(int d, int bits, int v_bits, int G, int Gv, int R, int64
   const int64_t rowK = (int64_t)d * bits / 8;
   std::vector<uint8_t> u((size_t)d);
   std::vector<uint8_t> col((size_t)G);
+  // Dense-and-sparse keys (k_out > 0): every key row that is quantized first gives up its
+  // k_out entries farthest from its lower median (orc_split_outliers), kept as
+  // (channel, binary16 value) in k_sparse [Tq][k_out][2]; the per-channel groups are
+  // then formed over the dense rows. Residual rows stay whole (they are binary16 already).
+  std::vector<uint16_t> dense((size_t)(Tq > 0 ? Tq : 1) * d);
+  std::vector<uint16_t> idx((size_t)k_out + 1), val((size_t)k_out + 1);
+  for (int64_t t = 0; t < Tq; ++t) {
+    if (k_out > 0) {
+      orc_split_outliers(k_hist + t * d, d, k_out, idx.data(), val.data(), dense.data() + t * d);
+      for (int r = 0; r < k_out; ++r) {
+        k_sparse[(t * k_out + r) * 2 + 0] = idx[(size_t)r];
+        k_sparse[(t * k_out + r) * 2 + 1] = val[(size_t)r];
+      }
+    } else {
+      std::memcpy(dense.data() + t * d, k_hist + t * d, sizeof(uint16_t) * (size_t)d);
+    }
+  }
   // keys: per channel, per group of G tokens
   for (int64_t g = 0; g < Tq / G; ++g) {
     for (int c = 0; c < d; ++c) {
-      const uint16_t* x = k_hist + (g * G) * d + c;
+      const uint16_t* x = dense.data() + (g * G) * d + c;
       uint16_t s_h, z_h;
       orc_quant_params(x, G, d, bits, &s_h, &z_h);
       orc_quantize_values(x, G, d, bits, s_h, z_h, col.data());
@@ -370,9 +393,10 @@ int64_t orc_cache_state(int d, int bits, int v_bits, int G, int Gv, int R, int64
 // Dequantized keys and values of one (batch row, kv head) from a packed state:
 // k_out, v_out [T][d] binary32. Quantized keys and all values use
 // x_hat = scale * (q - zero_point); residual keys are the binary16 values.
-int orc_dequantize_state(int d, int bits, int v_bits, int G, int Gv, int R, int64_t T, const uint8_t* k_codes,
-                         const uint16_t* k_meta, const uint16_t* k_resid, const uint8_t* v_codes,
-                         const uint16_t* v_meta, float* k_out, float* v_out) {
+int orc_dequantize_state(int d, int bits, int v_bits, int G, int Gv, int R, int64_t T, int k_out_n,
+                         const uint8_t* k_codes, const uint16_t* k_meta, const uint16_t* k_sparse,
+                         const uint16_t* k_resid, const uint8_t* v_codes, const uint16_t* v_meta, float* k_out,
+                         float* v_out) {
   if (d <= 0 || d % 16 || G <= 0 || Gv <= 0 || d % Gv || R < 0 || (R > 0 && R % G) || T < 0) return -1;
   const int64_t R_eff = R > 0 ? R : G;
   const int64_t Tq = (T / R_eff) * R_eff;
@@ -384,6 +408,8 @@ int orc_dequantize_state(int d, int bits, int v_bits, int G, int Gv, int R, int6
       orc_unpack_k_row(k_codes + t * rowK, d, bits, u.data());
       for (int c = 0; c < d; ++c)
         k_out[t * d + c] = orc_dequantize_value(u[(size_t)c], bits, k_meta[(g * d + c) * 2], k_meta[(g * d + c) * 2 + 1]);
+      for (int r = 0; r < k_out_n; ++r)  // isolated entries: the dense x_hat there is 0 + its own error
+        k_out[t * d + k_sparse[(t * k_out_n + r) * 2]] += orc_f32_from_f16(k_sparse[(t * k_out_n + r) * 2 + 1]);
     } else {
       for (int c = 0; c < d; ++c) k_out[t * d + c] = orc_f32_from_f16(k_resid[(t % R_eff) * d + c]);
     }

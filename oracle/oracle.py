@@ -74,11 +74,11 @@ def lib():
             L.orc_pack_v_token.restype = None
             L.orc_unpack_v_token.argtypes = [_u8p, ctypes.c_int, ctypes.c_int, ctypes.c_int64, _u8p]
             L.orc_unpack_v_token.restype = None
-            L.orc_cache_state.argtypes = [ctypes.c_int] * 6 + [ctypes.c_int64, _u16p, _u16p, _u8p, _u16p, _u16p, _u8p,
-                                                               _u16p, _u8p, _u8p]
+            L.orc_cache_state.argtypes = [ctypes.c_int] * 6 + [ctypes.c_int64, ctypes.c_int, _u16p, _u16p, _u8p, _u16p,
+                                                               _u16p, _u16p, _u8p, _u16p, _u8p, _u8p]
             L.orc_cache_state.restype = ctypes.c_int64
-            L.orc_dequantize_state.argtypes = [ctypes.c_int] * 6 + [ctypes.c_int64, _u8p, _u16p, _u16p, _u8p, _u16p,
-                                                                    _f32p, _f32p]
+            L.orc_dequantize_state.argtypes = [ctypes.c_int] * 6 + [ctypes.c_int64, ctypes.c_int, _u8p, _u16p, _u16p,
+                                                                    _u16p, _u8p, _u16p, _f32p, _f32p]
             L.orc_dequantize_state.restype = ctypes.c_int
             L.orc_sym_params.argtypes = [_u16p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, _u16p]
             L.orc_sym_params.restype = ctypes.c_int
@@ -210,12 +210,15 @@ class OracleState:
     v_meta: np.ndarray  # [T][d/Gv][2] uint16
     k_u: np.ndarray  # [Tq][d] unpacked key codes
     v_u: np.ndarray  # [T][d] unpacked value codes
-    k_sparse: np.ndarray = None  # symmetric scheme with outliers: [T][k][2] (channel, binary16 value)
+    k_sparse: np.ndarray = None  # isolated key entries [Tq][k][2] (channel, binary16 value), or None
 
 
-def cache_state(k_hist, v_hist, *, d: int, bits: int, G: int, Gv: int, R: int, v_bits: int = 0) -> OracleState:
+def cache_state(k_hist, v_hist, *, d: int, bits: int, G: int, Gv: int, R: int, v_bits: int = 0,
+                k_outliers: int = 0) -> OracleState:
     """Quantized cache of one (b, h) slice from its binary16 token history [T][d]; keys
-    with `bits`-bit codes, values with `v_bits`-bit codes (0: the same as the keys)."""
+    with `bits`-bit codes, values with `v_bits`-bit codes (0: the same as the keys). With
+    k_outliers > 0 every quantized key row gives up its k farthest entries (k_sparse)
+    before the per-channel groups are formed."""
     v_bits = v_bits or bits
     k = _as_u16(k_hist)
     v = _as_u16(v_hist)
@@ -231,17 +234,20 @@ def cache_state(k_hist, v_hist, *, d: int, bits: int, G: int, Gv: int, R: int, v
     v_meta = np.zeros((T, d // Gv, 2), np.uint16)
     k_u = np.zeros((Tq, d), np.uint8)
     v_u = np.zeros((T, d), np.uint8)
+    k_sparse = np.zeros((Tq, k_outliers, 2), np.uint16)
     # zero-size arrays still need a valid pointer
-    bufs = [np.zeros(1, a.dtype) if a.size == 0 else a for a in (k_codes, k_meta, k_resid, v_codes, v_meta, k_u, v_u)]
+    bufs = [np.zeros(1, a.dtype) if a.size == 0 else a
+            for a in (k_codes, k_meta, k_resid, v_codes, v_meta, k_u, v_u, k_sparse)]
     kk = k if k.size else np.zeros(1, np.uint16)
     vv = v if v.size else np.zeros(1, np.uint16)
-    rc = lib().orc_cache_state(d, bits, v_bits, G, Gv, R, T, _ptr(kk, _u16p), _ptr(vv, _u16p), _ptr(bufs[0], _u8p),
-                               _ptr(bufs[1], _u16p), _ptr(bufs[2], _u16p), _ptr(bufs[3], _u8p), _ptr(bufs[4], _u16p),
-                               _ptr(bufs[5], _u8p), _ptr(bufs[6], _u8p))
+    rc = lib().orc_cache_state(d, bits, v_bits, G, Gv, R, T, k_outliers, _ptr(kk, _u16p), _ptr(vv, _u16p),
+                               _ptr(bufs[0], _u8p), _ptr(bufs[1], _u16p), _ptr(bufs[7], _u16p), _ptr(bufs[2], _u16p),
+                               _ptr(bufs[3], _u8p), _ptr(bufs[4], _u16p), _ptr(bufs[5], _u8p), _ptr(bufs[6], _u8p))
     if rc < 0:
         raise ValueError("bad cache shape")
     assert rc == Tq
-    return OracleState(T, Tq, k_codes, k_meta, k_resid, v_codes, v_meta, k_u, v_u)
+    return OracleState(T, Tq, k_codes, k_meta, k_resid, v_codes, v_meta, k_u, v_u,
+                       k_sparse if k_outliers > 0 else None)
 
 
 def dequantize_state(st: OracleState, *, d: int, bits: int, G: int, Gv: int, R: int, v_bits: int = 0):
@@ -254,9 +260,11 @@ def dequantize_state(st: OracleState, *, d: int, bits: int, G: int, Gv: int, R: 
     def nz(a):
         return np.ascontiguousarray(a) if a.size else np.zeros(1, a.dtype)
 
-    rc = lib().orc_dequantize_state(d, bits, v_bits, G, Gv, R, T, _ptr(nz(st.k_codes), _u8p), _ptr(nz(st.k_meta), _u16p),
-                                    _ptr(nz(st.k_resid), _u16p), _ptr(nz(st.v_codes), _u8p),
-                                    _ptr(nz(st.v_meta), _u16p), _ptr(k_out, _f32p), _ptr(v_out, _f32p))
+    ks = st.k_sparse if st.k_sparse is not None else np.zeros((st.Tq, 0, 2), np.uint16)
+    rc = lib().orc_dequantize_state(d, bits, v_bits, G, Gv, R, T, ks.shape[1], _ptr(nz(st.k_codes), _u8p),
+                                    _ptr(nz(st.k_meta), _u16p), _ptr(nz(ks), _u16p), _ptr(nz(st.k_resid), _u16p),
+                                    _ptr(nz(st.v_codes), _u8p), _ptr(nz(st.v_meta), _u16p), _ptr(k_out, _f32p),
+                                    _ptr(v_out, _f32p))
     if rc != 0:
         raise ValueError("bad cache shape")
     return k_out[:T], v_out[:T]

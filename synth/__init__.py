@@ -214,6 +214,8 @@ WORKLOADS: dict[str, Workload] = {
                  notes="symmetric per-token int8 keys and values, batch 16, 8192-token prompt"),
         Workload("sym8o4-b16", 32, 8, 4, 128, 16, 8192, 32, 8, 128, 128, 0, 4, 20, 20268, symmetric=1, k_outliers=4,
                  notes="sym8-b16 with 4 key entries per token isolated in a sparse side list"),
+        Workload("kivi-int4o4", 32, 8, 4, 128, 16, 8192, 32, 4, 128, 64, 128, 4, 20, 20269, k_outliers=4,
+                 notes="kivi-int4 with 4 entries of every quantized key row isolated before the per-channel groups"),
     ]
 }
 

@@ -53,8 +53,14 @@ def gpu_slice_state(cache, layer: int, b: int, h: int, T: int):
             ksp = buf[off: off + Tq * g["kout"] * 4].cpu().numpy().view(np.uint16).reshape(Tq, g["kout"], 2)
         kr = np.zeros((0, g["d"]), np.uint16)
     else:
-        km = part("k_meta", (g["S_pad"] // g["G"]) * g["d"] * 4, (Tq // g["G"]) * g["d"] * 4).view(np.uint16)
+        km_groups = (g["S_pad"] // g["G"]) * g["d"] * 4
+        km_slice = km_groups + g["S_pad"] * g["kout"] * 4
+        km = part("k_meta", km_slice, (Tq // g["G"]) * g["d"] * 4).view(np.uint16)
         km = km.reshape(Tq // g["G"], g["d"], 2)
+        if g["kout"]:  # isolated entries of the quantized rows, after the groups' metadata
+            buf = cache.buffer("k_meta")
+            off = sl * km_slice + km_groups
+            ksp = buf[off: off + Tq * g["kout"] * 4].cpu().numpy().view(np.uint16).reshape(Tq, g["kout"], 2)
         kr = part("k_resid", g["R_eff"] * g["d"] * 2, (T - Tq) * g["d"] * 2).view(np.uint16).reshape(T - Tq, g["d"])
     npairs = (T + 1) // 2
     vc = part("v_codes", g["S_pad"] * g["rowV"], npairs * 2 * g["rowV"]).reshape(npairs, 2 * g["rowV"])
@@ -67,7 +73,7 @@ def oracle_slice_state(k_hist, v_hist, cache):
     if g["sym"]:
         return oracle.cache_state_sym(k_hist, v_hist, d=g["d"], k_outliers=g["kout"])
     return oracle.cache_state(k_hist, v_hist, d=g["d"], bits=g["bits"], G=g["G"], Gv=g["Gv"], R=g["R"],
-                              v_bits=g["vbits"])
+                              v_bits=g["vbits"], k_outliers=g["kout"])
 
 
 def assert_slice_equal(gpu: dict, st: oracle.OracleState, where: str = ""):
@@ -138,7 +144,7 @@ def oracle_slice_job(job):
             kh, vh = oracle.dequantize_state_sym(st, d=w.d_head)
         else:
             st = oracle.cache_state(k[:T], v[:T], d=w.d_head, bits=w.bits, G=w.k_group, Gv=w.v_group, R=w.residual,
-                                    v_bits=w.vbits)
+                                    v_bits=w.vbits, k_outliers=w.k_outliers)
             kh, vh = oracle.dequantize_state(st, d=w.d_head, bits=w.bits, G=w.k_group, Gv=w.v_group, R=w.residual,
                                              v_bits=w.vbits)
         if T in job["q"]:

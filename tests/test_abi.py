@@ -51,8 +51,9 @@ def good_cfg(**kw):
     (dict(symmetric=2), 1), (dict(symmetric=1, bits=4, v_group=128, residual_len=0), 2),
     (dict(symmetric=1, bits=8, v_bits=4, v_group=128, residual_len=0), 2),
     (dict(symmetric=1, bits=8, v_group=64, residual_len=0), 2), (dict(symmetric=1, bits=8, v_group=128), 1),
-    # outlier isolation: symmetric scheme only, 0..4 entries per token
-    (dict(k_outliers=2), 2), (dict(symmetric=1, bits=8, v_group=128, residual_len=0, k_outliers=5), 2),
+    # outlier isolation: 0..4 entries per token; with per-channel keys for r <= 4 only
+    (dict(k_outliers=2, gqa_ratio=8), 2), (dict(k_outliers=5), 2),
+    (dict(symmetric=1, bits=8, v_group=128, residual_len=0, k_outliers=5), 2),
     (dict(symmetric=1, bits=8, v_group=128, residual_len=0, k_outliers=-1), 2),
 ])
 def test_bad_configs_are_rejected(lib, kw, status):
@@ -111,6 +112,11 @@ def test_outlier_buffer_sizes(lib):
                                               residual_len=0, symmetric=1, k_outliers=k))
         assert sizes[1] == n * S_pad * (2 + 4 * k)
         assert sizes[0] == sizes[3] == n * S_pad * 128 and sizes[2] == 0
+    # per-channel keys: the entries follow the (scale, zero point) pairs of the key groups
+    for k in range(5):
+        sizes = kvq.kvq_buffer_sizes(good_cfg(n_layers=L, batch=B, n_kv_heads=H, max_seq_len=S, bits=4, k_group=32,
+                                              k_outliers=k))
+        assert sizes[1] == n * ((S_pad // 32) * 128 * 4 + S_pad * 4 * k)
 
 
 def _bufs(ptr=4096):

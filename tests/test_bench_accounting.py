@@ -11,7 +11,8 @@ import bench
 import oracle
 import synth
 
-NAMES = ["llama8b-int8", "kivi-int4", "kivi-int2", "kivi-k8v4", "long-int4-16k", "sym8-b16", "sym8o4-b16"]
+NAMES = ["llama8b-int8", "kivi-int4", "kivi-int2", "kivi-k8v4", "long-int4-16k", "sym8-b16", "sym8o4-b16",
+         "kivi-int4o4"]
 
 
 @pytest.mark.parametrize("name", NAMES)
@@ -24,7 +25,8 @@ def test_attention_bytes_equal_the_oracle_state(name, T):
     if w.symmetric:
         st = oracle.cache_state_sym(k, v, d=d, k_outliers=w.k_outliers)
     else:
-        st = oracle.cache_state(k, v, d=d, bits=w.bits, G=w.k_group, Gv=w.v_group, R=w.residual, v_bits=w.vbits)
+        st = oracle.cache_state(k, v, d=d, bits=w.bits, G=w.k_group, Gv=w.v_group, R=w.residual, v_bits=w.vbits,
+                                k_outliers=w.k_outliers)
     state = (st.k_codes.nbytes + st.k_meta.nbytes + (T - st.Tq) * d * 2 + st.v_codes.nbytes
              + st.v_meta.nbytes + (st.k_sparse.nbytes if st.k_sparse is not None else 0))
     io = w.n_q * d * 2 + w.n_q * d * 4  # binary16 queries in, binary32 outputs out
@@ -41,7 +43,8 @@ def test_prefill_bytes_equal_inputs_plus_state(name):
     if w.symmetric:
         st = oracle.cache_state_sym(k, v, d=d, k_outliers=w.k_outliers)
     else:
-        st = oracle.cache_state(k, v, d=d, bits=w.bits, G=w.k_group, Gv=w.v_group, R=w.residual, v_bits=w.vbits)
+        st = oracle.cache_state(k, v, d=d, bits=w.bits, G=w.k_group, Gv=w.v_group, R=w.residual, v_bits=w.vbits,
+                                k_outliers=w.k_outliers)
     written = (st.k_codes.nbytes + st.k_meta.nbytes + (T - st.Tq) * d * 2 + st.v_codes.nbytes
                + st.v_meta.nbytes + (st.k_sparse.nbytes if st.k_sparse is not None else 0))
     assert bench.prefill_bytes_per_layer(w, T) == 2 * T * d * 2 + written

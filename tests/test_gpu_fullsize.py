@@ -28,7 +28,7 @@ from bit_kv_cache_09_gb300.cache import QuantizedKVCache  # noqa: E402
 from synth.device import DeviceGenerator  # noqa: E402
 
 FULL = ["llama8b-int8", "kivi-int4", "kivi-int2", "kivi-k8v4", "llama8b-sym8", "sym8-b16", "sym8o4-b16",
-        "long-int4-16k", "long-int4-32k", "long-int4-64k"]
+        "kivi-int4o4", "long-int4-16k", "long-int4-32k", "long-int4-64k"]
 
 
 @pytest.fixture(scope="module")

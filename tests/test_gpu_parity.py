@@ -715,3 +715,81 @@ def test_zero_wait_limit_reports_a_timeout(B, H, S):
     cache.check_errors()  # the read cleared it
     _check_attention(cache, w, 0, S, k_host, v_host, q_host, kvq.DECODE_AUTO)
     cache.check_errors()
+
+
+@pytest.mark.parametrize("bits,v_bits,G,Gv,R,k_out,B,H", [
+    (4, 0, 32, 64, 64, 2, 2, 2),     # small grid (cluster CTAs)
+    (2, 0, 32, 32, 64, 4, 6, 8),     # large grid
+    (8, 0, 128, 128, 128, 1, 2, 3),
+    (8, 4, 64, 64, 128, 3, 6, 8),    # mixed widths, large grid
+])
+def test_per_channel_keys_with_isolated_entries(bits, v_bits, G, Gv, R, k_out, B, H):
+    """Per-channel keys with k_out isolated entries per quantized key row: the key-group
+    append kernel (prompt) and the step that fills the residual window split every row
+    before forming its groups; the decode kernel adds the entries' score terms for
+    quantized tokens. Codes, metadata, entry lists and residual bit-exact, dequantized keys
+    bit-exact, attention within 2e-3 at every checked step, through the fused step."""
+    R_eff = R
+    S = 2 * R_eff + 10
+    steps = R_eff - 10 + 3
+    w = small_workload(bits=bits, v_bits=v_bits, G=G, Gv=Gv, R=R, r=4, B=B, H=H, S=S, steps=steps, n_out=4,
+                       seed=9500 + bits + k_out, k_outliers=k_out)
+    cache = QuantizedKVCache.for_workload(w)
+    k_host, v_host = host_layer_inputs(w, 0, 0, w.max_seq)
+    cache.append(0, 0, _dev(k_host[:, :S]), _dev(v_host[:, :S]))
+    _check_all_slices(cache, w, 0, S, k_host, v_host)
+    flush_step = 3 * R_eff - 1 - S
+    for s in range(steps):
+        T = S + s
+        q_host = synth.gen_q(w.seed, 0, range(w.batch), T, w.n_q, w.d_head)
+        out = cache.decode_step(0, T, _dev(k_host[:, T:T + 1]), _dev(v_host[:, T:T + 1]), _dev(q_host),
+                                softmax_scale(w)).cpu().numpy()
+        if s not in (0, flush_step - 1, flush_step, steps - 1):
+            continue
+        _check_all_slices(cache, w, 0, T + 1, k_host, v_host)
+        for b in range(w.batch):
+            for h in range(w.n_kv):
+                st = oracle_slice_state(k_host[b, :T + 1, h], v_host[b, :T + 1, h], cache)
+                ref = oracle_attention(st, q_host[b, h * w.gqa:(h + 1) * w.gqa], cache, softmax_scale(w))
+                err = float(np.abs(out[b, h * w.gqa:(h + 1) * w.gqa] - ref).max())
+                assert err <= ATOL, (b, h, T + 1, err)
+    T = S + steps
+    kd, vd = cache.dequantize(0, T)
+    for b in range(w.batch):
+        for h in range(w.n_kv):
+            st = oracle_slice_state(k_host[b, :T, h], v_host[b, :T, h], cache)
+            assert st.k_sparse is not None and st.k_sparse.shape[1] == k_out
+            kh, vh = oracle.dequantize_state(st, d=128, bits=bits, G=G, Gv=Gv, R=R, v_bits=v_bits)
+            assert np.array_equal(kd[b, h].cpu().numpy().view(np.uint32), kh.view(np.uint32)), (b, h)
+            assert np.array_equal(vd[b, h].cpu().numpy().view(np.uint32), vh.view(np.uint32)), (b, h)
+
+
+def test_per_channel_key_outliers_on_adversarial_rows():
+    """The key-group kernel's row split on hand-built key rows (signed zeros, constant and
+    two-valued rows, extremes, subnormals, distance ties) in the prompt and in the residual
+    window a decode step flushes: state bit-exact, attention within 2e-3."""
+    w = small_workload(bits=4, G=32, Gv=64, R=64, r=4, B=2, H=2, S=128 + 10, steps=58, seed=9600, k_outliers=4)
+    cache = QuantizedKVCache.for_workload(w)
+    k_host, v_host = host_layer_inputs(w, 0, 0, w.max_seq)
+    k_host = np.array(k_host, dtype=np.float16)
+    rows = _adversarial_key_rows(np.random.default_rng(9600))
+    for i, row in enumerate(rows):
+        k_host[0, 3 + i, 0] = row            # prompt rows
+        k_host[1, 140 + i, 1] = row[::-1]    # rows flushed by a decode step
+    S = w.seq
+    cache.append(0, 0, _dev(k_host[:, :S]), _dev(v_host[:, :S]))
+    _check_all_slices(cache, w, 0, S, k_host, v_host)
+    for s in range(w.steps):
+        T = S + s
+        q_host = synth.gen_q(w.seed, 0, range(w.batch), T, w.n_q, w.d_head)
+        out = cache.decode_step(0, T, _dev(k_host[:, T:T + 1]), _dev(v_host[:, T:T + 1]), _dev(q_host),
+                                softmax_scale(w)).cpu().numpy()
+        if T + 1 not in (S + 1, 192, S + w.steps):
+            continue
+        _check_all_slices(cache, w, 0, T + 1, k_host, v_host)
+        for b in range(w.batch):
+            for h in range(w.n_kv):
+                st = oracle_slice_state(k_host[b, :T + 1, h], v_host[b, :T + 1, h], cache)
+                ref = oracle_attention(st, q_host[b, h * w.gqa:(h + 1) * w.gqa], cache, softmax_scale(w))
+                err = float(np.abs(out[b, h * w.gqa:(h + 1) * w.gqa] - ref).max())
+                assert err <= ATOL, (b, h, T + 1, err)

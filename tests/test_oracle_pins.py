@@ -684,3 +684,48 @@ def test_outliers_cut_the_error_on_outlier_channels():
     assert e4.max() * 10 < e0.max()
     for t in range(T):
         assert np.all(e4[t, st.k_sparse[t, :, 0]] == 0)
+
+
+# ----------------------------------------------------------------------------- outliers with per-channel keys
+def test_per_channel_keys_with_isolated_entries():
+    """Per-channel keys with k isolated entries per key row ("Sub-8-Bit KV Cache Quantization
+    Is Not a Free Lever for an RDNA4 Agent Swarm", § What the low-bit numbers actually cost:
+    dense-and-sparse). Two planted channels far from every row's median are the isolated
+    entries of every quantized row, in order of distance, with their exact binary16 values;
+    their dense columns are all +0, so their groups get scale 1 and zero point q_min; every
+    other channel's group parameters are those of its untouched column; dequantized keys
+    are exact on the isolated channels and within half a stored step elsewhere; residual
+    rows stay whole and the split of a row does not depend on later tokens."""
+    rng = np.random.default_rng(4242)
+    d, G, R, Gv = 128, 32, 64, 64
+    T = 3 * R + 20
+    big = (7, 91)
+    for bits in (8, 4, 2):
+        k = rng.standard_normal((T, d)).astype(np.float16)
+        k[:, big[0]] = (1000 + 50 * rng.standard_normal(T)).astype(np.float16)
+        k[:, big[1]] = (-2000 + 50 * rng.standard_normal(T)).astype(np.float16)
+        v = rng.standard_normal((T, d)).astype(np.float16)
+        st = oracle.cache_state(k, v, d=d, bits=bits, G=G, Gv=Gv, R=R, k_outliers=2)
+        Tq = st.Tq
+        assert Tq == 3 * R and st.k_sparse.shape == (Tq, 2, 2)
+        assert (st.k_sparse[:, 0, 0] == big[1]).all() and (st.k_sparse[:, 1, 0] == big[0]).all()
+        assert np.array_equal(st.k_sparse[:, 0, 1], k[:Tq, big[1]].view(np.uint16))
+        assert np.array_equal(st.k_sparse[:, 1, 1], k[:Tq, big[0]].view(np.uint16))
+        qmin_bits = int(np.float16(oracle.qmin(bits)).view(np.uint16))
+        for g in range(Tq // G):
+            for c in range(d):
+                if c in big:
+                    assert tuple(st.k_meta[g, c]) == (0x3C00, qmin_bits), (bits, g, c)
+                else:
+                    assert tuple(st.k_meta[g, c]) == oracle.quant_params(k[g * G:(g + 1) * G, c], bits), (bits, g, c)
+        kh, _ = oracle.dequantize_state(st, d=d, bits=bits, G=G, Gv=Gv, R=R)
+        for c in big:
+            assert np.array_equal(kh[:Tq, c], k[:Tq, c].astype(np.float32))
+        scales = st.k_meta[:, :, 0].view(np.float16).astype(np.float64)  # [group][channel]
+        err = np.abs(kh[:Tq].astype(np.float64) - k[:Tq].astype(np.float64))
+        bound = np.repeat(scales, G, axis=0) / 2 * (1 + 2.0**-20)
+        assert (err <= bound).all()
+        assert np.array_equal(st.k_resid[:T - Tq], k[Tq:].view(np.uint16))
+        assert np.array_equal(kh[Tq:], k[Tq:].astype(np.float32))
+        st2 = oracle.cache_state(k[:2 * R + 5], v[:2 * R + 5], d=d, bits=bits, G=G, Gv=Gv, R=R, k_outliers=2)
+        assert np.array_equal(st2.k_sparse, st.k_sparse[:st2.Tq])
