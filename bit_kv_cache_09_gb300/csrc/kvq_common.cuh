@@ -7,10 +7,10 @@
 //                  S_pad x kout isolated entries {channel u16, value binary16}
 //   k_resid slice: R_eff rows x d binary16
 //   v_codes slice: S_pad/2 pair rows of 2*rowV bytes (rowV = d*b/8)
-//   v_meta  slice: S_pad tokens x d/Gv x half2(scale, zero_point)
+//   v_meta  slice: S_pad/2 token pairs x d/Gv x {scale 2p, scale 2p+1, zp 2p, zp 2p+1}
 // Symmetric per-token scheme: k_meta slice = S_pad binary16 key scales (then, with kout
 // isolated entries per token, S_pad x kout x {channel u16, value binary16}), no k_resid,
-// Gv = d (v_meta holds half2(scale, 0)), every key quantized on append (Tq = T).
+// Gv = d (v_meta zero points are 0), every key quantized on append (Tq = T).
 #pragma once
 
 #include <cstddef>

@@ -296,7 +296,8 @@ __device__ __forceinline__ void lds_chunk(const uint8_t* p, uint32_t* w) {
   }
 }
 
-// value meta (scale, zero) of tokens tl and tl + 1 for every group: 2 * NVG half2
+// value meta of token pair (tl, tl + 1), tl even: per group the half2 of the two scales,
+// then the half2 of the two zero points (2 * NVG half2)
 template <int NVG>
 __device__ __forceinline__ void lds_vmeta(const __half2* p, __half2* m) {
   if (NVG == 1) {
@@ -512,7 +513,9 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
       const int64_t row = (int64_t)b * p.H + h;  // [B][1][H][d]
       uint16_t* pair = reinterpret_cast<uint16_t*>(p.v_codes_w + slice * p.v_codes_slice + (int64_t)(t_new >> 1) * 2 * ROWV);
       quant::quantize_value_row<VBITS, SYM>(p.v_new + row * kHeadDim, pair, t_new & 1,
-                                           p.v_meta_w + (slice * p.S_pad + t_new) * NVG, p.Gv, lane, append_s);
+                                           reinterpret_cast<__half*>(p.v_meta_w) +
+                                               (slice * (p.S_pad >> 1) + (t_new >> 1)) * NVG * 4 + (t_new & 1),
+                                           p.Gv, lane, append_s);
       if constexpr (SYM) {  // the key row is quantized per token right away (no residual window)
         uint8_t* kmb = reinterpret_cast<uint8_t*>(p.k_meta_w) + slice * p.k_meta_slice;
         quant::quantize_key_row_sym(p.k_new + row * kHeadDim, p.k_codes_w + slice * p.k_codes_slice + (int64_t)t_new * ROW,
@@ -902,7 +905,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
       for (int pi = 0; pi < 2; ++pi)
         lds_chunk<VBITS>(st + St::KB + (8 * hf + 4 * pi + j) * (2 * ROWV) + g * (ROWV / 4), vw[pi]);
       const __half2* vms = reinterpret_cast<const __half2*>(st + St::KB + St::VB) + 16 * hf * NVG;
-      __half2 mlo[2 * NVG], mhi[2 * NVG];  // tokens (2j, 2j+1) and (8+2j, 9+2j)
+      __half2 mlo[2 * NVG], mhi[2 * NVG];  // token pairs (2j, 2j+1) and (8+2j, 9+2j)
       lds_vmeta<NVG>(vms + (2 * j) * NVG, mlo);
       lds_vmeta<NVG>(vms + (8 + 2 * j) * NVG, mhi);
       uint32_t bf[NVG][NT][2];
@@ -911,8 +914,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
         uint32_t za[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const uint32_t m0 = h2_bits(e ? mhi[vg] : mlo[vg]), m1 = h2_bits(e ? mhi[NVG + vg] : mlo[NVG + vg]);
-          const uint32_t s2 = prmt2(m0, m1, 0x5410u);  // value scales of the token pair
+          const uint32_t s2 = h2_bits(e ? mhi[2 * vg] : mlo[2 * vg]);  // value scales of the token pair
           const uint32_t whi = hmul2(ph[hf][e], s2);
           if (NT == 1) {
             bf[vg][0][e] = hfma2(ph[hf][e], s2, (whi ^ 0x80008000u) & lo_mask);
@@ -920,7 +922,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
             bf[vg][0][e] = whi;
             bf[vg][NT - 1][e] = hfma2(ph[hf][e], s2, hneg2(whi));
           }
-          za[e] = prmt2(m0, m1, 0x7632u);  // zero points of the token pair
+          za[e] = h2_bits(e ? mhi[2 * vg + 1] : mlo[2 * vg + 1]);  // zero points of the token pair
         }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) mma16816(bacc[vg], kOne2, za[0], kOne2, za[1], bf[vg][nt][0], bf[vg][nt][1]);

@@ -213,8 +213,9 @@ __global__ void __launch_bounds__(128) decode_simt_kernel(DecodeParams p) {
       for (int tau = 0; tau < n_valid; ++tau) {
         const uint32_t word = v_s[(tau >> 1) * words_per_pair + unit];
         const uint32_t u = ((word >> (16 * (tau & 1))) >> shift) & MASK;
-        const __half2 m = vm_s[tau * p.n_vg + vg];
-        const float vh = __low2float(m) * ((float)u + qmin - __high2float(m));
+        // pair record {scale 2p, scale 2p+1, zp 2p, zp 2p+1} of group vg
+        const __half* rec = reinterpret_cast<const __half*>(vm_s) + ((tau >> 1) * p.n_vg + vg) * 4 + (tau & 1);
+        const float vh = __half2float(rec[0]) * ((float)u + qmin - __half2float(rec[2]));
         const float4 pa = *reinterpret_cast<const float4*>(&sc_s[tau][0]);
         const float4 pb = *reinterpret_cast<const float4*>(&sc_s[tau][4]);
         o[0] += pa.x * vh; o[1] += pa.y * vh; o[2] += pa.z * vh; o[3] += pa.w * vh;

@@ -217,7 +217,12 @@ __global__ void __launch_bounds__(256) v_token_kernel(AppendParams p) {
     }
     group_params<BITS>(mn, mx, s_h, z_h, s, rs, zp);
   }
-  if (valid && sl % lpg == 0) p.v_meta[(slice * p.S_pad + t) * p.n_vg + sl / lpg] = __halves2half2(s_h, z_h);
+  if (valid && sl % lpg == 0) {  // the token's half of its pair's record for this group
+    __half* rec = reinterpret_cast<__half*>(p.v_meta) + ((slice * (p.S_pad >> 1) + (t >> 1)) * p.n_vg + sl / lpg) * 4 +
+                  (int)(t & 1);
+    rec[0] = s_h;
+    rec[2] = z_h;
+  }
   const float zpu = __fsub_rn(zp, Q<BITS>::qmin);
   uint32_t u[16];
 #pragma unroll
@@ -411,7 +416,9 @@ __global__ void __launch_bounds__(256) dequant_kernel(DequantParams p, int64_t n
   }
   {
     const uint16_t* pair = reinterpret_cast<const uint16_t*>(p.v_codes + slice * p.v_codes_slice + (t >> 1) * 2 * p.rowV);
-    const __half2* meta = p.v_meta + (slice * p.S_pad + t) * p.n_vg;
+    // the pair's records {scale 2p, scale 2p+1, zp 2p, zp 2p+1}, one per group
+    const __half* rec = reinterpret_cast<const __half*>(p.v_meta) + (slice * (p.S_pad >> 1) + (t >> 1)) * p.n_vg * 4 +
+                        (int)(t & 1);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int c = c0 + e;
@@ -419,8 +426,9 @@ __global__ void __launch_bounds__(256) dequant_kernel(DequantParams p, int64_t n
       const int bit = pos * VBITS;
       const uint32_t unit = pair[2 * (bit >> 4) + (int)(t & 1)];
       const uint32_t u = (unit >> (bit & 15)) & ((1u << VBITS) - 1u);
-      const __half2 m = meta[c / p.Gv];
-      vx[e] = __fmul_rn(__low2float(m), __fsub_rn((float)((int)u + (int)Q<VBITS>::qmin), __high2float(m)));
+      const int jg = c / p.Gv;
+      vx[e] = __fmul_rn(__half2float(rec[4 * jg]),
+                        __fsub_rn((float)((int)u + (int)Q<VBITS>::qmin), __half2float(rec[4 * jg + 2])));
     }
   }
   *reinterpret_cast<float4*>(p.k_out + w * kHeadDim + c0) = make_float4(kx[0], kx[1], kx[2], kx[3]);

@@ -42,7 +42,10 @@ struct Q {
 //  * a any positive binary32 and b = 2^bits - 1 (odd, at most 8 bits; the scale's
 //    range/levels): the remainder is an integer multiple of ulp(a/b) below 2^9 of them,
 //    and a - m*b is an odd multiple of ulp(a/b)/2 for every midpoint m, so the quotient
-//    lies at least 2^-9 ulp from every midpoint.
+//    lies at least 2^-9 ulp from every midpoint;
+//  * a a positive binary16 value and b = 2048 - 2^bits (the far-group scale floor): b is
+//    a power of two times an odd number of at most 9 bits, and a quotient that is not a
+//    binary32 number lies at least 2^-10 ulp from every midpoint.
 __device__ __forceinline__ float div_rn(float a, float b, float rb) {
   const float q0 = __fmul_rn(a, rb);
   const float r = __fmaf_rn(-b, q0, a);
@@ -53,6 +56,11 @@ __device__ __forceinline__ float div_rn(float a, float b, float rb) {
 template <int BITS>
 __device__ __forceinline__ float inv_levels() {
   return __int_as_float(BITS == 8 ? 0x3B808081 : (BITS == 4 ? 0x3D888889 : 0x3EAAAAAB));
+}
+// RN(1 / (2048 - 2^BITS)) as binary32 bit patterns.
+template <int BITS>
+__device__ __forceinline__ float inv_far() {
+  return __int_as_float(BITS == 8 ? 0x3A124925 : (BITS == 4 ? 0x3A010204 : 0x3A004020));
 }
 
 // Group parameters from the (exact) binary32 min and max of binary16 inputs:
@@ -72,7 +80,7 @@ __device__ __forceinline__ void group_params(float xmin, float xmax, __half& s_h
     // binary16 holds every integer only up to 2048: a narrow group far from zero gets the
     // wider scale max|x| / (2048 - 2^BITS), so that |x / scale| <= 2048 - 2^BITS and the
     // zero point (|zp| <= 2048 - 2^(BITS-1)) is stored exactly
-    const float s_far = __fdiv_rn(fmaxf(fabsf(xmin), fabsf(xmax)), (float)(2048 - (1 << BITS)));
+    const float s_far = div_rn(fmaxf(fabsf(xmin), fabsf(xmax)), (float)(2048 - (1 << BITS)), inv_far<BITS>());
     s32 = fmaxf(s32, s_far);
     s_h = __float2half_ru(s32);
   }
@@ -122,12 +130,13 @@ __device__ __forceinline__ int v_channel_of_pos(int p) {
 }
 
 // One warp quantizes one value row (binary16, 128 channels; lane l holds channels
-// [4l, 4l+4)) per group of Gv channels, writes its (scale, zero point) pairs to
-// meta[0 .. d/Gv) and its codes, in stored-position order, into half `half_sel` of
-// the 16-bit units of its pair row. codes_s: 128 bytes of warp-private shared memory.
+// [4l, 4l+4)) per group of Gv channels, writes its scale and zero point of group j to
+// rec[4j] and rec[4j + 2] (rec: the token's half of its pair's metadata records) and its
+// codes, in stored-position order, into half `half_sel` of the 16-bit units of its pair
+// row. codes_s: 128 bytes of warp-private shared memory.
 // SYM: the symmetric per-token scheme (BITS 8, one group of d channels, zero point 0).
 template <int BITS, bool SYM = false>
-__device__ __forceinline__ void quantize_value_row(const __half* v_row, uint16_t* pair_row, int half_sel, __half2* meta,
+__device__ __forceinline__ void quantize_value_row(const __half* v_row, uint16_t* pair_row, int half_sel, __half* rec,
                                                    int Gv, int lane, uint8_t* codes_s) {
   float x[4];
   load4(v_row + 4 * lane, x);
@@ -149,7 +158,10 @@ __device__ __forceinline__ void quantize_value_row(const __half* v_row, uint16_t
     }
     group_params<BITS>(mn, mx, s_h, z_h, s, rs, zp);
   }
-  if (lane % lanes_per_group == 0) meta[lane / lanes_per_group] = __halves2half2(s_h, z_h);
+  if (lane % lanes_per_group == 0) {
+    rec[4 * (lane / lanes_per_group)] = s_h;
+    rec[4 * (lane / lanes_per_group) + 2] = z_h;
+  }
   const float zpu = __fsub_rn(zp, Q<BITS>::qmin);
 #pragma unroll
   for (int e = 0; e < 4; ++e) codes_s[4 * lane + e] = (uint8_t)quant_code<BITS>(x[e], s, rs, zpu);

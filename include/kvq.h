@@ -76,11 +76,14 @@
  *               d*b_v/8-byte row; the rows of tokens 2p and 2p+1 are interleaved in
  *               16-bit units (32-bit word k of pair row p = unit k of token 2p in the
  *               low half, unit k of token 2p+1 in the high half).
- *     v_meta  : S_pad tokens x (d / v_group) groups x {scale, zero_point} binary16.
+ *     v_meta  : S_pad/2 token pairs x (d / v_group) groups x a record of four binary16
+ *               values {scale of token 2p, scale of token 2p+1, zero point of token 2p,
+ *               zero point of token 2p+1} (8 bytes; 4 bytes per token and group).
  *   Symmetric scheme: k_codes and v_codes as above (b = 8); k_meta is S_pad binary16 key
  *   scales (one per token), followed when k_outliers = k > 0 by S_pad x k entries
- *   {channel (uint16), value (binary16)}; v_meta holds {scale, +0} per token
- *   (v_group == d); there is no k_resid (its size is 0 and its pointer may be NULL).
+ *   {channel (uint16), value (binary16)}; v_meta holds the pair records of one value
+ *   group per token (v_group == d) with zero points +0; there is no k_resid (its size is
+ *   0 and its pointer may be NULL).
  *   Every buffer must be 256-byte aligned (torch and cudaMalloc allocations are) and
  *   zero-filled before the first append.
  *

@@ -27,6 +27,7 @@ from .oracle import (  # noqa: F401
     pack_v_token,
     unpack_v_token,
     cache_state,
+    value_meta,
     dequantize_state,
     sym_params,
     sym_quantize,

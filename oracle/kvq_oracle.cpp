@@ -245,7 +245,10 @@ double orc_kv_bytes(int64_t L, int64_t n_kv, int64_t d_head, int64_t S, double b
 //   of the token's row (bits [pos*b, pos*b + b)), and the rows of tokens 2p and
 //   2p+1 are interleaved in 16-bit units: 32-bit word k of pair row p holds 16-bit
 //   unit k of token 2p in its low half and unit k of token 2p+1 in its high half.
-//   Metadata entries are (scale, zero_point) binary16 pairs.
+//   Key metadata entries are (scale, zero_point) binary16 pairs.
+//   Value metadata is stored per token pair: for tokens 2p and 2p+1 and value group j,
+//   the record at [p][j] holds four binary16 values, {scale of 2p, scale of 2p+1,
+//   zero point of 2p, zero point of 2p+1}.
 // ---------------------------------------------------------------------------
 
 static void put_bits(uint8_t* row, int64_t pos, int bits, uint32_t u) {
@@ -268,6 +271,10 @@ static uint32_t get_bits(const uint8_t* row, int64_t pos, int bits) {
 }
 
 int64_t orc_v_pos(int d, int c) { return (int64_t)(d / 8) * (c % 8) + 2 * (c / 16) + (c / 8) % 2; }
+
+// Index (in binary16 units) of token t's scale (part 0) or zero point (part 1) of value
+// group j, with ng groups per token, in the pair records described above.
+int64_t orc_v_meta_index(int64_t t, int ng, int j, int part) { return ((t / 2) * ng + j) * 4 + 2 * part + t % 2; }
 
 // Key row: u[d] codes -> row bytes (d*b/8).
 void orc_pack_k_row(const uint8_t* u, int d, int bits, uint8_t* row) {
@@ -315,7 +322,7 @@ void orc_unpack_v_token(const uint8_t* pairs, int d, int bits, int64_t t, uint8_
 // and values want different treatment).
 // Inputs k_hist, v_hist: [T][d] binary16. Outputs in the packed layout above:
 //   k_codes [floor(T/R_eff)*R_eff][d*b/8], k_meta [groups][d][2], k_resid [R_eff][d],
-//   v_codes [ceil(T/2)][2*d*b_v/8], v_meta [T][d/Gv][2]; with k_out > 0 isolated key entries
+//   v_codes [ceil(T/2)][2*d*b_v/8], v_meta [ceil(T/2)][d/Gv][4]; with k_out > 0 isolated key entries
 //   per quantized row, k_sparse [Tq][k_out][2] (see below).
 // Output buffers must be zero-initialised by the caller. Optional k_u [Tq][d] and
 // v_u [T][d] receive the unpacked codes. Returns Tq (quantized key tokens) or -1.
@@ -381,8 +388,8 @@ int64_t orc_cache_state(int d, int bits, int v_bits, int G, int Gv, int R, int64
       uint16_t s_h, z_h;
       orc_quant_params(x, Gv, 1, v_bits, &s_h, &z_h);
       orc_quantize_values(x, Gv, 1, v_bits, s_h, z_h, u.data() + (size_t)j * Gv);
-      v_meta[(t * ng + j) * 2 + 0] = s_h;
-      v_meta[(t * ng + j) * 2 + 1] = z_h;
+      v_meta[orc_v_meta_index(t, ng, j, 0)] = s_h;
+      v_meta[orc_v_meta_index(t, ng, j, 1)] = z_h;
     }
     orc_pack_v_token(u.data(), d, v_bits, t, v_codes);
     if (v_u) std::memcpy(v_u + t * d, u.data(), (size_t)d);
@@ -417,8 +424,8 @@ int orc_dequantize_state(int d, int bits, int v_bits, int G, int Gv, int R, int6
     orc_unpack_v_token(v_codes, d, v_bits, t, u.data());
     for (int c = 0; c < d; ++c) {
       int j = c / Gv;
-      v_out[t * d + c] =
-          orc_dequantize_value(u[(size_t)c], v_bits, v_meta[(t * ng + j) * 2], v_meta[(t * ng + j) * 2 + 1]);
+      v_out[t * d + c] = orc_dequantize_value(u[(size_t)c], v_bits, v_meta[orc_v_meta_index(t, ng, j, 0)],
+                                              v_meta[orc_v_meta_index(t, ng, j, 1)]);
     }
   }
   return 0;
@@ -501,7 +508,8 @@ int orc_split_outliers(const uint16_t* x, int n, int k, uint16_t* idx_out, uint1
 // kernel angle: one scale per token; [A] § Symmetric vs asymmetric): keys and values
 // are each quantized per token over all d channels with the symmetric quantizer; there
 // is no residual window. Layout: k_codes [T][d] (key rows as above), k_scale [T]
-// binary16, v_codes pair rows as above, v_meta [T][1][2] = (scale, 0). Optional k_u,
+// binary16, v_codes pair rows as above, v_meta [ceil(T/2)][1][4] pair records with
+// zero points +0. Optional k_u,
 // v_u [T][d] receive the unpacked codes. Returns 0, or -1 on a bad argument.
 // With k_out > 0 outliers per key row (see orc_split_outliers), the dense row is what
 // is quantized and k_sparse [T][k_out][2] receives the (channel, binary16 value) pairs.
@@ -530,8 +538,8 @@ int orc_cache_state_sym(int d, int64_t T, int k_out, const uint16_t* k_hist, con
     if (k_u) std::memcpy(k_u + t * d, u.data(), (size_t)d);
     orc_sym_params(v_hist + t * d, d, 1, bits, &s_h);
     orc_sym_quantize(v_hist + t * d, d, 1, bits, s_h, u.data());
-    v_meta[t * 2 + 0] = s_h;
-    v_meta[t * 2 + 1] = 0;  // binary16 +0
+    v_meta[orc_v_meta_index(t, 1, 0, 0)] = s_h;
+    v_meta[orc_v_meta_index(t, 1, 0, 1)] = 0;  // binary16 +0
     orc_pack_v_token(u.data(), d, bits, t, v_codes);
     if (v_u) std::memcpy(v_u + t * d, u.data(), (size_t)d);
   }
@@ -553,7 +561,8 @@ int orc_dequantize_state_sym(int d, int64_t T, int k_out_n, const uint8_t* k_cod
     for (int r = 0; r < k_out_n; ++r)
       k_out[t * d + k_sparse[(t * k_out_n + r) * 2]] += orc_f32_from_f16(k_sparse[(t * k_out_n + r) * 2 + 1]);
     orc_unpack_v_token(v_codes, d, bits, t, u.data());
-    for (int c = 0; c < d; ++c) v_out[t * d + c] = orc_sym_dequantize_value(u[(size_t)c], bits, v_meta[t * 2]);
+    for (int c = 0; c < d; ++c)
+      v_out[t * d + c] = orc_sym_dequantize_value(u[(size_t)c], bits, v_meta[orc_v_meta_index(t, 1, 0, 0)]);
   }
   return 0;
 }

@@ -207,7 +207,7 @@ class OracleState:
     k_meta: np.ndarray  # [Tq/G][d][2] uint16 (scale, zp) binary16 bits
     k_resid: np.ndarray  # [R_eff][d] uint16
     v_codes: np.ndarray  # [ceil(T/2)][2*d*b/8] uint8
-    v_meta: np.ndarray  # [T][d/Gv][2] uint16
+    v_meta: np.ndarray  # [ceil(T/2)][d/Gv][4] uint16 pair records {s(2p), s(2p+1), zp(2p), zp(2p+1)}
     k_u: np.ndarray  # [Tq][d] unpacked key codes
     v_u: np.ndarray  # [T][d] unpacked value codes
     k_sparse: np.ndarray = None  # isolated key entries [Tq][k][2] (channel, binary16 value), or None
@@ -231,7 +231,7 @@ def cache_state(k_hist, v_hist, *, d: int, bits: int, G: int, Gv: int, R: int, v
     k_meta = np.zeros((Tq // G, d, 2), np.uint16)
     k_resid = np.zeros((R_eff, d), np.uint16)
     v_codes = np.zeros(((T + 1) // 2, 2 * (d * v_bits // 8)), np.uint8)
-    v_meta = np.zeros((T, d // Gv, 2), np.uint16)
+    v_meta = np.zeros(((T + 1) // 2, d // Gv, 4), np.uint16)
     k_u = np.zeros((Tq, d), np.uint8)
     v_u = np.zeros((T, d), np.uint8)
     k_sparse = np.zeros((Tq, k_outliers, 2), np.uint16)
@@ -248,6 +248,15 @@ def cache_state(k_hist, v_hist, *, d: int, bits: int, G: int, Gv: int, R: int, v
     assert rc == Tq
     return OracleState(T, Tq, k_codes, k_meta, k_resid, v_codes, v_meta, k_u, v_u,
                        k_sparse if k_outliers > 0 else None)
+
+
+def value_meta(st: OracleState) -> np.ndarray:
+    """The value metadata of a state per token: [T][d/Gv][2] (scale, zero point) binary16
+    bits, read out of the pair records (token t sits in record t // 2, half t % 2)."""
+    rec = st.v_meta
+    t = np.arange(st.T)
+    return np.stack([rec[t // 2, :, t % 2], rec[t // 2, :, 2 + t % 2]], axis=-1) if st.T else np.zeros(
+        (0, rec.shape[1], 2), np.uint16)
 
 
 def dequantize_state(st: OracleState, *, d: int, bits: int, G: int, Gv: int, R: int, v_bits: int = 0):
@@ -308,7 +317,8 @@ def split_outliers(x, k: int):
 def cache_state_sym(k_hist, v_hist, *, d: int, k_outliers: int = 0) -> OracleState:
     """Symmetric per-token int8 cache of one (b, h) slice: keys and values each with one
     scale per token and zero point 0, no residual window. k_meta holds the per-token key
-    scales [T] (binary16 bits), v_meta [T][1][2] the value (scale, 0) pairs; with
+    scales [T] (binary16 bits), v_meta [ceil(T/2)][1][4] the value pair records (zero
+    points +0); with
     k_outliers > 0, k_sparse [T][k][2] the isolated key entries (channel, binary16)."""
     k = _as_u16(k_hist)
     v = _as_u16(v_hist)
@@ -317,7 +327,7 @@ def cache_state_sym(k_hist, v_hist, *, d: int, k_outliers: int = 0) -> OracleSta
     k_codes = np.zeros((T, d), np.uint8)
     k_meta = np.zeros((T,), np.uint16)
     v_codes = np.zeros(((T + 1) // 2, 2 * d), np.uint8)
-    v_meta = np.zeros((T, 1, 2), np.uint16)
+    v_meta = np.zeros(((T + 1) // 2, 1, 4), np.uint16)
     k_u = np.zeros((T, d), np.uint8)
     v_u = np.zeros((T, d), np.uint8)
     k_sparse = np.zeros((T, k_outliers, 2), np.uint16)

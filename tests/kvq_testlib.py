@@ -64,7 +64,7 @@ def gpu_slice_state(cache, layer: int, b: int, h: int, T: int):
         kr = part("k_resid", g["R_eff"] * g["d"] * 2, (T - Tq) * g["d"] * 2).view(np.uint16).reshape(T - Tq, g["d"])
     npairs = (T + 1) // 2
     vc = part("v_codes", g["S_pad"] * g["rowV"], npairs * 2 * g["rowV"]).reshape(npairs, 2 * g["rowV"])
-    vm = part("v_meta", g["S_pad"] * g["n_vg"] * 4, T * g["n_vg"] * 4).view(np.uint16).reshape(T, g["n_vg"], 2)
+    vm = part("v_meta", g["S_pad"] * g["n_vg"] * 4, npairs * g["n_vg"] * 8).view(np.uint16).reshape(npairs, g["n_vg"], 4)
     return dict(k_codes=kc, k_meta=km, k_resid=kr, v_codes=vc, v_meta=vm, Tq=Tq, k_sparse=ksp)
 
 

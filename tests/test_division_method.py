@@ -1,7 +1,7 @@
 """The quantizer kernels compute x / s as RN(x * RN(1/s)) followed by one
 exact-remainder fma correction (Markstein's method). This checks, on the CPU, that the
-sequence gives the IEEE binary32 quotient for the two operand classes the kernels use:
-binary16 by binary16, and any positive binary32 by 2^b - 1. Each fma is emulated
+sequence gives the IEEE binary32 quotient for the operand classes the kernels use:
+binary16 by binary16, any positive binary32 by 2^b - 1, and binary16 by 2048 - 2^b. Each fma is emulated
 exactly: the products and sums involved fit the 64-bit significand of the x87
 extended type, so rounding the extended result once to binary32 is the fma's rounding.
 """
@@ -60,8 +60,24 @@ def test_binary32_by_levels(bits):
     assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
 
 
+@pytest.mark.parametrize("bits", [8, 4, 2])
+def test_binary16_by_far_divisors(bits):
+    """max|x| / (2048 - 2^b), the scale floor of groups far from zero: every positive
+    binary16 numerator (exhaustive)."""
+    xs = _f16_all()
+    a = xs[xs > 0]
+    n = np.full(a.shape, np.float32(2048 - (1 << bits)), np.float32)
+    rn = np.float32(1) / n
+    got = markstein(a, n, rn)
+    ref = a / n
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
 def test_reciprocal_constants():
-    """The kernels' constants RN(1/(2^b - 1)) as binary32 bit patterns."""
+    """The kernels' constants RN(1/(2^b - 1)) and RN(1/(2048 - 2^b)) as binary32 bit patterns."""
     for bits, pat in ((8, 0x3B808081), (4, 0x3D888889), (2, 0x3EAAAAAB)):
         v = np.float32(1) / np.float32((1 << bits) - 1)
+        assert int(v.view(np.uint32)) == pat
+    for bits, pat in ((8, 0x3A124925), (4, 0x3A010204), (2, 0x3A004020)):
+        v = np.float32(1) / np.float32(2048 - (1 << bits))
         assert int(v.view(np.uint32)) == pat

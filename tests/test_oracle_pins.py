@@ -383,7 +383,8 @@ def test_keys_per_channel_values_per_token():
     assert ev[7].max() > 0.5
     # every key group's metadata is per channel: G tokens share one (scale, zp) per channel
     assert st.k_meta.shape == (T // G, d, 2)
-    assert st.v_meta.shape == (T, d // Gv, 2)
+    assert st.v_meta.shape == ((T + 1) // 2, d // Gv, 4)  # pair records
+    assert oracle.value_meta(st).shape == (T, d // Gv, 2)
 
 
 def test_residual_window_keeps_newest_tokens_in_f16():
@@ -450,7 +451,25 @@ def test_value_pair_rows_match_hand_derived_bytes(golden_dir):
         assert np.array_equal(pairs, want), (case, np.flatnonzero(pairs)[:4], pairs[np.flatnonzero(pairs)[:4]])
 
 
-# ----------------------------------------------------------------------------- layout self-consistency (parity unpinned)
+def test_value_meta_records_match_hand_derived_bytes(golden_dir):
+    """Value (scale, zero point) pairs of three tokens in the pair records, against records
+    derived by hand: scales before zero points, the even token before the odd one, the
+    odd half of the last record left 0."""
+    case = _golden_layout(golden_dir)["v_meta"]
+    d, bits, Gv = 128, case["bits"], case["Gv"]
+    T = len(case["groups"])
+    v = np.zeros((T, d), np.float64)
+    for t, groups in enumerate(case["groups"]):
+        for j, (lo, hi) in enumerate(groups):
+            v[t, j * Gv:(j + 1) * Gv] = lo
+            v[t, j * Gv + 1] = hi
+    k = np.zeros((T, d), np.float16)
+    st = oracle.cache_state(k, v.astype(np.float16), d=d, bits=bits, G=32, Gv=Gv, R=0)
+    want = np.array([int(h, 16) for h in case["records"]], np.uint16)
+    assert np.array_equal(st.v_meta.reshape(-1), want), [hex(x) for x in st.v_meta.reshape(-1)]
+
+
+# ----------------------------------------------------------------------------- layout self-consistency
 @pytest.mark.parametrize("bits", [2, 4, 8])
 def test_layout_pack_unpack_round_trip(bits):
     d = 128
@@ -581,8 +600,9 @@ def test_symmetric_cache_is_per_token():
     k = (rng.standard_normal((T, d)) * 2).astype(np.float16)
     v = (rng.standard_normal((T, d)) * 0.5).astype(np.float16)
     st = oracle.cache_state_sym(k, v, d=d)
-    assert st.Tq == T and st.k_meta.shape == (T,) and st.v_meta.shape == (T, 1, 2)
-    assert np.all(st.v_meta[:, 0, 1] == 0)
+    assert st.Tq == T and st.k_meta.shape == (T,) and st.v_meta.shape == ((T + 1) // 2, 1, 4)
+    assert np.all(oracle.value_meta(st)[:, 0, 1] == 0)
+    assert np.all(st.v_meta[:, 0, 2:] == 0) and st.v_meta[-1, 0, 1] == 0  # zero points; token 37 does not exist
     k2 = k.copy()
     k2[5] *= np.float16(8)
     st2 = oracle.cache_state_sym(k2, v, d=d)
@@ -592,7 +612,7 @@ def test_symmetric_cache_is_per_token():
     assert st2.k_meta[5] != st.k_meta[5]
     kh, vh = oracle.dequantize_state_sym(st, d=d)
     ks = np.array([oracle.f32_from_f16(int(h)) for h in st.k_meta])
-    vs = np.array([oracle.f32_from_f16(int(h)) for h in st.v_meta[:, 0, 0]])
+    vs = np.array([oracle.f32_from_f16(int(h)) for h in oracle.value_meta(st)[:, 0, 0]])
     assert np.all(np.abs(k.astype(np.float64) - kh) <= ks[:, None] / 2 * (1 + 2.0 ** -20))
     assert np.all(np.abs(v.astype(np.float64) - vh) <= vs[:, None] / 2 * (1 + 2.0 ** -20))
     # the packed rows decode to the same codes
