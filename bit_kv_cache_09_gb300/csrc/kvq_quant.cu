@@ -43,6 +43,7 @@ __device__ __forceinline__ void store_k4(uint8_t* row, int lane, const uint32_t*
 template <int BITS, int G>
 __global__ void __launch_bounds__(256, 4) k_group_kernel(AppendParams p) {
   constexpr int PER_WARP = G / 8;
+  static_assert(PER_WARP % 2 == 0, "rows are split in pairs");
   pdl_wait();
   pdl_allow_dependents();
   const int h = blockIdx.y, b = blockIdx.z;
@@ -55,7 +56,7 @@ __global__ void __launch_bounds__(256, 4) k_group_kernel(AppendParams p) {
   __shared__ float red_max[8][kHeadDim];
   __shared__ float s_sc[kHeadDim];
   __shared__ float s_rs[kHeadDim];
-  __shared__ float s_zp[kHeadDim];
+  __shared__ int s_zp[kHeadDim];
 
   // rows are kept as binary16 pairs (half the registers of binary32): the group
   // min/max of binary16 values is exact in binary16
@@ -80,13 +81,16 @@ __global__ void __launch_bounds__(256, 4) k_group_kernel(AppendParams p) {
     uint32_t* ent = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(p.k_meta) + slice * p.k_meta_slice +
                                                 (p.S_pad / G) * kHeadDim * 4);
 #pragma unroll
-    for (int k = 0; k < PER_WARP; ++k) {
-      const int64_t t = t0 + warp + 8 * k;
-      const uint32_t xb[4] = {x[k].x & 0xFFFFu, x[k].x >> 16, x[k].y & 0xFFFFu, x[k].y >> 16};
-      bool taken[4];
-      split_row_outliers<true>(xb, taken, ent + t * p.kout, p.kout, lane);
-      x[k].x &= (taken[0] ? 0xFFFF0000u : 0xFFFFFFFFu) & (taken[1] ? 0x0000FFFFu : 0xFFFFFFFFu);
-      x[k].y &= (taken[2] ? 0xFFFF0000u : 0xFFFFFFFFu) & (taken[3] ? 0x0000FFFFu : 0xFFFFFFFFu);
+    for (int k = 0; k < PER_WARP; k += 2) {  // rows in pairs: one sort of their packed order keys
+      const int64_t t = t0 + warp + 8 * k;     // row k + 1 is token t + 8
+      const uint32_t xa[4] = {x[k].x & 0xFFFFu, x[k].x >> 16, x[k].y & 0xFFFFu, x[k].y >> 16};
+      const uint32_t xc[4] = {x[k + 1].x & 0xFFFFu, x[k + 1].x >> 16, x[k + 1].y & 0xFFFFu, x[k + 1].y >> 16};
+      bool ta[4], tc[4];
+      split_two_rows_outliers(xa, xc, ta, tc, ent + t * p.kout, ent + (t + 8) * p.kout, p.kout, lane);
+      x[k].x &= (ta[0] ? 0xFFFF0000u : 0xFFFFFFFFu) & (ta[1] ? 0x0000FFFFu : 0xFFFFFFFFu);
+      x[k].y &= (ta[2] ? 0xFFFF0000u : 0xFFFFFFFFu) & (ta[3] ? 0x0000FFFFu : 0xFFFFFFFFu);
+      x[k + 1].x &= (tc[0] ? 0xFFFF0000u : 0xFFFFFFFFu) & (tc[1] ? 0x0000FFFFu : 0xFFFFFFFFu);
+      x[k + 1].y &= (tc[2] ? 0xFFFF0000u : 0xFFFFFFFFu) & (tc[3] ? 0x0000FFFFu : 0xFFFFFFFFu);
     }
   }
 #pragma unroll
@@ -121,12 +125,13 @@ __global__ void __launch_bounds__(256, 4) k_group_kernel(AppendParams p) {
     group_params<BITS>(a, z, s_h, z_h, s, rs, zp);
     s_sc[c] = s;
     s_rs[c] = rs;
-    s_zp[c] = __fsub_rn(zp, Q<BITS>::qmin);
+    s_zp[c] = (int)zp - (int)Q<BITS>::qmin;
     reinterpret_cast<__half2*>(reinterpret_cast<uint8_t*>(p.k_meta) + slice * p.k_meta_slice)[g * kHeadDim + c] =
         __halves2half2(s_h, z_h);
   }
   __syncthreads();
-  float s[4], rs[4], zp[4];
+  float s[4], rs[4];
+  int zp[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     s[e] = s_sc[4 * lane + e];
@@ -156,7 +161,7 @@ __global__ void __launch_bounds__(256, 4) k_group_kernel(AppendParams p) {
 // scale from max|x|, zero point 0).
 // ---------------------------------------------------------------------------
 template <int BITS, bool SYM = false>
-__global__ void __launch_bounds__(256) v_token_kernel(AppendParams p) {
+__global__ void __launch_bounds__(256, 6) v_token_kernel(AppendParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sl = lane & 7;
   // rows of batch row b = blockIdx.y in the input's order (token, kv head)
@@ -181,15 +186,19 @@ __global__ void __launch_bounds__(256) v_token_kernel(AppendParams p) {
   const int64_t slice = (int64_t)b * p.H + h;
 
   float x[16];
+  __half2 mn2, mx2;  // the lane's min and max in binary16 (exact), per half of the pairs
   {
     const uint4* src = reinterpret_cast<const uint4*>(p.v_in + w * kHeadDim + 16 * sl);
     const uint4 a = src[0], c = src[1];
     const uint32_t wd[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wd[k]));
+      const __half2 hk = *reinterpret_cast<const __half2*>(&wd[k]);
+      const float2 f = __half22float2(hk);
       x[2 * k] = f.x;
       x[2 * k + 1] = f.y;
+      mn2 = k ? __hmin2(mn2, hk) : hk;
+      mx2 = k ? __hmax2(mx2, hk) : hk;
     }
   }
   const int lpg = p.Gv >> 4;  // lanes per value group: 2, 4 or 8
@@ -205,12 +214,7 @@ __global__ void __launch_bounds__(256) v_token_kernel(AppendParams p) {
     z_h = __float2half_rn(0.0f);
     zp = 0.0f;
   } else {
-    float mn = x[0], mx = x[0];
-#pragma unroll
-    for (int i = 1; i < 16; ++i) {
-      mn = fminf(mn, x[i]);
-      mx = fmaxf(mx, x[i]);
-    }
+    float mn = fminf(__low2float(mn2), __high2float(mn2)), mx = fmaxf(__low2float(mx2), __high2float(mx2));
     for (int off = 1; off < lpg; off <<= 1) {
       mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
@@ -223,7 +227,7 @@ __global__ void __launch_bounds__(256) v_token_kernel(AppendParams p) {
     rec[0] = s_h;
     rec[2] = z_h;
   }
-  const float zpu = __fsub_rn(zp, Q<BITS>::qmin);
+  const int zpu = (int)zp - (int)Q<BITS>::qmin;
   uint32_t u[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) u[i] = quant_code<BITS>(x[i], s, rs, zpu);
@@ -329,7 +333,7 @@ __global__ void __launch_bounds__(256) k_token_sym_kernel(AppendParams p) {
   sym_params8(a, s_h, s, rs);
   uint32_t wv[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-  for (int i = 0; i < 16; ++i) wv[i >> 2] |= quant_code<8>(x[i], s, rs, 128.0f) << (8 * (i & 3));
+  for (int i = 0; i < 16; ++i) wv[i >> 2] |= quant_code<8>(x[i], s, rs, 128) << (8 * (i & 3));
   if (valid) {
     *reinterpret_cast<uint4*>(p.k_codes + slice * p.k_codes_slice + t * p.rowK + 16 * sl) =
         make_uint4(wv[0], wv[1], wv[2], wv[3]);
@@ -338,26 +342,50 @@ __global__ void __launch_bounds__(256) k_token_sym_kernel(AppendParams p) {
 }
 
 // ---------------------------------------------------------------------------
-// Symmetric per-token keys with outlier isolation (kout > 0): one warp per row (the
-// median and the farthest entries need the whole row), see quant::quantize_key_row_sym.
+// Symmetric per-token keys with outlier isolation (kout > 0): two rows per warp (the
+// median and the farthest entries need the whole row; the two rows' medians come from one
+// sort of their packed order keys), see quant::split_two_rows_outliers.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) k_token_sym_outlier_kernel(AppendParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t nb = p.n_new * p.H;
-  const int64_t wb = (int64_t)blockIdx.x * 8 + warp;
+  const int64_t wb0 = ((int64_t)blockIdx.x * 8 + warp) * 2;
   pdl_wait();
   pdl_allow_dependents();
-  if (wb >= nb) return;  // whole warp
-  const int64_t tt = wb / p.H;
-  const int h = (int)(wb % p.H);
+  if (wb0 >= nb) return;  // whole warp
   const int b = blockIdx.y;
-  const int64_t w = (int64_t)b * nb + wb;
-  const int64_t t = p.s_cur + tt;
-  const int64_t slice = (int64_t)b * p.H + h;
-  uint8_t* kmb = reinterpret_cast<uint8_t*>(p.k_meta) + slice * p.k_meta_slice;
-  quantize_key_row_sym<true>(p.k_in + w * kHeadDim, p.k_codes + slice * p.k_codes_slice + t * p.rowK,
-                       reinterpret_cast<__half*>(kmb) + t, reinterpret_cast<uint32_t*>(kmb + p.S_pad * 2) + t * p.kout,
-                       p.kout, lane);
+  const int n_rows = wb0 + 1 < nb ? 2 : 1;
+  uint32_t xb[2][4];
+  float x[2][4];
+  uint8_t* codes[2];
+  uint8_t* kmb[2];
+  int64_t t[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int64_t wb = k < n_rows ? wb0 + k : wb0;  // a lone last row is split twice, stored once
+    const int64_t tt = wb / p.H;
+    const int h = (int)(wb % p.H);
+    const int64_t slice = (int64_t)b * p.H + h;
+    t[k] = p.s_cur + tt;
+    codes[k] = p.k_codes + slice * p.k_codes_slice + t[k] * p.rowK;
+    kmb[k] = reinterpret_cast<uint8_t*>(p.k_meta) + slice * p.k_meta_slice;
+    const __half* row = p.k_in + ((int64_t)b * nb + wb) * kHeadDim + 4 * lane;
+    const uint2 raw = *reinterpret_cast<const uint2*>(row);
+    xb[k][0] = raw.x & 0xFFFFu; xb[k][1] = raw.x >> 16; xb[k][2] = raw.y & 0xFFFFu; xb[k][3] = raw.y >> 16;
+    load4(row, x[k]);
+  }
+  bool taken[2][4];
+  uint32_t* ent0 = reinterpret_cast<uint32_t*>(kmb[0] + p.S_pad * 2) + t[0] * p.kout;
+  uint32_t* ent1 = reinterpret_cast<uint32_t*>(kmb[1] + p.S_pad * 2) + t[1] * p.kout;
+  split_two_rows_outliers(xb[0], xb[1], taken[0], taken[1], ent0, ent1, p.kout, lane);
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    if (k >= n_rows) break;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (taken[k][e]) x[k][e] = 0.0f;
+    quantize_sym_row(x[k], codes[k], reinterpret_cast<__half*>(kmb[k]) + t[k], lane);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -465,7 +493,7 @@ cudaError_t launch_dequant_bits(const DequantParams& p, cudaStream_t stream) {
 cudaError_t launch_append(const AppendParams& p, int bits, int vbits, cudaStream_t stream) {
   if (p.sym) {  // symmetric per-token int8: keys and values quantized per token
     const int64_t rows = p.n_new * p.H;
-    cudaError_t e = p.kout > 0 ? launch_pdl(k_token_sym_outlier_kernel, dim3((unsigned)((rows + 7) / 8), (unsigned)p.B),
+    cudaError_t e = p.kout > 0 ? launch_pdl(k_token_sym_outlier_kernel, dim3((unsigned)((rows + 15) / 16), (unsigned)p.B),
                                             dim3(256), 0, stream, p)
                                : launch_pdl(k_token_sym_kernel, dim3((unsigned)((rows + 31) / 32), (unsigned)p.B),
                                             dim3(256), 0, stream, p);

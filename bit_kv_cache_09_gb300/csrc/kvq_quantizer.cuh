@@ -104,13 +104,13 @@ __device__ __forceinline__ void sym_params8(float amax, __half& s_h, float& s, f
 }
 
 // Code u = clamp(rint(x/s) + zp, q_min, q_max) - q_min of x in a group with binary16
-// scale s (rs = RN(1/s)); zpu = zp - q_min (an integer-valued binary32, so the shift
-// by q_min is exact and the clamp bounds become [0, 2^b - 1]).
+// scale s (rs = RN(1/s)); zpu = zp - q_min (an integer), so the clamp bounds become
+// [0, 2^b - 1]. rint rounds half to even; the integer steps are exact, so this equals the
+// binary32 formula.
 template <int BITS>
-__device__ __forceinline__ uint32_t quant_code(float x, float s, float rs, float zpu) {
-  float q = __fadd_rn(rintf(div_rn(x, s, rs)), zpu);
-  q = fminf(fmaxf(q, 0.0f), (float)((1 << BITS) - 1));
-  return (uint32_t)(int)q;
+__device__ __forceinline__ uint32_t quant_code(float x, float s, float rs, int zpu) {
+  const int q = __float2int_rn(div_rn(x, s, rs));
+  return (uint32_t)max(__viaddmin_s32(q, zpu, (1 << BITS) - 1), 0);
 }
 
 __device__ __forceinline__ void load4(const __half* p, float* x) {
@@ -162,7 +162,7 @@ __device__ __forceinline__ void quantize_value_row(const __half* v_row, uint16_t
     rec[4 * (lane / lanes_per_group)] = s_h;
     rec[4 * (lane / lanes_per_group) + 2] = z_h;
   }
-  const float zpu = __fsub_rn(zp, Q<BITS>::qmin);
+  const int zpu = (int)zp - (int)Q<BITS>::qmin;
 #pragma unroll
   for (int e = 0; e < 4; ++e) codes_s[4 * lane + e] = (uint8_t)quant_code<BITS>(x[e], s, rs, zpu);
   __syncwarp();
@@ -181,6 +181,15 @@ __device__ __forceinline__ void quantize_value_row(const __half* v_row, uint16_t
 // elements 4l .. 4l + 3: a bitonic sorting network over the 128 positions (Batcher),
 // compare-exchanges at distance 1 and 2 inside a lane, at distance 4j across lanes l and
 // l ^ j with a shuffle; position 63 is element 3 of lane 15 after the last stage.
+// PAIR: every word holds the 16-bit keys of two rows (low and high halves), sorted at once
+// with 16x2 SIMD min/max (the network does not depend on the data); the result holds both
+// rows' 64th smallest keys.
+template <bool PAIR = false>
+__device__ __forceinline__ uint32_t kmin(uint32_t a, uint32_t b) { return PAIR ? __vminu2(a, b) : min(a, b); }
+template <bool PAIR = false>
+__device__ __forceinline__ uint32_t kmax(uint32_t a, uint32_t b) { return PAIR ? __vmaxu2(a, b) : max(a, b); }
+
+template <bool PAIR = false>
 __device__ __forceinline__ uint32_t sorted_key_63(const uint32_t (&key_in)[4], int lane) {
   uint32_t a[4] = {key_in[0], key_in[1], key_in[2], key_in[3]};
 #pragma unroll
@@ -195,7 +204,7 @@ __device__ __forceinline__ uint32_t sorted_key_63(const uint32_t (&key_in)[4], i
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const uint32_t o = __shfl_xor_sync(0xffffffffu, a[e], lj);
-          a[e] = keep_min ? min(a[e], o) : max(a[e], o);
+          a[e] = keep_min ? kmin<PAIR>(a[e], o) : kmax<PAIR>(a[e], o);
         }
       } else {
 #pragma unroll
@@ -203,7 +212,7 @@ __device__ __forceinline__ uint32_t sorted_key_63(const uint32_t (&key_in)[4], i
           if (e & j) continue;                         // e is the lower position of the pair (e, e + j)
           const int i = 4 * lane + e;
           const bool up = (i & k) == 0;
-          const uint32_t lo = min(a[e], a[e + j]), hi = max(a[e], a[e + j]);
+          const uint32_t lo = kmin<PAIR>(a[e], a[e + j]), hi = kmax<PAIR>(a[e], a[e + j]);
           a[e] = up ? lo : hi;
           a[e + j] = up ? hi : lo;
         }
@@ -213,45 +222,24 @@ __device__ __forceinline__ uint32_t sorted_key_63(const uint32_t (&key_in)[4], i
   return __shfl_sync(0xffffffffu, a[3], 15);
 }
 
-// Dense-and-sparse split of one key row ("Sub-8-Bit KV Cache Quantization Is Not a Free
-// Lever for an RDNA4 Agent Swarm", § What the low-bit numbers actually cost: per-vector
-// dense-and-sparse quantization). The warp holds the row's 128 binary16 values, lane l the
-// bit patterns xb[0..3] of channels [4l, 4l+4); the row's kout entries farthest from its
-// lower median (the 64th smallest value) in binary32 |x - median|, in order of decreasing
-// distance, ties to the lower channel, go to entries[0 .. kout) as channel | binary16 << 16
-// (written by the lane that holds them) and are marked in `taken` (the caller replaces them
-// by +0). SORT picks how the lower median is found: a bitonic sort of the row's 128 order
-// keys (fewer instructions; the append kernels) or a radix select with warp ballots (the
-// fused decode step); both give the exact 64th smallest value.
-template <bool SORT>
-__device__ __forceinline__ void split_row_outliers(const uint32_t (&xb)[4], bool (&taken)[4], uint32_t* entries,
-                                                   int kout, int lane) {
-  // order-preserving 16-bit keys of the binary16 inputs (negative values bit-inverted,
-  // positive ones with the sign bit set); -0 and +0 get distinct keys, which leaves
-  // |x - median| unchanged
-  uint32_t key[4];
+// Order-preserving 16-bit keys of binary16 bit patterns (negative values bit-inverted,
+// positive ones with the sign bit set); -0 and +0 get distinct keys, which leaves
+// |x - median| unchanged.
+__device__ __forceinline__ void order_keys(const uint32_t (&xb)[4], uint32_t (&key)[4]) {
 #pragma unroll
   for (int e = 0; e < 4; ++e) key[e] = (xb[e] & 0x8000u) ? (~xb[e] & 0xFFFFu) : (xb[e] | 0x8000u);
-  uint32_t prefix = 0;
-  if constexpr (SORT) {
-    prefix = sorted_key_63(key, lane);
-  } else {  // most-significant-bit-first radix select of rank 63, one ballot per key and bit
-    int rank = 63;
-#pragma unroll
-    for (int bit = 15; bit >= 0; --bit) {
-      const uint32_t above = (0xFFFFu << (bit + 1)) & 0xFFFFu;  // the bits already decided
-      int n0 = 0;
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        n0 += __popc(__ballot_sync(0xffffffffu, ((key[e] ^ prefix) & above) == 0u && ((key[e] >> bit) & 1u) == 0u));
-      if (rank >= n0) {
-        rank -= n0;
-        prefix |= 1u << bit;
-      }
-    }
-  }
-  const uint32_t med_bits = (prefix & 0x8000u) ? (prefix & 0x7FFFu) : (~prefix & 0xFFFFu);
-  const float med = __half2float(__ushort_as_half((unsigned short)med_bits));
+}
+__device__ __forceinline__ float value_of_key(uint32_t k) {
+  const uint32_t bits = (k & 0x8000u) ? (k & 0x7FFFu) : (~k & 0xFFFFu);
+  return __half2float(__ushort_as_half((unsigned short)bits));
+}
+
+// The kout entries of a key row (xb as in split_row_outliers) farthest from `med` in
+// binary32 |x - med|, in order of decreasing distance, ties to the lower channel, to
+// entries[0 .. kout) as channel | binary16 << 16 (written by the lane that holds them),
+// marked in `taken`.
+__device__ __forceinline__ void take_farthest(const uint32_t (&xb)[4], float med, bool (&taken)[4], uint32_t* entries,
+                                              int kout, int lane) {
   float dist[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
@@ -285,11 +273,77 @@ __device__ __forceinline__ void split_row_outliers(const uint32_t (&xb)[4], bool
   }
 }
 
+// Dense-and-sparse split of one key row ("Sub-8-Bit KV Cache Quantization Is Not a Free
+// Lever for an RDNA4 Agent Swarm", § What the low-bit numbers actually cost: per-vector
+// dense-and-sparse quantization). The warp holds the row's 128 binary16 values, lane l the
+// bit patterns xb[0..3] of channels [4l, 4l+4); the row's kout entries farthest from its
+// lower median (the 64th smallest value) in binary32 |x - median|, in order of decreasing
+// distance, ties to the lower channel, go to entries[0 .. kout) as channel | binary16 << 16
+// (written by the lane that holds them) and are marked in `taken` (the caller replaces them
+// by +0). SORT picks how the lower median is found: a bitonic sort of the row's 128 order
+// keys (fewer instructions; the append kernels) or a radix select with warp ballots (the
+// fused decode step); both give the exact 64th smallest value.
+template <bool SORT>
+__device__ __forceinline__ void split_row_outliers(const uint32_t (&xb)[4], bool (&taken)[4], uint32_t* entries,
+                                                   int kout, int lane) {
+  uint32_t key[4];
+  order_keys(xb, key);
+  uint32_t prefix = 0;
+  if constexpr (SORT) {
+    prefix = sorted_key_63(key, lane);
+  } else {  // most-significant-bit-first radix select of rank 63, one ballot per key and bit
+    int rank = 63;
+#pragma unroll
+    for (int bit = 15; bit >= 0; --bit) {
+      const uint32_t above = (0xFFFFu << (bit + 1)) & 0xFFFFu;  // the bits already decided
+      int n0 = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        n0 += __popc(__ballot_sync(0xffffffffu, ((key[e] ^ prefix) & above) == 0u && ((key[e] >> bit) & 1u) == 0u));
+      if (rank >= n0) {
+        rank -= n0;
+        prefix |= 1u << bit;
+      }
+    }
+  }
+  take_farthest(xb, value_of_key(prefix), taken, entries, kout, lane);
+}
+
+// split_row_outliers (sorting) of two key rows held by the warp at once: their order keys
+// share one sort (PAIR), then each row takes its own farthest entries.
+__device__ __forceinline__ void split_two_rows_outliers(const uint32_t (&xa)[4], const uint32_t (&xb)[4],
+                                                        bool (&taken_a)[4], bool (&taken_b)[4], uint32_t* entries_a,
+                                                        uint32_t* entries_b, int kout, int lane) {
+  uint32_t ka[4], kb[4], kp[4];
+  order_keys(xa, ka);
+  order_keys(xb, kb);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) kp[e] = ka[e] | (kb[e] << 16);
+  const uint32_t med2 = sorted_key_63<true>(kp, lane);
+  take_farthest(xa, value_of_key(med2 & 0xFFFFu), taken_a, entries_a, kout, lane);
+  take_farthest(xb, value_of_key(med2 >> 16), taken_b, entries_b, kout, lane);
+}
+
 // One warp quantizes one key row of the symmetric per-token scheme (binary16, 128
 // channels; lane l holds channels [4l, 4l+4)): its binary16 scale to *scale_out and its
 // 8-bit codes, in channel order, to key_row. With kout > 0 the row's kout farthest
 // entries are split off first (split_row_outliers) and replaced by 0 before the scale
 // is taken.
+// The symmetric int8 codes and binary16 scale of one dense key row held by the warp (lane
+// l: channels [4l, 4l+4) as binary32 values), to key_row (channel order) and *scale_out.
+__device__ __forceinline__ void quantize_sym_row(const float (&x)[4], uint8_t* key_row, __half* scale_out, int lane) {
+  float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+  for (int off = 1; off < 32; off <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+  __half s_h;
+  float s, rs;
+  sym_params8(a, s_h, s, rs);
+  uint32_t w = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) w |= quant_code<8>(x[e], s, rs, 128) << (8 * e);
+  reinterpret_cast<uint32_t*>(key_row)[lane] = w;
+  if (lane == 0) *scale_out = s_h;
+}
+
 template <bool SORT = false>
 __device__ __forceinline__ void quantize_key_row_sym(const __half* k_row, uint8_t* key_row, __half* scale_out,
                                                      uint32_t* entries, int kout, int lane) {
@@ -304,16 +358,7 @@ __device__ __forceinline__ void quantize_key_row_sym(const __half* k_row, uint8_
     for (int e = 0; e < 4; ++e)
       if (taken[e]) x[e] = 0.0f;
   }
-  float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
-  for (int off = 1; off < 32; off <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
-  __half s_h;
-  float s, rs;
-  sym_params8(a, s_h, s, rs);
-  uint32_t w = 0;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) w |= quant_code<8>(x[e], s, rs, 128.0f) << (8 * e);
-  reinterpret_cast<uint32_t*>(key_row)[lane] = w;
-  if (lane == 0) *scale_out = s_h;
+  quantize_sym_row(x, key_row, scale_out, lane);
 }
 
 }  // namespace quant
