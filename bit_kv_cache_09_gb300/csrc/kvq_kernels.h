@@ -55,7 +55,7 @@ struct AppendParams {
   FastDiv fd_H;     // division by H of value-row indices below 2^31
   int rows_32;      // n_new * H < 2^31: value-row indices fit the fast division
   int sym;          // symmetric per-token int8 scheme (k_meta: one binary16 scale per token)
-  int kout;         // symmetric scheme: isolated key entries per token (after the S_pad scales)
+  int kout;         // isolated key entries per token (after the key scales or group metadata)
 };
 
 struct DequantParams {
@@ -72,7 +72,7 @@ struct DequantParams {
   int64_t k_codes_slice, v_codes_slice;
   int64_t k_meta_slice;  // bytes of k_meta per slice
   int sym;  // symmetric per-token int8 scheme (k_meta: one binary16 scale per token)
-  int kout;  // symmetric scheme: isolated key entries per token (after the S_pad scales)
+  int kout;  // isolated key entries per token (after the key scales or group metadata)
 };
 
 struct DecodeParams {
@@ -110,7 +110,7 @@ struct DecodeParams {
   int warps;          // warps per CTA of the tensor-core kernel: 4, or 8 (cluster merges only)
   int n_parts;        // partials merged through the workspace: n_split / cluster
   int sym;            // symmetric per-token int8 scheme (k_meta: one binary16 scale per token)
-  int kout;           // symmetric scheme: isolated key entries per token (after the S_pad scales)
+  int kout;           // isolated key entries per token (after the key scales or group metadata)
   int early;          // tensor-core kernel: the first stages are copied before the wait on the
                       // previous kernel of the stream (the caller guarantees it writes no cache
                       // memory of this layer); queries and new rows are read after the wait

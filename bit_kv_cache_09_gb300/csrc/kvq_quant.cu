@@ -152,6 +152,74 @@ __global__ void __launch_bounds__(256, 4) k_group_kernel(AppendParams p) {
 }
 
 // ---------------------------------------------------------------------------
+// Keys in groups of 32 tokens: one warp per (group, kv head, batch row), eight groups of
+// one (kv head, batch row) per CTA. Lane l holds channels [4l, 4l+4) of all 32 rows of
+// its group as binary16 pairs, so each channel's min and max are taken inside the lane
+// (exact in binary16) and the lane computes its four channels' parameters itself: no
+// shared memory, no CTA barrier. Rows as in k_group_kernel; without isolated key entries
+// (with them, k_group_kernel<BITS, 32> splits the rows first).
+// ---------------------------------------------------------------------------
+template <int BITS>
+__global__ void __launch_bounds__(256, 2) k_group32_kernel(AppendParams p) {
+  constexpr int G = 32;
+  pdl_wait();
+  pdl_allow_dependents();
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gi = (int)blockIdx.x * 8 + warp;
+  if (gi >= p.n_groups) return;  // whole warp
+  const int64_t g = p.group0 + gi;
+  const int64_t t0 = g * G;
+  const int64_t slice = (int64_t)b * p.H + h;
+
+  uint2 x[G];  // row k = token t0 + k, channels [4 lane, 4 lane + 4)
+  const __half* resid = p.k_resid + (slice * (int64_t)p.R_eff - p.group0 * G) * kHeadDim;
+  const __half* in = p.k_in + (((int64_t)b * p.n_new - p.s_cur) * p.H + h) * kHeadDim;
+  const int64_t in_stride = (int64_t)p.H * kHeadDim;
+#pragma unroll
+  for (int k = 0; k < G; ++k) {
+    const int64_t t = t0 + k;
+    const __half* row = (t < p.s_cur) ? resid + t * kHeadDim : in + t * in_stride;
+    x[k] = *reinterpret_cast<const uint2*>(row + 4 * lane);
+  }
+  __half2 mn2[2], mx2[2];
+#pragma unroll
+  for (int k = 0; k < G; ++k) {
+    const __half2 a = *reinterpret_cast<const __half2*>(&x[k].x), c = *reinterpret_cast<const __half2*>(&x[k].y);
+    mn2[0] = k ? __hmin2(mn2[0], a) : a;
+    mx2[0] = k ? __hmax2(mx2[0], a) : a;
+    mn2[1] = k ? __hmin2(mn2[1], c) : c;
+    mx2[1] = k ? __hmax2(mx2[1], c) : c;
+  }
+  const float mn[4] = {__low2float(mn2[0]), __high2float(mn2[0]), __low2float(mn2[1]), __high2float(mn2[1])};
+  const float mx[4] = {__low2float(mx2[0]), __high2float(mx2[0]), __low2float(mx2[1]), __high2float(mx2[1])};
+  float s[4], rs[4];
+  int zp[4];
+  uint32_t meta[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    __half s_h, z_h;
+    float zpf;
+    group_params<BITS>(mn[e], mx[e], s_h, z_h, s[e], rs[e], zpf);
+    zp[e] = (int)zpf - (int)Q<BITS>::qmin;
+    meta[e] = (uint32_t)__half_as_ushort(s_h) | ((uint32_t)__half_as_ushort(z_h) << 16);
+  }
+  // (scale, zero point) of channels [4 lane, 4 lane + 4): 16 bytes
+  *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.k_meta) + slice * p.k_meta_slice +
+                            (g * kHeadDim + 4 * lane) * 4) = make_uint4(meta[0], meta[1], meta[2], meta[3]);
+  uint8_t* codes = p.k_codes + slice * p.k_codes_slice;
+#pragma unroll
+  for (int k = 0; k < G; ++k) {
+    float xf[4];
+    load4(reinterpret_cast<const __half*>(&x[k]), xf);
+    uint32_t u[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) u[e] = quant_code<BITS>(xf[e], s[e], rs[e], zp[e]);
+    store_k4<BITS>(codes + (t0 + k) * p.rowK, lane, u);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Values (and the key residual copy): each warp quantizes four appended (batch row,
 // token, kv head) rows, in the input's own order; lanes 8r .. 8r+7 hold row r, lane
 // 8r + l its channels [16l, 16l + 16). A value group of Gv channels spans Gv/16 lanes.
@@ -289,10 +357,119 @@ __global__ void __launch_bounds__(256, 6) v_token_kernel(AppendParams p) {
 }
 
 // ---------------------------------------------------------------------------
+// 2-bit values (and the key residual copy): each warp quantizes eight appended (batch
+// row, token, kv head) rows, in the input's own order; lanes 4r .. 4r+3 hold row r, lane
+// 4r + l its channels [32l, 32l + 32). A value group of Gv channels spans Gv/32 lanes.
+// In the pair-row layout channel 32l + 8q + m (m < 8, q < 4) sits at position
+// 16m + 4l + q, so a lane's four codes of one m fill one byte of a 16-bit unit whose other
+// byte is lane l ^ 1's. Twice the channels per lane of v_token_kernel halve the per-row
+// work per code (the group parameters, the row index), which pays for 2-bit codes; with
+// 4- and 8-bit codes the fewer resident warps cost more (measured).
+// ---------------------------------------------------------------------------
+template <int BITS>
+__global__ void __launch_bounds__(256, 4) v_token32_kernel(AppendParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sl = lane & 3;
+  // rows of batch row b = blockIdx.y in the input's order (token, kv head)
+  const int64_t nb = p.n_new * p.H;
+  const int64_t wb_raw = ((int64_t)blockIdx.x * 8 + warp) * 8 + (lane >> 2);
+  pdl_wait();
+  pdl_allow_dependents();
+  const bool valid = wb_raw < nb;
+  const int64_t wb = valid ? wb_raw : nb - 1;  // lanes past the end read a real row and store nothing
+  int64_t tt;
+  int h;
+  if (p.rows_32) {
+    tt = fast_div((uint32_t)wb, p.fd_H);
+    h = (int)(wb - tt * p.H);
+  } else {
+    tt = wb / p.H;
+    h = (int)(wb % p.H);
+  }
+  const int b = blockIdx.y;
+  const int64_t w = (int64_t)b * nb + wb;
+  const int64_t t = p.s_cur + tt;
+  const int64_t slice = (int64_t)b * p.H + h;
+
+  float x[32];       // channel 32 sl + i
+  __half2 mn2, mx2;  // the lane's min and max in binary16 (exact), per half of the pairs
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(p.v_in + w * kHeadDim + 32 * sl);
+#pragma unroll
+    for (int k4 = 0; k4 < 4; ++k4) {
+      const uint4 a = src[k4];
+      const uint32_t wd[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const __half2 hk = *reinterpret_cast<const __half2*>(&wd[k]);
+        const float2 f = __half22float2(hk);
+        x[8 * k4 + 2 * k] = f.x;
+        x[8 * k4 + 2 * k + 1] = f.y;
+        mn2 = (k4 | k) ? __hmin2(mn2, hk) : hk;
+        mx2 = (k4 | k) ? __hmax2(mx2, hk) : hk;
+      }
+    }
+  }
+  const float mn0 = fminf(__low2float(mn2), __high2float(mn2)), mx0 = fmaxf(__low2float(mx2), __high2float(mx2));
+  const int lpg = p.Gv >> 5;  // lanes per value group: 1, 2 or 4
+  __half s_h, z_h;
+  float s, rs, zp;
+  {
+    float mn = mn0, mx = mx0;
+    for (int off = 1; off < lpg; off <<= 1) {
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    }
+    group_params<BITS>(mn, mx, s_h, z_h, s, rs, zp);
+  }
+  if (valid && sl % lpg == 0) {  // the token's half of its pair's record for this group
+    __half* rec = reinterpret_cast<__half*>(p.v_meta) + ((slice * (p.S_pad >> 1) + (t >> 1)) * p.n_vg + sl / lpg) * 4 +
+                  (int)(t & 1);
+    rec[0] = s_h;
+    rec[2] = z_h;
+  }
+  const int zpu = (int)zp - (int)Q<BITS>::qmin;
+
+  // the token's half of its pair row: 16-bit unit k at pair[2 k]
+  uint16_t* pair = reinterpret_cast<uint16_t*>(p.v_codes + slice * p.v_codes_slice + (t >> 1) * 2 * p.rowV) + (t & 1);
+  static_assert(BITS == 2, "2-bit codes only");
+  {
+    // unit 2m + sl/2: this lane's codes q = 0..3 at bits 2q of byte (sl & 1). Bytes of
+    // m = 0..3 and 4..7 are gathered in two words; even lanes store m = 0..3, odd lanes
+    // m = 4..7, each taking the other byte of its units from lane sl ^ 1.
+    uint32_t wm[2] = {0u, 0u};
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      uint32_t byte = 0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) byte |= quant_code<BITS>(x[8 * q + m], s, rs, zpu) << (2 * q);
+      wm[m >> 2] |= byte << (8 * (m & 3));
+    }
+    const bool odd = sl & 1;
+    const uint32_t recv = __shfl_xor_sync(0xffffffffu, odd ? wm[0] : wm[1], 1);
+    const uint32_t lo = odd ? recv : wm[0], hi = odd ? wm[1] : recv;  // even lane's bytes, odd lane's bytes
+    if (valid) {
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const int m = (odd ? 4 : 0) + jj;
+        pair[2 * (2 * m + (sl >> 1))] = (uint16_t)__byte_perm(lo, hi, (unsigned)(jj | ((4 + jj) << 4)));
+      }
+    }
+  }
+  // Keys of tokens past the last full residual window go to the residual.
+  if (valid && t >= p.A1) {
+    const uint4* ks = reinterpret_cast<const uint4*>(p.k_in + w * kHeadDim + 32 * sl);
+    uint4* kd = reinterpret_cast<uint4*>(p.k_resid + (slice * p.R_eff + (t - p.A1)) * kHeadDim + 32 * sl);
+#pragma unroll
+    for (int k4 = 0; k4 < 4; ++k4) kd[k4] = ks[k4];
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Symmetric per-token keys ("KV Cache Quantization — 8-bit and 4-bit", § Symmetric vs
 // asymmetric; one scale per token, "Sub-8-Bit KV Cache Quantization Is Not a Free Lever
-// for an RDNA4 Agent Swarm", § The RDNA4 kernel angle): rows assigned as in
-// v_token_kernel (four per warp, lane 8r + l holds channels [16l, 16l + 16)); the 8-bit
+// for an RDNA4 Agent Swarm", § The RDNA4 kernel angle): four appended rows per warp in
+// the input's order, lane 8r + l holding channels [16l, 16l + 16) of row r; the 8-bit
 // codes go to the key row in channel order (16 bytes per lane), the binary16 scale to
 // k_meta[slice][t].
 // ---------------------------------------------------------------------------
@@ -468,7 +645,10 @@ cudaError_t launch_keys(const AppendParams& p, cudaStream_t stream) {
   if (p.n_groups <= 0) return cudaSuccess;
   dim3 grid((unsigned)p.n_groups, (unsigned)p.H, (unsigned)p.B);
   switch (p.G) {
-    case 32: return launch_pdl(k_group_kernel<BITS, 32>, grid, dim3(256), 0, stream, p);
+    case 32:
+      if (p.kout > 0) return launch_pdl(k_group_kernel<BITS, 32>, grid, dim3(256), 0, stream, p);
+      return launch_pdl(k_group32_kernel<BITS>, dim3((unsigned)((p.n_groups + 7) / 8), (unsigned)p.H, (unsigned)p.B),
+                        dim3(256), 0, stream, p);
     case 64: return launch_pdl(k_group_kernel<BITS, 64>, grid, dim3(256), 0, stream, p);
     default: return launch_pdl(k_group_kernel<BITS, 128>, grid, dim3(256), 0, stream, p);
   }
@@ -477,8 +657,13 @@ cudaError_t launch_keys(const AppendParams& p, cudaStream_t stream) {
 template <int VBITS, bool SYM = false>
 cudaError_t launch_values(const AppendParams& p, cudaStream_t stream) {
   const int64_t rows = p.n_new * p.H;  // per batch row
-  return launch_pdl(v_token_kernel<VBITS, SYM>, dim3((unsigned)((rows + 31) / 32), (unsigned)p.B), dim3(256), 0, stream,
-                    p);
+  if constexpr (VBITS == 2 && !SYM) {
+    return launch_pdl(v_token32_kernel<VBITS>, dim3((unsigned)((rows + 63) / 64), (unsigned)p.B), dim3(256), 0, stream,
+                      p);
+  } else {
+    return launch_pdl(v_token_kernel<VBITS, SYM>, dim3((unsigned)((rows + 31) / 32), (unsigned)p.B), dim3(256), 0,
+                      stream, p);
+  }
 }
 
 template <int BITS, int VBITS>
