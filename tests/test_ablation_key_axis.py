@@ -1,13 +1,16 @@
 """Quality ablation on synthetic data: keys quantized per channel (groups of G tokens,
-the kernels' scheme) versus per token (groups of Gv channels, the values' scheme), at
-8, 4 and 2 bits, measured as the decode-attention output error and the KL divergence
-of the attention probabilities against unquantized binary16 keys and values.
+the kernels' scheme) versus per token (groups of Gv channels, the values' scheme), and
+per channel with the 4 entries of each key row farthest from its median kept aside as
+binary16 (dense-and-sparse), at 8, 4 and 2 bits, measured as the decode-attention output
+error and the KL divergence of the attention probabilities against unquantized binary16
+keys and values.
 
 The pages argue that keys carry outlier channels, so per-channel key grouping keeps
 low-bit attention usable where per-token grouping breaks ("KV Cache Quantization —
 8-bit and 4-bit", § The outlier problem: keys have outlier channels; "Sub-8-Bit KV
 Cache Quantization Is Not a Free Lever for an RDNA4 Agent Swarm", § The cache is two
-distributions, not one). Everything here runs on the oracle's quantizer and its
+distributions, not one; § What the low-bit numbers actually cost, on per-vector
+dense-and-sparse outlier isolation). Everything here runs on the oracle's quantizer and its
 binary64 attention; the table is printed (pytest -s) and a few robust orderings are
 asserted. The generator's outlier channels are a*z + 5 (z standard normal), i.e.
 large in magnitude and in spread across tokens.
@@ -62,8 +65,10 @@ def ablation(n_out, gain, bits, seed=77):
     kf, vf = k16.astype(np.float32), v16.astype(np.float32)
     ref = oracle.attention(q16, kf, vf, scale)
     p_ref = _probs(q16, kf, scale)
+    st_o = oracle.cache_state(k16, v16, d=D, bits=bits, G=G, Gv=GV, R=0, k_outliers=4)
+    k_cho, _ = oracle.dequantize_state(st_o, d=D, bits=bits, G=G, Gv=GV, R=0)
     res = {}
-    for name, kq in (("per-channel", k_ch), ("per-token", k_tok)):
+    for name, kq in (("per-channel", k_ch), ("per-token", k_tok), ("per-channel+4", k_cho)):
         out = oracle.attention(q16, kq, v_hat, scale)
         res[name] = (float(np.abs(out - ref).max()), _kl(p_ref, _probs(q16, kq, scale)))
     return res
@@ -75,10 +80,10 @@ CASES = [(4, 20.0, b) for b in (8, 4, 2)] + [(6, 50.0, b) for b in (8, 4, 2)]
 @pytest.fixture(scope="module")
 def table():
     rows = {c: ablation(*c) for c in CASES}
-    print("\noutliers  bits | out err per-channel  per-token | KL per-channel  per-token")
+    print("\noutliers  bits | out err per-channel  per-token  per-channel+4 | KL per-channel  per-token  per-channel+4")
     for (n_out, gain, bits), r in rows.items():
-        print(f"{n_out} x {gain:4.0f}  int{bits} | {r['per-channel'][0]:.2e}  {r['per-token'][0]:.2e} | "
-              f"{r['per-channel'][1]:.2e}  {r['per-token'][1]:.2e}")
+        print(f"{n_out} x {gain:4.0f}  int{bits} | {r['per-channel'][0]:.2e}  {r['per-token'][0]:.2e}  "
+              f"{r['per-channel+4'][0]:.2e} | {r['per-channel'][1]:.2e}  {r['per-token'][1]:.2e}  {r['per-channel+4'][1]:.2e}")
     return rows
 
 
@@ -101,3 +106,12 @@ def test_error_grows_as_bits_drop(table):
         for axis in ("per-channel", "per-token"):
             kls = [table[(n_out, gain, b)][axis][1] for b in (8, 4, 2)]
             assert kls[0] < kls[1] < kls[2]
+
+
+def test_isolated_entries_cut_the_error_of_per_channel_keys(table):
+    # four isolated entries per key row take the outlier channels' extremes out of the
+    # per-channel groups: the attention KL drops at every width for both outlier models
+    for (n_out, gain, bits), r in table.items():
+        assert r["per-channel+4"][1] < r["per-channel"][1] / 3, (n_out, gain, bits)
+        if bits < 8:
+            assert r["per-channel+4"][0] < r["per-channel"][0]
