@@ -240,36 +240,31 @@ __device__ __forceinline__ float value_of_key(uint32_t k) {
 // marked in `taken`.
 __device__ __forceinline__ void take_farthest(const uint32_t (&xb)[4], float med, bool (&taken)[4], uint32_t* entries,
                                               int kout, int lane) {
-  float dist[4];
+  // distances are non-negative binary32 values, which order like their bit patterns: one
+  // warp max of the bits per round, then the lowest lane holding that distance (its
+  // channels are the lowest), then that lane's lowest such channel
+  uint32_t db[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     taken[e] = false;
-    dist[e] = fabsf(__fsub_rn(__half2float(__ushort_as_half((unsigned short)xb[e])), med));
+    db[e] = __float_as_uint(fabsf(__fsub_rn(__half2float(__ushort_as_half((unsigned short)xb[e])), med)));
   }
   for (int r = 0; r < kout; ++r) {
-    float bd = -1.0f;
-    int bc = 1 << 30;
+    uint32_t mine = 0u;
 #pragma unroll
     for (int e = 0; e < 4; ++e)
-      if (!taken[e] && dist[e] > bd) {
-        bd = dist[e];
-        bc = 4 * lane + e;
-      }
+      if (!taken[e]) mine = max(mine, db[e] + 1u);  // + 1: an untaken +0 distance still beats a taken entry
+    const uint32_t best = __reduce_max_sync(0xffffffffu, mine);
+    const uint32_t owners = __ballot_sync(0xffffffffu, mine == best);
+    if (lane == __ffs(owners) - 1) {
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {  // farthest, ties to the lower channel
-      const float od = __shfl_xor_sync(0xffffffffu, bd, off);
-      const int oc = __shfl_xor_sync(0xffffffffu, bc, off);
-      if (od > bd || (od == bd && oc < bc)) {
-        bd = od;
-        bc = oc;
-      }
+      for (int e = 0; e < 4; ++e)
+        if (!taken[e] && db[e] + 1u == best) {
+          taken[e] = true;
+          entries[r] = (uint32_t)(4 * lane + e) | (xb[e] << 16);
+          break;
+        }
     }
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (bc == 4 * lane + e) {
-        taken[e] = true;
-        entries[r] = (uint32_t)bc | (xb[e] << 16);
-      }
   }
 }
 
