@@ -657,23 +657,23 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
       const uint32_t m = hmax2(hmax2(m01, m23), hmax2(m45, m67));
       mx = (u == 0) ? m : hmax2(mx, m);
     }
-    if (NT == 1) mx = hmax2(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-    mx = hmax2(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = hmax2(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    // the group's largest scale over the warp (every channel is folded by some lane);
     // scales are positive: the larger bit pattern is the larger value
-    const uint32_t smax = max(mx & 0xFFFFu, mx >> 16);
+    const uint32_t smax = __reduce_max_sync(0xffffffffu, max(mx & 0xFFFFu, mx >> 16));
     const int Es = min(15, 7 - (max((int)(smax >> 10), 1) - 15));  // in [-8, 15]
     const uint32_t pe = (uint32_t)(Es + 15) << 10;
     const uint32_t p2 = pe | (pe << 16);  // half2(2^Es, 2^Es)
     // bias = sum_c x_c (q_min - zp_c) on the tensor cores, from the fragments just
-    // computed: an extra key tile whose column 0 is k_scale 2^-8 (ones, lane g = 0)
-    // and column 1 zp_c k_scale 2^-8 (lane g = 1). With r <= 4, rows g < 4 run on
-    // the first half of the channels and rows g >= 4 on the second in the same MMA,
-    // so lane g = 5 supplies the second half's zero points in column 5 and a query's
-    // bias adds rows q and q + 4.
+    // computed: an extra key tile whose column 0 is (q_min - zp_c) k_scale 2^-8 (lane
+    // g = 0; q_min - zp_c is an integer of magnitude <= 2048, exact in binary16, and
+    // k_scale 2^-8 a power of two). With r <= 4, rows g < 4 run on the first half of the
+    // channels and rows g >= 4 on the second in the same MMA, so lane g = 4 supplies the
+    // second half's column 4 and a query's bias adds rows q (column 0) and q + 4
+    // (column 4).
     float bt[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    const uint32_t ones_col = (g == 0) ? kOne2 : 0u;
-    const uint32_t zsel = (g == 1 || (NT == 1 && g == 5)) ? kOne2 : 0u;
+    const bool bsel = g == 0 || (NT == 1 && g == 4);
+    const uint32_t nsel = bsel ? 0xBC00BC00u : 0u;  // half2(-1, -1) in the bias columns
+    const uint32_t qsel = bsel ? (uint32_t)__half_as_ushort(__float2half_rn(qmin)) * 0x00010001u : 0u;
 #pragma unroll
     for (int u = 0; u < NH; ++u) {
       const int h = hh + u;
@@ -700,23 +700,21 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
           for (int e = 0; e < 2; ++e) {
             const int pl = 4 * k + 2 * kk + e;
             const uint32_t z2 = prmt2(mw[u][k_pair_ca<BITS>(pl)], mw[u][k_pair_cb<BITS>(pl)], 0x7632u);
-            bz[e] = hmul2(hfma2(z2, zsel, ones_col), kc_bits<BITS>(pl));
+            bz[e] = hmul2(hfma2(z2, nsel, qsel), kc_bits<BITS>(pl));
           }
           mma16816(bt, f[4 * kk], f[4 * kk + 1], f[4 * kk + 2], f[4 * kk + 3], bz[0], bz[1]);
         }
       }
     }
     __syncwarp();
-    // lanes j = 0 hold columns 0 and 1 of rows g (hi) and g + 8 (lo), lanes j = 2 column 5
-    const float t0 = bt[0] + bt[2], tz = bt[1] + bt[3];
+    // lanes j = 0 hold column 0 of rows g (hi) and g + 8 (lo), lanes j = 2 column 4
+    const float t0 = bt[0] + bt[2];
     float bsum;
     if (NT == 1) {  // rows q and q + 4 hold query q's two halves of the channels
       const int q = qj;
-      const float ones = __shfl_sync(0xffffffffu, t0, 4 * q) + __shfl_sync(0xffffffffu, t0, 4 * q + 16);
-      const float zz = __shfl_sync(0xffffffffu, tz, 4 * q) + __shfl_sync(0xffffffffu, tz, 4 * q + 18);
-      bsum = qmin * ones - zz;
+      bsum = __shfl_sync(0xffffffffu, t0, 4 * q) + __shfl_sync(0xffffffffu, t0, 4 * q + 18);
     } else {
-      bsum = __shfl_sync(0xffffffffu, qmin * t0 - tz, lane & ~3);
+      bsum = __shfl_sync(0xffffffffu, t0, lane & ~3);
     }
     const int E = qe_mine + Es;
     qscale = pow2f(24 - E) * p.scale_log2;
@@ -1161,7 +1159,8 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? min_blocks<NT>() : (NW == 5
   int sidx = 0;
   uint32_t phase = 0;
   for (int i = 0; i < n_mine; ++i) {
-    if (!mbar_wait(smem_u32(&bars[warp][sidx]), phase, p.wait_ns)) {
+    // every lane takes the same decision (the stage's copies are the whole warp's)
+    if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars[warp][sidx]), phase, p.wait_ns))) {
       failed_at = i;
       break;
     }
