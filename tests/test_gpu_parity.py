@@ -107,6 +107,8 @@ CONFIGS = [
     (4, 128, 128, 128, 8),
     (4, 64, 32, 256, 3),
     (2, 128, 64, 0, 1),
+    (2, 64, 128, 128, 4),   # 2-bit values in groups of 128 channels (four lanes per group)
+    (4, 32, 64, 64, 2),     # 4-bit keys in groups of 32 tokens (one warp per group)
 ]
 
 
