@@ -359,15 +359,17 @@ __global__ void __launch_bounds__(256, 6) v_token_kernel(AppendParams p) {
 // ---------------------------------------------------------------------------
 // 2-bit values (and the key residual copy): each warp quantizes eight appended (batch
 // row, token, kv head) rows, in the input's own order; lanes 4r .. 4r+3 hold row r, lane
-// 4r + l its channels [32l, 32l + 32). A value group of Gv channels spans Gv/32 lanes.
-// In the pair-row layout channel 32l + 8q + m (m < 8, q < 4) sits at position
-// 16m + 4l + q, so a lane's four codes of one m fill one byte of a 16-bit unit whose other
-// byte is lane l ^ 1's. Twice the channels per lane of v_token_kernel halve the per-row
-// work per code (the group parameters, the row index), which pays for 2-bit codes; with
-// 4- and 8-bit codes the fewer resident warps cost more (measured).
+// 4r + l its channels [32l, 32l + 32) as binary16 pairs (converted to binary32 one pair at
+// a time where they are quantized). A value group of Gv channels spans Gv/32 lanes. In the
+// pair-row layout channel 32l + 8q + m (m < 8, q < 4) sits at position 16m + 4l + q, so a
+// lane's four codes of one m fill one byte of a 16-bit unit whose other byte is lane
+// l ^ 1's. Twice the channels per lane of v_token_kernel halve the per-row work per code
+// (the group parameters, the row index), which pays for 2-bit codes; with 4-bit codes
+// (each lane then fills whole units) it measured 6 % slower than v_token_kernel.
 // ---------------------------------------------------------------------------
 template <int BITS>
-__global__ void __launch_bounds__(256, 4) v_token32_kernel(AppendParams p) {
+__global__ void __launch_bounds__(256, 6) v_token32_kernel(AppendParams p) {
+  static_assert(BITS == 2, "2-bit codes only");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sl = lane & 3;
   // rows of batch row b = blockIdx.y in the input's order (token, kv head)
@@ -391,20 +393,17 @@ __global__ void __launch_bounds__(256, 4) v_token32_kernel(AppendParams p) {
   const int64_t t = p.s_cur + tt;
   const int64_t slice = (int64_t)b * p.H + h;
 
-  float x[32];       // channel 32 sl + i
+  uint32_t xh[16];   // channels 32 sl + 2k and 32 sl + 2k + 1 as a binary16 pair
   __half2 mn2, mx2;  // the lane's min and max in binary16 (exact), per half of the pairs
   {
     const uint4* src = reinterpret_cast<const uint4*>(p.v_in + w * kHeadDim + 32 * sl);
 #pragma unroll
     for (int k4 = 0; k4 < 4; ++k4) {
       const uint4 a = src[k4];
-      const uint32_t wd[4] = {a.x, a.y, a.z, a.w};
+      xh[4 * k4] = a.x; xh[4 * k4 + 1] = a.y; xh[4 * k4 + 2] = a.z; xh[4 * k4 + 3] = a.w;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const __half2 hk = *reinterpret_cast<const __half2*>(&wd[k]);
-        const float2 f = __half22float2(hk);
-        x[8 * k4 + 2 * k] = f.x;
-        x[8 * k4 + 2 * k + 1] = f.y;
+        const __half2 hk = *reinterpret_cast<const __half2*>(&xh[4 * k4 + k]);
         mn2 = (k4 | k) ? __hmin2(mn2, hk) : hk;
         mx2 = (k4 | k) ? __hmax2(mx2, hk) : hk;
       }
@@ -429,21 +428,31 @@ __global__ void __launch_bounds__(256, 4) v_token32_kernel(AppendParams p) {
     rec[2] = z_h;
   }
   const int zpu = (int)zp - (int)Q<BITS>::qmin;
+  // codes of channels 32 sl + 8q + m and + 1 (m even), from one binary16 pair
+  auto codes2 = [&](int q, int m, uint32_t& c0, uint32_t& c1) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&xh[(8 * q + m) >> 1]));
+    c0 = quant_code<BITS>(f.x, s, rs, zpu);
+    c1 = quant_code<BITS>(f.y, s, rs, zpu);
+  };
 
   // the token's half of its pair row: 16-bit unit k at pair[2 k]
   uint16_t* pair = reinterpret_cast<uint16_t*>(p.v_codes + slice * p.v_codes_slice + (t >> 1) * 2 * p.rowV) + (t & 1);
-  static_assert(BITS == 2, "2-bit codes only");
   {
     // unit 2m + sl/2: this lane's codes q = 0..3 at bits 2q of byte (sl & 1). Bytes of
     // m = 0..3 and 4..7 are gathered in two words; even lanes store m = 0..3, odd lanes
     // m = 4..7, each taking the other byte of its units from lane sl ^ 1.
     uint32_t wm[2] = {0u, 0u};
 #pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      uint32_t byte = 0;
+    for (int m = 0; m < 8; m += 2) {
+      uint32_t b0 = 0, b1 = 0;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) byte |= quant_code<BITS>(x[8 * q + m], s, rs, zpu) << (2 * q);
-      wm[m >> 2] |= byte << (8 * (m & 3));
+      for (int q = 0; q < 4; ++q) {
+        uint32_t c0, c1;
+        codes2(q, m, c0, c1);
+        b0 |= c0 << (2 * q);
+        b1 |= c1 << (2 * q);
+      }
+      wm[m >> 2] |= (b0 | (b1 << 8)) << (8 * (m & 3));
     }
     const bool odd = sl & 1;
     const uint32_t recv = __shfl_xor_sync(0xffffffffu, odd ? wm[0] : wm[1], 1);
