@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(256, 2) k_group32_kernel(AppendParams p) {
 // scale from max|x|, zero point 0).
 // ---------------------------------------------------------------------------
 template <int BITS, bool SYM = false>
-__global__ void __launch_bounds__(256, 6) v_token_kernel(AppendParams p) {
+__global__ void __launch_bounds__(256, 8) v_token_kernel(AppendParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sl = lane & 7;
   // rows of batch row b = blockIdx.y in the input's order (token, kv head)
@@ -253,18 +253,15 @@ __global__ void __launch_bounds__(256, 6) v_token_kernel(AppendParams p) {
   const int64_t t = p.s_cur + tt;
   const int64_t slice = (int64_t)b * p.H + h;
 
-  float x[16];
+  uint32_t wd[8];    // channels 16 sl + 2k, 16 sl + 2k + 1 as a binary16 pair
   __half2 mn2, mx2;  // the lane's min and max in binary16 (exact), per half of the pairs
   {
     const uint4* src = reinterpret_cast<const uint4*>(p.v_in + w * kHeadDim + 16 * sl);
     const uint4 a = src[0], c = src[1];
-    const uint32_t wd[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+    wd[0] = a.x; wd[1] = a.y; wd[2] = a.z; wd[3] = a.w; wd[4] = c.x; wd[5] = c.y; wd[6] = c.z; wd[7] = c.w;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const __half2 hk = *reinterpret_cast<const __half2*>(&wd[k]);
-      const float2 f = __half22float2(hk);
-      x[2 * k] = f.x;
-      x[2 * k + 1] = f.y;
       mn2 = k ? __hmin2(mn2, hk) : hk;
       mx2 = k ? __hmax2(mx2, hk) : hk;
     }
@@ -273,9 +270,8 @@ __global__ void __launch_bounds__(256, 6) v_token_kernel(AppendParams p) {
   __half s_h, z_h;
   float s, rs, zp;
   if constexpr (SYM) {
-    float a = fabsf(x[0]);
-#pragma unroll
-    for (int i = 1; i < 16; ++i) a = fmaxf(a, fabsf(x[i]));
+    const __half2 am = __hmax2(__habs2(mn2), __habs2(mx2));
+    float a = fmaxf(__low2float(am), __high2float(am));
 #pragma unroll
     for (int off = 1; off < 8; off <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
     sym_params8(a, s_h, s, rs);
@@ -298,7 +294,11 @@ __global__ void __launch_bounds__(256, 6) v_token_kernel(AppendParams p) {
   const int zpu = (int)zp - (int)Q<BITS>::qmin;
   uint32_t u[16];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) u[i] = quant_code<BITS>(x[i], s, rs, zpu);
+  for (int k = 0; k < 8; ++k) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wd[k]));
+    u[2 * k] = quant_code<BITS>(f.x, s, rs, zpu);
+    u[2 * k + 1] = quant_code<BITS>(f.y, s, rs, zpu);
+  }
 
   uint16_t* pair = reinterpret_cast<uint16_t*>(p.v_codes + slice * p.v_codes_slice + (t >> 1) * 2 * p.rowV) + (t & 1);
   if (BITS == 8) {
