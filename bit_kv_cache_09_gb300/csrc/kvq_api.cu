@@ -44,10 +44,14 @@ LayerPtrs layer_ptrs(const Geometry& g, const kvq_buffers* b, int layer) {
   return p;
 }
 
+// SM count of the current device (cached per device; 0 if the query fails)
 int device_sm_count() {
+  static std::atomic<int> cache[16];
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 16 && (n = cache[dev].load(std::memory_order_relaxed)) > 0) return n;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 16) cache[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
@@ -303,6 +307,7 @@ kvq_status kvq_quantize_append(const kvq_config* cfg, const kvq_buffers* bufs, i
   p.fd_H = kvq::make_fast_div((uint32_t)g.H);
   p.rows_32 = n_new * g.H < (int64_t(1) << 31);
   p.sym = g.sym;
+  p.wide_keys = g.kout > 0 || (int64_t)p.n_groups * g.H * g.B < 4 * (int64_t)device_sm_count();
   cudaError_t e = kvq::launch_append(p, g.bits, g.vbits, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }

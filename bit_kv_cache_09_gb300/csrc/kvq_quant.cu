@@ -36,13 +36,17 @@ __device__ __forceinline__ void store_k4(uint8_t* row, int lane, const uint32_t*
 }
 
 // ---------------------------------------------------------------------------
-// Keys: one CTA per (group, kv head, batch row); 8 warps, warp w holds tokens
-// w, w+8, ... of the group, lane l holds channels [4l, 4l+4). Token rows come from
-// the residual window (tokens < s_cur) or from the appended input. 4 CTAs per SM.
+// Keys: one CTA per (group, kv head, batch row); NW warps, warp w holds tokens
+// w, w+NW, ... of the group, lane l holds channels [4l, 4l+4). Token rows come from
+// the residual window (tokens < s_cur) or from the appended input. 8 warps at 4 CTAs per
+// SM in general; 16 warps at 3 CTAs per SM (half the rows per warp: 40 instead of 64
+// registers) where a warp has more to do per row (isolated entries: kivi-int4o4 prompt
+// append +11 %) or the grid is too small to fill the SMs (llama8b-int8 +9 %); with a
+// full grid the 16-warp CTAs measured 6 % slower (kivi-int4).
 // ---------------------------------------------------------------------------
-template <int BITS, int G>
-__global__ void __launch_bounds__(256, 4) k_group_kernel(AppendParams p) {
-  constexpr int PER_WARP = G / 8;
+template <int BITS, int G, int NW>
+__global__ void __launch_bounds__(32 * NW, NW == 16 ? 3 : 4) k_group_kernel(AppendParams p) {
+  constexpr int PER_WARP = G / NW;
   static_assert(PER_WARP % 2 == 0, "rows are split in pairs");
   pdl_wait();
   pdl_allow_dependents();
@@ -52,8 +56,8 @@ __global__ void __launch_bounds__(256, 4) k_group_kernel(AppendParams p) {
   const int64_t t0 = g * G;
   const int64_t slice = (int64_t)b * p.H + h;
 
-  __shared__ float red_min[8][kHeadDim];
-  __shared__ float red_max[8][kHeadDim];
+  __shared__ float red_min[NW][kHeadDim];
+  __shared__ float red_max[NW][kHeadDim];
   __shared__ float s_sc[kHeadDim];
   __shared__ float s_rs[kHeadDim];
   __shared__ int s_zp[kHeadDim];
@@ -70,7 +74,7 @@ __global__ void __launch_bounds__(256, 4) k_group_kernel(AppendParams p) {
   const int64_t in_stride = (int64_t)p.H * kHeadDim;
 #pragma unroll
   for (int k = 0; k < PER_WARP; ++k) {
-    const int64_t t = t0 + warp + 8 * k;
+    const int64_t t = t0 + warp + NW * k;
     const __half* row = (t < p.s_cur) ? resid + t * kHeadDim : in + t * in_stride;
     x[k] = *reinterpret_cast<const uint2*>(row + 4 * lane);
   }
@@ -82,11 +86,11 @@ __global__ void __launch_bounds__(256, 4) k_group_kernel(AppendParams p) {
                                                 (p.S_pad / G) * kHeadDim * 4);
 #pragma unroll
     for (int k = 0; k < PER_WARP; k += 2) {  // rows in pairs: one sort of their packed order keys
-      const int64_t t = t0 + warp + 8 * k;     // row k + 1 is token t + 8
+      const int64_t t = t0 + warp + NW * k;     // row k + 1 is token t + NW
       const uint32_t xa[4] = {x[k].x & 0xFFFFu, x[k].x >> 16, x[k].y & 0xFFFFu, x[k].y >> 16};
       const uint32_t xc[4] = {x[k + 1].x & 0xFFFFu, x[k + 1].x >> 16, x[k + 1].y & 0xFFFFu, x[k + 1].y >> 16};
       bool ta[4], tc[4];
-      split_two_rows_outliers(xa, xc, ta, tc, ent + t * p.kout, ent + (t + 8) * p.kout, p.kout, lane);
+      split_two_rows_outliers(xa, xc, ta, tc, ent + t * p.kout, ent + (t + NW) * p.kout, p.kout, lane);
       x[k].x &= (ta[0] ? 0xFFFF0000u : 0xFFFFFFFFu) & (ta[1] ? 0x0000FFFFu : 0xFFFFFFFFu);
       x[k].y &= (ta[2] ? 0xFFFF0000u : 0xFFFFFFFFu) & (ta[3] ? 0x0000FFFFu : 0xFFFFFFFFu);
       x[k + 1].x &= (tc[0] ? 0xFFFF0000u : 0xFFFFFFFFu) & (tc[1] ? 0x0000FFFFu : 0xFFFFFFFFu);
@@ -116,7 +120,7 @@ __global__ void __launch_bounds__(256, 4) k_group_kernel(AppendParams p) {
     const int c = threadIdx.x;
     float a = red_min[0][c], z = red_max[0][c];
 #pragma unroll
-    for (int w = 1; w < 8; ++w) {
+    for (int w = 1; w < NW; ++w) {
       a = fminf(a, red_min[w][c]);
       z = fmaxf(z, red_max[w][c]);
     }
@@ -141,7 +145,7 @@ __global__ void __launch_bounds__(256, 4) k_group_kernel(AppendParams p) {
   uint8_t* codes = p.k_codes + slice * p.k_codes_slice;
 #pragma unroll
   for (int k = 0; k < PER_WARP; ++k) {
-    const int64_t t = t0 + warp + 8 * k;
+    const int64_t t = t0 + warp + NW * k;
     float xf[4];
     load4(reinterpret_cast<const __half*>(&x[k]), xf);
     uint32_t u[4];
@@ -655,11 +659,15 @@ cudaError_t launch_keys(const AppendParams& p, cudaStream_t stream) {
   dim3 grid((unsigned)p.n_groups, (unsigned)p.H, (unsigned)p.B);
   switch (p.G) {
     case 32:
-      if (p.kout > 0) return launch_pdl(k_group_kernel<BITS, 32>, grid, dim3(256), 0, stream, p);
+      if (p.kout > 0) return launch_pdl(k_group_kernel<BITS, 32, 16>, grid, dim3(512), 0, stream, p);
       return launch_pdl(k_group32_kernel<BITS>, dim3((unsigned)((p.n_groups + 7) / 8), (unsigned)p.H, (unsigned)p.B),
                         dim3(256), 0, stream, p);
-    case 64: return launch_pdl(k_group_kernel<BITS, 64>, grid, dim3(256), 0, stream, p);
-    default: return launch_pdl(k_group_kernel<BITS, 128>, grid, dim3(256), 0, stream, p);
+    case 64:
+      return p.wide_keys ? launch_pdl(k_group_kernel<BITS, 64, 16>, grid, dim3(512), 0, stream, p)
+                         : launch_pdl(k_group_kernel<BITS, 64, 8>, grid, dim3(256), 0, stream, p);
+    default:
+      return p.wide_keys ? launch_pdl(k_group_kernel<BITS, 128, 16>, grid, dim3(512), 0, stream, p)
+                         : launch_pdl(k_group_kernel<BITS, 128, 8>, grid, dim3(256), 0, stream, p);
   }
 }
 
