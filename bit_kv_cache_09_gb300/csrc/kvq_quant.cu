@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(32 * NW, NW == 16 ? 3 : 4) k_group_kernel(Appe
     uint32_t u[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) u[e] = quant_code<BITS>(xf[e], s[e], rs[e], zp[e]);
-    store_k4<BITS>(codes + t * p.rowK, lane, u);
+    store_k4<BITS>(codes + t * (kHeadDim * BITS / 8), lane, u);
   }
 }
 
@@ -219,7 +219,7 @@ __global__ void __launch_bounds__(256, 2) k_group32_kernel(AppendParams p) {
     uint32_t u[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) u[e] = quant_code<BITS>(xf[e], s[e], rs[e], zp[e]);
-    store_k4<BITS>(codes + (t0 + k) * p.rowK, lane, u);
+    store_k4<BITS>(codes + (t0 + k) * (kHeadDim * BITS / 8), lane, u);
   }
 }
 
@@ -304,7 +304,8 @@ __global__ void __launch_bounds__(256, 8) v_token_kernel(AppendParams p) {
     u[2 * k + 1] = quant_code<BITS>(f.y, s, rs, zpu);
   }
 
-  uint16_t* pair = reinterpret_cast<uint16_t*>(p.v_codes + slice * p.v_codes_slice + (t >> 1) * 2 * p.rowV) + (t & 1);
+  uint16_t* pair =
+      reinterpret_cast<uint16_t*>(p.v_codes + slice * p.v_codes_slice + (t >> 1) * (2 * kHeadDim * BITS / 8)) + (t & 1);
   if (BITS == 8) {
     // unit 8m + l = (channel 16l + m, channel 16l + m + 8)
     if (valid) {
@@ -440,7 +441,8 @@ __global__ void __launch_bounds__(256, 6) v_token32_kernel(AppendParams p) {
   };
 
   // the token's half of its pair row: 16-bit unit k at pair[2 k]
-  uint16_t* pair = reinterpret_cast<uint16_t*>(p.v_codes + slice * p.v_codes_slice + (t >> 1) * 2 * p.rowV) + (t & 1);
+  uint16_t* pair =
+      reinterpret_cast<uint16_t*>(p.v_codes + slice * p.v_codes_slice + (t >> 1) * (2 * kHeadDim * BITS / 8)) + (t & 1);
   {
     // unit 2m + sl/2: this lane's codes q = 0..3 at bits 2q of byte (sl & 1). Bytes of
     // m = 0..3 and 4..7 are gathered in two words; even lanes store m = 0..3, odd lanes

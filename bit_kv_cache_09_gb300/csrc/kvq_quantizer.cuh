@@ -68,22 +68,20 @@ __device__ __forceinline__ float inv_far() {
 template <int BITS>
 __device__ __forceinline__ void group_params(float xmin, float xmax, __half& s_h, __half& z_h, float& s, float& rs,
                                              float& zp) {
-  if (xmax == xmin) {  // a constant group is widened to include 0
-    if (xmin > 0.0f) xmin = 0.0f;
-    if (xmax < 0.0f) xmax = 0.0f;
-  }
-  if (xmax == xmin) {
-    s_h = __float2half_rn(1.0f);  // all zeros: scale 1
-  } else {
-    const float range = __fsub_rn(xmax, xmin);
-    float s32 = div_rn(range, __fsub_rn(Q<BITS>::qmax, Q<BITS>::qmin), inv_levels<BITS>());
-    // binary16 holds every integer only up to 2048: a narrow group far from zero gets the
-    // wider scale max|x| / (2048 - 2^BITS), so that |x / scale| <= 2048 - 2^BITS and the
-    // zero point (|zp| <= 2048 - 2^(BITS-1)) is stored exactly
-    const float s_far = div_rn(fmaxf(fabsf(xmin), fabsf(xmax)), (float)(2048 - (1 << BITS)), inv_far<BITS>());
-    s32 = fmaxf(s32, s_far);
-    s_h = __float2half_ru(s32);
-  }
+  // a constant group is widened to include 0 (selects, not branches: every lane takes the
+  // same instructions; fminf/fmaxf may differ from the comparisons only in the sign of a
+  // zero, which changes neither the range nor the zero point)
+  const bool cst = xmax == xmin;
+  xmin = cst ? fminf(xmin, 0.0f) : xmin;
+  xmax = cst ? fmaxf(xmax, 0.0f) : xmax;
+  const float range = __fsub_rn(xmax, xmin);  // 0 exactly when xmax == xmin (gradual underflow)
+  float s32 = div_rn(range, __fsub_rn(Q<BITS>::qmax, Q<BITS>::qmin), inv_levels<BITS>());
+  // binary16 holds every integer only up to 2048: a narrow group far from zero gets the
+  // wider scale max|x| / (2048 - 2^BITS), so that |x / scale| <= 2048 - 2^BITS and the
+  // zero point (|zp| <= 2048 - 2^(BITS-1)) is stored exactly
+  const float s_far = div_rn(fmaxf(fabsf(xmin), fabsf(xmax)), (float)(2048 - (1 << BITS)), inv_far<BITS>());
+  s32 = fmaxf(s32, s_far);
+  s_h = range == 0.0f ? __float2half_rn(1.0f) : __float2half_ru(s32);  // all zeros: scale 1
   s = __half2float(s_h);
   rs = __frcp_rn(s);
   const float z = __fsub_rn(Q<BITS>::qmin, rintf(div_rn(xmin, s, rs)));  // an integer, |z| <= 2048
