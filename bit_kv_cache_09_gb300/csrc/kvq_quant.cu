@@ -497,8 +497,15 @@ __global__ void __launch_bounds__(256) k_token_sym_kernel(AppendParams p) {
   pdl_allow_dependents();
   const bool valid = wb_raw < nb;
   const int64_t wb = valid ? wb_raw : nb - 1;  // lanes past the end read a real row and store nothing
-  const int64_t tt = wb / p.H;
-  const int h = (int)(wb % p.H);
+  int64_t tt;
+  int h;
+  if (p.rows_32) {  // a 64-bit division costs a call to a long software routine
+    tt = fast_div((uint32_t)wb, p.fd_H);
+    h = (int)(wb - tt * p.H);
+  } else {
+    tt = wb / p.H;
+    h = (int)(wb % p.H);
+  }
   const int b = blockIdx.y;
   const int64_t w = (int64_t)b * nb + wb;
   const int64_t t = p.s_cur + tt;
@@ -555,8 +562,15 @@ __global__ void __launch_bounds__(256) k_token_sym_outlier_kernel(AppendParams p
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
     const int64_t wb = k < n_rows ? wb0 + k : wb0;  // a lone last row is split twice, stored once
-    const int64_t tt = wb / p.H;
-    const int h = (int)(wb % p.H);
+    int64_t tt;
+    int h;
+    if (p.rows_32) {
+      tt = fast_div((uint32_t)wb, p.fd_H);
+      h = (int)(wb - tt * p.H);
+    } else {
+      tt = wb / p.H;
+      h = (int)(wb % p.H);
+    }
     const int64_t slice = (int64_t)b * p.H + h;
     t[k] = p.s_cur + tt;
     codes[k] = p.k_codes + slice * p.k_codes_slice + t[k] * p.rowK;
