@@ -109,7 +109,12 @@ def whole_job_rate(units_per_rank: float, world: int, seconds: float) -> float:
     return units_per_rank * world / seconds
 
 
-DECODE_SOURCES = ("bit_kv_cache_09_gb300/csrc/kvq_decode_mma.cuh", "bit_kv_cache_09_gb300/csrc/kvq_merge.cuh")
+# every source the decode-attention kernel is compiled from (its own header, the merge, and
+# the shared layout, parameter and quantizer headers its fused append step uses)
+DECODE_SOURCES = tuple(
+    "bit_kv_cache_09_gb300/csrc/" + f
+    for f in ("kvq_decode_mma.cuh", "kvq_merge.cuh", "kvq_quantizer.cuh", "kvq_common.cuh", "kvq_kernels.h",
+              "kvq_decode_mma_b2.cu", "kvq_decode_mma_b4.cu", "kvq_decode_mma_b8.cu"))
 
 
 def decode_source_hash() -> str:
