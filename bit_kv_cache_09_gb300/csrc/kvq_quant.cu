@@ -228,8 +228,8 @@ __global__ void __launch_bounds__(256, 2) k_group32_kernel(AppendParams p) {
 // token, kv head) rows, in the input's own order; lanes 8r .. 8r+7 hold row r, lane
 // 8r + l its channels [16l, 16l + 16). A value group of Gv channels spans Gv/16 lanes.
 // In the pair-row layout channel 16l + i sits at position 16(i % 8) + 2l + i / 8, so
-// 8-bit codes fill their 16-bit units within a lane, 4-bit units take two lanes and
-// 2-bit units four. SYM: the symmetric per-token scheme (one group of d channels,
+// 8-bit codes fill their 16-bit units within a lane and 4-bit units take two lanes (2-bit
+// values: v_token32_kernel). SYM: the symmetric per-token scheme (one group of d channels,
 // scale from max|x|, zero point 0).
 // ---------------------------------------------------------------------------
 template <int BITS, bool SYM = false>
@@ -306,6 +306,7 @@ __global__ void __launch_bounds__(256, 8) v_token_kernel(AppendParams p) {
 
   uint16_t* pair =
       reinterpret_cast<uint16_t*>(p.v_codes + slice * p.v_codes_slice + (t >> 1) * (2 * kHeadDim * BITS / 8)) + (t & 1);
+  static_assert(BITS == 8 || BITS == 4, "2-bit values: v_token32_kernel");
   if (BITS == 8) {
     // unit 8m + l = (channel 16l + m, channel 16l + m + 8)
     if (valid) {
@@ -329,26 +330,6 @@ __global__ void __launch_bounds__(256, 8) v_token_kernel(AppendParams p) {
       for (int j = 0; j < 4; ++j) {
         const int m = odd ? 4 + j : j;
         pair[2 * (4 * m + (sl >> 1))] = (uint16_t)__byte_perm(lo, hi, (unsigned)(j | ((4 + j) << 4)));
-      }
-    }
-  } else {
-    // unit 2m + l/4: 4-bit pieces of the four lanes 4(l/4) .. 4(l/4) + 3 (lane q at bit 4q);
-    // piece m of a lane holds channels 16l + m and 16l + m + 8. Lane q stores m = 2q, 2q+1.
-    uint32_t wd = 0;
-#pragma unroll
-    for (int m = 0; m < 8; ++m) wd |= (u[m] | (u[m + 8] << 2)) << (4 * m);
-    const int base = lane & ~3, q = sl & 3;
-    uint32_t wq[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) wq[k] = __shfl_sync(0xffffffffu, wd, base + k);
-    if (valid) {
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int m = 2 * q + e;
-        uint32_t unit = 0;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) unit |= ((wq[k] >> (4 * m)) & 0xFu) << (4 * k);
-        pair[2 * (2 * m + (sl >> 2))] = (uint16_t)unit;
       }
     }
   }
