@@ -539,7 +539,8 @@ def main():
         d2h = out.numel() * 4
         e2e = {"value": round(e_bytes * world / (e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
                "tokens_per_s": round(w.batch * KE * world / (e_ms / 1e3), 1),
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": KE, "cuda_graph": use_graph}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": KE, "cuda_graph": use_graph,
+               "device_ms": round(b0.elapsed_time(b1), 3), "host_ms": round(t_host * 1e3, 3)}
 
     cache.check_errors()  # no bounded wait of any timed launch ran out
     cpu = None
