@@ -354,6 +354,7 @@ def test_mixed_widths_have_no_simt_path():
 
 @pytest.mark.parametrize("bits,v_bits,G,Gv,R,B,H,S", [
     (4, 0, 128, 64, 128, 32, 4, 2049),
+    (4, 0, 64, 64, 128, 32, 4, 2049),  # 64-token key groups on the 8-warp key kernel (full grid)
     (2, 0, 32, 32, 128, 32, 4, 2049),
     (8, 4, 128, 64, 128, 12, 4, 4000),
     (8, 0, 128, 128, 0, 12, 4, 4000),
