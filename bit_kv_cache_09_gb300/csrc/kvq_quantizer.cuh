@@ -176,12 +176,15 @@ __device__ __forceinline__ void quantize_value_row(const __half* v_row, uint16_t
 }
 
 // The 64th smallest (index 63 in ascending order) of the warp's 128 keys, lane l holding
-// elements 4l .. 4l + 3: a bitonic sorting network over the 128 positions (Batcher),
-// compare-exchanges at distance 1 and 2 inside a lane, at distance 4j across lanes l and
-// l ^ j with a shuffle; position 63 is element 3 of lane 15 after the last stage.
-// PAIR: every word holds the 16-bit keys of two rows (low and high halves), sorted at once
-// with 16x2 SIMD min/max (the network does not depend on the data); the result holds both
-// rows' 64th smallest keys.
+// elements 4l .. 4l + 3. A bitonic sorting network (Batcher) sorts the two halves of 64
+// positions, lanes 0-15 ascending and lanes 16-31 descending, which together form a
+// bitonic sequence; one compare-exchange at distance 64 (the network's next step) then
+// leaves the 64 smallest keys in positions 0-63, and their maximum is the 64th smallest:
+// the rest of the last merge stage is not needed. Compare-exchanges at distance 1 and 2
+// run inside a lane, at distance 4j across lanes l and l ^ j with a shuffle.
+// PAIR: every word holds the 16-bit keys of two rows (low and high halves), handled at
+// once with 16x2 SIMD min/max (the network does not depend on the data); the result
+// holds both rows' 64th smallest keys.
 template <bool PAIR = false>
 __device__ __forceinline__ uint32_t kmin(uint32_t a, uint32_t b) { return PAIR ? __vminu2(a, b) : min(a, b); }
 template <bool PAIR = false>
@@ -191,12 +194,12 @@ template <bool PAIR = false>
 __device__ __forceinline__ uint32_t sorted_key_63(const uint32_t (&key_in)[4], int lane) {
   uint32_t a[4] = {key_in[0], key_in[1], key_in[2], key_in[3]};
 #pragma unroll
-  for (int k = 2; k <= 128; k <<= 1) {
+  for (int k = 2; k <= 64; k <<= 1) {
 #pragma unroll
     for (int j = k >> 1; j > 0; j >>= 1) {
       if (j >= 4) {
         const int lj = j >> 2;                         // partner lane distance
-        const bool up = k == 128 || ((lane & (k >> 2)) == 0);  // this block sorts ascending
+        const bool up = (lane & (k >> 2)) == 0;        // this block sorts ascending
         const bool low = (lane & lj) == 0;             // this lane holds the lower positions
         const bool keep_min = (up == low);
 #pragma unroll
@@ -217,7 +220,17 @@ __device__ __forceinline__ uint32_t sorted_key_63(const uint32_t (&key_in)[4], i
       }
     }
   }
-  return __shfl_sync(0xffffffffu, a[3], 15);
+  // distance 64: lanes 0-15 keep the minima of positions i and i + 64 (lane l ^ 16), the
+  // 64 smallest keys; their maximum over the 16 lanes (lanes 16-31 reduce their own half)
+  uint32_t m = 0u;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const uint32_t lo = kmin<PAIR>(a[e], __shfl_xor_sync(0xffffffffu, a[e], 16));
+    m = e ? kmax<PAIR>(m, lo) : lo;
+  }
+#pragma unroll
+  for (int off = 8; off > 0; off >>= 1) m = kmax<PAIR>(m, __shfl_xor_sync(0xffffffffu, m, off));
+  return __shfl_sync(0xffffffffu, m, 0);
 }
 
 // Order-preserving 16-bit keys of binary16 bit patterns (negative values bit-inverted,
