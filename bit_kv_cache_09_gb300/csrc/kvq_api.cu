@@ -307,7 +307,7 @@ kvq_status kvq_quantize_append(const kvq_config* cfg, const kvq_buffers* bufs, i
   p.fd_H = kvq::make_fast_div((uint32_t)g.H);
   p.rows_32 = n_new * g.H < (int64_t(1) << 31);
   p.sym = g.sym;
-  p.wide_keys = g.kout > 0 || (int64_t)p.n_groups * g.H * g.B < 4 * (int64_t)device_sm_count();
+  p.wide_keys = g.kout > 0;
   cudaError_t e = kvq::launch_append(p, g.bits, g.vbits, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }

@@ -56,8 +56,7 @@ struct AppendParams {
   int rows_32;      // n_new * H < 2^31: value-row indices fit the fast division
   int sym;          // symmetric per-token int8 scheme (k_meta: one binary16 scale per token)
   int kout;         // isolated key entries per token (after the key scales or group metadata)
-  int wide_keys;    // key groups of 64/128 tokens on 16-warp CTAs (isolated entries, or a grid
-                    // of fewer CTAs than four per SM); else 8 warps
+  int wide_keys;    // key groups of 64/128 tokens on 16-warp CTAs (isolated key entries); else 8
 };
 
 struct DequantParams {

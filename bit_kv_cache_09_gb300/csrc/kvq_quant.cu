@@ -41,8 +41,8 @@ __device__ __forceinline__ void store_k4(uint8_t* row, int lane, const uint32_t*
 // the residual window (tokens < s_cur) or from the appended input. 8 warps at 4 CTAs per
 // SM in general; 16 warps at 3 CTAs per SM (half the rows per warp: 40 instead of 64
 // registers) where a warp has more to do per row (isolated entries: kivi-int4o4 prompt
-// append +11 %) or the grid is too small to fill the SMs (llama8b-int8 +9 %); with a
-// full grid the 16-warp CTAs measured 6 % slower (kivi-int4).
+// append +11 %); without isolated entries the 16-warp CTAs measured slower, with a full
+// grid (kivi-int4 -6 %) and at batch 1 (llama8b-int8 -5 %).
 // ---------------------------------------------------------------------------
 template <int BITS, int G, int NW>
 __global__ void __launch_bounds__(32 * NW, NW == 16 ? 3 : 4) k_group_kernel(AppendParams p) {
