@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(256, 2) k_group32_kernel(AppendParams p) {
 // values: v_token32_kernel). SYM: the symmetric per-token scheme (one group of d channels,
 // scale from max|x|, zero point 0).
 // ---------------------------------------------------------------------------
-template <int BITS, bool SYM = false>
+template <int BITS, bool SYM = false, int LPG = 8>
 __global__ void __launch_bounds__(256, 8) v_token_kernel(AppendParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sl = lane & 7;
@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(256, 8) v_token_kernel(AppendParams p) {
       mx2 = k ? __hmax2(mx2, hk) : hk;
     }
   }
-  const int lpg = p.Gv >> 4;  // lanes per value group: 2, 4 or 8
+  constexpr int lpg = LPG;  // lanes per value group (Gv / 16): 2, 4 or 8
   __half s_h, z_h;
   float s, rs, zp;
   if constexpr (SYM) {
@@ -283,6 +283,7 @@ __global__ void __launch_bounds__(256, 8) v_token_kernel(AppendParams p) {
     zp = 0.0f;
   } else {
     float mn = fminf(__low2float(mn2), __high2float(mn2)), mx = fmaxf(__low2float(mx2), __high2float(mx2));
+#pragma unroll
     for (int off = 1; off < lpg; off <<= 1) {
       mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
@@ -675,8 +676,13 @@ cudaError_t launch_values(const AppendParams& p, cudaStream_t stream) {
     return launch_pdl(v_token32_kernel<VBITS>, dim3((unsigned)((rows + 63) / 64), (unsigned)p.B), dim3(256), 0, stream,
                       p);
   } else {
-    return launch_pdl(v_token_kernel<VBITS, SYM>, dim3((unsigned)((rows + 31) / 32), (unsigned)p.B), dim3(256), 0,
-                      stream, p);
+    const dim3 grid((unsigned)((rows + 31) / 32), (unsigned)p.B);
+    if constexpr (SYM) return launch_pdl(v_token_kernel<VBITS, true, 8>, grid, dim3(256), 0, stream, p);
+    switch (p.Gv) {  // lanes per value group as a constant: the group reduction unrolls
+      case 32: return launch_pdl(v_token_kernel<VBITS, false, 2>, grid, dim3(256), 0, stream, p);
+      case 64: return launch_pdl(v_token_kernel<VBITS, false, 4>, grid, dim3(256), 0, stream, p);
+      default: return launch_pdl(v_token_kernel<VBITS, false, 8>, grid, dim3(256), 0, stream, p);
+    }
   }
 }
 
